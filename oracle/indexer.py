@@ -1,0 +1,433 @@
+"""Plain CPU statement of the lightning-indexer hot path (fp64), for tests only.
+
+Test infrastructure (see the package docstring). Page citations name the page
+and its section:
+
+* [DSA] "DeepSeek V3.2 稀疏注意力 DSA 推理流程图解" (aiinfra.pub)
+* [V41] "V4.1 索引器接入稀疏 MQA logits" (prhub.com.cn, vLLM PR #56254 review)
+* [PACK] "修复 DSV4 FlashInfer 稀疏 MLA 在打包 KV 布局下的地址错误"
+  (prhub.com.cn, vLLM PR #47493 review)
+
+Shapes: H = 64 heads, D = 128 dims ([DSA] "Indexer 内部六步" step ①: 64 heads
+of 128 dims for q, one shared 128-dim k). The indexer k cache stores 132 bytes
+per token ([DSA] cost table and data-flow item 1): 128 e4m3 bytes plus a 4-byte
+fp32 scale. Where a block keeps them is not printed; the reading used here (and
+by the library) is the split block layout: block ``b`` starts at byte
+``b * block_stride``; token ``i`` of the block has its 128 value bytes at
+``i * 128`` and its fp32 scale at ``block_size * 128 + 4 * i``.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+from .codecs import E4M3_MAX, e4m3_decode, e4m3_encode
+
+H = 64
+D = 128
+TOKEN_BYTES = D + 4
+
+
+# ----------------------------------------------------------------------------
+# a1: k quantisation fused with the cache insert
+# ----------------------------------------------------------------------------
+
+def k_quant(k) -> tuple[np.ndarray, np.ndarray]:
+    """Per-token FP8 quantisation of k, one fp32 scale per 128 values.
+
+    [DSA] step ⑤: k is quantised and written into the cache in one operation
+    (``indexer_k_quant_and_cache(k, kv_cache, slot_mapping, quant_block_size,
+    scale_fmt)``); step ④ fixes one scale per 128 elements. The scale format is
+    fp32 ``amax / 448`` so the largest magnitude maps onto the e4m3 maximum.
+
+    Steps, all in IEEE binary32 as the format fixes: ``amax = max |k_d|``;
+    ``scale = amax / 448``; ``k8_d = e4m3(k_d / scale)``. A token whose scale is
+    zero (all-zero k, or amax so small the division underflows) stores scale 0
+    and all-zero bytes, so its logits are exactly 0.
+
+    k: [n, 128] array of fp32 values (bf16 inputs widened exactly).
+    Returns (k8 uint8 [n, 128], scale float32 [n]).
+    """
+    k = np.asarray(k, dtype=np.float32)
+    n = k.shape[0]
+    k8 = np.zeros((n, D), dtype=np.uint8)
+    scale = np.zeros(n, dtype=np.float32)
+    for t in range(n):
+        amax = np.float32(np.max(np.abs(k[t]))) if D else np.float32(0)
+        s = np.float32(amax / np.float32(E4M3_MAX))
+        scale[t] = s
+        if s == 0:
+            continue
+        k8[t] = e4m3_encode(k[t] / s)
+    return k8, scale
+
+
+def k_quant_and_cache(k, slot_mapping, cache: np.ndarray, block_size: int) -> None:
+    """Quantise each token of ``k`` and write it to its slot of the paged cache.
+
+    [DSA] step ⑤ and data-flow item 1 (132 bytes per token). ``slot_mapping[i]``
+    is the physical slot ``block * block_size + offset`` of token i; a negative
+    slot skips the token (the padding convention of slot-mapped inserts).
+
+    cache: uint8 [num_blocks, block_stride], modified in place.
+    """
+    k8, scale = k_quant(k)
+    slots = np.asarray(slot_mapping, dtype=np.int64)
+    for i, slot in enumerate(slots):
+        if slot < 0:
+            continue
+        blk, off = divmod(int(slot), block_size)
+        cache[blk, off * D:(off + 1) * D] = k8[i]
+        base = block_size * D + 4 * off
+        cache[blk, base:base + 4] = np.frombuffer(scale[i:i + 1].tobytes(), dtype=np.uint8)
+
+
+def cache_token(cache: np.ndarray, block_size: int, block: int, offset: int):
+    """(k8 [128] uint8, scale float32) of one token in the split block layout."""
+    k8 = cache[block, offset * D:(offset + 1) * D]
+    base = block_size * D + 4 * offset
+    scale = np.frombuffer(cache[block, base:base + 4].tobytes(), dtype=np.float32)[0]
+    return k8, scale
+
+
+def gather_k(cache: np.ndarray, block_size: int, block_table_row, n_tok: int):
+    """Copy the first ``n_tok`` tokens of one request out of the paged cache.
+
+    [DSA] "prefill 和 decode 用完全不同的内核": prefill works on gathered k;
+    [V41] 实现拆解 and the key-symbol list name the prefill gather
+    (``_gather_prefill_chunk_k``). Token ``p`` lives in block
+    ``block_table_row[p // block_size]`` at offset ``p % block_size``.
+
+    Returns (k8 uint8 [n_tok, 128], kscale float32 [n_tok]).
+    """
+    k8 = np.zeros((n_tok, D), dtype=np.uint8)
+    ks = np.zeros(n_tok, dtype=np.float32)
+    for p in range(n_tok):
+        blk = int(block_table_row[p // block_size])
+        k8[p], ks[p] = cache_token(cache, block_size, blk, p % block_size)
+    return k8, ks
+
+
+# ----------------------------------------------------------------------------
+# a3 / a4: the logit definition
+# ----------------------------------------------------------------------------
+
+def _dequant_k(k8, kscale) -> np.ndarray:
+    """k[s] as the cache represents it: e4m3 values times the token's fp32 scale."""
+    return e4m3_decode(k8) * np.asarray(kscale, dtype=np.float64)[:, None]
+
+
+def logits_row(q8_row, w_row, k8, kscale) -> np.ndarray:
+    """Scores of one query row against tokens ``k8``/``kscale`` (fp64).
+
+    [DSA] step ⑥: ``logits[t, s] = sum_h weights[t, h] * (q[t, h] . k[s])`` with
+    64 heads; step ④: every q-side coefficient (q scale, softmax scale, head
+    scale) is already folded into ``weights``, so q enters as its raw e4m3
+    values. k enters dequantised (value times the token's stored scale).
+
+    q8_row [64, 128] uint8, w_row [64] values, k8 [S, 128] uint8, kscale [S].
+    """
+    q = e4m3_decode(q8_row)                       # [64, 128]
+    k = _dequant_k(k8, kscale)                    # [S, 128]
+    per_head = q @ k.T                            # [64, S]: q[t,h] . k[s]
+    w = np.asarray(w_row, dtype=np.float64)
+    return w @ per_head                           # sum_h w[h] * (q[h] . k[s])
+
+
+def mqa_logits(q8, w, k8, kscale, row_ks, row_ke) -> np.ndarray:
+    """Prefill logits on gathered k, with ragged causal row limits.
+
+    Row ``t`` scores the tokens ``s`` in ``[row_ks[t], row_ke[t])``; every other
+    column of the ``[T, S]`` result is ``-inf`` (not visible). Causality is
+    carried by the limits: a query at position ``p`` sees ``s <= p``, so its
+    ``row_ke`` is ``p + 1`` ([DSA] step ⑥; [V41] ``row_ks``/``row_ke`` in the
+    rows-metadata snippet).
+    """
+    q8 = np.asarray(q8)
+    T = q8.shape[0]
+    S = np.asarray(k8).shape[0]
+    out = np.full((T, S), -np.inf)
+    for t in range(T):
+        lo = max(int(row_ks[t]), 0)
+        hi = min(int(row_ke[t]), S)
+        if hi <= lo:
+            continue
+        out[t, lo:hi] = logits_row(q8[t], w[t], k8[lo:hi], kscale[lo:hi])
+    return out
+
+
+def decode_row_limit(ctx_len: int, next_n: int, j: int) -> int:
+    """Number of visible tokens for query ``j`` of a request with ``next_n`` new queries.
+
+    The request's own new tokens are already in the cache, so the context holds
+    ``ctx_len`` tokens and query j (0-based among the last ``next_n``
+    positions) sits at position ``ctx_len - next_n + j``; it sees everything up
+    to and including itself.
+    """
+    return ctx_len - next_n + j + 1
+
+
+def paged_decode_logits(q8, w, cache, block_size, block_table, ctx_lens, next_n=1) -> np.ndarray:
+    """Decode logits read through the block table of the paged cache.
+
+    [DSA] "prefill 和 decode 用完全不同的内核": decode does not gather, it reads the
+    paged cache directly. Row ``r = b * next_n + j`` belongs to request ``b``.
+    Result ``[rows, max ctx_len]``: visible columns hold the logit, columns in
+    ``[limit, ctx_len)`` hold ``-inf``, columns ``>= ctx_len`` hold NaN (the
+    library leaves them untouched).
+    """
+    ctx_lens = np.asarray(ctx_lens, dtype=np.int64)
+    B = len(ctx_lens)
+    rows = B * next_n
+    width = int(ctx_lens.max()) if B else 0
+    out = np.full((rows, width), np.nan)
+    for b in range(B):
+        L = int(ctx_lens[b])
+        k8, ks = gather_k(cache, block_size, block_table[b], L)
+        for j in range(next_n):
+            r = b * next_n + j
+            lim = max(min(decode_row_limit(L, next_n, j), L), 0)
+            out[r, :L] = -np.inf
+            if lim > 0:
+                out[r, :lim] = logits_row(q8[r], w[r], k8[:lim], ks[:lim])
+    return out
+
+
+# ----------------------------------------------------------------------------
+# a5: top-k with -1 fill
+# ----------------------------------------------------------------------------
+
+def topk_row(values, ks: int, ke: int, k: int) -> np.ndarray:
+    """Top-``k`` request-local indices of one row, ``-1`` for empty slots.
+
+    [DSA] opening section and data-flow item 2: keep the 2048 highest-scoring
+    history tokens; the index table is int32 and ``-1`` marks an empty entry.
+    The row's candidates are the columns ``[ks, ke)``; results are reported as
+    ``s - ks``. When at most ``k`` columns are visible all of them are kept (in
+    column order). Otherwise the order is a stable sort by value descending,
+    then index ascending, so ties at the threshold keep the lower index. Empty
+    slots sit at the tail.
+    """
+    values = np.asarray(values, dtype=np.float64)
+    ks = int(ks)
+    ke = int(ke)
+    n = max(ke - ks, 0)
+    out = np.full(k, -1, dtype=np.int64)
+    if n <= k:
+        out[:n] = np.arange(n)
+        return out
+    seg = values[ks:ke]
+    order = np.lexsort((np.arange(n), -seg))
+    out[:] = order[:k]
+    return out
+
+
+def topk(logits, row_ks, row_ke, k: int) -> np.ndarray:
+    """``topk_row`` for every row: ``[rows, k]`` int64."""
+    logits = np.asarray(logits)
+    rows = logits.shape[0]
+    ks = np.zeros(rows, dtype=np.int64) if row_ks is None else np.asarray(row_ks)
+    return np.stack([topk_row(logits[r], ks[r], row_ke[r], k) for r in range(rows)]) if rows else \
+        np.zeros((0, k), dtype=np.int64)
+
+
+# ----------------------------------------------------------------------------
+# a6: request-local index -> physical slot
+# ----------------------------------------------------------------------------
+
+def packed_block_span(block_stride: int, token_stride: int) -> int:
+    """Tokens per physical block of a pool: ``block_stride // token_stride``.
+
+    [PACK] 实现拆解 item 1 and the ``_packed_block_span`` snippet: the span is
+    the pool's per-block stride over its per-token stride and must divide
+    exactly, else the layout is rejected.
+    """
+    if token_stride <= 0 or block_stride % token_stride != 0:
+        raise ValueError(
+            f"block stride {block_stride} is not a multiple of the token stride {token_stride}")
+    return block_stride // token_stride
+
+
+def req_to_global_slots(local, row_to_req, block_table, block_size: int, block_span: int) -> np.ndarray:
+    """Request-local positions -> physical slots, ``-1`` preserved.
+
+    [DSA] "几个容易踩的点": the indexer emits positions inside the request, the
+    attention kernel needs paged-cache slots (``triton_convert_req_index_to_global_index``).
+    [PACK] remap snippet: slot ``= (v // block_size) -> its physical block`` times
+    ``block_span`` plus ``v % block_size``; negative entries stay ``-1``.
+    Position ``v`` of row ``r`` uses block ``block_table[req(r), v // block_size]``.
+    """
+    local = np.asarray(local, dtype=np.int64)
+    rows, k = local.shape
+    out = np.full((rows, k), -1, dtype=np.int64)
+    for r in range(rows):
+        req = r if row_to_req is None else int(row_to_req[r])
+        for i in range(k):
+            v = int(local[r, i])
+            if v < 0:
+                continue
+            blk = int(block_table[req][v // block_size])
+            out[r, i] = blk * block_span + v % block_size
+    return out
+
+
+# ----------------------------------------------------------------------------
+# a7: candidate expansion (V4.1 hierarchical variant)
+# ----------------------------------------------------------------------------
+
+def expand_candidates_row(cand, ks: int, ke: int, cand_block_size: int, sbk: int):
+    """Flatten, filter, sort, dedupe and tail-pad one row of candidate blocks.
+
+    [V41] 实现拆解 item 3 and the expansion snippet, in the page's order:
+
+    1. each candidate block id ``c`` (in units of ``cand_block_size`` tokens) is
+       split into ``R = cand_block_size / sbk`` sparse blocks ``c*R + j``;
+    2. only sparse blocks inside the row's KV range are kept:
+       ``0 <= x < ceil((ke - ks) / sbk)``; negative ids are padding;
+    3. the kept ids are sorted ascending. Reading adopted here: duplicates are
+       removed after sorting (the page sorts without dedupe and says duplicates
+       are tolerated in production; scoring a token twice would let it enter the
+       top-k twice, so the unique set is taken);
+    4. ids are anchored at ``ks // sbk`` (``ks`` is required to be a multiple of
+       ``sbk``);
+    5. the tail is padded with the last valid id (or with the anchor when none
+       is valid);
+    6. ``end`` counts the valid sparse token columns: every kept block is whole
+       except the last, which holds ``min(max(ke - start_of_last, 1), sbk)``.
+
+    Returns (sparse_idx int64 [len(cand) * R], end int).
+    """
+    R = cand_block_size // sbk
+    kv_len = max(ke - ks, 0)
+    max_block = (kv_len + sbk - 1) // sbk
+    kept = []
+    for c in cand:
+        c = int(c)
+        if c < 0:
+            continue
+        for j in range(R):
+            x = c * R + j
+            if 0 <= x < max_block:
+                kept.append(x)
+    uniq = sorted(set(kept))
+    n = len(uniq)
+    base = ks // sbk
+    width = len(cand) * R
+    si = np.empty(width, dtype=np.int64)
+    for i in range(width):
+        if i < n:
+            si[i] = uniq[i] + base
+        else:
+            si[i] = (uniq[-1] + base) if n else base
+    if n == 0:
+        end = 0
+    else:
+        last_start = uniq[-1] * sbk + ks
+        end = (n - 1) * sbk + min(max(ke - last_start, 1), sbk)
+    return si, end
+
+
+def expand_candidates(cand, row_ks, row_ke, cand_block_size: int, sbk: int):
+    """``expand_candidates_row`` over every row: (sparse_idx [rows, K*R], end [rows])."""
+    cand = np.asarray(cand)
+    rows = cand.shape[0]
+    sis, ends = [], []
+    for r in range(rows):
+        ks = 0 if row_ks is None else int(row_ks[r])
+        si, e = expand_candidates_row(cand[r], ks, int(row_ke[r]), cand_block_size, sbk)
+        sis.append(si)
+        ends.append(e)
+    R = cand_block_size // sbk
+    return (np.stack(sis) if rows else np.zeros((0, cand.shape[1] * R), dtype=np.int64),
+            np.asarray(ends, dtype=np.int64))
+
+
+# ----------------------------------------------------------------------------
+# a8: sparse logits, a9: sparse top-k + remap
+# ----------------------------------------------------------------------------
+
+def sparse_column_token(si_row, c: int, sbk: int) -> int:
+    """Absolute k position scored by sparse column ``c``: ``si[c // sbk] * sbk + c % sbk``."""
+    return int(si_row[c // sbk]) * sbk + c % sbk
+
+
+def sparse_logits_decode(q8, w, cache, block_size, block_table, row_to_req, si, end, sbk) -> np.ndarray:
+    """V4.1 sparse logits read from the paged cache (decode, ``ks = 0``).
+
+    [V41] 功能与动机 and 实现拆解 item 3: only the candidate sparse blocks are
+    scored; the logit is the same weighted head sum. Column ``c`` of row ``r``
+    scores token ``sparse_column_token(si[r], c)`` of request ``row_to_req[r]``;
+    columns ``c >= end[r]`` are not valid and hold ``-inf``.
+    Result: fp64 ``[rows, si.shape[1] * sbk]``.
+    """
+    si = np.asarray(si)
+    rows, n_si = si.shape
+    out = np.full((rows, n_si * sbk), -np.inf)
+    for r in range(rows):
+        req = r if row_to_req is None else int(row_to_req[r])
+        e = int(end[r])
+        if e <= 0:
+            continue
+        toks = [sparse_column_token(si[r], c, sbk) for c in range(e)]
+        k8 = np.zeros((e, D), dtype=np.uint8)
+        ks = np.zeros(e, dtype=np.float32)
+        for i, p in enumerate(toks):
+            blk = int(block_table[req][p // block_size])
+            k8[i], ks[i] = cache_token(cache, block_size, blk, p % block_size)
+        out[r, :e] = logits_row(q8[r], w[r], k8, ks)
+    return out
+
+
+def sparse_logits_prefill(q8, w, k8, kscale, si, end, sbk) -> np.ndarray:
+    """V4.1 sparse logits over gathered k (prefill chunk); same column rule as decode."""
+    si = np.asarray(si)
+    rows, n_si = si.shape
+    out = np.full((rows, n_si * sbk), -np.inf)
+    for r in range(rows):
+        e = int(end[r])
+        if e <= 0:
+            continue
+        toks = np.array([sparse_column_token(si[r], c, sbk) for c in range(e)])
+        out[r, :e] = logits_row(q8[r], w[r], k8[toks], kscale[toks])
+    return out
+
+
+def sparse_topk_remap_row(values, end: int, si_row, ks: int, sbk: int, k: int):
+    """Top-``k`` over the first ``end`` sparse columns, then map columns to positions.
+
+    [V41] 实现拆解 item 3 (``sparse_topk_remap``: top-k over the bf16 sparse
+    logits, then ``_sparse_topk_remap_kernel`` maps each sparse column back to
+    its request-local position) and the rows-metadata snippet (``col_indices``
+    holds the column top-k). Column ``c`` maps to
+    ``(si[c // sbk] - ks // sbk) * sbk + c % sbk``; ``-1`` stays ``-1``.
+
+    Returns (cols int64 [k], positions int64 [k]).
+    """
+    cols = topk_row(values, 0, end, k)
+    pos = np.full(k, -1, dtype=np.int64)
+    base = ks // sbk
+    for i, c in enumerate(cols):
+        if c < 0:
+            continue
+        pos[i] = (int(si_row[c // sbk]) - base) * sbk + int(c) % sbk
+    return cols, pos
+
+
+def dense_masked_topk_row(sparse_values, end: int, si_row, ks: int, ke: int, sbk: int, k: int):
+    """The dense-masked selection the sparse path must reproduce.
+
+    [V41] 功能与动机 (the old consumer scored the whole context and masked
+    everything outside the candidates) and the test list (sparse and
+    dense-masked ``torch.topk`` agree on the selected values): scatter the
+    sparse scores to their context positions, leave every other position at
+    ``-inf``, and select over ``[ks, ke)``. Returns request-local indices.
+    """
+    dense = np.full(max(ke, 0), -np.inf)
+    for c in range(end):
+        dense[sparse_column_token(si_row, c, sbk)] = sparse_values[c]
+    sel = topk_row(dense, ks, ke, k)
+    # a position that only carries -inf was never a candidate: it is an empty slot
+    keep = [int(i) for i in sel if i >= 0 and np.isfinite(dense[ks + int(i)])]
+    out = np.full(k, -1, dtype=np.int64)
+    out[:len(keep)] = keep
+    return out

@@ -1,0 +1,352 @@
+"""Pins for the oracle's indexer functions (CPU only).
+
+Each function is checked against something other than itself: hand-worked
+examples (golden fixtures with their source), closed forms with one-hot inputs,
+exact rational arithmetic, brute force over all subsets, token-level brute
+force, invariants (linearity, paging transparency, sparse = dense-masked), and
+library routines on special cases.
+"""
+
+import itertools
+import json
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import indexer as O
+from oracle.codecs import bf16_decode, e4m3_decode, e4m3_encode
+from sparse_attention_indexer_fp8_gb300 import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------- k quant
+
+def test_k_quant_hand_worked():
+    k = np.zeros((4, 128), dtype=np.float32)
+    k[0, 5] = 448.0                      # scale exactly 1: the byte is the e4m3 max
+    k[2, 0] = 7.0                        # amax 7 -> scale 7/448 = 2^-6 exactly
+    k[2, 1] = 0.5                        # 0.5 / 2^-6 = 32 -> 0x60
+    k[2, 2] = -3.5                       # -224 -> 0xF6
+    k[2, 3] = 2.0 ** -16                 # 2^-10 after scaling: tie with 0 -> +0
+    k[3, :] = -1.0                       # amax 1: every value maps to -448 (or just below)
+    k8, s = O.k_quant(k)
+    assert s[0] == np.float32(1.0)
+    assert k8[0, 5] == 0x7E and np.count_nonzero(k8[0]) == 1
+    assert s[1] == 0 and not k8[1].any()
+    assert s[2] == np.float32(2.0 ** -6)
+    assert list(k8[2, :4]) == [0x7E, 0x60, 0xF6, 0x00]
+    assert s[3] == np.float32(1.0) / np.float32(448.0)
+    assert np.all(k8[3] == 0xFE)
+
+
+def test_k_quant_matches_torch_cast():
+    # the division and the cast done by library routines for a random batch
+    rng = np.random.default_rng(3)
+    k = (rng.standard_normal((64, 128)) * rng.uniform(0.01, 100, (64, 1))).astype(np.float32)
+    k8, s = O.k_quant(k)
+    kt = torch.from_numpy(k)
+    st = kt.abs().amax(dim=1) / torch.tensor(448.0)
+    assert np.array_equal(st.numpy(), s)
+    ref = (kt / st[:, None]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ref, k8)
+
+
+def test_k_quant_bf16_inputs_and_underflow():
+    kb = W.make_k(5, 0, 16)
+    k = bf16_decode(kb)
+    k8, s = O.k_quant(k)
+    assert np.all(s > 0)
+    recon = e4m3_decode(k8) * s[:, None]
+    assert np.all(np.abs(recon - k) <= np.abs(k) * 2.0 ** -4 + s[:, None] * 2.0 ** -9 + 1e-30)
+    tiny = np.zeros((1, 128), dtype=np.float32)
+    tiny[0, 0] = np.float32(1e-45)       # smallest subnormal: amax/448 underflows to 0
+    k8, s = O.k_quant(tiny)
+    assert s[0] == 0 and not k8.any()
+
+
+def test_cache_layout_hand_worked():
+    bs, stride = 64, W.block_stride_bytes(64)
+    assert stride == 8704
+    cache = np.zeros((4, stride), dtype=np.uint8)
+    k = np.zeros((2, 128), dtype=np.float32)
+    k[0, 0] = 448.0
+    k[1, 127] = -448.0
+    O.k_quant_and_cache(k, [130, -1], cache, bs)       # slot 130 -> block 2, offset 2
+    assert cache[2, 256] == 0x7E                        # value row at offset 2*128
+    assert np.count_nonzero(cache) == 1 + 2             # value byte + scale 1.0 = 0x3F800000
+    assert list(cache[2, 8192 + 8:8192 + 12]) == [0x00, 0x00, 0x80, 0x3F]
+    k8, s = O.cache_token(cache, bs, 2, 2)
+    assert k8[0] == 0x7E and s == 1.0
+
+
+# ---------------------------------------------------------------- logits
+
+def _one_hot_q(rows, h, d, code):
+    q8 = np.zeros((rows, 64, 128), dtype=np.uint8)
+    q8[:, h, d] = code
+    return q8
+
+
+def test_logits_one_hot_closed_form():
+    rng = np.random.default_rng(0)
+    for _ in range(20):
+        h, d, d2 = rng.integers(0, 64), rng.integers(0, 128), rng.integers(0, 128)
+        a, b = int(rng.integers(1, 126)), int(rng.integers(1, 126))
+        q8 = _one_hot_q(1, h, d, a)
+        w = rng.standard_normal((1, 64))
+        k8 = np.zeros((3, 128), dtype=np.uint8)
+        k8[0, d] = b
+        k8[1, d2] = b                                     # other dim: contributes only if d2 == d
+        kscale = np.array([0.5, 2.0, 3.0], dtype=np.float32)
+        out = O.logits_row(q8[0], w[0], k8, kscale)
+        expect0 = w[0, h] * e4m3_decode(a) * e4m3_decode(b) * 0.5
+        expect1 = w[0, h] * e4m3_decode(a) * e4m3_decode(b) * 2.0 if d2 == d else 0.0
+        assert out[0] == pytest.approx(expect0, rel=1e-15, abs=0)
+        assert out[1] == pytest.approx(expect1, rel=1e-15, abs=1e-300)
+        assert out[2] == 0.0
+
+
+def test_logits_head_dot_is_exact():
+    # the per-head dot product is exact in fp64; compare with rational arithmetic
+    rng = np.random.default_rng(1)
+    q8 = rng.integers(0, 254, (64, 128)).astype(np.uint8)
+    q8[q8 == 0x7F] = 0x7E
+    k8 = rng.integers(0, 254, (2, 128)).astype(np.uint8)
+    k8[k8 == 0x7F] = 0x7E
+    w = np.zeros(64)
+    for h in (0, 17, 63):
+        w[:] = 0
+        w[h] = 1.0
+        got = O.logits_row(q8, w, k8, np.ones(2, dtype=np.float32))
+        for s in range(2):
+            exact = sum(Fraction(float(e4m3_decode(q8[h, d]))) * Fraction(float(e4m3_decode(k8[s, d])))
+                        for d in range(128))
+            assert Fraction(got[s]) == exact
+
+
+def test_logits_linear_in_weights_and_scale():
+    rng = np.random.default_rng(2)
+    q8, w = W.make_q(9, 2)
+    w = w.astype(np.float64)
+    k8, ks = W.make_random_cache_tokens(9, 50)
+    a = O.logits_row(q8[0], w[0], k8, ks)
+    b = O.logits_row(q8[0], w[1], k8, ks)
+    c = O.logits_row(q8[0], w[0] + w[1], k8, ks)
+    assert np.allclose(a + b, c, rtol=1e-12, atol=1e-18)
+    ks2 = ks.copy()
+    ks2[7] *= 2
+    d = O.logits_row(q8[0], w[0], k8, ks2)
+    assert d[7] == pytest.approx(2 * a[7], rel=1e-14)
+    assert np.array_equal(np.delete(d, 7), np.delete(a, 7))
+    # heads are interchangeable: permuting q heads together with the weights changes nothing
+    perm = rng.permutation(64)
+    e = O.logits_row(q8[0][perm], w[0][perm], k8, ks)
+    assert np.allclose(e, a, rtol=1e-12, atol=1e-18)
+
+
+def test_prefill_logits_masks_outside_row_limits():
+    q8, w = W.make_q(4, 3)
+    k8, ks = W.make_random_cache_tokens(4, 40)
+    out = O.mqa_logits(q8, w, k8, ks, [0, 5, 10], [40, 6, 10])
+    assert np.all(np.isfinite(out[0]))
+    assert np.isfinite(out[1, 5]) and np.sum(np.isfinite(out[1])) == 1
+    assert not np.isfinite(out[2]).any()
+    assert np.all(out[1, :5] == -np.inf)
+
+
+def test_paged_decode_equals_contiguous_scoring():
+    """Paging is transparent: scores read through a shuffled block table equal the gathered ones."""
+    wl = W.tiny_decode()
+    pool = wl.pool
+    cache = np.zeros((pool.num_blocks, W.block_stride_bytes()), dtype=np.uint8)
+    per_req = []
+    for b in range(wl.batch):
+        kb = bf16_decode(W.make_k(wl.seed, b, int(pool.ctx_lens[b])))
+        O.k_quant_and_cache(kb, pool.slot_mapping(b), cache, pool.block_size)
+        per_req.append(O.k_quant(kb))
+    paged = O.paged_decode_logits(wl.q8, wl.w, cache, pool.block_size, pool.block_table, pool.ctx_lens, 1)
+    for b in range(wl.batch):
+        L = int(pool.ctx_lens[b])
+        k8, ks = per_req[b]
+        ref = O.logits_row(wl.q8[b], wl.w[b], k8, ks)
+        assert np.array_equal(paged[b, :L], ref)
+        assert np.all(np.isnan(paged[b, L:]))
+    # next_n = 2: the first query of each request cannot see the second one's token
+    q8 = np.repeat(wl.q8, 2, axis=0)
+    w = np.repeat(wl.w, 2, axis=0)
+    p2 = O.paged_decode_logits(q8, w, cache, pool.block_size, pool.block_table, pool.ctx_lens, 2)
+    for b in range(wl.batch):
+        L = int(pool.ctx_lens[b])
+        assert p2[2 * b, L - 1] == -np.inf and np.isfinite(p2[2 * b, L - 2])
+        assert np.isfinite(p2[2 * b + 1, L - 1])
+
+
+def test_gather_roundtrip():
+    bs = 16
+    stride = W.block_stride_bytes(bs)
+    k = bf16_decode(W.make_k(3, 0, 100))
+    table = np.array([5, 0, 3, 7, 1, 2, 6])
+    cache = np.zeros((8, stride), dtype=np.uint8)
+    slots = table[np.arange(100) // bs] * bs + np.arange(100) % bs
+    O.k_quant_and_cache(k, slots, cache, bs)
+    k8, ks = O.gather_k(cache, bs, table, 100)
+    k8r, ksr = O.k_quant(k)
+    assert np.array_equal(k8, k8r) and np.array_equal(ks, ksr)
+
+
+# ---------------------------------------------------------------- top-k
+
+def _brute_force_topk_sets(vals, k):
+    """Every k-subset whose minimum is at least the maximum of the rest (all valid answers)."""
+    n = len(vals)
+    good = []
+    for comb in itertools.combinations(range(n), k):
+        rest = [vals[i] for i in range(n) if i not in comb]
+        if not rest or min(vals[i] for i in comb) >= max(rest):
+            good.append(set(comb))
+    return good
+
+
+def test_topk_brute_force_small():
+    rng = np.random.default_rng(5)
+    for trial in range(200):
+        n = int(rng.integers(1, 12))
+        k = int(rng.integers(1, 6))
+        vals = rng.integers(-3, 4, n).astype(np.float64)   # many ties
+        ks = int(rng.integers(0, 3))
+        row = np.concatenate([np.full(ks, 99.0), vals])    # columns before ks must be ignored
+        got = O.topk_row(row, ks, ks + n, k)
+        if n <= k:
+            assert list(got[:n]) == list(range(n)) and np.all(got[n:] == -1)
+            continue
+        sel = set(int(i) for i in got)
+        valid = _brute_force_topk_sets(list(vals), k)
+        assert sel in valid
+        # tie rule: the lexicographically smallest valid set (lower index wins)
+        assert sorted(sel) == min(sorted(s) for s in valid)
+
+
+def test_topk_values_match_torch_topk():
+    x = W.make_logits(8, 4, 5000)
+    got = O.topk(x, None, [5000, 4000, 2048, 100], 2048)
+    for r in range(4):
+        n = [5000, 4000, 2048, 100][r]
+        sel = got[r][got[r] >= 0]
+        assert len(sel) == min(n, 2048) and len(set(sel.tolist())) == len(sel)
+        ref = torch.topk(torch.from_numpy(x[r, :n]).double(), min(n, 2048)).values.numpy()
+        assert np.array_equal(np.sort(x[r, sel].astype(np.float64)), np.sort(ref))
+
+
+# ---------------------------------------------------------------- expansion
+
+def test_expand_golden():
+    with open(os.path.join(GOLDEN, "expand_candidates.json")) as f:
+        spec = json.load(f)
+    for c in spec["cases"]:
+        si, end = O.expand_candidates_row(c["cand"], c["ks"], c["ke"], c["cand_block_size"], c["sbk"])
+        assert list(si) == c["sparse_idx"], c["note"]
+        assert end == c["end"], c["note"]
+
+
+def test_expand_brute_force_invariants():
+    rng = np.random.default_rng(6)
+    for trial in range(400):
+        sbk = int(rng.choice([8, 16, 64]))
+        R = int(rng.choice([1, 2, 4]))
+        cbs = sbk * R
+        K = int(rng.choice([1, 2, 4, 8, 16]))
+        ks = sbk * int(rng.integers(0, 4))
+        ke = ks + int(rng.integers(0, 12 * cbs))
+        nblk = (ke - ks + cbs - 1) // cbs + 2
+        cand = rng.integers(-1, nblk + 1, K)
+        si, end = O.expand_candidates_row(cand, ks, ke, cbs, sbk)
+        # token-level brute force: relative position x is covered when its candidate block was published
+        pub = set(int(c) for c in cand if c >= 0)
+        covered = [x for x in range(ke - ks) if x // cbs in pub]
+        assert end == len(covered)
+        # the valid prefix lists the covered sparse blocks once each, ascending, anchored at ks // sbk
+        blocks = sorted(set((ks + x) // sbk for x in covered))
+        n = len(blocks)
+        assert list(si[:n]) == blocks
+        if n:
+            assert np.all(si[n:] == blocks[-1])
+        else:
+            assert np.all(si == ks // sbk)
+        # columns [0, end) address exactly the covered tokens
+        toks = [O.sparse_column_token(si, c, sbk) for c in range(end)]
+        assert toks == [ks + x for x in covered]
+
+
+# ---------------------------------------------------------------- remap and slots
+
+def test_slot_remap_golden():
+    with open(os.path.join(GOLDEN, "slot_remap.json")) as f:
+        spec = json.load(f)
+    bt = np.array([spec["block_table"]])
+    for c in spec["cases"]:
+        out = O.req_to_global_slots(np.array([[c["local"]]]), None, bt, spec["block_size"], c["block_span"])
+        assert out[0, 0] == c["slot"], c
+    for c in spec["span_cases"]:
+        if c["span"] is None:
+            with pytest.raises(ValueError):
+                O.packed_block_span(c["block_stride"], c["token_stride"])
+        else:
+            assert O.packed_block_span(c["block_stride"], c["token_stride"]) == c["span"]
+
+
+def test_slots_span_equal_block_size_is_the_plain_slot():
+    # with block_span == block_size the slot is the ordinary block*block_size + offset
+    pool = W.make_pool(3, [300, 70])
+    local = np.array([[0, 5, 299, -1], [69, 64, -1, -1]])
+    out = O.req_to_global_slots(local, None, pool.block_table, 64, 64)
+    for b in range(2):
+        sm = pool.slot_mapping(b)
+        for i in range(4):
+            v = local[b, i]
+            assert out[b, i] == (-1 if v < 0 else sm[v])
+
+
+# ---------------------------------------------------------------- sparse path
+
+def _tiny_hier():
+    ctx = np.array([1000, 777, 2048], dtype=np.int32)
+    pool = W.make_pool(21, ctx)
+    cache = np.zeros((pool.num_blocks, W.block_stride_bytes()), dtype=np.uint8)
+    for b in range(3):
+        O.k_quant_and_cache(bf16_decode(W.make_k(21, b, int(ctx[b]))), pool.slot_mapping(b), cache, 64)
+    q8, w = W.make_q(21, 3)
+    cand = W.make_candidates(21, 3, 8, 16, n_dup=2, n_pad=1, n_oob=1)
+    return pool, cache, q8, w, cand
+
+
+def test_sparse_logits_equal_dense_at_mapped_positions():
+    pool, cache, q8, w, cand = _tiny_hier()
+    for sbk, cbs in ((64, 64), (16, 64), (8, 16)):
+        si, end = O.expand_candidates(cand, None, pool.ctx_lens, cbs, sbk)
+        sp = O.sparse_logits_decode(q8, w, cache, 64, pool.block_table, None, si, end, sbk)
+        dense = O.paged_decode_logits(q8, w, cache, 64, pool.block_table, pool.ctx_lens, 1)
+        for r in range(3):
+            for c in range(sp.shape[1]):
+                if c < end[r]:
+                    assert sp[r, c] == dense[r, O.sparse_column_token(si[r], c, sbk)]
+                else:
+                    assert sp[r, c] == -np.inf
+
+
+def test_sparse_topk_equals_dense_masked_topk():
+    pool, cache, q8, w, cand = _tiny_hier()
+    for k in (64, 300, 2048):
+        si, end = O.expand_candidates(cand, None, pool.ctx_lens, 64, 64)
+        sp = O.sparse_logits_decode(q8, w, cache, 64, pool.block_table, None, si, end, 64)
+        for r in range(3):
+            cols, pos = O.sparse_topk_remap_row(sp[r], int(end[r]), si[r], 0, 64, k)
+            ref = O.dense_masked_topk_row(sp[r], int(end[r]), si[r], 0, int(pool.ctx_lens[r]), 64, k)
+            m = min(k, int(end[r]))
+            assert np.all(pos[m:] == -1) and np.all(ref[m:] == -1)
+            assert set(pos[:m].tolist()) == set(ref[:m].tolist())
+            for c, p in zip(cols[:m], pos[:m]):
+                assert O.sparse_column_token(si[r], int(c), 64) == p
