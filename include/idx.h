@@ -1,0 +1,327 @@
+/*
+ * idx.h - C ABI of libidx, the GB300 (sm_103a) FP8 lightning indexer.
+ *
+ * The lightning indexer of DeepSeek Sparse Attention scores every query row t
+ * against every visible history token s,
+ *
+ *     logits[t, s] = sum_{h < 64} w[t, h] * (q[t, h] . k[s])
+ *
+ * keeps the 2048 best tokens per row and hands their positions to the main
+ * attention ("DeepSeek V3.2 稀疏注意力 DSA 推理流程图解", section "Indexer 内部六步",
+ * step 6). q is 64 heads x 128 dims of FP8 e4m3; every q-side coefficient is
+ * folded into w (step 4), so the kernels multiply by no other factor. k is one
+ * shared 128-dim e4m3 vector per token with one fp32 scale, stored as 132 bytes
+ * per token in a paged cache (the page's cost table and data-flow item 1).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every pointer argument is a DEVICE pointer unless stated otherwise. The
+ *   caller owns every buffer; the library allocates nothing (the V4.1 review,
+ *   "评论区精华": the forward pass allocates nothing, scratch is passed in).
+ * - e4m3 bytes are passed as uint8_t, bf16 as uint16_t bit patterns.
+ * - 2-D arguments carry an explicit row stride ("ld_*", in ELEMENTS of the
+ *   argument's own type unless the name says bytes), so column slices of larger
+ *   buffers work (the V4.1 review asks the kernels to take strides).
+ * - Each call validates its host-side scalars and returns an idx_status_t. It
+ *   never reads device memory to validate, never synchronises the stream and has
+ *   no fallback path: an unsupported configuration is an error, not a slower
+ *   route (the V4.1 review: fail closed, no PyTorch fallback).
+ * - Work is enqueued on `stream` (0 = legacy default stream of the current
+ *   device). Errors from the launch itself are reported as IDX_ERR_CUDA.
+ * - Device-side problems (a bounded wait that ran out) are recorded in a device
+ *   flag; idx_device_error() synchronises and reports it.
+ * - idx_last_error() returns a thread-local human-readable message for the most
+ *   recent non-OK status.
+ *
+ * Paged cache layout (the "split block" layout)
+ * ---------------------------------------------
+ * Block b starts at byte b * block_stride_bytes of the cache. Token i of a block
+ * keeps its 128 e4m3 bytes at offset i * 128 and its fp32 scale at offset
+ * block_size * 128 + 4 * i. block_stride_bytes must be a multiple of 16 and at
+ * least block_size * 132; rounding it up to a multiple of 512 (8704 bytes for 64
+ * tokens) matches the block-stride alignment rule of the V4.1 review
+ * ("实现拆解" item 4). The physical slot of a token is
+ * block * block_size + offset.
+ */
+#ifndef IDX_H_
+#define IDX_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum idx_status {
+  IDX_OK = 0,
+  IDX_ERR_INVALID_ARG = 1,   /* a pointer is NULL, a size is negative, a stride too small */
+  IDX_ERR_UNSUPPORTED = 2,   /* well-formed but outside what the kernels implement */
+  IDX_ERR_CUDA = 3,          /* a CUDA runtime or driver call failed */
+  IDX_ERR_DEVICE = 4         /* a kernel reported a device-side failure (idx_device_error) */
+} idx_status_t;
+
+enum { IDX_F32 = 0, IDX_BF16 = 1 };          /* element types of weights, k and logits */
+enum { IDX_SCALE_FP32 = 0 };                 /* k scale format: fp32 amax / 448 */
+
+/* operation codes of idx_workspace_bytes */
+enum {
+  IDX_OP_K_QUANT_AND_CACHE = 1,
+  IDX_OP_GATHER_K = 2,
+  IDX_OP_MQA_LOGITS_PREFILL = 3,
+  IDX_OP_PAGED_MQA_LOGITS_DECODE = 4,
+  IDX_OP_TOPK = 5,
+  IDX_OP_EXPAND_CANDIDATES = 6,
+  IDX_OP_SPARSE_TOPK_REMAP = 7,
+  IDX_OP_REQ_TO_GLOBAL_SLOTS = 8
+};
+
+#define IDX_HEADS 64
+#define IDX_HEAD_DIM 128
+#define IDX_TOKEN_BYTES 132
+
+/*
+ * idx_k_quant_and_cache - quantise k to e4m3 and insert it into the paged cache.
+ *
+ * "DeepSeek V3.2 稀疏注意力 DSA 推理流程图解", "Indexer 内部六步" step 5: k
+ * quantisation is fused with the cache insert. Per token, in IEEE binary32:
+ * amax = max_d |k_d|; scale = amax / 448; byte_d = e4m3_rn_satfinite(k_d / scale).
+ * A zero scale (all-zero k, or amax / 448 underflowing) stores scale 0 and zero
+ * bytes. One scale per 128 values (step 4 fixes the 128-element scale block).
+ *
+ *   k             [n_tok, 128] of k_dtype (IDX_BF16 or IDX_F32), row stride ld_k
+ *                 elements (ld_k >= 128).
+ *   slot_mapping  int64 [n_tok]: physical slot of each token; a negative slot, or
+ *                 one >= num_blocks * block_size, skips the token.
+ *   cache         uint8 [num_blocks, block_stride_bytes], written in place.
+ *   block_size    tokens per block, one of 16, 32, 64, 128.
+ *   scale_fmt     IDX_SCALE_FP32.
+ * Errors: IDX_ERR_INVALID_ARG for NULL pointers with n_tok > 0, n_tok < 0,
+ * ld_k < 128, block_stride_bytes < block_size * 132; IDX_ERR_UNSUPPORTED for
+ * another block_size, block_stride_bytes % 16 != 0, another dtype or scale_fmt.
+ */
+idx_status_t idx_k_quant_and_cache(const void* k, int k_dtype, int64_t ld_k, int32_t n_tok,
+                                   const int64_t* slot_mapping, uint8_t* cache,
+                                   int32_t num_blocks, int32_t block_size,
+                                   int64_t block_stride_bytes, int scale_fmt,
+                                   cudaStream_t stream);
+
+/*
+ * idx_gather_k - copy the first n_tok tokens of one request out of the cache.
+ *
+ * Prefill scores gathered k ("Indexer 内部六步", the prefill/decode kernel table;
+ * the V4.1 review's _gather_prefill_chunk_k). Token p comes from block
+ * block_table[p / block_size], offset p % block_size.
+ *
+ *   block_table   int32 [ceil(n_tok / block_size)] physical block ids.
+ *   k8_out        uint8 [n_tok, 128] contiguous.
+ *   kscale_out    float [n_tok].
+ * Errors: IDX_ERR_INVALID_ARG / IDX_ERR_UNSUPPORTED as for the insert.
+ */
+idx_status_t idx_gather_k(const uint8_t* cache, int32_t block_size, int64_t block_stride_bytes,
+                          const int32_t* block_table, int32_t n_tok,
+                          uint8_t* k8_out, float* kscale_out, cudaStream_t stream);
+
+/*
+ * idx_mqa_logits_prefill - logits of T query rows against gathered k.
+ *
+ * Dense mode (sparse_idx == NULL): row t scores tokens s in [row_ks[t], row_ke[t])
+ * of k8/kscale (causality is carried by the limits: a query at position p has
+ * row_ke = p + 1). logits[t, s] for s in [0, S) is written: the logit inside the
+ * row's range, -inf outside it.
+ *
+ * Sparse mode (V4.1 hierarchical variant, the V4.1 review "功能与动机" and
+ * "实现拆解" item 3): sparse_idx[t, i] (i < n_si) are absolute sparse-block ids
+ * in units of sbk tokens (as idx_expand_candidates produces them); column c of
+ * row t scores token sparse_idx[t, c / sbk] * sbk + c % sbk when c < end[t], and
+ * holds -inf otherwise. Columns [0, n_si * sbk) are written.
+ *
+ *   q        uint8 e4m3 [T, 64, 128]; ld_q = row stride in BYTES (multiple of 16,
+ *            >= 8192); heads are contiguous 128-byte rows.
+ *   w        [T, 64] of w_dtype (IDX_F32 or IDX_BF16), row stride ld_w elements.
+ *   k8       uint8 [S, 128] contiguous; kscale float [S]; both 16-byte aligned.
+ *   row_ks   int32 [T] or NULL (all zero); row_ke int32 [T] (dense mode).
+ *   sbk      8, 16, 32, 64 or 128 (sparse mode).
+ *   logits   [T, ld_out] of out_dtype (IDX_F32 or IDX_BF16).
+ *   ws       workspace (idx_workspace_bytes(IDX_OP_MQA_LOGITS_PREFILL, ...) bytes;
+ *            currently 0, may be NULL).
+ * Errors: IDX_ERR_INVALID_ARG for NULL / negative / too-small strides;
+ * IDX_ERR_UNSUPPORTED for misaligned q, k8 or kscale, or an sbk outside the set.
+ */
+idx_status_t idx_mqa_logits_prefill(const uint8_t* q, int64_t ld_q, const void* w, int w_dtype,
+                                    int64_t ld_w, const uint8_t* k8, const float* kscale,
+                                    int32_t S, const int32_t* row_ks, const int32_t* row_ke,
+                                    int32_t T, const int32_t* sparse_idx, int64_t ld_si,
+                                    int32_t n_si, const int32_t* end, int32_t sbk,
+                                    void* logits, int out_dtype, int64_t ld_out,
+                                    void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * idx_paged_mqa_logits_decode - decode logits read straight from the paged cache.
+ *
+ * "Indexer 内部六步", the prefill/decode table: decode does not gather k, it reads
+ * the paged cache through the block table. Request b has next_n query rows
+ * r = b * next_n + j (j < next_n); its context holds ctx_lens[b] tokens, the
+ * last next_n of which are the queries themselves, so row r sees tokens
+ * [0, ctx_lens[b] - next_n + j + 1).
+ *
+ * Dense mode (sparse_idx == NULL): logits[r, s] is written for s < ctx_lens[b]:
+ * the logit where visible, -inf for the causally hidden tail; columns
+ * >= ctx_lens[b] are left untouched.
+ *
+ * Sparse mode: as in idx_mqa_logits_prefill with k positions relative to the
+ * request (row_ks = 0): column c of row r scores token
+ * sparse_idx[r, c / sbk] * sbk + c % sbk of request r / next_n when c < end[r];
+ * sbk must divide block_size.
+ *
+ *   q, w               as for prefill, rows = B * next_n.
+ *   cache              uint8 [num_blocks, block_stride_bytes] (16-byte aligned).
+ *   block_table        int32 [B, ld_bt]: physical block of each logical block.
+ *   ctx_lens           int32 [B].
+ *   next_n             1, 2 or 4 in dense mode; any value >= 1 in sparse mode.
+ *   logits             [B * next_n, ld_out] of out_dtype; dense mode needs
+ *                      ld_out >= max(ctx_lens) (not checked: ctx_lens is device data).
+ *   block_table rows must cover ceil(ctx_lens[b] / block_size) blocks, and every
+ *   sparse_idx entry below end must address a token inside the request.
+ * Errors: as for prefill; IDX_ERR_UNSUPPORTED for another block_size or next_n.
+ */
+idx_status_t idx_paged_mqa_logits_decode(const uint8_t* q, int64_t ld_q, const void* w,
+                                         int w_dtype, int64_t ld_w, const uint8_t* cache,
+                                         int32_t num_blocks, int32_t block_size,
+                                         int64_t block_stride_bytes, const int32_t* block_table,
+                                         int64_t ld_bt, const int32_t* ctx_lens, int32_t B,
+                                         int32_t next_n, const int32_t* sparse_idx,
+                                         int64_t ld_si, int32_t n_si, const int32_t* end,
+                                         int32_t sbk, void* logits, int out_dtype,
+                                         int64_t ld_out, void* ws, size_t ws_bytes,
+                                         cudaStream_t stream);
+
+/*
+ * idx_topk - per-row top-k with -1 fill.
+ *
+ * "DeepSeek V3.2 稀疏注意力 DSA 推理流程图解", opening section and data-flow
+ * item 2: keep the k (2048) highest-scoring tokens; the index table is int32
+ * and -1 marks an empty entry. Row r considers columns [row_ks[r], row_ke[r])
+ * of `logits` and writes request-local indices s - row_ks[r]. When at most k
+ * columns are visible all are written in column order, then -1. Otherwise the k
+ * indices of the largest values are written in unspecified order; among values
+ * exactly equal at the threshold an unspecified subset is kept. NaN sorts above
+ * +inf.
+ *
+ *   logits   [rows, ld] of dtype (IDX_F32 or IDX_BF16).
+ *   row_ks   int32 [rows] or NULL (all zero); row_ke int32 [rows].
+ *   out      int32 [rows, ld_out], ld_out >= k.
+ *   ws       idx_workspace_bytes(IDX_OP_TOPK, rows, max_cols, k) bytes (0 now).
+ * Errors: IDX_ERR_INVALID_ARG for NULL pointers, k < 1, ld_out < k;
+ * IDX_ERR_UNSUPPORTED for k > 4096.
+ */
+idx_status_t idx_topk(const void* logits, int dtype, int64_t ld, const int32_t* row_ks,
+                      const int32_t* row_ke, int32_t rows, int32_t k, int32_t* out,
+                      int64_t ld_out, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * idx_expand_candidates - flatten, filter, sort, dedupe and tail-pad candidate blocks.
+ *
+ * The V4.1 review, "实现拆解" item 3 and the candidate-expansion snippet. Per
+ * row, with R = cand_block_size / sbk and max_block = ceil((ke - ks) / sbk):
+ * every candidate c >= 0 expands to the sparse blocks c * R + j (j < R); those in
+ * [0, max_block) are kept, sorted ascending and deduplicated (n unique); entry
+ * i < n is x_i + ks / sbk, entries i >= n repeat the last valid id (or hold
+ * ks / sbk when n == 0); end = (n - 1) * sbk + min(max(ke - (x_last * sbk + ks), 1), sbk)
+ * valid columns, or 0. Deduplication is this library's reading: the page sorts
+ * without deduplicating and notes that duplicates only waste work in
+ * production, but a duplicated block would enter the top-k twice.
+ *
+ *   cand          int32 [rows, ld_c] candidate block ids (n_cand used, a power of two).
+ *   row_ks        int32 [rows] or NULL; every ks must be a multiple of sbk
+ *                 (a row that violates this gets end = 0 and is recorded in the
+ *                 device error flag).
+ *   row_ke        int32 [rows].
+ *   sparse_idx    int32 [rows, ld_si], n_cand * R entries written.
+ *   end           int32 [rows].
+ * Errors: IDX_ERR_UNSUPPORTED unless n_cand is a power of two with
+ * n_cand * R <= 1024, sbk divides cand_block_size and R is a power of two.
+ */
+idx_status_t idx_expand_candidates(const int32_t* cand, int64_t ld_c, int32_t rows,
+                                   int32_t n_cand, const int32_t* row_ks, const int32_t* row_ke,
+                                   int32_t cand_block_size, int32_t sbk, int32_t* sparse_idx,
+                                   int64_t ld_si, int32_t* end, cudaStream_t stream);
+
+/*
+ * idx_sparse_topk_remap - top-k over sparse columns, then map columns to positions.
+ *
+ * The V4.1 review, "实现拆解" item 3 (top-k on the sparse logits, then the remap
+ * kernel maps each sparse column back to its request-local position) and the
+ * rows-metadata snippet (col_indices holds the column top-k). Row r selects
+ * among columns [0, end[r]) exactly as idx_topk does, writes the chosen columns
+ * to col_scratch (if not NULL) and the positions
+ * (sparse_idx[r, c / sbk] - row_ks[r] / sbk) * sbk + c % sbk to `positions`;
+ * empty entries are -1 in both.
+ *
+ *   sparse_logits  [rows, ld] of dtype (IDX_BF16 as the V4.1 path uses, or IDX_F32).
+ *   row_ks         int32 [rows] or NULL.
+ * Errors: as for idx_topk.
+ */
+idx_status_t idx_sparse_topk_remap(const void* sparse_logits, int dtype, int64_t ld,
+                                   const int32_t* end, const int32_t* sparse_idx, int64_t ld_si,
+                                   const int32_t* row_ks, int32_t sbk, int32_t rows, int32_t k,
+                                   int32_t* col_scratch, int64_t ld_col, int32_t* positions,
+                                   int64_t ld_pos, void* ws, size_t ws_bytes,
+                                   cudaStream_t stream);
+
+/*
+ * idx_req_to_global_slots - request-local positions to physical cache slots.
+ *
+ * "DeepSeek V3.2 ...", section "几个容易踩的点": the indexer emits positions
+ * inside the request, the attention kernel needs paged-cache slots. The DSV4
+ * packed-KV fix ("修复 DSV4 FlashInfer 稀疏 MLA 在打包 KV 布局下的地址错误",
+ * 实现拆解 and the remap snippet) generalises the slot to
+ * block * block_span + offset for pools whose blocks hold block_span >= block_size
+ * token strides. Entry v >= 0 of row r becomes
+ * block_table[req(r), v / block_size] * block_span + v % block_size; negative
+ * entries, and entries whose block index v / block_size >= ld_bt, become -1.
+ *
+ *   local        int32 [rows, ld_l], k entries per row.
+ *   row_to_req   int32 [rows] or NULL (row r belongs to request r).
+ *   block_table  int32 [*, ld_bt].
+ *   slots        int32 [rows, ld_s]. May alias `local` when ld_s == ld_l.
+ * Errors: IDX_ERR_UNSUPPORTED when block_span < block_size.
+ */
+idx_status_t idx_req_to_global_slots(const int32_t* local, int64_t ld_l, int32_t rows, int32_t k,
+                                     const int32_t* row_to_req, const int32_t* block_table,
+                                     int64_t ld_bt, int32_t block_size, int32_t block_span,
+                                     int32_t* slots, int64_t ld_s, cudaStream_t stream);
+
+/*
+ * idx_block_span - tokens per physical block of a pool (host only).
+ *
+ * The DSV4 packed-KV fix, 实现拆解 item 1: block_span = block_stride /
+ * token_stride, rejected when it does not divide exactly.
+ * Returns IDX_ERR_UNSUPPORTED (span untouched) when it does not divide,
+ * IDX_ERR_INVALID_ARG for non-positive strides or a NULL span.
+ */
+idx_status_t idx_block_span(int64_t block_stride, int64_t token_stride, int32_t* span);
+
+/* Workspace bytes an operation needs for the given sizes (host only). */
+size_t idx_workspace_bytes(int op, int32_t rows, int32_t max_cols, int32_t k);
+
+/* Static description of a status code (host only). */
+const char* idx_status_string(idx_status_t status);
+
+/* Thread-local message of the most recent non-OK status on this thread (host only). */
+const char* idx_last_error(void);
+
+/*
+ * idx_device_error - synchronise `stream`, then read and clear the device-side
+ * error flag of the current device. Returns IDX_OK when no kernel recorded a
+ * failure, IDX_ERR_DEVICE (message in idx_last_error) when one did, and
+ * IDX_ERR_CUDA when the synchronisation itself failed.
+ */
+idx_status_t idx_device_error(cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* IDX_H_ */

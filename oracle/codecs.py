@@ -46,11 +46,6 @@ def _e4m3_value(code: int) -> float:
 #: value of every byte 0..255 as fp64 (NaN for 0x7F and 0xFF)
 E4M3_TABLE = np.array([_e4m3_value(c) for c in range(256)], dtype=np.float64)
 
-# Codes 0x00..0x7E are the non-negative finite values in strictly increasing order
-# (the byte order of a sign-magnitude float with a monotone exponent field).
-_E4M3_POS = E4M3_TABLE[:127].copy()
-
-
 def e4m3_decode(codes) -> np.ndarray:
     """e4m3 bytes (any integer array) -> fp64 values."""
     return E4M3_TABLE[np.asarray(codes, dtype=np.int64) & 0xFF]
@@ -59,22 +54,29 @@ def e4m3_decode(codes) -> np.ndarray:
 def e4m3_encode(x) -> np.ndarray:
     """Values (fp32 or fp64) -> e4m3 bytes, RNE with saturation to +-448.
 
-    The nearest representable magnitude is found by bracketing ``|x|`` between
-    two consecutive codes; an exact midpoint goes to the even code (its mantissa
-    LSB is the byte's LSB). The sign bit is copied, so -0 and tiny negatives
-    encode as 0x80.
+    Straight from the field layout: a magnitude below 2^-6 is subnormal and its
+    code is its multiple of 2^-9 rounded half-to-even; otherwise, writing
+    ``|x| = 2^e * (1 + f)`` with ``f`` in [0, 1), the 3-bit mantissa is ``8 f``
+    rounded half-to-even (a carry to 8 bumps the exponent) and the code is
+    ``(e + 7) << 3 | mantissa``. Magnitudes of 448 and above saturate to 448
+    (code 0x7E). The sign bit is copied, so -0 and tiny negatives encode as
+    0x80; NaN encodes as 0x7F. ``np.rint`` rounds half to even, and every
+    scaling here is by a power of two, so no step rounds twice.
     """
     x = np.asarray(x, dtype=np.float64)
     mag = np.abs(x)
-    finite_mag = np.where(np.isnan(mag), 0.0, mag)
-    lo = np.searchsorted(_E4M3_POS, finite_mag, side="right") - 1
-    lo = np.clip(lo, 0, 126)
-    hi = np.minimum(lo + 1, 126)
-    d_lo = finite_mag - _E4M3_POS[lo]
-    d_hi = _E4M3_POS[hi] - finite_mag
-    take_hi = (d_hi < d_lo) | ((d_hi == d_lo) & ((lo & 1) == 1))
-    code = np.where(take_hi, hi, lo)
-    code = np.where(finite_mag >= E4M3_MAX, 126, code)
+    finite_mag = np.where(np.isnan(mag) | (mag >= E4M3_MAX), 0.0, mag)
+    sub = finite_mag < 2.0 ** -6
+    code_sub = np.rint(finite_mag * 2.0 ** 9)                 # 0..8; 8 is the smallest normal
+    frac, exp2 = np.frexp(finite_mag)                          # finite_mag = frac * 2^exp2, frac in [0.5, 1)
+    e = exp2 - 1
+    man = np.rint((2.0 * frac - 1.0) * 8.0)
+    carry = man == 8.0
+    e = np.where(carry, e + 1, e)
+    man = np.where(carry, 0.0, man)
+    code_norm = ((e + 7) << 3) + man.astype(np.int64)
+    code = np.where(sub, code_sub.astype(np.int64), code_norm)
+    code = np.where(mag >= E4M3_MAX, 126, np.minimum(code, 126))
     code = code | (np.signbit(x).astype(np.int64) << 7)
     code = np.where(np.isnan(x), 0x7F, code)
     return code.astype(np.uint8)

@@ -1,0 +1,890 @@
+// a3 / a4 / a8: FP8 MQA logits on the 5th-generation tensor core.
+//
+//   logits[t, s] = kscale[s] * sum_{h < 64} w[t, h] * sum_{d < 128} q8[t, h, d] * k8[s, d]
+//
+// ("DeepSeek V3.2 稀疏注意力 DSA 推理流程图解", "Indexer 内部六步" step 6: the 64
+// head dot products collapsed into one score by the per-head weights; step 4:
+// all q-side coefficients live in the weights. k is the dequantised cache
+// entry, its fp32 scale applied per column.)
+//
+// One kernel serves the four ways the path reads k:
+//   decode dense   - the paged cache through the block table, no gather (the
+//                    page's prefill/decode kernel table);
+//   decode sparse  - only the candidate sparse blocks of each row (the V4.1
+//                    review, "功能与动机" and "实现拆解" item 3);
+//   prefill dense  - gathered contiguous k with ragged causal row limits;
+//   prefill sparse - gathered k restricted to each row's sparse blocks.
+//
+// Orientation. A tile is 128 consecutive output columns (tokens). The MMA is
+// D[128 x N] += A[128 x 32] * B[N x 32]^T, four times over K = 128, with
+// A = the tile's 128 k rows (e4m3, K-major, 128-byte swizzle) and B = the
+// group's q (N = 64 heads x NQ query rows, K-major), so the fp32 accumulator
+// in tensor memory holds one TOKEN per lane and one (query, head) per column.
+// Each epilogue thread therefore owns one token and reduces its 64 head
+// columns against the weights in registers: the weighted head sum needs no
+// cross-thread traffic and the [rows x 64 heads x tokens] intermediate never
+// leaves the SM.
+//
+// Roles (192 threads, one CTA per SM, persistent):
+//   warp 0     TMA producer: k boxes (one per cache block / sparse block) and
+//              their scales into a ring of shared-memory stages, q per group;
+//              block-table lookups for the next tile are issued before the
+//              wait for a free stage so their latency hides behind it.
+//   warp 1     allocates tensor memory; one lane issues tcgen05.mma and
+//              commits stage / accumulator barriers.
+//   warps 2-5  epilogue: tcgen05.ld of the accumulator, weighted head sum,
+//              scale, causal / range mask, coalesced store (fp32 or bf16).
+// The flattened (group, tile) sequence is split evenly over the CTAs; every
+// role walks the same sequence. Every wait is bounded; on expiry the CTA
+// records a device error code and leaves in order.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+
+namespace idx {
+
+namespace {
+
+constexpr int kTile = 128;
+constexpr int kEpiWarps = 4;
+constexpr int kThreads = 64 + kEpiWarps * 32;
+constexpr int kKvStageBytes = kTile * kDim;       // 16 KB
+constexpr int kScaleStageBytes = 2048;            // up to 16 boxes, each in a 128-byte slot
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+
+enum Mode : int { kDecodeDense = 0, kDecodeSparse = 1, kPrefillDense = 2, kPrefillSparse = 3 };
+
+// bits of g_logits_error: low byte = the role whose wait expired
+__device__ unsigned int g_logits_error = 0;
+
+struct LogitsParams {
+  int mode;
+  int n_groups;
+  int tiles_per_group;  // modes with a fixed column count; unused for decode dense
+  int n_rows;           // q / w / output rows
+  int next_n;
+  int nq;               // rows per group in the dense modes
+  const void* w;
+  int w_bf16;
+  int64_t ld_w;
+  int paged;
+  int unit;             // tokens per k box (cache block, sparse block or 128)
+  int scale_slot;       // bytes between the scale boxes of one stage (>= 128)
+  int block_size;
+  const int32_t* block_table;
+  int64_t ld_bt;
+  const int32_t* ctx_lens;
+  int S;
+  const int32_t* row_ks;
+  const int32_t* row_ke;
+  const int32_t* sparse_idx;
+  int64_t ld_si;
+  int n_si;
+  const int32_t* end;
+  int sbk;
+  void* out;
+  int out_bf16;
+  int64_t ld_out;
+};
+
+template <int NQ>
+struct Cfg {
+  static constexpr int N = 64 * NQ;
+  static constexpr int kStages = NQ == 1 ? 11 : (NQ == 2 ? 10 : 8);
+  static constexpr int kAccStages = NQ == 4 ? 2 : 4;
+  static constexpr int kTmemCols = kAccStages * N;  // 256 or 512
+  static constexpr int kQStageBytes = NQ * 64 * kDim;
+  static constexpr int kOffKv = 0;
+  static constexpr int kOffQ = kOffKv + kStages * kKvStageBytes;
+  static constexpr int kOffScale = kOffQ + 2 * kQStageBytes;
+  static constexpr int kOffW = kOffScale + kStages * kScaleStageBytes;
+  static constexpr int kOffBar = kOffW + kEpiWarps * NQ * 64 * 4;
+  static constexpr int kNumBars = 2 * kStages + 2 * kAccStages + 4;
+  static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 1024;  // + alignment slack
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+struct Group {
+  int row0;    // first q row of the group
+  int nq;      // rows in the group
+  int req;     // request whose block table is used (paged modes)
+  int ncols;   // columns written per row: [0, ncols)
+  int tiles;   // 128-column tiles
+  int act_lo;  // union of the rows' visible columns: [act_lo, act_hi)
+  int act_hi;
+};
+
+__device__ __forceinline__ Group load_group(const LogitsParams& p, int g) {
+  Group G;
+  switch (p.mode) {
+    case kDecodeDense: {
+      const int L = max(__ldg(p.ctx_lens + g), 0);
+      G.row0 = g * p.next_n;
+      G.nq = p.next_n;
+      G.req = g;
+      G.ncols = L;
+      G.tiles = (L + kTile - 1) / kTile;
+      G.act_lo = 0;
+      G.act_hi = L;
+      break;
+    }
+    case kPrefillDense: {
+      G.row0 = g * p.nq;
+      G.nq = min(p.nq, p.n_rows - G.row0);
+      G.req = 0;
+      G.ncols = p.S;
+      G.tiles = p.tiles_per_group;
+      int lo = INT32_MAX, hi = 0;
+      for (int j = 0; j < G.nq; ++j) {
+        const int ks = p.row_ks ? max(__ldg(p.row_ks + G.row0 + j), 0) : 0;
+        const int ke = min(__ldg(p.row_ke + G.row0 + j), p.S);
+        if (ke > ks) {
+          lo = min(lo, ks);
+          hi = max(hi, ke);
+        }
+      }
+      G.act_lo = hi > 0 ? lo : 0;
+      G.act_hi = hi;
+      break;
+    }
+    default: {  // sparse modes: one row per group
+      G.row0 = g;
+      G.nq = 1;
+      G.req = p.mode == kDecodeSparse ? g / p.next_n : 0;
+      G.ncols = p.n_si * p.sbk;
+      G.tiles = p.tiles_per_group;
+      G.act_lo = 0;
+      G.act_hi = min(max(__ldg(p.end + g), 0), G.ncols);
+      break;
+    }
+  }
+  return G;
+}
+
+__device__ __forceinline__ bool tile_active(const Group& G, int t) {
+  return t * kTile < G.act_hi && t * kTile + kTile > G.act_lo;
+}
+
+// Walks this CTA's share of the flattened (group, tile) sequence.
+struct Walker {
+  int g, t;
+  long long left;
+  Group G;
+  __device__ __forceinline__ void init(const LogitsParams& p, int g0, int t0, long long n) {
+    g = g0;
+    t = t0;
+    left = n;
+    if (left > 0) G = load_group(p, g);
+  }
+  __device__ __forceinline__ void advance(const LogitsParams& p) {
+    if (--left <= 0) return;
+    if (++t >= G.tiles) {
+      do {
+        ++g;
+        G = load_group(p, g);
+      } while (G.tiles == 0);
+      t = 0;
+    }
+  }
+};
+
+// Bounded wait. All threads that call it for the same barrier get the same
+// answer only if they also agree on abort; callers make the result warp-uniform.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                         unsigned int role) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > kTimeoutNs) {
+      *abort_flag = 1;
+      atomicOr(&g_logits_error, role);
+      return false;
+    }
+  }
+}
+
+// Block-wide inclusive scan of one int per thread (blockDim.x = kThreads).
+__device__ __forceinline__ long long block_scan(long long v, long long* warp_tot, long long* total) {
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  long long incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  long long before = 0, all = 0;
+  for (int w = 0; w < kThreads / 32; ++w) {
+    if (w < warp) before += warp_tot[w];
+    all += warp_tot[w];
+  }
+  *total = all;
+  __syncthreads();
+  return before + incl;
+}
+
+// Coordinates of one k box: cache block (0 when contiguous) and row inside it.
+struct Box {
+  int blk;
+  int row;
+  bool valid;
+};
+
+__device__ __forceinline__ Box box_coords(const LogitsParams& p, const Group& G, int t, int u) {
+  Box b;
+  const int c0 = t * kTile + u * p.unit;
+  b.valid = c0 < G.act_hi && c0 + p.unit > G.act_lo;
+  b.blk = 0;
+  b.row = 0;
+  if (!b.valid) return b;
+  int tok = c0;
+  if (p.mode == kDecodeSparse || p.mode == kPrefillSparse) {
+    tok = __ldg(p.sparse_idx + static_cast<int64_t>(G.row0) * p.ld_si + c0 / p.sbk) * p.sbk;
+  }
+  if (p.paged) {
+    b.blk = __ldg(p.block_table + static_cast<int64_t>(G.req) * p.ld_bt + tok / p.block_size);
+    b.row = tok % p.block_size;
+  } else {
+    b.row = tok;
+  }
+  return b;
+}
+
+template <int NQ>
+__global__ void __launch_bounds__(kThreads, 1)
+mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_kv,
+                  const __grid_constant__ CUtensorMap map_scale, const LogitsParams p) {
+  using C = Cfg<NQ>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint8_t* kv_s = smem + C::kOffKv;
+  uint8_t* q_s = smem + C::kOffQ;
+  uint8_t* sc_s = smem + C::kOffScale;
+  float* w_s = reinterpret_cast<float*>(smem + C::kOffW);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + C::kStages;
+  uint64_t* acc_full = bars + 2 * C::kStages;
+  uint64_t* acc_empty = acc_full + C::kAccStages;
+  uint64_t* q_full = acc_empty + C::kAccStages;
+  uint64_t* q_empty = q_full + 2;
+
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  __shared__ int s_g0, s_t0;
+  __shared__ long long s_count;
+  __shared__ long long s_warp_tot[kThreads / 32];
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1 + kEpiWarps);
+    }
+    for (int a = 0; a < C::kAccStages; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], kEpiWarps);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
+    }
+    fence_mbar_init();
+    s_abort = 0;
+    tma_prefetch_map(&map_q);
+    tma_prefetch_map(&map_kv);
+    tma_prefetch_map(&map_scale);
+  }
+  if (warp == 1) {
+    tmem_alloc(&s_tmem, C::kTmemCols);
+    tmem_relinquish();
+  }
+
+  // ---- this CTA's share of the (group, tile) sequence ----
+  long long total;
+  if (p.mode == kDecodeDense) {
+    long long running = 0;
+    // pass 1: total tile count
+    for (int base = 0; base < p.n_groups; base += kThreads) {
+      const int g = base + threadIdx.x;
+      const long long v = g < p.n_groups ? (max(__ldg(p.ctx_lens + g), 0) + kTile - 1) / kTile : 0;
+      long long chunk;
+      block_scan(v, s_warp_tot, &chunk);
+      running += chunk;
+    }
+    total = running;
+  } else {
+    total = static_cast<long long>(p.n_groups) * p.tiles_per_group;
+  }
+  const long long u0 = total * blockIdx.x / gridDim.x;
+  const long long u1 = total * (blockIdx.x + 1) / gridDim.x;
+  if (threadIdx.x == 0) {
+    s_count = u1 - u0;
+    s_g0 = 0;
+    s_t0 = 0;
+  }
+  if (p.mode == kDecodeDense) {
+    long long running = 0;
+    for (int base = 0; base < p.n_groups && running <= u0; base += kThreads) {
+      const int g = base + threadIdx.x;
+      const long long v = g < p.n_groups ? (max(__ldg(p.ctx_lens + g), 0) + kTile - 1) / kTile : 0;
+      long long chunk;
+      const long long incl = block_scan(v, s_warp_tot, &chunk) + running;
+      if (g < p.n_groups && v > 0 && incl - v <= u0 && u0 < incl) {
+        s_g0 = g;
+        s_t0 = static_cast<int>(u0 - (incl - v));
+      }
+      running += chunk;
+    }
+  } else if (threadIdx.x == 0 && p.tiles_per_group > 0) {
+    s_g0 = static_cast<int>(u0 / p.tiles_per_group);
+    s_t0 = static_cast<int>(u0 % p.tiles_per_group);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = s_tmem;
+  const long long count = s_count;
+  volatile int* abort_flag = &s_abort;
+
+  if (warp == 0) {
+    // =========================== TMA producer ===========================
+    const uint64_t pol_stream = l2_policy_evict_first();
+    const uint64_t pol_keep = l2_policy_evict_last();
+    const int upt = kTile / p.unit;  // boxes per tile (<= 16)
+    const uint32_t box_bytes = static_cast<uint32_t>(p.unit) * (kDim + 4);
+    int st = 0;
+    uint32_t ph = 0;
+    int qs = 0;
+    uint32_t qph = 0;
+    int q_group = -1;
+    bool ok = true;
+    Walker W;
+    W.init(p, s_g0, s_t0, count);
+    // software pipeline: the coordinates of the next active tile are fetched
+    // before waiting for the stage of the current one
+    bool have_pend = false;
+    int pend_g = 0, pend_row0 = 0;
+    Box pend_box;
+    pend_box.valid = false;
+    auto issue = [&](int g, int row0, const Box& bx) -> bool {
+      if (g != q_group) {
+        bool got = true;
+        if (lane == 0) got = wait_bar(&q_empty[qs], qph ^ 1u, abort_flag, 1u);
+        got = __shfl_sync(0xFFFFFFFFu, got, 0);
+        if (!got) return false;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&q_full[qs], C::kQStageBytes);
+          tma_load_3d(q_s + qs * C::kQStageBytes, &map_q, &q_full[qs], 0, 0, row0, pol_keep);
+        }
+        q_group = g;
+        if (++qs == 2) {
+          qs = 0;
+          qph ^= 1u;
+        }
+      }
+      bool got = true;
+      if (lane == 0) got = wait_bar(&empty[st], ph ^ 1u, abort_flag, 2u);
+      got = __shfl_sync(0xFFFFFFFFu, got, 0);
+      if (!got) return false;
+      const unsigned vm = __ballot_sync(0xFFFFFFFFu, lane < upt && bx.valid);
+      if (lane == 0) mbar_arrive_expect_tx(&full[st], __popc(vm) * box_bytes);
+      __syncwarp();
+      if (lane < upt && bx.valid) {
+        tma_load_3d(kv_s + st * kKvStageBytes + lane * p.unit * kDim, &map_kv, &full[st], 0, bx.row,
+                    bx.blk, pol_stream);
+        tma_load_2d(sc_s + st * kScaleStageBytes + lane * p.scale_slot, &map_scale, &full[st],
+                    bx.row, bx.blk, pol_stream);
+      }
+      if (++st == C::kStages) {
+        st = 0;
+        ph ^= 1u;
+      }
+      return true;
+    };
+    while (W.left > 0 && ok) {
+      if (tile_active(W.G, W.t)) {
+        Box bx;
+        bx.valid = false;
+        if (lane < upt) bx = box_coords(p, W.G, W.t, lane);
+        if (have_pend) ok = issue(pend_g, pend_row0, pend_box);
+        have_pend = true;
+        pend_g = W.g;
+        pend_row0 = W.G.row0;
+        pend_box = bx;
+      }
+      W.advance(p);
+    }
+    if (have_pend && ok) ok = issue(pend_g, pend_row0, pend_box);
+    // drain: wait for every load still in flight before the CTA can exit
+    if (lane == 0) {
+      for (int s = 0; s < C::kStages; ++s) {
+        // the most recent phase of stage s was issued with parity ph (s < st) or ph ^ 1
+        const uint32_t par = s < st ? ph : (ph ^ 1u);
+        uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(&full[s], par) && global_timer_ns() - t0 < kTimeoutNs) {
+        }
+      }
+      for (int i = 0; i < 2; ++i) {
+        const uint32_t par = i < qs ? qph : (qph ^ 1u);
+        uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(&q_full[i], par) && global_timer_ns() - t0 < kTimeoutNs) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // =========================== MMA issuer ===========================
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_e4m3_f32(kTile, C::N);
+      int st = 0, as = 0, qs = 0;
+      uint32_t ph = 0, aph = 0, qph = 0;
+      int q_group = -1;
+      Walker W;
+      W.init(p, s_g0, s_t0, count);
+      bool ok = true;
+      while (W.left > 0 && ok) {
+        if (tile_active(W.G, W.t)) {
+          if (W.g != q_group) {
+            if (q_group >= 0) {
+              umma_commit(&q_empty[qs]);
+              if (++qs == 2) {
+                qs = 0;
+                qph ^= 1u;
+              }
+            }
+            if (!wait_bar(&q_full[qs], qph, abort_flag, 3u)) break;
+            q_group = W.g;
+          }
+          if (!wait_bar(&full[st], ph, abort_flag, 4u)) break;
+          if (!wait_bar(&acc_empty[as], aph ^ 1u, abort_flag, 5u)) break;
+          tc_fence_after();
+          const uint64_t a_desc = sw128_kmajor_desc(smem_u32(kv_s + st * kKvStageBytes));
+          const uint64_t b_desc = sw128_kmajor_desc(smem_u32(q_s + qs * C::kQStageBytes));
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(as * C::N);
+#pragma unroll
+          for (int k = 0; k < kDim / 32; ++k) {
+            // +32 bytes along K inside the 128-byte swizzled rows = +2 in the >>4 address field
+            umma_e4m3(d_tmem, a_desc + 2 * k, b_desc + 2 * k, idesc, k > 0 ? 1u : 0u);
+          }
+          umma_commit(&empty[st]);
+          umma_commit(&acc_full[as]);
+          if (++st == C::kStages) {
+            st = 0;
+            ph ^= 1u;
+          }
+          if (++as == C::kAccStages) {
+            as = 0;
+            aph ^= 1u;
+          }
+        }
+        W.advance(p);
+      }
+      if (q_group >= 0) umma_commit(&q_empty[qs]);
+      (void)ok;
+    }
+    __syncwarp();
+  } else {
+    // =========================== epilogue ===========================
+    const int ew = warp - 2;
+    const int quarter = warp & 3;  // tensor-memory lanes this warp may read
+    const int trow = quarter * 32 + lane;
+    float* wsm = w_s + ew * NQ * 64;
+    int st = 0, as = 0;
+    uint32_t ph = 0, aph = 0;
+    int cur_g = -1;
+    int lim_lo[NQ], lim_hi[NQ];
+    Walker W;
+    W.init(p, s_g0, s_t0, count);
+    const float ninf = -__int_as_float(0x7f800000);
+    while (W.left > 0) {
+      const Group& G = W.G;
+      if (W.g != cur_g) {
+        cur_g = W.g;
+        __syncwarp();
+        for (int i = lane; i < NQ * 64; i += 32) {
+          const int j = i >> 6;
+          float v = 0.f;
+          if (j < G.nq) {
+            const int64_t off = static_cast<int64_t>(G.row0 + j) * p.ld_w + (i & 63);
+            v = p.w_bf16
+                    ? __uint_as_float(static_cast<uint32_t>(
+                                          __ldg(reinterpret_cast<const uint16_t*>(p.w) + off))
+                                      << 16)
+                    : __ldg(reinterpret_cast<const float*>(p.w) + off);
+          }
+          wsm[i] = v;
+        }
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < NQ; ++j) {
+          int lo = 0, hi = 0;
+          if (j < G.nq) {
+            if (p.mode == kDecodeDense) {
+              hi = min(max(G.ncols - p.next_n + j + 1, 0), G.ncols);
+            } else if (p.mode == kPrefillDense) {
+              lo = p.row_ks ? max(__ldg(p.row_ks + G.row0 + j), 0) : 0;
+              hi = min(__ldg(p.row_ke + G.row0 + j), p.S);
+            } else {
+              hi = G.act_hi;
+            }
+          }
+          lim_lo[j] = lo;
+          lim_hi[j] = hi;
+        }
+      }
+      const int c = W.t * kTile + trow;
+      if (tile_active(G, W.t)) {
+        bool got = wait_bar(&full[st], ph, abort_flag, 6u);
+        if (!__all_sync(0xFFFFFFFFu, got)) break;
+        const int box = trow / p.unit;
+        const float scale = *reinterpret_cast<const float*>(
+            sc_s + st * kScaleStageBytes + box * p.scale_slot + (trow - box * p.unit) * 4);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+        if (++st == C::kStages) {
+          st = 0;
+          ph ^= 1u;
+        }
+        got = wait_bar(&acc_full[as], aph, abort_flag, 7u);
+        if (!__all_sync(0xFFFFFFFFu, got)) break;
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                               static_cast<uint32_t>(as * C::N);
+#pragma unroll
+        for (int j = 0; j < NQ; ++j) {
+          if (j < G.nq) {
+            uint32_t a0[32], a1[32];
+            tmem_ld_x32(taddr + j * 64, a0);
+            tmem_ld_x32(taddr + j * 64 + 32, a1);
+            tmem_wait_ld(a0);
+            reg_fence(a1);
+            const float4* w4 = reinterpret_cast<const float4*>(wsm + j * 64);
+            float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int h = 0; h < 32; h += 4) {
+              const float4 wv = w4[h >> 2];
+              s[(h >> 2) & 7] = fmaf(wv.x, __uint_as_float(a0[h + 0]), s[(h >> 2) & 7]);
+              s[(h >> 2) & 7] = fmaf(wv.y, __uint_as_float(a0[h + 1]), s[(h >> 2) & 7]);
+              s[(h >> 2) & 7] = fmaf(wv.z, __uint_as_float(a0[h + 2]), s[(h >> 2) & 7]);
+              s[(h >> 2) & 7] = fmaf(wv.w, __uint_as_float(a0[h + 3]), s[(h >> 2) & 7]);
+            }
+#pragma unroll
+            for (int h = 0; h < 32; h += 4) {
+              const float4 wv = w4[(32 + h) >> 2];
+              s[(h >> 2) & 7] = fmaf(wv.x, __uint_as_float(a1[h + 0]), s[(h >> 2) & 7]);
+              s[(h >> 2) & 7] = fmaf(wv.y, __uint_as_float(a1[h + 1]), s[(h >> 2) & 7]);
+              s[(h >> 2) & 7] = fmaf(wv.z, __uint_as_float(a1[h + 2]), s[(h >> 2) & 7]);
+              s[(h >> 2) & 7] = fmaf(wv.w, __uint_as_float(a1[h + 3]), s[(h >> 2) & 7]);
+            }
+            const float sum = ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
+            const float logit = sum * scale;
+            if (c < G.ncols) {
+              const float v = (c >= lim_lo[j] && c < lim_hi[j]) ? logit : ninf;
+              const int64_t o = static_cast<int64_t>(G.row0 + j) * p.ld_out + c;
+              if (p.out_bf16) {
+                reinterpret_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(v);
+              } else {
+                reinterpret_cast<float*>(p.out)[o] = v;
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[as]);
+        if (++as == C::kAccStages) {
+          as = 0;
+          aph ^= 1u;
+        }
+      } else if (c < G.ncols) {
+#pragma unroll
+        for (int j = 0; j < NQ; ++j) {
+          if (j < G.nq) {
+            const int64_t o = static_cast<int64_t>(G.row0 + j) * p.ld_out + c;
+            if (p.out_bf16) {
+              reinterpret_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(ninf);
+            } else {
+              reinterpret_cast<float*>(p.out)[o] = ninf;
+            }
+          }
+        }
+      }
+      W.advance(p);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, C::kTmemCols);
+}
+
+template <int NQ>
+idx_status_t launch_logits(const CUtensorMap& mq, const CUtensorMap& mkv, const CUtensorMap& msc,
+                           const LogitsParams& p, int grid, cudaStream_t stream, const char* fn) {
+  auto kern = mqa_logits_kernel<NQ>;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg<NQ>::kSmemBytes);
+    if (e != cudaSuccess) return fail(IDX_ERR_CUDA, "%s: cudaFuncSetAttribute: %s", fn, cudaGetErrorString(e));
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  kern<<<grid, kThreads, Cfg<NQ>::kSmemBytes, stream>>>(mq, mkv, msc, p);
+  return check_launch(fn);
+}
+
+idx_status_t dispatch(int nq_tmpl, const CUtensorMap& mq, const CUtensorMap& mkv,
+                      const CUtensorMap& msc, const LogitsParams& p, long long max_tiles,
+                      cudaStream_t stream, const char* fn) {
+  const int sms = device_sm_count();
+  if (sms <= 0) return fail(IDX_ERR_CUDA, "%s: cannot query the SM count", fn);
+  long long grid = sms;
+  if (max_tiles >= 0 && max_tiles < grid) grid = max_tiles;
+  if (grid <= 0) return IDX_OK;
+  switch (nq_tmpl) {
+    case 1: return launch_logits<1>(mq, mkv, msc, p, static_cast<int>(grid), stream, fn);
+    case 2: return launch_logits<2>(mq, mkv, msc, p, static_cast<int>(grid), stream, fn);
+    case 4: return launch_logits<4>(mq, mkv, msc, p, static_cast<int>(grid), stream, fn);
+  }
+  return fail(IDX_ERR_UNSUPPORTED, "%s: rows per group %d", fn, nq_tmpl);
+}
+
+idx_status_t make_q_map(CUtensorMap* m, const uint8_t* q, int64_t ld_q, int rows, int nq_box) {
+  const uint64_t dims[3] = {static_cast<uint64_t>(kDim), static_cast<uint64_t>(kHeads),
+                            static_cast<uint64_t>(rows)};
+  const uint64_t strides[2] = {static_cast<uint64_t>(kDim), static_cast<uint64_t>(ld_q)};
+  const uint32_t box[3] = {static_cast<uint32_t>(kDim), static_cast<uint32_t>(kHeads),
+                           static_cast<uint32_t>(nq_box)};
+  return encode_tensor_map(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, q, dims, strides, box,
+                           CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+idx_status_t check_common(const char* fn, const uint8_t* q, int64_t ld_q, const void* w,
+                          int w_dtype, int64_t ld_w, int rows, void* out, int out_dtype,
+                          int64_t ld_out) {
+  if (!q || !w || !out) return fail(IDX_ERR_INVALID_ARG, "%s: NULL pointer", fn);
+  if (w_dtype != IDX_F32 && w_dtype != IDX_BF16) return fail(IDX_ERR_UNSUPPORTED, "%s: w_dtype %d", fn, w_dtype);
+  if (out_dtype != IDX_F32 && out_dtype != IDX_BF16) return fail(IDX_ERR_UNSUPPORTED, "%s: out_dtype %d", fn, out_dtype);
+  if (ld_w < kHeads) return fail(IDX_ERR_INVALID_ARG, "%s: ld_w < 64", fn);
+  if (ld_q < kHeads * kDim) return fail(IDX_ERR_INVALID_ARG, "%s: ld_q < 8192 bytes", fn);
+  if (ld_q % 16 != 0 || !aligned(q, 16)) {
+    return fail(IDX_ERR_UNSUPPORTED, "%s: q must be 16-byte aligned with ld_q a multiple of 16", fn);
+  }
+  if (rows < 0) return fail(IDX_ERR_INVALID_ARG, "%s: negative row count", fn);
+  (void)ld_out;
+  return IDX_OK;
+}
+
+bool sbk_ok(int32_t sbk) { return sbk == 8 || sbk == 16 || sbk == 32 || sbk == 64 || sbk == 128; }
+
+}  // namespace
+
+unsigned int logits_read_and_clear_error(cudaStream_t stream, cudaError_t* err) {
+  unsigned int v = 0;
+  const unsigned int zero = 0;
+  *err = cudaStreamSynchronize(stream);
+  if (*err != cudaSuccess) return 0;
+  *err = cudaMemcpyFromSymbol(&v, g_logits_error, sizeof(v));
+  if (*err != cudaSuccess) return 0;
+  if (v) *err = cudaMemcpyToSymbol(g_logits_error, &zero, sizeof(zero));
+  return v;
+}
+
+}  // namespace idx
+
+using namespace idx;
+
+extern "C" idx_status_t idx_paged_mqa_logits_decode(
+    const uint8_t* q, int64_t ld_q, const void* w, int w_dtype, int64_t ld_w, const uint8_t* cache,
+    int32_t num_blocks, int32_t block_size, int64_t block_stride_bytes, const int32_t* block_table,
+    int64_t ld_bt, const int32_t* ctx_lens, int32_t B, int32_t next_n, const int32_t* sparse_idx,
+    int64_t ld_si, int32_t n_si, const int32_t* end, int32_t sbk, void* logits, int out_dtype,
+    int64_t ld_out, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  (void)ws;
+  (void)ws_bytes;
+  const char* fn = "idx_paged_mqa_logits_decode";
+  if (B < 0 || next_n < 1) return fail(IDX_ERR_INVALID_ARG, "%s: B < 0 or next_n < 1", fn);
+  if (B == 0) return IDX_OK;
+  const int64_t rows64 = static_cast<int64_t>(B) * next_n;
+  if (rows64 > INT32_MAX) return fail(IDX_ERR_UNSUPPORTED, "%s: too many rows", fn);
+  const int rows = static_cast<int>(rows64);
+  idx_status_t st = check_common(fn, q, ld_q, w, w_dtype, ld_w, rows, logits, out_dtype, ld_out);
+  if (st != IDX_OK) return st;
+  if (!cache || !block_table || !ctx_lens) return fail(IDX_ERR_INVALID_ARG, "%s: NULL pointer", fn);
+  if (num_blocks < 1) return fail(IDX_ERR_INVALID_ARG, "%s: num_blocks < 1", fn);
+  if (!(block_size == 16 || block_size == 32 || block_size == 64 || block_size == 128)) {
+    return fail(IDX_ERR_UNSUPPORTED, "%s: block_size %d is not one of 16, 32, 64, 128", fn, block_size);
+  }
+  if (block_stride_bytes < static_cast<int64_t>(block_size) * kTokenBytes) {
+    return fail(IDX_ERR_INVALID_ARG, "%s: block_stride_bytes < block_size * 132", fn);
+  }
+  if (block_stride_bytes % 16 != 0 || !aligned(cache, 16)) {
+    return fail(IDX_ERR_UNSUPPORTED, "%s: cache must be 16-byte aligned with a stride multiple of 16", fn);
+  }
+  if (ld_bt < 1) return fail(IDX_ERR_INVALID_ARG, "%s: ld_bt < 1", fn);
+
+  LogitsParams p{};
+  p.n_rows = rows;
+  p.next_n = next_n;
+  p.w = w;
+  p.w_bf16 = w_dtype == IDX_BF16;
+  p.ld_w = ld_w;
+  p.paged = 1;
+  p.block_size = block_size;
+  p.block_table = block_table;
+  p.ld_bt = ld_bt;
+  p.ctx_lens = ctx_lens;
+  p.out = logits;
+  p.out_bf16 = out_dtype == IDX_BF16;
+  p.ld_out = ld_out;
+  int nq_tmpl = 1;
+  long long max_tiles = -1;
+  if (sparse_idx) {
+    if (!end) return fail(IDX_ERR_INVALID_ARG, "%s: sparse mode needs end", fn);
+    if (!sbk_ok(sbk) || block_size % sbk != 0) {
+      return fail(IDX_ERR_UNSUPPORTED, "%s: sbk %d must be one of 8..128 and divide block_size %d", fn, sbk, block_size);
+    }
+    if (n_si < 1 || ld_si < n_si) return fail(IDX_ERR_INVALID_ARG, "%s: n_si < 1 or ld_si < n_si", fn);
+    const int64_t ncols = static_cast<int64_t>(n_si) * sbk;
+    if (ncols > INT32_MAX / 2) return fail(IDX_ERR_UNSUPPORTED, "%s: too many sparse columns", fn);
+    if (ld_out < ncols) return fail(IDX_ERR_INVALID_ARG, "%s: ld_out < n_si * sbk", fn);
+    p.mode = kDecodeSparse;
+    p.n_groups = rows;
+    p.tiles_per_group = static_cast<int>((ncols + kTile - 1) / kTile);
+    p.unit = sbk;
+    p.sparse_idx = sparse_idx;
+    p.ld_si = ld_si;
+    p.n_si = n_si;
+    p.end = end;
+    p.sbk = sbk;
+    max_tiles = static_cast<long long>(p.n_groups) * p.tiles_per_group;
+  } else {
+    if (!(next_n == 1 || next_n == 2 || next_n == 4)) {
+      return fail(IDX_ERR_UNSUPPORTED, "%s: dense decode supports next_n 1, 2 or 4 (got %d)", fn, next_n);
+    }
+    p.mode = kDecodeDense;
+    p.n_groups = B;
+    p.nq = next_n;
+    p.unit = block_size;
+    nq_tmpl = next_n;
+  }
+  p.scale_slot = p.unit * 4 < 128 ? 128 : p.unit * 4;
+
+  CUtensorMap mq, mkv, msc;
+  st = make_q_map(&mq, q, ld_q, rows, nq_tmpl);
+  if (st != IDX_OK) return st;
+  {
+    const uint64_t dims[3] = {static_cast<uint64_t>(kDim), static_cast<uint64_t>(block_size),
+                              static_cast<uint64_t>(num_blocks)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(kDim), static_cast<uint64_t>(block_stride_bytes)};
+    const uint32_t box[3] = {static_cast<uint32_t>(kDim), static_cast<uint32_t>(p.unit), 1u};
+    st = encode_tensor_map(&mkv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, cache, dims, strides, box,
+                           CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != IDX_OK) return st;
+  }
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(block_size), static_cast<uint64_t>(num_blocks)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(block_stride_bytes)};
+    const uint32_t box[2] = {static_cast<uint32_t>(p.unit), 1u};
+    st = encode_tensor_map(&msc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                           cache + static_cast<int64_t>(block_size) * kDim, dims, strides, box,
+                           CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (st != IDX_OK) return st;
+  }
+  return dispatch(nq_tmpl, mq, mkv, msc, p, max_tiles, stream, fn);
+}
+
+extern "C" idx_status_t idx_mqa_logits_prefill(const uint8_t* q, int64_t ld_q, const void* w,
+                                               int w_dtype, int64_t ld_w, const uint8_t* k8,
+                                               const float* kscale, int32_t S,
+                                               const int32_t* row_ks, const int32_t* row_ke,
+                                               int32_t T, const int32_t* sparse_idx, int64_t ld_si,
+                                               int32_t n_si, const int32_t* end, int32_t sbk,
+                                               void* logits, int out_dtype, int64_t ld_out,
+                                               void* ws, size_t ws_bytes, cudaStream_t stream) {
+  (void)ws;
+  (void)ws_bytes;
+  const char* fn = "idx_mqa_logits_prefill";
+  if (T < 0 || S < 0) return fail(IDX_ERR_INVALID_ARG, "%s: negative T or S", fn);
+  if (T == 0) return IDX_OK;
+  idx_status_t st = check_common(fn, q, ld_q, w, w_dtype, ld_w, T, logits, out_dtype, ld_out);
+  if (st != IDX_OK) return st;
+  if (S == 0) return sparse_idx ? fail(IDX_ERR_INVALID_ARG, "%s: sparse mode with S == 0", fn) : IDX_OK;
+  if (!k8 || !kscale) return fail(IDX_ERR_INVALID_ARG, "%s: NULL k8 or kscale", fn);
+  if (!aligned(k8, 16) || !aligned(kscale, 16)) {
+    return fail(IDX_ERR_UNSUPPORTED, "%s: k8 and kscale must be 16-byte aligned", fn);
+  }
+  LogitsParams p{};
+  p.n_rows = T;
+  p.next_n = 1;
+  p.w = w;
+  p.w_bf16 = w_dtype == IDX_BF16;
+  p.ld_w = ld_w;
+  p.paged = 0;
+  p.block_size = 1;
+  p.S = S;
+  p.row_ks = row_ks;
+  p.row_ke = row_ke;
+  p.out = logits;
+  p.out_bf16 = out_dtype == IDX_BF16;
+  p.ld_out = ld_out;
+  int nq_tmpl;
+  if (sparse_idx) {
+    if (!end) return fail(IDX_ERR_INVALID_ARG, "%s: sparse mode needs end", fn);
+    if (!sbk_ok(sbk)) return fail(IDX_ERR_UNSUPPORTED, "%s: sbk %d is not one of 8..128", fn, sbk);
+    if (n_si < 1 || ld_si < n_si) return fail(IDX_ERR_INVALID_ARG, "%s: n_si < 1 or ld_si < n_si", fn);
+    const int64_t ncols = static_cast<int64_t>(n_si) * sbk;
+    if (ncols > INT32_MAX / 2) return fail(IDX_ERR_UNSUPPORTED, "%s: too many sparse columns", fn);
+    if (ld_out < ncols) return fail(IDX_ERR_INVALID_ARG, "%s: ld_out < n_si * sbk", fn);
+    p.mode = kPrefillSparse;
+    p.n_groups = T;
+    p.tiles_per_group = static_cast<int>((ncols + kTile - 1) / kTile);
+    p.unit = sbk;
+    p.sparse_idx = sparse_idx;
+    p.ld_si = ld_si;
+    p.n_si = n_si;
+    p.end = end;
+    p.sbk = sbk;
+    nq_tmpl = 1;
+  } else {
+    if (!row_ke) return fail(IDX_ERR_INVALID_ARG, "%s: dense mode needs row_ke", fn);
+    if (ld_out < S) return fail(IDX_ERR_INVALID_ARG, "%s: ld_out < S", fn);
+    p.mode = kPrefillDense;
+    p.nq = 4;
+    p.n_groups = (T + 3) / 4;
+    p.tiles_per_group = (S + kTile - 1) / kTile;
+    p.unit = kTile;
+    nq_tmpl = 4;
+  }
+  p.scale_slot = p.unit * 4 < 128 ? 128 : p.unit * 4;
+  CUtensorMap mq, mkv, msc;
+  st = make_q_map(&mq, q, ld_q, T, nq_tmpl);
+  if (st != IDX_OK) return st;
+  {
+    const uint64_t dims[3] = {static_cast<uint64_t>(kDim), static_cast<uint64_t>(S), 1ull};
+    const uint64_t strides[2] = {static_cast<uint64_t>(kDim), static_cast<uint64_t>(kDim) * S};
+    const uint32_t box[3] = {static_cast<uint32_t>(kDim), static_cast<uint32_t>(p.unit), 1u};
+    st = encode_tensor_map(&mkv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, k8, dims, strides, box,
+                           CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != IDX_OK) return st;
+  }
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(S), 1ull};
+    const uint64_t strides[1] = {(static_cast<uint64_t>(S) * 4 + 15) / 16 * 16};
+    const uint32_t box[2] = {static_cast<uint32_t>(p.unit), 1u};
+    st = encode_tensor_map(&msc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, kscale, dims, strides, box,
+                           CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (st != IDX_OK) return st;
+  }
+  return dispatch(nq_tmpl, mq, mkv, msc, p, static_cast<long long>(p.n_groups) * p.tiles_per_group,
+                  stream, fn);
+}

@@ -1,0 +1,394 @@
+// a5 idx_topk and a9 idx_sparse_topk_remap: per-row radix selection of the k
+// largest scores with -1 fill.
+//
+// "DeepSeek V3.2 稀疏注意力 DSA 推理流程图解", opening section: the scorer keeps
+// the 2048 highest-scoring history tokens; data-flow item 2: the result is an
+// int32 table with -1 for empty entries. The V4.1 review ("实现拆解" item 3)
+// runs the same selection over the bf16 sparse logits and then maps each chosen
+// sparse column back to its request-local position; here that remap is the
+// selection's store step.
+//
+// Design: one 1024-thread block per row. Scores are mapped to order-preserving
+// 32-bit keys and selected by three radix digits (11, 11 and 10 bits). Level 0
+// histograms the row from global memory; each later level histograms only the
+// elements that tie with the threshold digit of the level above, and those
+// elements are also compacted into shared memory, so normally the row is read
+// from global memory exactly twice. When a tie bucket overflows its
+// shared-memory buffer the next level re-reads global memory with a prefix
+// filter instead (correct for any input, slower). Elements above the threshold
+// are written as soon as their digit decides them; at the last level exactly
+// the number still missing is taken from the fully tied bucket. Writes use
+// warp-aggregated shared-memory counters, so the output is a set in no
+// particular order.
+#include "common.cuh"
+
+namespace idx {
+namespace {
+
+constexpr int kThreads = 1024;
+constexpr int kBins = 2048;
+constexpr int kCapA = 12288;  // tie bucket of level 0 (collected from global memory)
+constexpr int kCapB = 4096;   // tie bucket of level 1 (collected from bucket A)
+constexpr int kSmemDyn = (kCapA + kCapB) * 8;
+constexpr int kMaxK = 4096;
+
+struct TopkParams {
+  const void* logits;
+  int64_t ld;
+  const int32_t* row_ks;   // plain: range start (NULL = 0); remap: ks of the position base
+  const int32_t* row_ke;   // plain: range end
+  const int32_t* end;      // remap: range is [0, end[r])
+  const int32_t* si;       // remap: sparse block ids
+  int64_t ld_si;
+  int sbk;
+  int k;
+  int32_t* out;
+  int64_t ld_out;
+  int32_t* cols;           // remap: optional chosen columns
+  int64_t ld_cols;
+};
+
+template <bool kBf16>
+__device__ __forceinline__ uint32_t key_at(const void* row, int64_t c) {
+  if constexpr (kBf16) {
+    return f32_key(static_cast<uint32_t>(__ldg(static_cast<const uint16_t*>(row) + c)) << 16);
+  } else {
+    return f32_key(__float_as_uint(__ldg(static_cast<const float*>(row) + c)));
+  }
+}
+
+__device__ __forceinline__ int digit(uint32_t key, int level) {
+  return level == 0 ? static_cast<int>(key >> 21)
+                    : (level == 1 ? static_cast<int>((key >> 10) & 0x7FF)
+                                  : static_cast<int>(key & 0x3FF));
+}
+
+// True when the bits of `key` above `level` equal those of `prefix`.
+__device__ __forceinline__ bool prefix_match(uint32_t key, uint32_t prefix, int level) {
+  if (level == 0) return true;
+  const uint32_t mask = level == 1 ? 0xFFE00000u : 0xFFFFFC00u;
+  return (key & mask) == (prefix & mask);
+}
+
+// Warp-aggregated slot reservation: returns this lane's slot (valid if pred).
+__device__ __forceinline__ int warp_reserve(int* counter, bool pred) {
+  const unsigned m = __ballot_sync(0xFFFFFFFFu, pred);
+  if (m == 0) return 0;
+  const int lane = threadIdx.x & 31;
+  const int leader = __ffs(m) - 1;
+  int base = 0;
+  if (lane == leader) base = atomicAdd(counter, __popc(m));
+  base = __shfl_sync(0xFFFFFFFFu, base, leader);
+  return base + __popc(m & ((1u << lane) - 1u));
+}
+
+struct Shared {
+  uint32_t hist[2][kBins];
+  int warp_tot[32];
+  int n_out;      // entries written so far
+  int n_a;        // entries offered to bucket A
+  int n_b;        // entries offered to bucket B
+  int n_tie;      // tickets drawn at the last level
+  int thr;
+  int need;
+};
+
+// Finds the digit `thr` at which the running count of larger digits reaches
+// `need`; sets sh.thr and reduces sh.need to what must come from bucket `thr`.
+__device__ void find_threshold(Shared& sh, const uint32_t* hist, int nbins) {
+  const int need = sh.need;          // read before any thread can update it
+  const int per = nbins / kThreads;  // 1 or 2 (nbins is 1024 or 2048)
+  const int tid = threadIdx.x;
+  int c[2] = {0, 0};
+  int local = 0;
+  for (int j = 0; j < per; ++j) {
+    c[j] = static_cast<int>(hist[nbins - 1 - (tid * per + j)]);
+    local += c[j];
+  }
+  // exclusive scan of `local` over threads (descending bin order)
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) sh.warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int v = sh.warp_tot[lane];
+    int wi = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xFFFFFFFFu, wi, o);
+      if (lane >= o) wi += n;
+    }
+    sh.warp_tot[lane] = wi - v;
+  }
+  __syncthreads();
+  int before = sh.warp_tot[warp] + incl - local;
+  for (int j = 0; j < per; ++j) {
+    if (before < need && before + c[j] >= need) {
+      sh.thr = nbins - 1 - (tid * per + j);
+      sh.need = need - before;
+    }
+    before += c[j];
+  }
+  __syncthreads();
+}
+
+template <bool kRemap>
+__device__ __forceinline__ void store_one(const TopkParams& p, int row, int64_t lo, int64_t base_blk,
+                                          int slot, int64_t col) {
+  if constexpr (kRemap) {
+    const int32_t blk = __ldg(p.si + row * p.ld_si + col / p.sbk);
+    p.out[row * p.ld_out + slot] =
+        static_cast<int32_t>((blk - base_blk) * p.sbk + col % p.sbk);
+    if (p.cols) p.cols[row * p.ld_cols + slot] = static_cast<int32_t>(col);
+  } else {
+    p.out[row * p.ld_out + slot] = static_cast<int32_t>(col - lo);
+  }
+}
+
+// One selection pass at `level` over a source of (key, column) pairs.
+// Elements matching the prefix with digit > thr are stored; digit == thr are
+// handed to the next level (appended to `next_keys/next_cols` if room, and
+// counted into `next_hist`), or, at the last level, stored while tickets last.
+template <bool kRemap>
+__device__ __forceinline__ void visit(const TopkParams& p, Shared& sh, int row, int64_t lo,
+                                      int64_t base_blk, int level, uint32_t prefix, bool valid,
+                                      uint32_t key, int64_t col, uint32_t* next_keys,
+                                      int32_t* next_cols, int* next_n, int next_cap,
+                                      uint32_t* next_hist) {
+  const bool in = valid && prefix_match(key, prefix, level);
+  const int d = in ? digit(key, level) : -1;
+  const int thr = sh.thr;
+  const bool above = in && d > thr;
+  const bool tie = in && d == thr;
+  const int s = warp_reserve(&sh.n_out, above);
+  if (above) store_one<kRemap>(p, row, lo, base_blk, s, col);
+  if (level < 2) {
+    if (next_keys) {
+      const int t = warp_reserve(next_n, tie);
+      if (tie && t < next_cap) {
+        next_keys[t] = key;
+        next_cols[t] = static_cast<int32_t>(col);
+      }
+    }
+    if (tie) atomicAdd(&next_hist[digit(key, level + 1)], 1u);
+  } else {
+    const int t = warp_reserve(&sh.n_tie, tie);
+    if (tie && t < sh.need) {
+      const int slot = atomicAdd(&sh.n_out, 1);
+      store_one<kRemap>(p, row, lo, base_blk, slot, col);
+    }
+  }
+}
+
+template <bool kBf16, bool kRemap>
+__global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p) {
+  extern __shared__ __align__(16) uint8_t dyn[];
+  __shared__ Shared sh;
+  uint32_t* keys_a = reinterpret_cast<uint32_t*>(dyn);
+  int32_t* cols_a = reinterpret_cast<int32_t*>(dyn + kCapA * 4);
+  uint32_t* keys_b = reinterpret_cast<uint32_t*>(dyn + kCapA * 8);
+  int32_t* cols_b = reinterpret_cast<int32_t*>(dyn + kCapA * 8 + kCapB * 4);
+
+  const int row = blockIdx.x;
+  const int tid = threadIdx.x;
+  int64_t lo, hi, base_blk = 0;
+  if constexpr (kRemap) {
+    lo = 0;
+    hi = __ldg(p.end + row);
+    base_blk = p.row_ks ? __ldg(p.row_ks + row) / p.sbk : 0;
+  } else {
+    lo = p.row_ks ? __ldg(p.row_ks + row) : 0;
+    hi = __ldg(p.row_ke + row);
+  }
+  const int64_t n = hi > lo ? hi - lo : 0;
+  const int K = p.k;
+  const void* rowp = kBf16
+      ? static_cast<const void*>(static_cast<const uint16_t*>(p.logits) + row * p.ld)
+      : static_cast<const void*>(static_cast<const float*>(p.logits) + row * p.ld);
+
+  if (n <= K) {
+    for (int i = tid; i < K; i += kThreads) {
+      if (i < n) {
+        store_one<kRemap>(p, row, lo, base_blk, i, lo + i);
+      } else {
+        p.out[row * p.ld_out + i] = -1;
+        if constexpr (kRemap) {
+          if (p.cols) p.cols[row * p.ld_cols + i] = -1;
+        }
+      }
+    }
+    return;
+  }
+
+  for (int i = tid; i < kBins; i += kThreads) {
+    sh.hist[0][i] = 0;
+    sh.hist[1][i] = 0;
+  }
+  if (tid == 0) {
+    sh.n_out = 0;
+    sh.n_a = 0;
+    sh.n_b = 0;
+    sh.n_tie = 0;
+    sh.need = K;
+  }
+  __syncthreads();
+
+  // level-0 histogram straight from global memory
+  const int64_t iters = (n + kThreads - 1) / kThreads;
+  for (int64_t it = 0; it < iters; ++it) {
+    const int64_t c = lo + it * kThreads + tid;
+    if (c < hi) atomicAdd(&sh.hist[0][digit(key_at<kBf16>(rowp, c), 0)], 1u);
+  }
+  __syncthreads();
+  find_threshold(sh, sh.hist[0], kBins);
+
+  // level 0: store digit > thr, collect the tie bucket into A, histogram its next digit
+  for (int64_t it = 0; it < iters; ++it) {
+    const int64_t c = lo + it * kThreads + tid;
+    const bool valid = c < hi;
+    const uint32_t key = valid ? key_at<kBf16>(rowp, c) : 0u;
+    visit<kRemap>(p, sh, row, lo, base_blk, 0, 0u, valid, key, c, keys_a, cols_a, &sh.n_a, kCapA,
+                  sh.hist[1]);
+  }
+  uint32_t prefix = static_cast<uint32_t>(sh.thr) << 21;
+  __syncthreads();
+  for (int i = tid; i < kBins; i += kThreads) sh.hist[0][i] = 0;  // free since level 0 is done
+  find_threshold(sh, sh.hist[1], kBins);
+  prefix |= static_cast<uint32_t>(sh.thr) << 10;
+
+  // level 1: from bucket A when it held every tie, else global memory with a prefix filter
+  const bool a_ok = sh.n_a <= kCapA;
+  const int na = sh.n_a;
+  if (a_ok) {
+    for (int base = 0; base < na; base += kThreads) {
+      const int i = base + tid;
+      const bool valid = i < na;
+      visit<kRemap>(p, sh, row, lo, base_blk, 1, prefix, valid, valid ? keys_a[i] : 0u,
+                    valid ? cols_a[i] : 0, keys_b, cols_b, &sh.n_b, kCapB, sh.hist[0]);
+    }
+  } else {
+    for (int64_t it = 0; it < iters; ++it) {
+      const int64_t c = lo + it * kThreads + tid;
+      const bool valid = c < hi;
+      const uint32_t key = valid ? key_at<kBf16>(rowp, c) : 0u;
+      visit<kRemap>(p, sh, row, lo, base_blk, 1, prefix, valid, key, c, keys_b, cols_b, &sh.n_b,
+                    kCapB, sh.hist[0]);
+    }
+  }
+  __syncthreads();
+  find_threshold(sh, sh.hist[0], kBins / 2);
+  prefix |= static_cast<uint32_t>(sh.thr);
+
+  // level 2: every remaining candidate shares the full key prefix; take the bucket
+  // above the threshold and exactly `need` of the tied keys
+  const int nb = sh.n_b;
+  if (nb <= kCapB) {
+    for (int base = 0; base < nb; base += kThreads) {
+      const int i = base + tid;
+      const bool valid = i < nb;
+      visit<kRemap>(p, sh, row, lo, base_blk, 2, prefix, valid, valid ? keys_b[i] : 0u,
+                    valid ? cols_b[i] : 0, nullptr, nullptr, nullptr, 0, nullptr);
+    }
+  } else if (a_ok) {
+    for (int base = 0; base < na; base += kThreads) {
+      const int i = base + tid;
+      const bool valid = i < na;
+      visit<kRemap>(p, sh, row, lo, base_blk, 2, prefix, valid, valid ? keys_a[i] : 0u,
+                    valid ? cols_a[i] : 0, nullptr, nullptr, nullptr, 0, nullptr);
+    }
+  } else {
+    for (int64_t it = 0; it < iters; ++it) {
+      const int64_t c = lo + it * kThreads + tid;
+      const bool valid = c < hi;
+      const uint32_t key = valid ? key_at<kBf16>(rowp, c) : 0u;
+      visit<kRemap>(p, sh, row, lo, base_blk, 2, prefix, valid, key, c, nullptr, nullptr,
+                    nullptr, 0, nullptr);
+    }
+  }
+}
+
+}  // namespace
+}  // namespace idx
+
+using namespace idx;
+
+namespace {
+
+template <bool kBf16, bool kRemap>
+idx_status_t launch_topk(const TopkParams& p, int rows, cudaStream_t stream, const char* fn) {
+  auto kern = topk_kernel<kBf16, kRemap>;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemDyn);
+    if (e != cudaSuccess) return fail(IDX_ERR_CUDA, "%s: cudaFuncSetAttribute: %s", fn, cudaGetErrorString(e));
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  kern<<<rows, kThreads, kSmemDyn, stream>>>(p);
+  return check_launch(fn);
+}
+
+}  // namespace
+
+extern "C" idx_status_t idx_topk(const void* logits, int dtype, int64_t ld, const int32_t* row_ks,
+                                 const int32_t* row_ke, int32_t rows, int32_t k, int32_t* out,
+                                 int64_t ld_out, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  (void)ws;
+  (void)ws_bytes;
+  const char* fn = "idx_topk";
+  if (rows < 0 || k < 1) return fail(IDX_ERR_INVALID_ARG, "%s: rows < 0 or k < 1", fn);
+  if (k > kMaxK) return fail(IDX_ERR_UNSUPPORTED, "%s: k %d exceeds %d", fn, k, kMaxK);
+  if (ld_out < k) return fail(IDX_ERR_INVALID_ARG, "%s: ld_out < k", fn);
+  if (dtype != IDX_F32 && dtype != IDX_BF16) return fail(IDX_ERR_UNSUPPORTED, "%s: dtype %d", fn, dtype);
+  if (rows == 0) return IDX_OK;
+  if (!logits || !row_ke || !out) return fail(IDX_ERR_INVALID_ARG, "%s: NULL pointer", fn);
+  TopkParams p{};
+  p.logits = logits;
+  p.ld = ld;
+  p.row_ks = row_ks;
+  p.row_ke = row_ke;
+  p.k = k;
+  p.out = out;
+  p.ld_out = ld_out;
+  return dtype == IDX_BF16 ? launch_topk<true, false>(p, rows, stream, fn)
+                           : launch_topk<false, false>(p, rows, stream, fn);
+}
+
+extern "C" idx_status_t idx_sparse_topk_remap(const void* sparse_logits, int dtype, int64_t ld,
+                                              const int32_t* end, const int32_t* sparse_idx,
+                                              int64_t ld_si, const int32_t* row_ks, int32_t sbk,
+                                              int32_t rows, int32_t k, int32_t* col_scratch,
+                                              int64_t ld_col, int32_t* positions, int64_t ld_pos,
+                                              void* ws, size_t ws_bytes, cudaStream_t stream) {
+  (void)ws;
+  (void)ws_bytes;
+  const char* fn = "idx_sparse_topk_remap";
+  if (rows < 0 || k < 1 || sbk < 1) return fail(IDX_ERR_INVALID_ARG, "%s: rows < 0, k < 1 or sbk < 1", fn);
+  if (k > kMaxK) return fail(IDX_ERR_UNSUPPORTED, "%s: k %d exceeds %d", fn, k, kMaxK);
+  if (ld_pos < k || (col_scratch && ld_col < k)) return fail(IDX_ERR_INVALID_ARG, "%s: output stride < k", fn);
+  if (dtype != IDX_F32 && dtype != IDX_BF16) return fail(IDX_ERR_UNSUPPORTED, "%s: dtype %d", fn, dtype);
+  if (rows == 0) return IDX_OK;
+  if (!sparse_logits || !end || !sparse_idx || !positions) return fail(IDX_ERR_INVALID_ARG, "%s: NULL pointer", fn);
+  TopkParams p{};
+  p.logits = sparse_logits;
+  p.ld = ld;
+  p.row_ks = row_ks;
+  p.end = end;
+  p.si = sparse_idx;
+  p.ld_si = ld_si;
+  p.sbk = sbk;
+  p.k = k;
+  p.out = positions;
+  p.ld_out = ld_pos;
+  p.cols = col_scratch;
+  p.ld_cols = ld_col;
+  return dtype == IDX_BF16 ? launch_topk<true, true>(p, rows, stream, fn)
+                           : launch_topk<false, true>(p, rows, stream, fn);
+}

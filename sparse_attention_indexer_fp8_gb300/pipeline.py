@@ -1,0 +1,106 @@
+"""Orchestration of whole indexer steps over the C ABI (no arithmetic of its own).
+
+``fill_paged_cache`` inserts a workload's k into a device cache through
+``idx_k_quant_and_cache``; ``DecodeStep`` owns the device buffers of one dense
+decode step (k insert of the new tokens, paged logits, top-k, slot conversion)
+and ``HierarchicalStep`` those of one V4.1 consumer-layer step (candidate
+expansion, sparse logits, sparse top-k with remap, slot conversion). Buffers are
+allocated once at construction; ``run`` allocates nothing.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import (idx_expand_candidates, idx_k_quant_and_cache, idx_paged_mqa_logits_decode,
+               idx_req_to_global_slots, idx_sparse_topk_remap, idx_topk)
+from . import workloads as W
+
+
+def fill_paged_cache(pool: W.PagedPool, seed: int, cache: torch.Tensor, chunk_tokens: int = 1 << 21,
+                     stream=None) -> None:
+    """Quantise and insert every request's k (drawn by ``workloads.make_k``) into ``cache``."""
+    dev = cache.device
+    pend_k, pend_s, n = [], [], 0
+
+    def flush():
+        nonlocal pend_k, pend_s, n
+        if not pend_k:
+            return
+        k = torch.from_numpy(np.concatenate(pend_k).view(np.int16)).pin_memory().to(dev, non_blocking=True)
+        s = torch.from_numpy(np.concatenate(pend_s)).pin_memory().to(dev, non_blocking=True)
+        idx_k_quant_and_cache(k.view(torch.bfloat16), s, cache, pool.block_size, stream=stream)
+        torch.cuda.current_stream(dev).synchronize()
+        pend_k, pend_s, n = [], [], 0
+
+    for b in range(len(pool.ctx_lens)):
+        L = int(pool.ctx_lens[b])
+        pend_k.append(W.make_k(seed, b, L))
+        pend_s.append(pool.slot_mapping(b))
+        n += L
+        if n >= chunk_tokens:
+            flush()
+    flush()
+
+
+class DecodeStep:
+    """One dense decode step of the indexer for a fixed batch shape."""
+
+    def __init__(self, batch: int, max_ctx: int, topk: int = W.TOPK, next_n: int = 1,
+                 block_size: int = W.BLOCK_SIZE, block_span: int | None = None, device="cuda"):
+        rows = batch * next_n
+        self.batch, self.next_n, self.topk = batch, next_n, topk
+        self.block_size = block_size
+        self.block_span = block_size if block_span is None else block_span
+        self.logits = torch.empty((rows, max_ctx), dtype=torch.float32, device=device)
+        self.local = torch.empty((rows, topk), dtype=torch.int32, device=device)
+        self.slots = torch.empty((rows, topk), dtype=torch.int32, device=device)
+        self.row_ke = torch.empty(rows, dtype=torch.int32, device=device)
+
+    def run(self, q, w, cache, block_table, ctx_lens, new_k=None, new_slots=None, row_ke=None,
+            stream=None):
+        """Insert new k (optional), score, select, convert; returns the slot table."""
+        if new_k is not None:
+            idx_k_quant_and_cache(new_k, new_slots, cache, self.block_size, stream=stream)
+        idx_paged_mqa_logits_decode(q, w, cache, self.block_size, block_table, ctx_lens, self.logits,
+                                    next_n=self.next_n, stream=stream)
+        ke = ctx_lens if (row_ke is None and self.next_n == 1) else row_ke
+        idx_topk(self.logits, None, ke, self.topk, self.local, stream=stream)
+        idx_req_to_global_slots(self.local, None if self.next_n == 1 else self._row_to_req(ctx_lens),
+                                block_table, self.block_size, self.block_span, self.slots,
+                                stream=stream)
+        return self.slots
+
+    def _row_to_req(self, ctx_lens):
+        if not hasattr(self, "_r2r"):
+            self._r2r = torch.arange(self.batch, dtype=torch.int32, device=ctx_lens.device)
+            self._r2r = self._r2r.repeat_interleave(self.next_n)
+        return self._r2r
+
+
+class HierarchicalStep:
+    """One V4.1 consumer-layer decode step: expand, sparse score (bf16), select + remap, slots."""
+
+    def __init__(self, rows: int, n_cand: int, cand_block_size: int = 64, sbk: int = 64,
+                 topk: int = W.TOPK, block_size: int = W.BLOCK_SIZE, device="cuda"):
+        R = cand_block_size // sbk
+        self.cand_block_size, self.sbk, self.topk, self.block_size = cand_block_size, sbk, topk, block_size
+        self.sparse_idx = torch.empty((rows, n_cand * R), dtype=torch.int32, device=device)
+        self.end = torch.empty(rows, dtype=torch.int32, device=device)
+        self.logits = torch.empty((rows, n_cand * R * sbk), dtype=torch.bfloat16, device=device)
+        self.cols = torch.empty((rows, topk), dtype=torch.int32, device=device)
+        self.positions = torch.empty((rows, topk), dtype=torch.int32, device=device)
+        self.slots = torch.empty((rows, topk), dtype=torch.int32, device=device)
+
+    def run(self, q, w, cache, block_table, ctx_lens, cand, stream=None):
+        idx_expand_candidates(cand, None, ctx_lens, self.cand_block_size, self.sbk, self.sparse_idx,
+                              self.end, stream=stream)
+        idx_paged_mqa_logits_decode(q, w, cache, self.block_size, block_table, ctx_lens, self.logits,
+                                    sparse_idx=self.sparse_idx, end=self.end, sbk=self.sbk,
+                                    stream=stream)
+        idx_sparse_topk_remap(self.logits, self.end, self.sparse_idx, None, self.sbk, self.topk,
+                              self.positions, col_scratch=self.cols, stream=stream)
+        idx_req_to_global_slots(self.positions, None, block_table, self.block_size, self.block_size,
+                                self.slots, stream=stream)
+        return self.slots

@@ -1,0 +1,76 @@
+"""The C-ABI library loads and exports every entry point of include/idx.h (CPU only).
+
+Also exercises the host-only entry points and argument validation paths that
+return before any CUDA call.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sparse_attention_indexer_fp8_gb300 import _lib
+    from sparse_attention_indexer_fp8_gb300.build import build_library
+
+    build_library()
+    return _lib.load()
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "idx.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\S.*?\b(idx_\w+)\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared()
+    for required in ("idx_k_quant_and_cache", "idx_mqa_logits_prefill", "idx_paged_mqa_logits_decode",
+                     "idx_topk", "idx_expand_candidates", "idx_sparse_topk_remap",
+                     "idx_req_to_global_slots"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from sparse_attention_indexer_fp8_gb300 import _lib
+
+    for name in _declared():
+        assert hasattr(lib, name), name
+        assert name in _lib.SIGNATURES, f"binding has no signature for {name}"
+
+
+def test_host_helpers(lib):
+    span = ctypes.c_int32(0)
+    assert lib.idx_block_span(8704, 128, ctypes.byref(span)) == 0 and span.value == 68
+    assert lib.idx_block_span(8704, 132, ctypes.byref(span)) == 2   # not divisible -> unsupported
+    assert b"does not" not in lib.idx_status_string(0)
+    assert lib.idx_status_string(2) == b"unsupported configuration"
+    assert b"multiple" in lib.idx_last_error()
+    assert lib.idx_block_span(0, 128, ctypes.byref(span)) == 1
+    assert lib.idx_workspace_bytes(5, 128, 131072, 2048) == 0
+
+
+def test_validation_rejects_before_touching_the_device(lib):
+    fake = ctypes.c_void_p(0x1000)   # never dereferenced: every call below fails validation first
+    # block size outside {16, 32, 64, 128}
+    assert lib.idx_k_quant_and_cache(fake, 1, 128, 4, fake, fake, 8, 48, 8704, 0, None) == 2
+    # block stride too small for 64 tokens of 132 bytes
+    assert lib.idx_k_quant_and_cache(fake, 1, 128, 4, fake, fake, 8, 64, 8000, 0, None) == 1
+    # k above the selection limit, NULL logits
+    assert lib.idx_topk(fake, 0, 4096, None, fake, 4, 5000, fake, 5000, None, 0, None) == 2
+    assert lib.idx_topk(None, 0, 4096, None, fake, 4, 2048, fake, 2048, None, 0, None) == 1
+    # candidate count not a power of two
+    assert lib.idx_expand_candidates(fake, 64, 4, 48, None, fake, 64, 64, fake, 64, fake, None) == 2
+    # block_span smaller than block_size
+    assert lib.idx_req_to_global_slots(fake, 8, 1, 8, None, fake, 8, 64, 32, fake, 8, None) == 2
+    # dense decode with next_n = 3
+    assert lib.idx_paged_mqa_logits_decode(fake, 8192, fake, 0, 64, fake, 16, 64, 8704, fake, 8, fake,
+                                           2, 3, None, 0, 0, None, 0, fake, 0, 4096, None, 0, None) == 2
+    # misaligned q stride
+    assert lib.idx_mqa_logits_prefill(fake, 8200, fake, 0, 64, fake, fake, 64, None, fake, 4, None, 0,
+                                      0, None, 0, fake, 0, 64, None, 0, None) == 2

@@ -1,0 +1,412 @@
+"""Parity of every CUDA entry point with the CPU oracle on small seeded inputs.
+
+Sizes span several 128-token tiles, ragged tails, every supported block size,
+strided inputs and outputs, and the degenerate cases (empty rows, rows with at
+most k visible tokens, all-equal scores). Integer and byte outputs must match
+bit for bit; logits within 1e-3 + 2e-3 * |oracle|; top-k sets exactly up to
+ties within that tolerance.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import sparse_attention_indexer_fp8_gb300 as idx
+from oracle import indexer as O
+from oracle.codecs import bf16_decode, bf16_encode
+from sparse_attention_indexer_fp8_gb300 import workloads as W
+from tests.checks import BF16_REL, assert_logits_close, assert_topk_row, assert_topk_values_exact
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library():
+    from sparse_attention_indexer_fp8_gb300.build import build_library
+
+    build_library()
+    idx.library()
+    yield
+    idx.idx_device_error()
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def dev_bf16(u16):
+    return dev(np.asarray(u16, dtype=np.uint16).view(np.int16)).view(torch.bfloat16)
+
+
+def host_bf16(t):
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def build_caches(pool, seed, block_size=64, stride=None):
+    """GPU cache filled by the kernel, oracle cache filled by the oracle, same k."""
+    stride = stride or W.block_stride_bytes(block_size)
+    gcache = torch.zeros((pool.num_blocks, stride), dtype=torch.uint8, device=DEV)
+    ocache = np.zeros((pool.num_blocks, stride), dtype=np.uint8)
+    ks = []
+    for b in range(len(pool.ctx_lens)):
+        kb = W.make_k(seed, b, int(pool.ctx_lens[b]))
+        ks.append(kb)
+        O.k_quant_and_cache(bf16_decode(kb), pool.slot_mapping(b), ocache, block_size)
+    k_all = dev_bf16(np.concatenate(ks))
+    slots = dev(np.concatenate([pool.slot_mapping(b) for b in range(len(pool.ctx_lens))]))
+    idx.idx_k_quant_and_cache(k_all, slots, gcache, block_size)
+    return gcache, ocache
+
+
+# ------------------------------------------------------------------ a1 k quant + insert
+
+def test_k_quant_and_cache_bitexact_tiny_pool():
+    wl = W.tiny_decode()
+    g, o = build_caches(wl.pool, wl.seed)
+    assert np.array_equal(g.cpu().numpy(), o)
+
+
+def test_k_quant_skips_negative_and_out_of_range_slots_f32_strided_bs16():
+    rng = np.random.default_rng(4)
+    bs, nb = 16, 40
+    stride = W.block_stride_bytes(bs)
+    n = 300
+    k = (rng.standard_normal((n, 192)) * rng.uniform(0.01, 50, (n, 1))).astype(np.float32)
+    slots = rng.permutation(nb * bs)[:n].astype(np.int64)
+    slots[::17] = -1
+    slots[5] = nb * bs + 3                      # beyond the pool: skipped
+    gk = dev(k)[:, :128]                         # ld_k = 192
+    gcache = torch.zeros((nb, stride), dtype=torch.uint8, device=DEV)
+    idx.idx_k_quant_and_cache(gk, dev(slots), gcache, bs)
+    ocache = np.zeros((nb, stride), dtype=np.uint8)
+    keep = slots < nb * bs
+    O.k_quant_and_cache(k[keep, :128], slots[keep], ocache, bs)
+    assert np.array_equal(gcache.cpu().numpy(), ocache)
+
+
+def test_k_quant_special_values():
+    k = np.zeros((6, 128), dtype=np.float32)
+    k[1, 3] = 448.0
+    k[2, :] = np.float32(1e-45)                  # amax / 448 underflows: scale 0
+    k[3, :] = np.linspace(-1e30, 1e30, 128, dtype=np.float32)
+    k[4, :] = -0.0
+    k[5, :] = np.float32(2.0) ** np.arange(-64, 64, dtype=np.float32)
+    bs = 32
+    stride = W.block_stride_bytes(bs)
+    slots = np.array([0, 5, 33, 40, 63, 64], dtype=np.int64)
+    gcache = torch.zeros((3, stride), dtype=torch.uint8, device=DEV)
+    idx.idx_k_quant_and_cache(dev(k), dev(slots), gcache, bs)
+    ocache = np.zeros((3, stride), dtype=np.uint8)
+    O.k_quant_and_cache(k, slots, ocache, bs)
+    assert np.array_equal(gcache.cpu().numpy(), ocache)
+
+
+def test_gather_k_matches_oracle():
+    wl = W.tiny_decode()
+    g, o = build_caches(wl.pool, wl.seed)
+    b = 2
+    L = int(wl.pool.ctx_lens[b])
+    k8 = torch.empty((L, 128), dtype=torch.uint8, device=DEV)
+    ks = torch.empty(L, dtype=torch.float32, device=DEV)
+    idx.idx_gather_k(g, 64, dev(wl.pool.block_table[b]), L, k8, ks)
+    ok8, oks = O.gather_k(o, 64, wl.pool.block_table[b], L)
+    assert np.array_equal(k8.cpu().numpy(), ok8) and np.array_equal(ks.cpu().numpy(), oks)
+
+
+# ------------------------------------------------------------------ a4 decode logits
+
+@pytest.mark.parametrize("next_n,block_size,out_bf16,w_bf16", [
+    (1, 64, False, False), (2, 64, True, False), (4, 64, False, True), (1, 16, False, False),
+    (1, 32, True, True), (2, 128, False, False)])
+def test_decode_dense_logits(next_n, block_size, out_bf16, w_bf16):
+    ctx = np.array([1000, 2048, 3000, 4096, 1, 5, 130, 127], dtype=np.int32)
+    ctx = np.maximum(ctx, next_n)
+    pool = W.make_pool(77 + next_n, ctx, block_size=block_size, extra_blocks=7)
+    g, o = build_caches(pool, 77, block_size)
+    rows = len(ctx) * next_n
+    q8, w = W.make_q(78, rows, w_bf16=w_bf16)
+    # strided q and w: slices of larger buffers
+    qbig = np.zeros((rows, 2, 64, 128), dtype=np.uint8)
+    qbig[:, 0] = q8
+    gq = dev(qbig.reshape(rows, 2 * 64, 128))[:, :64, :]
+    wbig = np.zeros((rows, 80), dtype=w.dtype)
+    wbig[:, :64] = w
+    gw = (dev_bf16(wbig) if w_bf16 else dev(wbig))[:, :64]
+    L_max = int(ctx.max())
+    out = torch.full((rows, L_max + 40), 7.0, device=DEV,
+                     dtype=torch.bfloat16 if out_bf16 else torch.float32)
+    idx.idx_paged_mqa_logits_decode(gq, gw, g, block_size, dev(pool.block_table), dev(ctx), out,
+                                    next_n=next_n)
+    wv = bf16_decode(w) if w_bf16 else w
+    ref = O.paged_decode_logits(q8, wv, o, block_size, pool.block_table, ctx, next_n)
+    got = out.float().cpu().numpy()
+    for r in range(rows):
+        L = int(ctx[r // next_n])
+        assert_logits_close(got[r, :L], ref[r, :L], f"row {r}", BF16_REL if out_bf16 else 0.0)
+        assert np.all(got[r, L:] == 7.0), "columns beyond the context must stay untouched"
+
+
+def _hier_inputs(seed, block_size=64):
+    ctx = np.array([1000, 777, 4096, 2500, 64, 3], dtype=np.int32)
+    pool = W.make_pool(seed, ctx, block_size=block_size)
+    g, o = build_caches(pool, seed, block_size)
+    q8, w = W.make_q(seed, len(ctx))
+    cand = W.make_candidates(seed, len(ctx), 16, 64, n_dup=3, n_pad=2, n_oob=2)
+    return ctx, pool, g, o, q8, w, cand
+
+
+@pytest.mark.parametrize("sbk,cbs,out_bf16", [(64, 64, True), (16, 64, True), (8, 16, False),
+                                              (32, 64, False)])
+def test_decode_sparse_logits_and_remap(sbk, cbs, out_bf16):
+    ctx, pool, g, o, q8, w, cand = _hier_inputs(90 + sbk)
+    rows = len(ctx)
+    R = cbs // sbk
+    si = torch.empty((rows, cand.shape[1] * R), dtype=torch.int32, device=DEV)
+    end = torch.empty(rows, dtype=torch.int32, device=DEV)
+    idx.idx_expand_candidates(dev(cand), None, dev(ctx), cbs, sbk, si, end)
+    osi, oend = O.expand_candidates(cand, None, ctx, cbs, sbk)
+    assert np.array_equal(si.cpu().numpy(), osi) and np.array_equal(end.cpu().numpy(), oend)
+    ncols = si.shape[1] * sbk
+    out = torch.empty((rows, ncols), device=DEV, dtype=torch.bfloat16 if out_bf16 else torch.float32)
+    idx.idx_paged_mqa_logits_decode(dev(q8), dev(w), g, 64, dev(pool.block_table), dev(ctx), out,
+                                    sparse_idx=si, end=end, sbk=sbk)
+    ref = O.sparse_logits_decode(q8, w, o, 64, pool.block_table, None, osi, oend, sbk)
+    got = out.float().cpu().numpy()
+    assert_logits_close(got, ref, "sparse logits", BF16_REL if out_bf16 else 0.0)
+    # selection + remap on the kernel's own sparse scores
+    k = 300
+    pos = torch.empty((rows, k), dtype=torch.int32, device=DEV)
+    cols = torch.empty((rows, k), dtype=torch.int32, device=DEV)
+    idx.idx_sparse_topk_remap(out, end, si, None, sbk, k, pos, col_scratch=cols)
+    pos, cols = pos.cpu().numpy(), cols.cpu().numpy()
+    for r in range(rows):
+        e = int(oend[r])
+        assert_topk_values_exact(cols[r], got[r, :e], k, f"sparse top-k row {r}")
+        m = min(k, e)
+        for c, p_ in zip(cols[r, :m], pos[r, :m]):
+            assert O.sparse_column_token(osi[r], int(c), sbk) == p_
+        assert np.all(pos[r, m:] == -1)
+        assert_topk_row(cols[r], ref[r, :e], k, f"sparse top-k vs oracle row {r}",
+                        BF16_REL if out_bf16 else 0.0)
+
+
+# ------------------------------------------------------------------ a3 prefill logits
+
+@pytest.mark.parametrize("T,w_bf16,out_bf16,ragged", [(256, False, False, False), (255, True, True, True),
+                                                      (7, False, False, True)])
+def test_prefill_dense_logits(T, w_bf16, out_bf16, ragged):
+    S = 4096 if T > 7 else 300
+    k8, kscale = W.make_random_cache_tokens(31, S)
+    q8, w = W.make_q(32, T, w_bf16=w_bf16)
+    if ragged:
+        rng = np.random.default_rng(5)
+        ks = rng.integers(0, S, T).astype(np.int32)
+        ke = np.minimum(ks + rng.integers(0, S, T), S).astype(np.int32)
+        ke[::9] = ks[::9]                           # empty rows
+    else:
+        ks = np.zeros(T, dtype=np.int32)
+        ke = np.arange(S - T, S, dtype=np.int32) + 1
+    out = torch.empty((T, S + 8), device=DEV, dtype=torch.bfloat16 if out_bf16 else torch.float32)
+    idx.idx_mqa_logits_prefill(dev(q8), dev_bf16(w) if w_bf16 else dev(w), dev(k8), dev(kscale),
+                               dev(ks), dev(ke), out)
+    wv = bf16_decode(w) if w_bf16 else w
+    ref = O.mqa_logits(q8, wv, k8, kscale, ks, ke)
+    assert_logits_close(out.float().cpu().numpy()[:, :S], ref, "prefill logits",
+                        BF16_REL if out_bf16 else 0.0)
+
+
+def test_prefill_sparse_logits():
+    S, T, sbk = 3000, 40, 16
+    k8, kscale = W.make_random_cache_tokens(41, S)
+    q8, w = W.make_q(42, T)
+    rng = np.random.default_rng(6)
+    ks = (rng.integers(0, 60, T) * sbk).astype(np.int32)
+    ke = np.minimum(ks + rng.integers(1, 2000, T), S).astype(np.int32)
+    cand = W.make_candidates(43, T, 16, 40)
+    si = torch.empty((T, 64), dtype=torch.int32, device=DEV)
+    end = torch.empty(T, dtype=torch.int32, device=DEV)
+    idx.idx_expand_candidates(dev(cand), dev(ks), dev(ke), 64, sbk, si, end)
+    osi, oend = O.expand_candidates(cand, ks, ke, 64, sbk)
+    assert np.array_equal(si.cpu().numpy(), osi) and np.array_equal(end.cpu().numpy(), oend)
+    out = torch.empty((T, 64 * sbk), device=DEV, dtype=torch.float32)
+    idx.idx_mqa_logits_prefill(dev(q8), dev(w), dev(k8), dev(kscale), dev(ks), dev(ke), out,
+                               sparse_idx=si, end=end, sbk=sbk)
+    ref = O.sparse_logits_prefill(q8, w, k8, kscale, osi, oend, sbk)
+    assert_logits_close(out.cpu().numpy(), ref, "sparse prefill logits")
+    k = 512
+    pos = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    cols = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    idx.idx_sparse_topk_remap(out, end, si, dev(ks), sbk, k, pos, col_scratch=cols)
+    pos, cols = pos.cpu().numpy(), cols.cpu().numpy()
+    for r in range(T):
+        e = int(oend[r])
+        # the chosen sparse columns against the oracle's sparse scores (tie-tolerant) ...
+        assert_topk_row(cols[r], ref[r, :e], k, f"sparse prefill top-k row {r}")
+        # ... and each position is its column's token, relative to the row start
+        m = min(k, e)
+        expect = [O.sparse_column_token(osi[r], int(c), sbk) - int(ks[r]) for c in cols[r, :m]]
+        assert pos[r, :m].tolist() == expect and np.all(pos[r, m:] == -1)
+
+
+# ------------------------------------------------------------------ a5 top-k
+
+def _run_topk(x, ks, ke, k, bf16=False, ld_pad=0, out_pad=0):
+    rows, width = x.shape
+    if bf16:
+        xb = bf16_encode(x)
+        buf = np.zeros((rows, width + ld_pad), dtype=np.uint16)
+        buf[:, :width] = xb
+        t = dev_bf16(buf)
+        vals = bf16_decode(xb)
+    else:
+        buf = np.zeros((rows, width + ld_pad), dtype=np.float32)
+        buf[:, :width] = x
+        t = dev(buf)
+        vals = x
+    out = torch.full((rows, k + out_pad), -7, dtype=torch.int32, device=DEV)
+    idx.idx_topk(t, None if ks is None else dev(ks), dev(ke), k, out)
+    return out.cpu().numpy(), vals
+
+
+@pytest.mark.parametrize("width,k", [(100, 2048), (2048, 2048), (2049, 2048), (5000, 2048),
+                                     (40000, 2048), (5000, 1), (5000, 4096), (3000, 777)])
+def test_topk_random(width, k):
+    x = W.make_logits(width + k, 6, width)
+    rng = np.random.default_rng(width)
+    ks = rng.integers(0, max(width // 3, 1), 6).astype(np.int32)
+    ke = np.minimum(ks + rng.integers(width // 2, width + 1, 6), width).astype(np.int32)
+    ke[0], ks[0] = width, 0
+    out, vals = _run_topk(x, ks, ke, k, ld_pad=5, out_pad=3)
+    for r in range(6):
+        seg = vals[r, ks[r]:ke[r]]
+        assert_topk_values_exact(out[r], seg, k, f"row {r}")
+        assert np.all(out[r, k:] == -7), "columns beyond k must stay untouched"
+        ref = O.topk_row(vals[r], ks[r], ke[r], k)
+        if len(np.unique(seg)) == len(seg):      # no ties: the index set is unique
+            assert set(out[r, :k].tolist()) == set(ref.tolist())
+
+
+def test_topk_ties_overflow_and_special_values():
+    width, k = 40000, 2048
+    x = W.make_logits(9, 6, width, ties=True)
+    x[1, :] = 0.5                                     # all equal: every bucket ties
+    x[2, :] = (1.0 + np.arange(width) * 2.0 ** -22).astype(np.float32)  # one top-11-bit bucket
+    x[3, ::3] = -np.inf                               # -inf never beats a finite score
+    x[4, :30000] = 0.25                               # bucket A overflows, B holds the rest
+    x[4, 30000:] = (0.25 + np.arange(10000) * 2.0 ** -24).astype(np.float32)
+    x[5, :] = np.float32(-3.0)
+    x[5, 123] = np.float32(3.0)
+    out, vals = _run_topk(x, None, np.full(6, width, dtype=np.int32), k)
+    for r in range(6):
+        assert_topk_values_exact(out[r], vals[r], k, f"row {r}")
+    assert 123 in set(out[5].tolist())
+
+
+def test_topk_bf16_and_wide_rows():
+    x = W.make_logits(10, 4, 131072)
+    out, vals = _run_topk(x, None, np.full(4, 131072, dtype=np.int32), 2048, bf16=True)
+    for r in range(4):
+        assert_topk_values_exact(out[r], vals[r], 2048, f"bf16 row {r}")
+    out, vals = _run_topk(x, None, np.array([131072, 65536, 2048, 0], dtype=np.int32), 2048)
+    for r in range(4):
+        n = [131072, 65536, 2048, 0][r]
+        assert_topk_values_exact(out[r], vals[r, :n], 2048, f"fp32 row {r}")
+        ref = O.topk_row(vals[r], 0, n, 2048)
+        assert set(out[r].tolist()) == set(ref.tolist())
+
+
+# ------------------------------------------------------------------ a7 expansion, a6 slots
+
+def test_expand_candidates_random_vs_oracle():
+    rng = np.random.default_rng(12)
+    for sbk, R, K in [(64, 1, 64), (8, 2, 16), (16, 4, 32), (8, 8, 128), (64, 1, 1024), (32, 2, 2)]:
+        rows = 37
+        cbs = sbk * R
+        ks = (rng.integers(0, 50, rows) * sbk).astype(np.int32)
+        ke = (ks + rng.integers(0, 40 * cbs, rows)).astype(np.int32)
+        cand = rng.integers(-2, 45, (rows, K + 3)).astype(np.int32)   # ld_c = K + 3
+        gsi = torch.full((rows, K * R + 2), -9, dtype=torch.int32, device=DEV)
+        gend = torch.empty(rows, dtype=torch.int32, device=DEV)
+        idx.idx_expand_candidates(dev(cand)[:, :K], dev(ks), dev(ke), cbs, sbk, gsi[:, :K * R], gend)
+        osi, oend = O.expand_candidates(cand[:, :K], ks, ke, cbs, sbk)
+        s = gsi.cpu().numpy()
+        assert np.array_equal(s[:, :K * R], osi), (sbk, R, K)
+        assert np.all(s[:, K * R:] == -9)
+        assert np.array_equal(gend.cpu().numpy(), oend), (sbk, R, K)
+
+
+def test_expand_candidates_golden():
+    import json
+    import os
+
+    with open(os.path.join(os.path.dirname(__file__), "golden", "expand_candidates.json")) as f:
+        spec = json.load(f)
+    for c in spec["cases"]:
+        cand = np.array([c["cand"]], dtype=np.int32)
+        si = torch.empty((1, len(c["sparse_idx"])), dtype=torch.int32, device=DEV)
+        end = torch.empty(1, dtype=torch.int32, device=DEV)
+        idx.idx_expand_candidates(dev(cand), dev(np.array([c["ks"]], np.int32)),
+                                  dev(np.array([c["ke"]], np.int32)), c["cand_block_size"], c["sbk"],
+                                  si, end)
+        assert si.cpu().numpy()[0].tolist() == c["sparse_idx"], c["note"]
+        assert int(end.cpu()[0]) == c["end"], c["note"]
+
+
+def test_expand_candidates_flags_misaligned_ks():
+    cand = dev(np.array([[0, 1, 2, 3]], dtype=np.int32))
+    si = torch.empty((1, 4), dtype=torch.int32, device=DEV)
+    end = torch.empty(1, dtype=torch.int32, device=DEV)
+    idx.idx_expand_candidates(cand, dev(np.array([10], np.int32)), dev(np.array([500], np.int32)),
+                              64, 64, si, end)
+    with pytest.raises(idx.IdxError):
+        idx.idx_device_error()
+    assert int(end.cpu()[0]) == 0
+    idx.idx_device_error()   # the flag was cleared
+
+
+def test_req_to_global_slots_vs_oracle():
+    import json
+    import os
+
+    with open(os.path.join(os.path.dirname(__file__), "golden", "slot_remap.json")) as f:
+        spec = json.load(f)
+    bt = np.array([spec["block_table"]], dtype=np.int32)
+    for c in spec["cases"]:
+        loc = dev(np.array([[c["local"]]], dtype=np.int32))
+        out = torch.empty_like(loc)
+        idx.idx_req_to_global_slots(loc, None, dev(bt), spec["block_size"], c["block_span"], out)
+        assert int(out.cpu()[0, 0]) == c["slot"]
+    rng = np.random.default_rng(3)
+    rows, k, nreq = 50, 2048, 7
+    bt = rng.integers(0, 5000, (nreq, 300)).astype(np.int32)
+    r2r = rng.integers(0, nreq, rows).astype(np.int32)
+    local = rng.integers(-1, 300 * 64, (rows, k)).astype(np.int32)
+    for span in (64, 68, 80):
+        out = torch.empty((rows, k + 1), dtype=torch.int32, device=DEV)
+        idx.idx_req_to_global_slots(dev(local), dev(r2r), dev(bt), 64, span, out[:, :k])
+        ref = O.req_to_global_slots(local, r2r, bt, 64, span)
+        assert np.array_equal(out.cpu().numpy()[:, :k], ref)
+    g = dev(local)                                     # in place
+    idx.idx_req_to_global_slots(g, dev(r2r), dev(bt), 64, 64, g)
+    assert np.array_equal(g.cpu().numpy(), O.req_to_global_slots(local, r2r, bt, 64, 64))
+
+
+def test_sparse_topk_remap_vs_oracle_bf16():
+    rows, n_si, sbk, k = 9, 64, 64, 2048
+    x = W.make_logits(20, rows, n_si * sbk)
+    xb = bf16_encode(x)
+    rng = np.random.default_rng(20)
+    si = np.sort(rng.choice(4000, (rows, n_si)), axis=1).astype(np.int32)
+    end = np.array([4096, 4000, 2048, 2047, 100, 0, 1, 3000, 4096], dtype=np.int32)
+    pos = torch.empty((rows, k), dtype=torch.int32, device=DEV)
+    cols = torch.empty((rows, k), dtype=torch.int32, device=DEV)
+    idx.idx_sparse_topk_remap(dev_bf16(xb), dev(end), dev(si), None, sbk, k, pos, col_scratch=cols)
+    pos, cols = pos.cpu().numpy(), cols.cpu().numpy()
+    vals = bf16_decode(xb)
+    for r in range(rows):
+        e = int(end[r])
+        assert_topk_values_exact(cols[r], vals[r, :e], k, f"row {r}")
+        m = min(k, e)
+        expect = [(int(si[r, c // sbk])) * sbk + c % sbk for c in cols[r, :m]]
+        assert pos[r, :m].tolist() == expect and np.all(pos[r, m:] == -1)
