@@ -7,7 +7,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/idx.h"
+#include "idx.h"
 
 namespace idx {
 

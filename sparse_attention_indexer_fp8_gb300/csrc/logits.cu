@@ -46,7 +46,11 @@ namespace idx {
 namespace {
 
 constexpr int kTile = 128;
-constexpr int kEpiWarps = 4;
+#ifndef IDX_EPI_WARPGROUPS
+#define IDX_EPI_WARPGROUPS 2
+#endif
+constexpr int kEpiWG = IDX_EPI_WARPGROUPS;  // epilogue warpgroups, alternating tiles
+constexpr int kEpiWarps = 4 * kEpiWG;
 constexpr int kThreads = 64 + kEpiWarps * 32;
 constexpr int kKvStageBytes = kTile * kDim;       // 16 KB
 constexpr int kScaleStageBytes = 2048;            // up to 16 boxes, each in a 128-byte slot
@@ -68,6 +72,8 @@ struct LogitsParams {
   int w_bf16;
   int64_t ld_w;
   int paged;
+  const uint8_t* kv_base;     // cache (paged) or k8 (contiguous)
+  int64_t kv_block_stride;    // bytes between cache blocks (paged)
   int unit;             // tokens per k box (cache block, sparse block or 128)
   int scale_slot;       // bytes between the scale boxes of one stage (>= 128)
   int block_size;
@@ -92,6 +98,11 @@ struct Cfg {
   static constexpr int N = 64 * NQ;
   static constexpr int kStages = NQ == 1 ? 11 : (NQ == 2 ? 10 : 8);
   static constexpr int kAccStages = NQ == 4 ? 2 : 4;
+  // tiles per tcgen05.commit: one commit covers the MMAs of kCommit consecutive
+  // tiles (commits are costly next to a 4-MMA tile); one accumulator-ready
+  // barrier per commit group
+  static constexpr int kCommit = NQ == 4 ? 1 : 2;
+  static constexpr int kAccFull = kAccStages / kCommit;
   static constexpr int kTmemCols = kAccStages * N;  // 256 or 512
   static constexpr int kQStageBytes = NQ * 64 * kDim;
   static constexpr int kOffKv = 0;
@@ -99,7 +110,7 @@ struct Cfg {
   static constexpr int kOffScale = kOffQ + 2 * kQStageBytes;
   static constexpr int kOffW = kOffScale + kStages * kScaleStageBytes;
   static constexpr int kOffBar = kOffW + kEpiWarps * NQ * 64 * 4;
-  static constexpr int kNumBars = 2 * kStages + 2 * kAccStages + 4;
+  static constexpr int kNumBars = 2 * kStages + kAccFull + kAccStages + 4;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 1024;  // + alignment slack
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
@@ -234,19 +245,22 @@ struct Box {
   bool valid;
 };
 
-__device__ __forceinline__ Box box_coords(const LogitsParams& p, const Group& G, int t, int u) {
+// Box u of tile t of a group whose first row is row0, whose request is req and
+// whose rows see the columns [act_lo, act_hi).
+__device__ __forceinline__ Box box_at(const LogitsParams& p, int row0, int req, int act_lo,
+                                      int act_hi, int t, int u) {
   Box b;
   const int c0 = t * kTile + u * p.unit;
-  b.valid = c0 < G.act_hi && c0 + p.unit > G.act_lo;
+  b.valid = c0 < act_hi && c0 + p.unit > act_lo;
   b.blk = 0;
   b.row = 0;
   if (!b.valid) return b;
   int tok = c0;
   if (p.mode == kDecodeSparse || p.mode == kPrefillSparse) {
-    tok = __ldg(p.sparse_idx + static_cast<int64_t>(G.row0) * p.ld_si + c0 / p.sbk) * p.sbk;
+    tok = __ldg(p.sparse_idx + static_cast<int64_t>(row0) * p.ld_si + c0 / p.sbk) * p.sbk;
   }
   if (p.paged) {
-    b.blk = __ldg(p.block_table + static_cast<int64_t>(G.req) * p.ld_bt + tok / p.block_size);
+    b.blk = __ldg(p.block_table + static_cast<int64_t>(req) * p.ld_bt + tok / p.block_size);
     b.row = tok % p.block_size;
   } else {
     b.row = tok;
@@ -269,7 +283,7 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   uint64_t* full = bars;
   uint64_t* empty = bars + C::kStages;
   uint64_t* acc_full = bars + 2 * C::kStages;
-  uint64_t* acc_empty = acc_full + C::kAccStages;
+  uint64_t* acc_empty = acc_full + C::kAccFull;
   uint64_t* q_full = acc_empty + C::kAccStages;
   uint64_t* q_empty = q_full + 2;
 
@@ -278,6 +292,9 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   __shared__ int s_g0, s_t0;
   __shared__ long long s_count;
   __shared__ long long s_warp_tot[kThreads / 32];
+  __shared__ int4 s_tile[2][32];   // producer batches: (group, tile, row0, req)
+  __shared__ int2 s_act[2][32];    //                   (act_lo, act_hi)
+  __shared__ int s_ntile[2];
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -285,12 +302,12 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1 + kEpiWarps);
+      // released by the 4 warps of the epilogue warpgroup that owns the tile, once
+      // its accumulator is ready (so the MMAs no longer read the stage)
+      mbar_init(&empty[s], 4);
     }
-    for (int a = 0; a < C::kAccStages; ++a) {
-      mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], kEpiWarps);
-    }
+    for (int a = 0; a < C::kAccFull; ++a) mbar_init(&acc_full[a], 1);
+    for (int a = 0; a < C::kAccStages; ++a) mbar_init(&acc_empty[a], 4);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&q_full[i], 1);
       mbar_init(&q_empty[i], 1);
@@ -355,9 +372,15 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
 
   if (warp == 0) {
     // =========================== TMA producer ===========================
+    // Boxes are prepared a batch at a time, one lane per box: lane 0 walks the
+    // next batch of active tiles and publishes it in shared memory, then every
+    // lane fetches the sparse-index / block-table entries of its own box. The
+    // next batch is fetched before the current one is issued, so those dependent
+    // loads overlap with the waits for free stages instead of serialising.
     const uint64_t pol_stream = l2_policy_evict_first();
     const uint64_t pol_keep = l2_policy_evict_last();
-    const int upt = kTile / p.unit;  // boxes per tile (<= 16)
+    const int upt = kTile / p.unit;  // boxes per tile, 1..16
+    const int tpb = 32 / upt;        // tiles per batch
     const uint32_t box_bytes = static_cast<uint32_t>(p.unit) * (kDim + 4);
     int st = 0;
     uint32_t ph = 0;
@@ -367,61 +390,85 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     bool ok = true;
     Walker W;
     W.init(p, s_g0, s_t0, count);
-    // software pipeline: the coordinates of the next active tile are fetched
-    // before waiting for the stage of the current one
-    bool have_pend = false;
-    int pend_g = 0, pend_row0 = 0;
-    Box pend_box;
-    pend_box.valid = false;
-    auto issue = [&](int g, int row0, const Box& bx) -> bool {
-      if (g != q_group) {
+    auto fill = [&](int buf) {  // lane 0
+      int n = 0;
+      while (W.left > 0 && n < tpb) {
+        if (tile_active(W.G, W.t)) {
+          s_tile[buf][n] = make_int4(W.g, W.t, W.G.row0, W.G.req);
+          s_act[buf][n] = make_int2(W.G.act_lo, W.G.act_hi);
+          ++n;
+        }
+        W.advance(p);
+      }
+      s_ntile[buf] = n;
+    };
+    auto coords = [&](int buf) -> Box {
+      Box b;
+      b.valid = false;
+      b.blk = 0;
+      b.row = 0;
+      const int ti = lane / upt;
+      if (ti < s_ntile[buf]) {
+        const int4 tl = s_tile[buf][ti];
+        const int2 act = s_act[buf][ti];
+        b = box_at(p, tl.z, tl.w, act.x, act.y, tl.y, lane - ti * upt);
+      }
+      return b;
+    };
+    auto issue_batch = [&](int buf, const Box& bx) -> bool {
+      const int n = s_ntile[buf];
+      for (int ti = 0; ti < n; ++ti) {
+        const int4 tl = s_tile[buf][ti];
+        if (tl.x != q_group) {
+          bool got = true;
+          if (lane == 0) got = wait_bar(&q_empty[qs], qph ^ 1u, abort_flag, 1u);
+          got = __shfl_sync(0xFFFFFFFFu, got, 0);
+          if (!got) return false;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&q_full[qs], C::kQStageBytes);
+            tma_load_3d(q_s + qs * C::kQStageBytes, &map_q, &q_full[qs], 0, 0, tl.z, pol_keep);
+          }
+          q_group = tl.x;
+          if (++qs == 2) {
+            qs = 0;
+            qph ^= 1u;
+          }
+        }
         bool got = true;
-        if (lane == 0) got = wait_bar(&q_empty[qs], qph ^ 1u, abort_flag, 1u);
+        if (lane == 0) got = wait_bar(&empty[st], ph ^ 1u, abort_flag, 2u);
         got = __shfl_sync(0xFFFFFFFFu, got, 0);
         if (!got) return false;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&q_full[qs], C::kQStageBytes);
-          tma_load_3d(q_s + qs * C::kQStageBytes, &map_q, &q_full[qs], 0, 0, row0, pol_keep);
+        const bool mine = (lane / upt == ti) && bx.valid;
+        const unsigned vm = __ballot_sync(0xFFFFFFFFu, mine);
+        if (lane == 0) mbar_arrive_expect_tx(&full[st], __popc(vm) * box_bytes);
+        __syncwarp();
+        if (mine) {
+          const int u = lane - ti * upt;
+          tma_load_3d(kv_s + st * kKvStageBytes + u * p.unit * kDim, &map_kv, &full[st], 0, bx.row,
+                      bx.blk, pol_stream);
+          tma_load_2d(sc_s + st * kScaleStageBytes + u * p.scale_slot, &map_scale, &full[st],
+                      bx.row, bx.blk, pol_stream);
         }
-        q_group = g;
-        if (++qs == 2) {
-          qs = 0;
-          qph ^= 1u;
+        if (++st == C::kStages) {
+          st = 0;
+          ph ^= 1u;
         }
-      }
-      bool got = true;
-      if (lane == 0) got = wait_bar(&empty[st], ph ^ 1u, abort_flag, 2u);
-      got = __shfl_sync(0xFFFFFFFFu, got, 0);
-      if (!got) return false;
-      const unsigned vm = __ballot_sync(0xFFFFFFFFu, lane < upt && bx.valid);
-      if (lane == 0) mbar_arrive_expect_tx(&full[st], __popc(vm) * box_bytes);
-      __syncwarp();
-      if (lane < upt && bx.valid) {
-        tma_load_3d(kv_s + st * kKvStageBytes + lane * p.unit * kDim, &map_kv, &full[st], 0, bx.row,
-                    bx.blk, pol_stream);
-        tma_load_2d(sc_s + st * kScaleStageBytes + lane * p.scale_slot, &map_scale, &full[st],
-                    bx.row, bx.blk, pol_stream);
-      }
-      if (++st == C::kStages) {
-        st = 0;
-        ph ^= 1u;
       }
       return true;
     };
-    while (W.left > 0 && ok) {
-      if (tile_active(W.G, W.t)) {
-        Box bx;
-        bx.valid = false;
-        if (lane < upt) bx = box_coords(p, W.G, W.t, lane);
-        if (have_pend) ok = issue(pend_g, pend_row0, pend_box);
-        have_pend = true;
-        pend_g = W.g;
-        pend_row0 = W.G.row0;
-        pend_box = bx;
-      }
-      W.advance(p);
+    if (lane == 0) fill(0);
+    __syncwarp();
+    Box cur = coords(0);
+    int buf = 0;
+    while (ok && s_ntile[buf] > 0) {
+      if (lane == 0) fill(buf ^ 1);
+      __syncwarp();
+      const Box nxt = coords(buf ^ 1);
+      ok = issue_batch(buf, cur);
+      cur = nxt;
+      buf ^= 1;
+      __syncwarp();
     }
-    if (have_pend && ok) ok = issue(pend_g, pend_row0, pend_box);
     // drain: wait for every load still in flight before the CTA can exit
     if (lane == 0) {
       for (int s = 0; s < C::kStages; ++s) {
@@ -445,6 +492,7 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       int st = 0, as = 0, qs = 0;
       uint32_t ph = 0, aph = 0, qph = 0;
       int q_group = -1;
+      long long ai = 0;  // active tiles issued
       Walker W;
       W.init(p, s_g0, s_t0, count);
       bool ok = true;
@@ -472,8 +520,8 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             // +32 bytes along K inside the 128-byte swizzled rows = +2 in the >>4 address field
             umma_e4m3(d_tmem, a_desc + 2 * k, b_desc + 2 * k, idesc, k > 0 ? 1u : 0u);
           }
-          umma_commit(&empty[st]);
-          umma_commit(&acc_full[as]);
+          if ((ai + 1) % C::kCommit == 0) umma_commit(&acc_full[(ai / C::kCommit) % C::kAccFull]);
+          ++ai;
           if (++st == C::kStages) {
             st = 0;
             ph ^= 1u;
@@ -485,18 +533,28 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         }
         W.advance(p);
       }
+      // an unfinished commit group (odd tile count) still needs its commit
+      if (ai % C::kCommit != 0) umma_commit(&acc_full[((ai - 1) / C::kCommit) % C::kAccFull]);
       if (q_group >= 0) umma_commit(&q_empty[qs]);
       (void)ok;
     }
     __syncwarp();
   } else {
     // =========================== epilogue ===========================
+    // kEpiWG warpgroups take the commit groups of active tiles in turn, so
+    // consecutive tiles overlap their TMEM-load / FMA / store latency chains.
+    // Ring positions follow from the active-tile ordinal. Every accumulator
+    // stage and every accumulator-ready barrier belongs to one warpgroup for the
+    // whole kernel (kAccFull is a multiple of kEpiWG), so no barrier is ever
+    // waited on more than one phase ahead.
+    static_assert(C::kAccFull % kEpiWG == 0, "accumulator barriers per warpgroup");
     const int ew = warp - 2;
+    const int wg = ew / 4;
     const int quarter = warp & 3;  // tensor-memory lanes this warp may read
     const int trow = quarter * 32 + lane;
     float* wsm = w_s + ew * NQ * 64;
-    int st = 0, as = 0;
-    uint32_t ph = 0, aph = 0;
+    long long ai = 0;  // active tiles seen
+    long long ti = 0;  // tiles seen
     int cur_g = -1;
     int lim_lo[NQ], lim_hi[NQ];
     Walker W;
@@ -504,7 +562,9 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     const float ninf = -__int_as_float(0x7f800000);
     while (W.left > 0) {
       const Group& G = W.G;
-      if (W.g != cur_g) {
+      const bool active = tile_active(G, W.t);
+      const bool mine = active ? ((ai / C::kCommit) % kEpiWG) == wg : (ti % kEpiWG) == wg;
+      if (mine && W.g != cur_g) {
         cur_g = W.g;
         __syncwarp();
         for (int i = lane; i < NQ * 64; i += 32) {
@@ -539,21 +599,23 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         }
       }
       const int c = W.t * kTile + trow;
-      if (tile_active(G, W.t)) {
+      if (mine && active) {
+        const int st = static_cast<int>(ai % C::kStages);
+        const uint32_t ph = static_cast<uint32_t>((ai / C::kStages) & 1);
+        const int as = static_cast<int>(ai % C::kAccStages);
+        const long long cg = ai / C::kCommit;
+        const int af = static_cast<int>(cg % C::kAccFull);
+        const uint32_t afph = static_cast<uint32_t>((cg / C::kAccFull) & 1);
         bool got = wait_bar(&full[st], ph, abort_flag, 6u);
         if (!__all_sync(0xFFFFFFFFu, got)) break;
         const int box = trow / p.unit;
         const float scale = *reinterpret_cast<const float*>(
             sc_s + st * kScaleStageBytes + box * p.scale_slot + (trow - box * p.unit) * 4);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[st]);
-        if (++st == C::kStages) {
-          st = 0;
-          ph ^= 1u;
-        }
-        got = wait_bar(&acc_full[as], aph, abort_flag, 7u);
+        got = wait_bar(&acc_full[af], afph, abort_flag, 7u);
         if (!__all_sync(0xFFFFFFFFu, got)) break;
         tc_fence_after();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);  // the MMAs of this tile are done with the stage
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                static_cast<uint32_t>(as * C::N);
 #pragma unroll
@@ -565,24 +627,27 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             tmem_wait_ld(a0);
             reg_fence(a1);
             const float4* w4 = reinterpret_cast<const float4*>(wsm + j * 64);
-            float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            float sacc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int h = 0; h < 32; h += 4) {
               const float4 wv = w4[h >> 2];
-              s[(h >> 2) & 7] = fmaf(wv.x, __uint_as_float(a0[h + 0]), s[(h >> 2) & 7]);
-              s[(h >> 2) & 7] = fmaf(wv.y, __uint_as_float(a0[h + 1]), s[(h >> 2) & 7]);
-              s[(h >> 2) & 7] = fmaf(wv.z, __uint_as_float(a0[h + 2]), s[(h >> 2) & 7]);
-              s[(h >> 2) & 7] = fmaf(wv.w, __uint_as_float(a0[h + 3]), s[(h >> 2) & 7]);
+              float& a = sacc[(h >> 2) & 7];
+              a = fmaf(wv.x, __uint_as_float(a0[h + 0]), a);
+              a = fmaf(wv.y, __uint_as_float(a0[h + 1]), a);
+              a = fmaf(wv.z, __uint_as_float(a0[h + 2]), a);
+              a = fmaf(wv.w, __uint_as_float(a0[h + 3]), a);
             }
 #pragma unroll
             for (int h = 0; h < 32; h += 4) {
               const float4 wv = w4[(32 + h) >> 2];
-              s[(h >> 2) & 7] = fmaf(wv.x, __uint_as_float(a1[h + 0]), s[(h >> 2) & 7]);
-              s[(h >> 2) & 7] = fmaf(wv.y, __uint_as_float(a1[h + 1]), s[(h >> 2) & 7]);
-              s[(h >> 2) & 7] = fmaf(wv.z, __uint_as_float(a1[h + 2]), s[(h >> 2) & 7]);
-              s[(h >> 2) & 7] = fmaf(wv.w, __uint_as_float(a1[h + 3]), s[(h >> 2) & 7]);
+              float& a = sacc[(h >> 2) & 7];
+              a = fmaf(wv.x, __uint_as_float(a1[h + 0]), a);
+              a = fmaf(wv.y, __uint_as_float(a1[h + 1]), a);
+              a = fmaf(wv.z, __uint_as_float(a1[h + 2]), a);
+              a = fmaf(wv.w, __uint_as_float(a1[h + 3]), a);
             }
-            const float sum = ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
+            const float sum =
+                ((sacc[0] + sacc[1]) + (sacc[2] + sacc[3])) + ((sacc[4] + sacc[5]) + (sacc[6] + sacc[7]));
             const float logit = sum * scale;
             if (c < G.ncols) {
               const float v = (c >= lim_lo[j] && c < lim_hi[j]) ? logit : ninf;
@@ -598,11 +663,7 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[as]);
-        if (++as == C::kAccStages) {
-          as = 0;
-          aph ^= 1u;
-        }
-      } else if (c < G.ncols) {
+      } else if (mine && c < G.ncols) {
 #pragma unroll
         for (int j = 0; j < NQ; ++j) {
           if (j < G.nq) {
@@ -615,6 +676,8 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
           }
         }
       }
+      ai += active ? 1 : 0;
+      ++ti;
       W.advance(p);
     }
   }
@@ -739,6 +802,8 @@ extern "C" idx_status_t idx_paged_mqa_logits_decode(
   p.w_bf16 = w_dtype == IDX_BF16;
   p.ld_w = ld_w;
   p.paged = 1;
+  p.kv_base = cache;
+  p.kv_block_stride = block_stride_bytes;
   p.block_size = block_size;
   p.block_table = block_table;
   p.ld_bt = ld_bt;
@@ -830,6 +895,8 @@ extern "C" idx_status_t idx_mqa_logits_prefill(const uint8_t* q, int64_t ld_q, c
   p.w_bf16 = w_dtype == IDX_BF16;
   p.ld_w = ld_w;
   p.paged = 0;
+  p.kv_base = k8;
+  p.kv_block_stride = 0;
   p.block_size = 1;
   p.S = S;
   p.row_ks = row_ks;

@@ -164,6 +164,8 @@ __device__ __forceinline__ void visit(const TopkParams& p, Shared& sh, int row, 
   const bool in = valid && prefix_match(key, prefix, level);
   const int d = in ? digit(key, level) : -1;
   const int thr = sh.thr;
+  // most elements fall below the threshold digit: skip the reservations warp-wide
+  if (!__any_sync(0xFFFFFFFFu, d >= thr)) return;
   const bool above = in && d > thr;
   const bool tie = in && d == thr;
   const int s = warp_reserve(&sh.n_out, above);
@@ -182,6 +184,57 @@ __device__ __forceinline__ void visit(const TopkParams& p, Shared& sh, int row, 
     if (tie && t < sh.need) {
       const int slot = atomicAdd(&sh.n_out, 1);
       store_one<kRemap>(p, row, lo, base_blk, slot, col);
+    }
+  }
+}
+
+// Calls f(valid, column, key) for every column of [lo, hi), uniformly across
+// every warp of the block (f may use warp collectives). The aligned middle is
+// read with 16-byte loads, four per thread in flight; the unaligned head and
+// tail (fewer than one vector each) are read element by element.
+template <bool kBf16, typename F>
+__device__ __forceinline__ void sweep_row(const void* rowp, int64_t lo, int64_t hi, F&& f) {
+  constexpr int kVec = kBf16 ? 8 : 4;
+  constexpr int kEsz = kBf16 ? 2 : 4;
+  constexpr int kUnroll = 4;
+  const int tid = threadIdx.x;
+  const uintptr_t base = reinterpret_cast<uintptr_t>(rowp);
+  int64_t a1 = lo + (kVec - static_cast<int64_t>(((base / kEsz) + lo) % kVec)) % kVec;
+  if (a1 > hi) a1 = hi;
+  const int64_t nvec = (hi - a1) / kVec;
+  const int64_t a2 = a1 + nvec * kVec;
+  // head [lo, a1) and tail [a2, hi): at most 2 * (kVec - 1) elements
+  {
+    const int nh = static_cast<int>(a1 - lo);
+    const int nt = static_cast<int>(hi - a2);
+    const bool valid = tid < nh + nt;
+    const int64_t c = tid < nh ? lo + tid : a2 + (tid - nh);
+    f(valid, c, valid ? key_at<kBf16>(rowp, c) : 0u);
+  }
+  const uint4* vp = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(rowp) + a1 * kEsz);
+  for (int64_t v0 = 0; v0 < nvec; v0 += static_cast<int64_t>(kThreads) * kUnroll) {
+    uint4 r[kUnroll];
+#pragma unroll
+    for (int j = 0; j < kUnroll; ++j) {
+      const int64_t v = v0 + j * kThreads + tid;
+      r[j] = v < nvec ? __ldg(vp + v) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int j = 0; j < kUnroll; ++j) {
+      const int64_t v = v0 + j * kThreads + tid;
+      const bool valid = v < nvec;
+      const int64_t c = a1 + v * kVec;
+      const uint32_t w[4] = {r[j].x, r[j].y, r[j].z, r[j].w};
+#pragma unroll
+      for (int e = 0; e < kVec; ++e) {
+        uint32_t key;
+        if constexpr (kBf16) {
+          key = f32_key(((w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu) << 16);
+        } else {
+          key = f32_key(w[e]);
+        }
+        f(valid, c + e, key);
+      }
     }
   }
 }
@@ -240,22 +293,17 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p) {
   __syncthreads();
 
   // level-0 histogram straight from global memory
-  const int64_t iters = (n + kThreads - 1) / kThreads;
-  for (int64_t it = 0; it < iters; ++it) {
-    const int64_t c = lo + it * kThreads + tid;
-    if (c < hi) atomicAdd(&sh.hist[0][digit(key_at<kBf16>(rowp, c), 0)], 1u);
-  }
+  sweep_row<kBf16>(rowp, lo, hi, [&](bool valid, int64_t, uint32_t key) {
+    if (valid) atomicAdd(&sh.hist[0][key >> 21], 1u);
+  });
   __syncthreads();
   find_threshold(sh, sh.hist[0], kBins);
 
   // level 0: store digit > thr, collect the tie bucket into A, histogram its next digit
-  for (int64_t it = 0; it < iters; ++it) {
-    const int64_t c = lo + it * kThreads + tid;
-    const bool valid = c < hi;
-    const uint32_t key = valid ? key_at<kBf16>(rowp, c) : 0u;
+  sweep_row<kBf16>(rowp, lo, hi, [&](bool valid, int64_t c, uint32_t key) {
     visit<kRemap>(p, sh, row, lo, base_blk, 0, 0u, valid, key, c, keys_a, cols_a, &sh.n_a, kCapA,
                   sh.hist[1]);
-  }
+  });
   uint32_t prefix = static_cast<uint32_t>(sh.thr) << 21;
   __syncthreads();
   for (int i = tid; i < kBins; i += kThreads) sh.hist[0][i] = 0;  // free since level 0 is done
@@ -273,13 +321,10 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p) {
                     valid ? cols_a[i] : 0, keys_b, cols_b, &sh.n_b, kCapB, sh.hist[0]);
     }
   } else {
-    for (int64_t it = 0; it < iters; ++it) {
-      const int64_t c = lo + it * kThreads + tid;
-      const bool valid = c < hi;
-      const uint32_t key = valid ? key_at<kBf16>(rowp, c) : 0u;
+    sweep_row<kBf16>(rowp, lo, hi, [&](bool valid, int64_t c, uint32_t key) {
       visit<kRemap>(p, sh, row, lo, base_blk, 1, prefix, valid, key, c, keys_b, cols_b, &sh.n_b,
                     kCapB, sh.hist[0]);
-    }
+    });
   }
   __syncthreads();
   find_threshold(sh, sh.hist[0], kBins / 2);
@@ -303,13 +348,10 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p) {
                     valid ? cols_a[i] : 0, nullptr, nullptr, nullptr, 0, nullptr);
     }
   } else {
-    for (int64_t it = 0; it < iters; ++it) {
-      const int64_t c = lo + it * kThreads + tid;
-      const bool valid = c < hi;
-      const uint32_t key = valid ? key_at<kBf16>(rowp, c) : 0u;
-      visit<kRemap>(p, sh, row, lo, base_blk, 2, prefix, valid, key, c, nullptr, nullptr,
-                    nullptr, 0, nullptr);
-    }
+    sweep_row<kBf16>(rowp, lo, hi, [&](bool valid, int64_t c, uint32_t key) {
+      visit<kRemap>(p, sh, row, lo, base_blk, 2, prefix, valid, key, c, nullptr, nullptr, nullptr,
+                    0, nullptr);
+    });
   }
 }
 

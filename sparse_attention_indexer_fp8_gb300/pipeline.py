@@ -18,18 +18,30 @@ from . import (idx_expand_candidates, idx_k_quant_and_cache, idx_paged_mqa_logit
 from . import workloads as W
 
 
-def fill_paged_cache(pool: W.PagedPool, seed: int, cache: torch.Tensor, chunk_tokens: int = 1 << 21,
-                     stream=None) -> None:
-    """Quantise and insert every request's k (drawn by ``workloads.make_k``) into ``cache``."""
+def fill_paged_cache(pool: W.PagedPool, seed: int, cache: torch.Tensor, device_k: bool = False,
+                     chunk_tokens: int = 1 << 21, stream=None) -> None:
+    """Quantise and insert every request's k into ``cache`` through ``idx_k_quant_and_cache``.
+
+    k comes from ``workloads.make_k`` (host generator) or, with ``device_k``,
+    from ``workloads.make_k_device`` (for pools too large to draw on the host).
+    """
     dev = cache.device
+    if device_k:
+        for b in range(len(pool.ctx_lens)):
+            L = int(pool.ctx_lens[b])
+            k = W.make_k_device(seed, b, L, dev)
+            s = torch.from_numpy(pool.slot_mapping(b)).to(dev)
+            idx_k_quant_and_cache(k, s, cache, pool.block_size, stream=stream)
+        torch.cuda.current_stream(dev).synchronize()
+        return
     pend_k, pend_s, n = [], [], 0
 
     def flush():
         nonlocal pend_k, pend_s, n
         if not pend_k:
             return
-        k = torch.from_numpy(np.concatenate(pend_k).view(np.int16)).pin_memory().to(dev, non_blocking=True)
-        s = torch.from_numpy(np.concatenate(pend_s)).pin_memory().to(dev, non_blocking=True)
+        k = torch.from_numpy(np.concatenate(pend_k).view(np.int16)).to(dev)
+        s = torch.from_numpy(np.concatenate(pend_s)).to(dev)
         idx_k_quant_and_cache(k.view(torch.bfloat16), s, cache, pool.block_size, stream=stream)
         torch.cuda.current_stream(dev).synchronize()
         pend_k, pend_s, n = [], [], 0

@@ -71,6 +71,21 @@ def make_k(seed: int, request: int, n_tok: int) -> np.ndarray:
     return k.view(torch.int16).numpy().view(np.uint16)
 
 
+def make_k_device(seed: int, request: int, n_tok: int, device) -> torch.Tensor:
+    """k of one request drawn on the device (torch's CUDA generator): bf16 [n_tok, 128], N(0, 1).
+
+    For pools too large to draw on the host. Deterministic for a given seed,
+    request and PyTorch build; a checker that needs the same k calls this
+    function again and copies the result to the host.
+    """
+    g = torch.Generator(device=device)
+    s = int(seed)
+    for x in (8, request):
+        s = (s * 1_000_003 + int(x) + 1) % (2**62)
+    g.manual_seed(s)
+    return torch.randn(n_tok, D, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+
+
 def make_random_cache_tokens(seed: int, n_tok: int):
     """Directly drawn cache contents (k8 uint8 [n, 128] without NaN codes, kscale f32 [n])."""
     g = _gen(seed, 3)
