@@ -223,19 +223,24 @@ def run_decode(args, rank, world, local, dist):
     new_k = torch.stack([W.make_k_device(wl.seed, b, int(L[b]), dev)[-1] for b in range(B)])
     new_slots = torch.from_numpy(np.array([pool.slot_mapping(b)[-1] for b in range(B)])).to(dev)
     L_max = int(L.max())
-    logits = torch.empty((B, L_max), dtype=torch.float32, device=dev)
+    ld = (L_max + 63) // 64 * 64          # 256-byte aligned rows for the selection's vector loads
+    logits = torch.empty((B, ld), dtype=torch.float32, device=dev)
     local_idx = torch.empty((B, wl.topk), dtype=torch.int32, device=dev)
     slots = torch.empty((B, wl.topk), dtype=torch.int32, device=dev)
+    # selection workspace: the logits kernel histograms each row's first radix
+    # digit, the top-k consumes and re-zeroes it
+    ws = torch.zeros((B, 1024), dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step(ev=None):
         idx.idx_k_quant_and_cache(new_k, new_slots, cache, pool.block_size, stream=stream)
         if ev is not None:
             ev[0].record(stream)
-        idx.idx_paged_mqa_logits_decode(q, w, cache, pool.block_size, bt, ctx, logits, stream=stream)
+        idx.idx_paged_mqa_logits_decode(q, w, cache, pool.block_size, bt, ctx, logits, ws=ws,
+                                        stream=stream)
         if ev is not None:
             ev[1].record(stream)
-        idx.idx_topk(logits, None, ctx, wl.topk, local_idx, stream=stream)
+        idx.idx_topk(logits, None, ctx, wl.topk, local_idx, ws=ws, stream=stream)
         idx.idx_req_to_global_slots(local_idx, None, bt, pool.block_size, wl.block_span, slots,
                                     stream=stream)
 

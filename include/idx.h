@@ -33,6 +33,21 @@
  * - idx_last_error() returns a thread-local human-readable message for the most
  *   recent non-OK status.
  *
+ * Selection workspace
+ * -------------------
+ * The top-k's first radix pass histograms the top 10 bits of every score's
+ * order-preserving key. The logits entry points can produce that histogram
+ * while they write the scores, so the selection does not read the scores twice:
+ * pass the same device buffer of idx_workspace_bytes(op, rows, 0, 0) bytes
+ * (1024 uint32 per row, 16-byte aligned) as `ws` to a logits call and then to
+ * idx_topk / idx_sparse_topk_remap over the same rows and the same visible
+ * columns (decode with next_n = 1: columns [0, ctx_len); sparse modes: [0, end)).
+ * The buffer must be all zero before the logits call (clear it once after
+ * allocating it); the selection zeroes every row it consumes, so the buffer is
+ * ready for the next step. Supported by the kernels with one query per group:
+ * dense decode with next_n = 1 and both sparse modes. ws = NULL selects the
+ * two-pass selection.
+ *
  * Paged cache layout (the "split block" layout)
  * ---------------------------------------------
  * Block b starts at byte b * block_stride_bytes of the cache. Token i of a block
@@ -144,8 +159,8 @@ idx_status_t idx_gather_k(const uint8_t* cache, int32_t block_size, int64_t bloc
  *   row_ks   int32 [T] or NULL (all zero); row_ke int32 [T] (dense mode).
  *   sbk      8, 16, 32, 64 or 128 (sparse mode).
  *   logits   [T, ld_out] of out_dtype (IDX_F32 or IDX_BF16).
- *   ws       workspace (idx_workspace_bytes(IDX_OP_MQA_LOGITS_PREFILL, ...) bytes;
- *            currently 0, may be NULL).
+ *   ws       NULL, or the selection workspace (see "Selection workspace" below);
+ *            sparse mode only.
  * Errors: IDX_ERR_INVALID_ARG for NULL / negative / too-small strides;
  * IDX_ERR_UNSUPPORTED for misaligned q, k8 or kscale, or an sbk outside the set.
  */
@@ -180,6 +195,7 @@ idx_status_t idx_mqa_logits_prefill(const uint8_t* q, int64_t ld_q, const void* 
  *   block_table        int32 [B, ld_bt]: physical block of each logical block.
  *   ctx_lens           int32 [B].
  *   next_n             1, 2 or 4 in dense mode; any value >= 1 in sparse mode.
+ *   ws                 NULL, or the selection workspace (next_n = 1 or sparse mode).
  *   logits             [B * next_n, ld_out] of out_dtype; dense mode needs
  *                      ld_out >= max(ctx_lens) (not checked: ctx_lens is device data).
  *   block_table rows must cover ceil(ctx_lens[b] / block_size) blocks, and every
@@ -212,7 +228,8 @@ idx_status_t idx_paged_mqa_logits_decode(const uint8_t* q, int64_t ld_q, const v
  *   logits   [rows, ld] of dtype (IDX_F32 or IDX_BF16).
  *   row_ks   int32 [rows] or NULL (all zero); row_ke int32 [rows].
  *   out      int32 [rows, ld_out], ld_out >= k.
- *   ws       idx_workspace_bytes(IDX_OP_TOPK, rows, max_cols, k) bytes (0 now).
+ *   ws       NULL, or the selection workspace filled by the logits call that
+ *            wrote `logits` (consumed and zeroed).
  * Errors: IDX_ERR_INVALID_ARG for NULL pointers, k < 1, ld_out < k;
  * IDX_ERR_UNSUPPORTED for k > 4096.
  */
@@ -303,7 +320,7 @@ idx_status_t idx_req_to_global_slots(const int32_t* local, int64_t ld_l, int32_t
  */
 idx_status_t idx_block_span(int64_t block_stride, int64_t token_stride, int32_t* span);
 
-/* Workspace bytes an operation needs for the given sizes (host only). */
+/* Bytes of the optional selection workspace of an operation for `rows` rows (host only). */
 size_t idx_workspace_bytes(int op, int32_t rows, int32_t max_cols, int32_t k);
 
 /* Static description of a status code (host only). */

@@ -101,11 +101,18 @@ const char* idx_status_string(idx_status_t status) {
 const char* idx_last_error(void) { return idx::g_last_error; }
 
 size_t idx_workspace_bytes(int op, int32_t rows, int32_t max_cols, int32_t k) {
-  (void)op;
-  (void)rows;
   (void)max_cols;
   (void)k;
-  return 0;
+  switch (op) {
+    case IDX_OP_MQA_LOGITS_PREFILL:
+    case IDX_OP_PAGED_MQA_LOGITS_DECODE:
+    case IDX_OP_TOPK:
+    case IDX_OP_SPARSE_TOPK_REMAP:
+      // optional first-digit histogram: 1024 uint32 counters per row
+      return rows > 0 ? static_cast<size_t>(rows) * 1024 * sizeof(uint32_t) : 0;
+    default:
+      return 0;
+  }
 }
 
 idx_status_t idx_block_span(int64_t block_stride, int64_t token_stride, int32_t* span) {

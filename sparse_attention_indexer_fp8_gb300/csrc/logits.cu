@@ -91,12 +91,17 @@ struct LogitsParams {
   void* out;
   int out_bf16;
   int64_t ld_out;
+  // optional: per-row histogram of the top 10 key bits of every visible logit
+  // (kHistBins uint32 per row), accumulated for the selection's first digit
+  uint32_t* hist;
 };
+
+constexpr int kHistBins = 1024;  // first selection digit: the top 10 bits of the order-preserving key
 
 template <int NQ>
 struct Cfg {
   static constexpr int N = 64 * NQ;
-  static constexpr int kStages = NQ == 1 ? 11 : (NQ == 2 ? 10 : 8);
+  static constexpr int kStages = NQ == 1 ? 10 : (NQ == 2 ? 10 : 8);
   static constexpr int kAccStages = NQ == 4 ? 2 : 4;
   // tiles per tcgen05.commit: one commit covers the MMAs of kCommit consecutive
   // tiles (commits are costly next to a 4-MMA tile); one accumulator-ready
@@ -109,7 +114,10 @@ struct Cfg {
   static constexpr int kOffQ = kOffKv + kStages * kKvStageBytes;
   static constexpr int kOffScale = kOffQ + 2 * kQStageBytes;
   static constexpr int kOffW = kOffScale + kStages * kScaleStageBytes;
-  static constexpr int kOffBar = kOffW + kEpiWarps * NQ * 64 * 4;
+  // per epilogue warp, one query per group: 1024 bins of 16-bit counts
+  static constexpr int kHistWords = NQ == 1 ? kHistBins / 2 : 0;
+  static constexpr int kOffHist = kOffW + kEpiWarps * NQ * 64 * 4;
+  static constexpr int kOffBar = kOffHist + kEpiWarps * kHistWords * 4;
   static constexpr int kNumBars = 2 * kStages + kAccFull + kAccStages + 4;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 1024;  // + alignment slack
   static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -268,6 +276,42 @@ __device__ __forceinline__ Box box_at(const LogitsParams& p, int row0, int req, 
   return b;
 }
 
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+__device__ __forceinline__ void fma2(uint64_t& acc, uint64_t a, uint64_t b) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+
+__device__ __forceinline__ float hsum2(uint64_t v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return lo + hi;
+}
+
+// sum_h w[h] * acc[h] over the 64 head columns of one query (a0: heads 0-31,
+// a1: heads 32-63), with the packed two-lane fp32 FMA of sm_100+: half the FMA
+// instructions of the scalar form, four independent two-lane accumulators.
+template <typename WFn>
+__device__ __forceinline__ float weighted_head_sum(const uint32_t (&a0)[32], const uint32_t (&a1)[32],
+                                                   WFn w) {
+  uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+  for (int h = 0; h < 32; h += 2) {
+    fma2(acc[(h >> 1) & 3], pack2(__uint_as_float(a0[h]), __uint_as_float(a0[h + 1])),
+         pack2(w(h), w(h + 1)));
+  }
+#pragma unroll
+  for (int h = 0; h < 32; h += 2) {
+    fma2(acc[(h >> 1) & 3], pack2(__uint_as_float(a1[h]), __uint_as_float(a1[h + 1])),
+         pack2(w(32 + h), w(33 + h)));
+  }
+  return (hsum2(acc[0]) + hsum2(acc[1])) + (hsum2(acc[2]) + hsum2(acc[3]));
+}
+
 template <int NQ>
 __global__ void __launch_bounds__(kThreads, 1)
 mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_kv,
@@ -279,6 +323,7 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   uint8_t* q_s = smem + C::kOffQ;
   uint8_t* sc_s = smem + C::kOffScale;
   float* w_s = reinterpret_cast<float*>(smem + C::kOffW);
+  uint32_t* hist_s = reinterpret_cast<uint32_t*>(smem + C::kOffHist);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* full = bars;
   uint64_t* empty = bars + C::kStages;
@@ -553,10 +598,39 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     const int quarter = warp & 3;  // tensor-memory lanes this warp may read
     const int trow = quarter * 32 + lane;
     float* wsm = w_s + ew * NQ * 64;
+    // private histogram of this warp's visible logits for the current group;
+    // flushed to the row's global histogram when the warp moves to another group
+    uint32_t* wh = hist_s + ew * C::kHistWords;
+    const bool do_hist = C::kHistWords > 0 && p.hist != nullptr;
+    int hist_row = -1;
+    int hist_tiles = 0;  // tiles counted since the last flush: 16-bit bins hold < 2048 tiles
+    if (do_hist) {
+      for (int i = lane; i < C::kHistWords; i += 32) wh[i] = 0;
+      __syncwarp();
+    }
+    auto flush_hist = [&]() {
+      if (!do_hist || hist_row < 0) return;
+      __syncwarp();
+      uint32_t* g = p.hist + static_cast<int64_t>(hist_row) * kHistBins;
+      for (int i = lane; i < C::kHistWords; i += 32) {
+        const uint32_t v = wh[i];
+        if (v) {
+          if (v & 0xFFFFu) atomicAdd(g + 2 * i, v & 0xFFFFu);
+          if (v >> 16) atomicAdd(g + 2 * i + 1, v >> 16);
+          wh[i] = 0;
+        }
+      }
+      __syncwarp();
+      hist_row = -1;
+      hist_tiles = 0;
+    };
     long long ai = 0;  // active tiles seen
     long long ti = 0;  // tiles seen
     int cur_g = -1;
     int lim_lo[NQ], lim_hi[NQ];
+    // one query per group: its 64 weights live in registers for the whole group
+    constexpr bool kRegW = NQ == 1;
+    float wreg[kRegW ? 64 : 1];
     Walker W;
     W.init(p, s_g0, s_t0, count);
     const float ninf = -__int_as_float(0x7f800000);
@@ -565,6 +639,7 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       const bool active = tile_active(G, W.t);
       const bool mine = active ? ((ai / C::kCommit) % kEpiWG) == wg : (ti % kEpiWG) == wg;
       if (mine && W.g != cur_g) {
+        flush_hist();
         cur_g = W.g;
         __syncwarp();
         for (int i = lane; i < NQ * 64; i += 32) {
@@ -581,6 +656,10 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
           wsm[i] = v;
         }
         __syncwarp();
+        if constexpr (kRegW) {
+#pragma unroll
+          for (int i = 0; i < 64; ++i) wreg[i] = wsm[i];
+        }
 #pragma unroll
         for (int j = 0; j < NQ; ++j) {
           int lo = 0, hi = 0;
@@ -618,51 +697,61 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         if (lane == 0) mbar_arrive(&empty[st]);  // the MMAs of this tile are done with the stage
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                static_cast<uint32_t>(as * C::N);
+        // The weighted head sum of every query is reduced into registers first;
+        // the accumulator is handed back to the MMA warp before any global store,
+        // so the release (which orders this thread's earlier writes) never waits
+        // on the logits stores.
+        float logit[NQ];
 #pragma unroll
         for (int j = 0; j < NQ; ++j) {
+          logit[j] = 0.f;
           if (j < G.nq) {
             uint32_t a0[32], a1[32];
             tmem_ld_x32(taddr + j * 64, a0);
             tmem_ld_x32(taddr + j * 64 + 32, a1);
             tmem_wait_ld(a0);
             reg_fence(a1);
-            const float4* w4 = reinterpret_cast<const float4*>(wsm + j * 64);
-            float sacc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int h = 0; h < 32; h += 4) {
-              const float4 wv = w4[h >> 2];
-              float& a = sacc[(h >> 2) & 7];
-              a = fmaf(wv.x, __uint_as_float(a0[h + 0]), a);
-              a = fmaf(wv.y, __uint_as_float(a0[h + 1]), a);
-              a = fmaf(wv.z, __uint_as_float(a0[h + 2]), a);
-              a = fmaf(wv.w, __uint_as_float(a0[h + 3]), a);
+            float sum;
+            if constexpr (kRegW) {
+              sum = weighted_head_sum(a0, a1, [&](int h) { return wreg[h]; });
+            } else {
+              const float* wj = wsm + j * 64;
+              sum = weighted_head_sum(a0, a1, [&](int h) { return wj[h]; });
             }
-#pragma unroll
-            for (int h = 0; h < 32; h += 4) {
-              const float4 wv = w4[(32 + h) >> 2];
-              float& a = sacc[(h >> 2) & 7];
-              a = fmaf(wv.x, __uint_as_float(a1[h + 0]), a);
-              a = fmaf(wv.y, __uint_as_float(a1[h + 1]), a);
-              a = fmaf(wv.z, __uint_as_float(a1[h + 2]), a);
-              a = fmaf(wv.w, __uint_as_float(a1[h + 3]), a);
-            }
-            const float sum =
-                ((sacc[0] + sacc[1]) + (sacc[2] + sacc[3])) + ((sacc[4] + sacc[5]) + (sacc[6] + sacc[7]));
-            const float logit = sum * scale;
-            if (c < G.ncols) {
-              const float v = (c >= lim_lo[j] && c < lim_hi[j]) ? logit : ninf;
-              const int64_t o = static_cast<int64_t>(G.row0 + j) * p.ld_out + c;
-              if (p.out_bf16) {
-                reinterpret_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(v);
-              } else {
-                reinterpret_cast<float*>(p.out)[o] = v;
-              }
-            }
+            logit[j] = sum * scale;
           }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[as]);
+        if (c < G.ncols) {
+#pragma unroll
+          for (int j = 0; j < NQ; ++j) {
+            if (j < G.nq) {
+              const bool vis = c >= lim_lo[j] && c < lim_hi[j];
+              const float v = vis ? logit[j] : ninf;
+              const int64_t o = static_cast<int64_t>(G.row0 + j) * p.ld_out + c;
+              uint32_t bits;
+              if (p.out_bf16) {
+                const __nv_bfloat16 b = __float2bfloat16_rn(v);
+                reinterpret_cast<__nv_bfloat16*>(p.out)[o] = b;
+                bits = static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16;
+              } else {
+                reinterpret_cast<float*>(p.out)[o] = v;
+                bits = __float_as_uint(v);
+              }
+              if (do_hist && vis) {
+                // the key of the value as stored, so the selection sees the same digit
+                const uint32_t bin = f32_key(bits) >> 22;
+                atomicAdd(wh + (bin >> 1), 1u << ((bin & 1u) * 16));
+              }
+            }
+          }
+        }
+        if (do_hist) {
+          hist_row = G.row0;  // warp-uniform: every lane of the warp sets it
+          if (++hist_tiles == 2047) flush_hist();
+        }
       } else if (mine && c < G.ncols) {
 #pragma unroll
         for (int j = 0; j < NQ; ++j) {
@@ -680,6 +769,7 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       ++ti;
       W.advance(p);
     }
+    flush_hist();
   }
 
   tc_fence_before();
@@ -747,6 +837,26 @@ idx_status_t check_common(const char* fn, const uint8_t* q, int64_t ld_q, const 
   return IDX_OK;
 }
 
+// The optional workspace receives, per output row, the histogram of the top 10
+// bits of the order-preserving key of every visible logit (the first digit of
+// the selection); it must be zero on entry. Kernels with one query per group
+// accumulate it.
+idx_status_t attach_histogram(const char* fn, LogitsParams* p, int nq_tmpl, int rows, void* ws,
+                              size_t ws_bytes) {
+  if (!ws) return IDX_OK;
+  if (nq_tmpl != 1) {
+    return fail(IDX_ERR_UNSUPPORTED,
+                "%s: the histogram workspace needs one query per group (next_n 1 or sparse mode)", fn);
+  }
+  const size_t need = static_cast<size_t>(rows) * kHistBins * sizeof(uint32_t);
+  if (ws_bytes < need) {
+    return fail(IDX_ERR_INVALID_ARG, "%s: workspace of %zu bytes, %zu needed", fn, ws_bytes, need);
+  }
+  if (!aligned(ws, 16)) return fail(IDX_ERR_UNSUPPORTED, "%s: workspace must be 16-byte aligned", fn);
+  p->hist = static_cast<uint32_t*>(ws);
+  return IDX_OK;
+}
+
 bool sbk_ok(int32_t sbk) { return sbk == 8 || sbk == 16 || sbk == 32 || sbk == 64 || sbk == 128; }
 
 }  // namespace
@@ -772,8 +882,6 @@ extern "C" idx_status_t idx_paged_mqa_logits_decode(
     int64_t ld_bt, const int32_t* ctx_lens, int32_t B, int32_t next_n, const int32_t* sparse_idx,
     int64_t ld_si, int32_t n_si, const int32_t* end, int32_t sbk, void* logits, int out_dtype,
     int64_t ld_out, void* ws, size_t ws_bytes, cudaStream_t stream) {
-  (void)ws;
-  (void)ws_bytes;
   const char* fn = "idx_paged_mqa_logits_decode";
   if (B < 0 || next_n < 1) return fail(IDX_ERR_INVALID_ARG, "%s: B < 0 or next_n < 1", fn);
   if (B == 0) return IDX_OK;
@@ -843,6 +951,8 @@ extern "C" idx_status_t idx_paged_mqa_logits_decode(
     nq_tmpl = next_n;
   }
   p.scale_slot = p.unit * 4 < 128 ? 128 : p.unit * 4;
+  st = attach_histogram(fn, &p, nq_tmpl, rows, ws, ws_bytes);
+  if (st != IDX_OK) return st;
 
   CUtensorMap mq, mkv, msc;
   st = make_q_map(&mq, q, ld_q, rows, nq_tmpl);
@@ -876,8 +986,6 @@ extern "C" idx_status_t idx_mqa_logits_prefill(const uint8_t* q, int64_t ld_q, c
                                                int32_t n_si, const int32_t* end, int32_t sbk,
                                                void* logits, int out_dtype, int64_t ld_out,
                                                void* ws, size_t ws_bytes, cudaStream_t stream) {
-  (void)ws;
-  (void)ws_bytes;
   const char* fn = "idx_mqa_logits_prefill";
   if (T < 0 || S < 0) return fail(IDX_ERR_INVALID_ARG, "%s: negative T or S", fn);
   if (T == 0) return IDX_OK;
@@ -933,6 +1041,8 @@ extern "C" idx_status_t idx_mqa_logits_prefill(const uint8_t* q, int64_t ld_q, c
     nq_tmpl = 4;
   }
   p.scale_slot = p.unit * 4 < 128 ? 128 : p.unit * 4;
+  st = attach_histogram(fn, &p, nq_tmpl, T, ws, ws_bytes);
+  if (st != IDX_OK) return st;
   CUtensorMap mq, mkv, msc;
   st = make_q_map(&mq, q, ld_q, T, nq_tmpl);
   if (st != IDX_OK) return st;

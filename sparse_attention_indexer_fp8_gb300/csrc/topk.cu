@@ -26,7 +26,8 @@ namespace idx {
 namespace {
 
 constexpr int kThreads = 1024;
-constexpr int kBins = 2048;
+constexpr int kBins = 2048;      // bins of the second and third digits (11 bits each)
+constexpr int kBins0 = 1024;     // bins of the first digit (the top 10 key bits)
 constexpr int kCapA = 12288;  // tie bucket of level 0 (collected from global memory)
 constexpr int kCapB = 4096;   // tie bucket of level 1 (collected from bucket A)
 constexpr int kSmemDyn = (kCapA + kCapB) * 8;
@@ -46,6 +47,7 @@ struct TopkParams {
   int64_t ld_out;
   int32_t* cols;           // remap: optional chosen columns
   int64_t ld_cols;
+  uint32_t* hist;          // optional: precomputed first-digit histogram per row (kBins0 each)
 };
 
 template <bool kBf16>
@@ -57,16 +59,17 @@ __device__ __forceinline__ uint32_t key_at(const void* row, int64_t c) {
   }
 }
 
+// Digits of the key, most significant first: bits 31-22, 21-11, 10-0.
 __device__ __forceinline__ int digit(uint32_t key, int level) {
-  return level == 0 ? static_cast<int>(key >> 21)
-                    : (level == 1 ? static_cast<int>((key >> 10) & 0x7FF)
-                                  : static_cast<int>(key & 0x3FF));
+  return level == 0 ? static_cast<int>(key >> 22)
+                    : (level == 1 ? static_cast<int>((key >> 11) & 0x7FF)
+                                  : static_cast<int>(key & 0x7FF));
 }
 
 // True when the bits of `key` above `level` equal those of `prefix`.
 __device__ __forceinline__ bool prefix_match(uint32_t key, uint32_t prefix, int level) {
   if (level == 0) return true;
-  const uint32_t mask = level == 1 ? 0xFFE00000u : 0xFFFFFC00u;
+  const uint32_t mask = level == 1 ? 0xFFC00000u : 0xFFFFF800u;
   return (key & mask) == (prefix & mask);
 }
 
@@ -169,7 +172,7 @@ __device__ __forceinline__ void visit(const TopkParams& p, Shared& sh, int row, 
   const bool above = in && d > thr;
   const bool tie = in && d == thr;
   const int s = warp_reserve(&sh.n_out, above);
-  if (above) store_one<kRemap>(p, row, lo, base_blk, s, col);
+  if (above && s < p.k) store_one<kRemap>(p, row, lo, base_blk, s, col);
   if (level < 2) {
     if (next_keys) {
       const int t = warp_reserve(next_n, tie);
@@ -183,7 +186,7 @@ __device__ __forceinline__ void visit(const TopkParams& p, Shared& sh, int row, 
     const int t = warp_reserve(&sh.n_tie, tie);
     if (tie && t < sh.need) {
       const int slot = atomicAdd(&sh.n_out, 1);
-      store_one<kRemap>(p, row, lo, base_blk, slot, col);
+      if (slot < p.k) store_one<kRemap>(p, row, lo, base_blk, slot, col);
     }
   }
 }
@@ -239,6 +242,97 @@ __device__ __forceinline__ void sweep_row(const void* rowp, int64_t lo, int64_t 
   }
 }
 
+// Exclusive prefix sum of v over the warp; *total receives the warp's sum.
+__device__ __forceinline__ int warp_excl_scan(int v, int* total) {
+  const int lane = threadIdx.x & 31;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  *total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+  return incl - v;
+}
+
+// The level-0 pass over the aligned body of the row, batched: every thread
+// classifies the 16 elements it loaded (above the threshold digit, tied with
+// it, or below), and one warp scan per class reserves output / bucket slots for
+// all of them. Most elements are below the threshold and cost a handful of
+// integer operations; the collectives are paid once per 16 elements.
+template <bool kBf16, bool kRemap>
+__device__ __forceinline__ void level0_body(const TopkParams& p, Shared& sh, int row, int64_t lo,
+                                            int64_t base_blk, const void* rowp, int64_t a1,
+                                            int64_t nvec, uint32_t* keys_a, int32_t* cols_a) {
+  constexpr int kVec = kBf16 ? 8 : 4;
+  constexpr int kEsz = kBf16 ? 2 : 4;
+  constexpr int kUnroll = kBf16 ? 2 : 4;
+  constexpr int kPer = kVec * kUnroll;  // 16 elements per thread per step
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int thr = sh.thr;
+  const uint4* vp = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(rowp) + a1 * kEsz);
+  for (int64_t v0 = 0; v0 < nvec; v0 += static_cast<int64_t>(kThreads) * kUnroll) {
+    uint32_t key[kPer];
+    int n_ab = 0, n_tie = 0;
+#pragma unroll
+    for (int j = 0; j < kUnroll; ++j) {
+      const int64_t v = v0 + j * kThreads + tid;
+      const uint4 r = v < nvec ? __ldg(vp + v) : make_uint4(0, 0, 0, 0);
+      const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+      for (int e = 0; e < kVec; ++e) {
+        uint32_t k;
+        if constexpr (kBf16) {
+          k = f32_key(((w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu) << 16);
+        } else {
+          k = f32_key(w[e]);
+        }
+        // out-of-range vectors get key 0, whose digit 0 is never above any threshold
+        // and is only a tie when the threshold digit itself is 0 (guarded below)
+        key[j * kVec + e] = v < nvec ? k : 0u;
+        const int d = static_cast<int>(key[j * kVec + e] >> 22);
+        n_ab += (v < nvec && d > thr) ? 1 : 0;
+        n_tie += (v < nvec && d == thr) ? 1 : 0;
+      }
+    }
+    int tot_ab, tot_tie;
+    int off_ab = warp_excl_scan(n_ab, &tot_ab);
+    int off_tie = warp_excl_scan(n_tie, &tot_tie);
+    if (tot_ab == 0 && tot_tie == 0) continue;
+    int base_ab = 0, base_tie = 0;
+    if (lane == 0) {
+      if (tot_ab) base_ab = atomicAdd(&sh.n_out, tot_ab);
+      if (tot_tie) base_tie = atomicAdd(&sh.n_a, tot_tie);
+    }
+    base_ab = __shfl_sync(0xFFFFFFFFu, base_ab, 0) + off_ab;
+    base_tie = __shfl_sync(0xFFFFFFFFu, base_tie, 0) + off_tie;
+    if (n_ab == 0 && n_tie == 0) continue;
+#pragma unroll
+    for (int j = 0; j < kUnroll; ++j) {
+      const int64_t v = v0 + j * kThreads + tid;
+      if (v >= nvec) continue;
+#pragma unroll
+      for (int e = 0; e < kVec; ++e) {
+        const uint32_t k = key[j * kVec + e];
+        const int d = static_cast<int>(k >> 22);
+        const int64_t c = a1 + v * kVec + e;
+        if (d > thr) {
+          if (base_ab < p.k) store_one<kRemap>(p, row, lo, base_blk, base_ab, c);
+          ++base_ab;
+        } else if (d == thr) {
+          if (base_tie < kCapA) {
+            keys_a[base_tie] = k;
+            cols_a[base_tie] = static_cast<int32_t>(c);
+          }
+          ++base_tie;
+          atomicAdd(&sh.hist[1][digit(k, 1)], 1u);
+        }
+      }
+    }
+  }
+}
+
 template <bool kBf16, bool kRemap>
 __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p) {
   extern __shared__ __align__(16) uint8_t dyn[];
@@ -266,6 +360,10 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p) {
       : static_cast<const void*>(static_cast<const float*>(p.logits) + row * p.ld);
 
   if (n <= K) {
+    if (p.hist) {
+      uint32_t* g = p.hist + static_cast<int64_t>(row) * kBins0;
+      for (int i = tid; i < kBins0; i += kThreads) g[i] = 0;
+    }
     for (int i = tid; i < K; i += kThreads) {
       if (i < n) {
         store_one<kRemap>(p, row, lo, base_blk, i, lo + i);
@@ -293,22 +391,45 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p) {
   __syncthreads();
 
   // level-0 histogram straight from global memory
-  sweep_row<kBf16>(rowp, lo, hi, [&](bool valid, int64_t, uint32_t key) {
-    if (valid) atomicAdd(&sh.hist[0][key >> 21], 1u);
-  });
+  if (p.hist) {
+    // first digit counted by the kernel that wrote the scores; hand the
+    // workspace back zeroed for the next use
+    uint32_t* g = p.hist + static_cast<int64_t>(row) * kBins0;
+    for (int i = tid; i < kBins0; i += kThreads) {
+      sh.hist[0][i] = g[i];
+      g[i] = 0;
+    }
+  } else {
+    sweep_row<kBf16>(rowp, lo, hi, [&](bool valid, int64_t, uint32_t key) {
+      if (valid) atomicAdd(&sh.hist[0][key >> 22], 1u);
+    });
+  }
   __syncthreads();
-  find_threshold(sh, sh.hist[0], kBins);
+  find_threshold(sh, sh.hist[0], kBins0);
 
   // level 0: store digit > thr, collect the tie bucket into A, histogram its next digit
-  sweep_row<kBf16>(rowp, lo, hi, [&](bool valid, int64_t c, uint32_t key) {
-    visit<kRemap>(p, sh, row, lo, base_blk, 0, 0u, valid, key, c, keys_a, cols_a, &sh.n_a, kCapA,
-                  sh.hist[1]);
-  });
-  uint32_t prefix = static_cast<uint32_t>(sh.thr) << 21;
+  {
+    constexpr int kVec = kBf16 ? 8 : 4;
+    constexpr int kEsz = kBf16 ? 2 : 4;
+    const uintptr_t base = reinterpret_cast<uintptr_t>(rowp);
+    int64_t a1 = lo + (kVec - static_cast<int64_t>(((base / kEsz) + lo) % kVec)) % kVec;
+    if (a1 > hi) a1 = hi;
+    const int64_t nvec = (hi - a1) / kVec;
+    const int64_t a2 = a1 + nvec * kVec;
+    // unaligned head [lo, a1) and tail [a2, hi), element by element
+    const int nh = static_cast<int>(a1 - lo);
+    const int nt = static_cast<int>(hi - a2);
+    const bool valid = tid < nh + nt;
+    const int64_t c = tid < nh ? lo + tid : a2 + (tid - nh);
+    visit<kRemap>(p, sh, row, lo, base_blk, 0, 0u, valid, valid ? key_at<kBf16>(rowp, c) : 0u, c,
+                  keys_a, cols_a, &sh.n_a, kCapA, sh.hist[1]);
+    level0_body<kBf16, kRemap>(p, sh, row, lo, base_blk, rowp, a1, nvec, keys_a, cols_a);
+  }
+  uint32_t prefix = static_cast<uint32_t>(sh.thr) << 22;
   __syncthreads();
   for (int i = tid; i < kBins; i += kThreads) sh.hist[0][i] = 0;  // free since level 0 is done
   find_threshold(sh, sh.hist[1], kBins);
-  prefix |= static_cast<uint32_t>(sh.thr) << 10;
+  prefix |= static_cast<uint32_t>(sh.thr) << 11;
 
   // level 1: from bucket A when it held every tie, else global memory with a prefix filter
   const bool a_ok = sh.n_a <= kCapA;
@@ -327,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p) {
     });
   }
   __syncthreads();
-  find_threshold(sh, sh.hist[0], kBins / 2);
+  find_threshold(sh, sh.hist[0], kBins);
   prefix |= static_cast<uint32_t>(sh.thr);
 
   // level 2: every remaining candidate shares the full key prefix; take the bucket
@@ -353,6 +474,15 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p) {
                     0, nullptr);
     });
   }
+  // With exact counts exactly k entries were written. A histogram that does not
+  // match the scores (a misused workspace) can leave a short row: complete it.
+  __syncthreads();
+  for (int i = sh.n_out + tid; i < K; i += kThreads) {
+    p.out[row * p.ld_out + i] = -1;
+    if constexpr (kRemap) {
+      if (p.cols) p.cols[row * p.ld_cols + i] = -1;
+    }
+  }
 }
 
 }  // namespace
@@ -361,6 +491,19 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p) {
 using namespace idx;
 
 namespace {
+
+// The optional workspace holds, per row, the first-digit histogram that the
+// logits entry points accumulate when given the same workspace.
+idx_status_t attach_hist(const char* fn, TopkParams* p, int rows, void* ws, size_t ws_bytes) {
+  if (!ws) return IDX_OK;
+  const size_t need = static_cast<size_t>(rows) * kBins0 * sizeof(uint32_t);
+  if (ws_bytes < need) {
+    return fail(IDX_ERR_INVALID_ARG, "%s: workspace of %zu bytes, %zu needed", fn, ws_bytes, need);
+  }
+  if (!aligned(ws, 16)) return fail(IDX_ERR_UNSUPPORTED, "%s: workspace must be 16-byte aligned", fn);
+  p->hist = static_cast<uint32_t*>(ws);
+  return IDX_OK;
+}
 
 template <bool kBf16, bool kRemap>
 idx_status_t launch_topk(const TopkParams& p, int rows, cudaStream_t stream, const char* fn) {
@@ -382,8 +525,6 @@ idx_status_t launch_topk(const TopkParams& p, int rows, cudaStream_t stream, con
 extern "C" idx_status_t idx_topk(const void* logits, int dtype, int64_t ld, const int32_t* row_ks,
                                  const int32_t* row_ke, int32_t rows, int32_t k, int32_t* out,
                                  int64_t ld_out, void* ws, size_t ws_bytes, cudaStream_t stream) {
-  (void)ws;
-  (void)ws_bytes;
   const char* fn = "idx_topk";
   if (rows < 0 || k < 1) return fail(IDX_ERR_INVALID_ARG, "%s: rows < 0 or k < 1", fn);
   if (k > kMaxK) return fail(IDX_ERR_UNSUPPORTED, "%s: k %d exceeds %d", fn, k, kMaxK);
@@ -392,6 +533,8 @@ extern "C" idx_status_t idx_topk(const void* logits, int dtype, int64_t ld, cons
   if (rows == 0) return IDX_OK;
   if (!logits || !row_ke || !out) return fail(IDX_ERR_INVALID_ARG, "%s: NULL pointer", fn);
   TopkParams p{};
+  idx_status_t st = attach_hist(fn, &p, rows, ws, ws_bytes);
+  if (st != IDX_OK) return st;
   p.logits = logits;
   p.ld = ld;
   p.row_ks = row_ks;
@@ -409,8 +552,6 @@ extern "C" idx_status_t idx_sparse_topk_remap(const void* sparse_logits, int dty
                                               int32_t rows, int32_t k, int32_t* col_scratch,
                                               int64_t ld_col, int32_t* positions, int64_t ld_pos,
                                               void* ws, size_t ws_bytes, cudaStream_t stream) {
-  (void)ws;
-  (void)ws_bytes;
   const char* fn = "idx_sparse_topk_remap";
   if (rows < 0 || k < 1 || sbk < 1) return fail(IDX_ERR_INVALID_ARG, "%s: rows < 0, k < 1 or sbk < 1", fn);
   if (k > kMaxK) return fail(IDX_ERR_UNSUPPORTED, "%s: k %d exceeds %d", fn, k, kMaxK);
@@ -419,6 +560,8 @@ extern "C" idx_status_t idx_sparse_topk_remap(const void* sparse_logits, int dty
   if (rows == 0) return IDX_OK;
   if (!sparse_logits || !end || !sparse_idx || !positions) return fail(IDX_ERR_INVALID_ARG, "%s: NULL pointer", fn);
   TopkParams p{};
+  idx_status_t st = attach_hist(fn, &p, rows, ws, ws_bytes);
+  if (st != IDX_OK) return st;
   p.logits = sparse_logits;
   p.ld = ld;
   p.row_ks = row_ks;

@@ -65,10 +65,13 @@ class DecodeStep:
         self.batch, self.next_n, self.topk = batch, next_n, topk
         self.block_size = block_size
         self.block_span = block_size if block_span is None else block_span
-        self.logits = torch.empty((rows, max_ctx), dtype=torch.float32, device=device)
+        ld = (max_ctx + 63) // 64 * 64   # 256-byte aligned rows: vector loads in the selection
+        self.logits = torch.empty((rows, ld), dtype=torch.float32, device=device)
         self.local = torch.empty((rows, topk), dtype=torch.int32, device=device)
         self.slots = torch.empty((rows, topk), dtype=torch.int32, device=device)
         self.row_ke = torch.empty(rows, dtype=torch.int32, device=device)
+        # selection workspace (first-digit histograms), zero between steps
+        self.ws = torch.zeros((rows, 1024), dtype=torch.int32, device=device) if next_n == 1 else None
 
     def run(self, q, w, cache, block_table, ctx_lens, new_k=None, new_slots=None, row_ke=None,
             stream=None):
@@ -76,9 +79,9 @@ class DecodeStep:
         if new_k is not None:
             idx_k_quant_and_cache(new_k, new_slots, cache, self.block_size, stream=stream)
         idx_paged_mqa_logits_decode(q, w, cache, self.block_size, block_table, ctx_lens, self.logits,
-                                    next_n=self.next_n, stream=stream)
+                                    next_n=self.next_n, ws=self.ws, stream=stream)
         ke = ctx_lens if (row_ke is None and self.next_n == 1) else row_ke
-        idx_topk(self.logits, None, ke, self.topk, self.local, stream=stream)
+        idx_topk(self.logits, None, ke, self.topk, self.local, ws=self.ws, stream=stream)
         idx_req_to_global_slots(self.local, None if self.next_n == 1 else self._row_to_req(ctx_lens),
                                 block_table, self.block_size, self.block_span, self.slots,
                                 stream=stream)
@@ -104,15 +107,16 @@ class HierarchicalStep:
         self.cols = torch.empty((rows, topk), dtype=torch.int32, device=device)
         self.positions = torch.empty((rows, topk), dtype=torch.int32, device=device)
         self.slots = torch.empty((rows, topk), dtype=torch.int32, device=device)
+        self.ws = torch.zeros((rows, 1024), dtype=torch.int32, device=device)
 
     def run(self, q, w, cache, block_table, ctx_lens, cand, stream=None):
         idx_expand_candidates(cand, None, ctx_lens, self.cand_block_size, self.sbk, self.sparse_idx,
                               self.end, stream=stream)
         idx_paged_mqa_logits_decode(q, w, cache, self.block_size, block_table, ctx_lens, self.logits,
                                     sparse_idx=self.sparse_idx, end=self.end, sbk=self.sbk,
-                                    stream=stream)
+                                    ws=self.ws, stream=stream)
         idx_sparse_topk_remap(self.logits, self.end, self.sparse_idx, None, self.sbk, self.topk,
-                              self.positions, col_scratch=self.cols, stream=stream)
+                              self.positions, col_scratch=self.cols, ws=self.ws, stream=stream)
         idx_req_to_global_slots(self.positions, None, block_table, self.block_size, self.block_size,
                                 self.slots, stream=stream)
         return self.slots

