@@ -311,6 +311,44 @@ idx_status_t idx_req_to_global_slots(const int32_t* local, int64_t ld_l, int32_t
                                      int32_t* slots, int64_t ld_s, cudaStream_t stream);
 
 /*
+ * idx_paged_mqa_topk_decode_noalloc - decode scoring and top-k for callers that
+ * cannot allocate device memory.
+ *
+ * The paper has no counterpart to this entry point; it exists for callers of
+ * this library that are not allowed to call cudaMalloc: code that runs inside
+ * an engine which plans every device buffer ahead of time and forbids new
+ * allocations while it serves, or a plugin that is handed raw device pointers
+ * and no allocator. Such callers cannot provide the selection workspace, so
+ * this call keeps it in a scratch array built into the library (4 KB per row,
+ * IDX_NOALLOC_MAX_ROWS rows = 4 MB on every device that loads the library,
+ * held until the process exits). It allocates nothing and frees nothing.
+ *
+ * It computes exactly what idx_paged_mqa_logits_decode (dense mode, next_n = 1,
+ * fp32 logits) followed by idx_topk over columns [0, ctx_lens[b]) compute,
+ * writing the scores to `logits` [B, ld_logits] and the top-k request-local
+ * indices (-1 filled) to `out` [B, ld_out]; the other arguments are as for
+ * idx_paged_mqa_logits_decode.
+ *
+ * The first call on a device looks up the scratch array's device address (a
+ * runtime query, no allocation); make that first call before any stream
+ * capture. Every call clears the scratch rows it uses before scoring. All
+ * calls on a device share the one array, so calls whose work overlaps on the
+ * GPU (other streams, other host threads) race on it and must be serialised
+ * by the caller.
+ * Errors: IDX_ERR_UNSUPPORTED when B > IDX_NOALLOC_MAX_ROWS; otherwise those of
+ * the two entry points it runs.
+ */
+#define IDX_NOALLOC_MAX_ROWS 1024
+idx_status_t idx_paged_mqa_topk_decode_noalloc(const uint8_t* q, int64_t ld_q, const void* w,
+                                               int w_dtype, int64_t ld_w, const uint8_t* cache,
+                                               int32_t num_blocks, int32_t block_size,
+                                               int64_t block_stride_bytes,
+                                               const int32_t* block_table, int64_t ld_bt,
+                                               const int32_t* ctx_lens, int32_t B, float* logits,
+                                               int64_t ld_logits, int32_t k, int32_t* out,
+                                               int64_t ld_out, cudaStream_t stream);
+
+/*
  * idx_block_span - tokens per physical block of a pool (host only).
  *
  * The DSV4 packed-KV fix, 实现拆解 item 1: block_span = block_stride /

@@ -44,6 +44,9 @@ SIGNATURES = {
                                       c_i32, c_ptr, c_i64, c_ptr, c_i64, c_ptr, c_size, c_ptr]),
     "idx_req_to_global_slots": (c_int, [c_ptr, c_i64, c_i32, c_i32, c_ptr, c_ptr, c_i64, c_i32, c_i32,
                                         c_ptr, c_i64, c_ptr]),
+    "idx_paged_mqa_topk_decode_noalloc": (c_int, [c_ptr, c_i64, c_ptr, c_int, c_i64, c_ptr, c_i32,
+                                                  c_i32, c_i64, c_ptr, c_i64, c_ptr, c_i32, c_ptr,
+                                                  c_i64, c_i32, c_ptr, c_i64, c_ptr]),
     "idx_block_span": (c_int, [c_i64, c_i64, ctypes.POINTER(c_i32)]),
     "idx_workspace_bytes": (c_size, [c_int, c_i32, c_i32, c_i32]),
     "idx_status_string": (ctypes.c_char_p, [c_int]),
