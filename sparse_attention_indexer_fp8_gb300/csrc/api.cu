@@ -132,15 +132,17 @@ idx_status_t idx_block_span(int64_t block_stride, int64_t token_stride, int32_t*
 
 idx_status_t idx_device_error(cudaStream_t stream) {
   cudaError_t e = cudaSuccess;
-  unsigned int a = idx::logits_read_and_clear_error(stream, &e);
+  long long info[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  unsigned int a = idx::logits_read_and_clear_error(stream, &e, info);
   if (e != cudaSuccess) return idx::fail(IDX_ERR_CUDA, "idx_device_error: %s", cudaGetErrorString(e));
   unsigned int b = idx::index_ops_read_and_clear_error(stream, &e);
   if (e != cudaSuccess) return idx::fail(IDX_ERR_CUDA, "idx_device_error: %s", cudaGetErrorString(e));
   if (a || b) {
     return idx::fail(IDX_ERR_DEVICE,
-                     "device error flags: logits 0x%08x (bounded wait expired; low byte = role), "
+                     "device error flags: logits 0x%08x (bit w: wait site w expired; first: site %lld "
+                     "block %lld tile-ordinal %lld group %lld tile %lld barrier %lld parity %lld), "
                      "index ops 0x%08x (1 = a row's ks is not a multiple of sbk)",
-                     a, b);
+                     a, info[0], info[1], info[2], info[3], info[4], info[5], info[6], b);
   }
   return IDX_OK;
 }

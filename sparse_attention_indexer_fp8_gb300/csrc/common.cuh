@@ -29,7 +29,7 @@ idx_status_t encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, int 
                                CUtensorMapSwizzle swizzle);
 
 // Per-translation-unit readers of device error flags, registered in api.cu.
-unsigned int logits_read_and_clear_error(cudaStream_t stream, cudaError_t* err);
+unsigned int logits_read_and_clear_error(cudaStream_t stream, cudaError_t* err, long long* info);
 unsigned int index_ops_read_and_clear_error(cudaStream_t stream, cudaError_t* err);
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }

@@ -58,8 +58,12 @@ constexpr uint64_t kTimeoutNs = 2000000000ull;
 
 enum Mode : int { kDecodeDense = 0, kDecodeSparse = 1, kPrefillDense = 2, kPrefillSparse = 3 };
 
-// bits of g_logits_error: low byte = the role whose wait expired
+// Bit (1 << w) of g_logits_error: wait site w (1..7) expired. The first
+// expiry also records where it happened in g_logits_error_info:
+// {site, block, tile ordinal, group, tile, barrier index, parity, 0}.
 __device__ unsigned int g_logits_error = 0;
+__device__ unsigned int g_logits_error_taken = 0;
+__device__ long long g_logits_error_info[8];
 
 struct LogitsParams {
   int mode;
@@ -209,8 +213,10 @@ struct Walker {
 
 // Bounded wait. All threads that call it for the same barrier get the same
 // answer only if they also agree on abort; callers make the result warp-uniform.
+// `ord`, `g`, `t` and `bar_idx` only describe the wait for the error record.
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                         unsigned int role) {
+                                         unsigned int site, long long ord = -1, int g = -1,
+                                         int t = -1, int bar_idx = -1) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (;;) {
@@ -218,7 +224,17 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
     if (*abort_flag) return false;
     if (global_timer_ns() - t0 > kTimeoutNs) {
       *abort_flag = 1;
-      atomicOr(&g_logits_error, role);
+      atomicOr(&g_logits_error, 1u << site);
+      if (atomicCAS(&g_logits_error_taken, 0u, 1u) == 0u) {
+        g_logits_error_info[0] = site;
+        g_logits_error_info[1] = blockIdx.x;
+        g_logits_error_info[2] = ord;
+        g_logits_error_info[3] = g;
+        g_logits_error_info[4] = t;
+        g_logits_error_info[5] = bar_idx;
+        g_logits_error_info[6] = parity;
+        g_logits_error_info[7] = 0;
+      }
       return false;
     }
   }
@@ -466,7 +482,7 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         const int4 tl = s_tile[buf][ti];
         if (tl.x != q_group) {
           bool got = true;
-          if (lane == 0) got = wait_bar(&q_empty[qs], qph ^ 1u, abort_flag, 1u);
+          if (lane == 0) got = wait_bar(&q_empty[qs], qph ^ 1u, abort_flag, 1u, -1, tl.x, tl.y, qs);
           got = __shfl_sync(0xFFFFFFFFu, got, 0);
           if (!got) return false;
           if (lane == 0) {
@@ -480,7 +496,7 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
           }
         }
         bool got = true;
-        if (lane == 0) got = wait_bar(&empty[st], ph ^ 1u, abort_flag, 2u);
+        if (lane == 0) got = wait_bar(&empty[st], ph ^ 1u, abort_flag, 2u, -1, tl.x, tl.y, st);
         got = __shfl_sync(0xFFFFFFFFu, got, 0);
         if (!got) return false;
         const bool mine = (lane / upt == ti) && bx.valid;
@@ -551,11 +567,11 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 qph ^= 1u;
               }
             }
-            if (!wait_bar(&q_full[qs], qph, abort_flag, 3u)) break;
+            if (!wait_bar(&q_full[qs], qph, abort_flag, 3u, ai, W.g, W.t, qs)) break;
             q_group = W.g;
           }
-          if (!wait_bar(&full[st], ph, abort_flag, 4u)) break;
-          if (!wait_bar(&acc_empty[as], aph ^ 1u, abort_flag, 5u)) break;
+          if (!wait_bar(&full[st], ph, abort_flag, 4u, ai, W.g, W.t, st)) break;
+          if (!wait_bar(&acc_empty[as], aph ^ 1u, abort_flag, 5u, ai, W.g, W.t, as)) break;
           tc_fence_after();
           const uint64_t a_desc = sw128_kmajor_desc(smem_u32(kv_s + st * kKvStageBytes));
           const uint64_t b_desc = sw128_kmajor_desc(smem_u32(q_s + qs * C::kQStageBytes));
@@ -590,8 +606,9 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     // consecutive tiles overlap their TMEM-load / FMA / store latency chains.
     // Ring positions follow from the active-tile ordinal. Every accumulator
     // stage and every accumulator-ready barrier belongs to one warpgroup for the
-    // whole kernel (kAccFull is a multiple of kEpiWG), so no barrier is ever
-    // waited on more than one phase ahead.
+    // whole kernel (kAccFull is a multiple of kEpiWG). The commit of group
+    // cg + kAccFull needs an accumulator stage that group cg's first tile
+    // releases, so a barrier never runs ahead of the one wait per group below.
     static_assert(C::kAccFull % kEpiWG == 0, "accumulator barriers per warpgroup");
     const int ew = warp - 2;
     const int wg = ew / 4;
@@ -626,6 +643,12 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     };
     long long ai = 0;  // active tiles seen
     long long ti = 0;  // tiles seen
+    // A warp waits a commit group's accumulator-ready barrier once, at the
+    // group's first tile. Waiting again at the second tile would be unsafe: once
+    // the first tile's accumulator is released the MMA warp may already commit
+    // the group two ahead (an unpaired last tile of the range commits at once)
+    // to the same barrier, moving it two phases past this wait's parity.
+    long long waited_cg = -1;
     int cur_g = -1;
     int lim_lo[NQ], lim_hi[NQ];
     // one query per group: its 64 weights live in registers for the whole group
@@ -685,13 +708,16 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         const long long cg = ai / C::kCommit;
         const int af = static_cast<int>(cg % C::kAccFull);
         const uint32_t afph = static_cast<uint32_t>((cg / C::kAccFull) & 1);
-        bool got = wait_bar(&full[st], ph, abort_flag, 6u);
+        bool got = wait_bar(&full[st], ph, abort_flag, 6u, ai, W.g, W.t, st);
         if (!__all_sync(0xFFFFFFFFu, got)) break;
         const int box = trow / p.unit;
         const float scale = *reinterpret_cast<const float*>(
             sc_s + st * kScaleStageBytes + box * p.scale_slot + (trow - box * p.unit) * 4);
-        got = wait_bar(&acc_full[af], afph, abort_flag, 7u);
-        if (!__all_sync(0xFFFFFFFFu, got)) break;
+        if (cg != waited_cg) {
+          got = wait_bar(&acc_full[af], afph, abort_flag, 7u, ai, W.g, W.t, af);
+          if (!__all_sync(0xFFFFFFFFu, got)) break;
+          waited_cg = cg;
+        }
         tc_fence_after();
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[st]);  // the MMAs of this tile are done with the stage
@@ -861,14 +887,20 @@ bool sbk_ok(int32_t sbk) { return sbk == 8 || sbk == 16 || sbk == 32 || sbk == 6
 
 }  // namespace
 
-unsigned int logits_read_and_clear_error(cudaStream_t stream, cudaError_t* err) {
+unsigned int logits_read_and_clear_error(cudaStream_t stream, cudaError_t* err, long long* info) {
   unsigned int v = 0;
   const unsigned int zero = 0;
   *err = cudaStreamSynchronize(stream);
   if (*err != cudaSuccess) return 0;
   *err = cudaMemcpyFromSymbol(&v, g_logits_error, sizeof(v));
   if (*err != cudaSuccess) return 0;
-  if (v) *err = cudaMemcpyToSymbol(g_logits_error, &zero, sizeof(zero));
+  if (v) {
+    *err = cudaMemcpyFromSymbol(info, g_logits_error_info, 8 * sizeof(long long));
+    if (*err != cudaSuccess) return v;
+    *err = cudaMemcpyToSymbol(g_logits_error, &zero, sizeof(zero));
+    if (*err != cudaSuccess) return v;
+    *err = cudaMemcpyToSymbol(g_logits_error_taken, &zero, sizeof(zero));
+  }
   return v;
 }
 

@@ -1,0 +1,144 @@
+"""The named workloads at full size, in the launch configuration the benchmark times.
+
+Each test runs one whole step through the library (the same entry points,
+buffers and selection workspace as bench.py) and checks sampled rows against
+the oracle, computed one row at a time: logits within 1e-3 + 2e-3 * |oracle|
+(plus bf16 rounding for bf16 scores), top-k sets up to ties within that
+tolerance, slots and remaps bit-exact, and the expansion bit-exact on every
+row. Large pools draw k with the device generator; the oracle draws the same k
+by calling that generator again.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import sparse_attention_indexer_fp8_gb300 as idx
+from oracle import indexer as O
+from oracle.codecs import bf16_decode
+from sparse_attention_indexer_fp8_gb300 import workloads as W
+from sparse_attention_indexer_fp8_gb300.pipeline import DecodeStep, HierarchicalStep, fill_paged_cache
+from tests.checks import BF16_REL, assert_logits_close, assert_topk_row
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library():
+    from sparse_attention_indexer_fp8_gb300.build import build_library
+
+    build_library()
+    idx.library()
+    yield
+    idx.idx_device_error()
+
+
+def _k_host(seed, b, n):
+    return bf16_decode(W.make_k_device(seed, b, n, DEV).view(torch.int16).cpu().numpy().view(np.uint16))
+
+
+def _decode(wl, n_rows):
+    pool = wl.pool
+    cache = torch.zeros((pool.num_blocks, W.block_stride_bytes()), dtype=torch.uint8, device=DEV)
+    fill_paged_cache(pool, wl.seed, cache, device_k=True)
+    stp = DecodeStep(wl.batch, int(pool.ctx_lens.max()))
+    bt = torch.from_numpy(pool.block_table).to(DEV)
+    ctx = torch.from_numpy(pool.ctx_lens).to(DEV)
+    slots = stp.run(torch.from_numpy(wl.q8).to(DEV), torch.from_numpy(wl.w).to(DEV), cache, bt, ctx)
+    idx.idx_device_error()
+    lg, loc, sl = stp.logits.cpu().numpy(), stp.local.cpu().numpy(), slots.cpu().numpy()
+    assert not stp.ws.any().item()
+    rng = np.random.default_rng(wl.seed)
+    for b in sorted(rng.choice(wl.batch, size=n_rows, replace=False).tolist()):
+        L = int(pool.ctx_lens[b])
+        k8, ks = O.k_quant(_k_host(wl.seed, b, L))
+        ref = O.logits_row(wl.q8[b], wl.w[b], k8, ks)
+        assert_logits_close(lg[b, :L], ref, f"row {b}")
+        assert_topk_row(loc[b], ref, wl.topk, f"top-k row {b}")
+        sm = pool.slot_mapping(b)
+        assert np.array_equal(sl[b], np.where(loc[b] >= 0, sm[np.clip(loc[b], 0, L - 1)], -1))
+
+
+def test_paged_decode_b64_8k_32k():
+    _decode(W.paged_decode(), 6)
+
+
+def test_long_decode_b128_64k_128k():
+    _decode(W.long_decode(), 3)
+
+
+def test_prefill_chunk_8192_on_32k():
+    wl = W.prefill_chunk()
+    T, S = wl.q8.shape[0], wl.S
+    pool = W.make_pool(wl.seed, [S])
+    cache = torch.zeros((pool.num_blocks, W.block_stride_bytes()), dtype=torch.uint8, device=DEV)
+    k = W.make_k_device(wl.seed, 0, S, DEV)
+    idx.idx_k_quant_and_cache(k, torch.from_numpy(pool.slot_mapping(0)).to(DEV), cache, 64)
+    k8 = torch.empty((S, 128), dtype=torch.uint8, device=DEV)
+    kscale = torch.empty(S, dtype=torch.float32, device=DEV)
+    idx.idx_gather_k(cache, 64, torch.from_numpy(pool.block_table[0]).to(DEV), S, k8, kscale)
+    q = torch.from_numpy(wl.q8).to(DEV)
+    w = torch.from_numpy(wl.w.view(np.int16)).to(DEV).view(torch.bfloat16)
+    ks, ke = torch.from_numpy(wl.row_ks).to(DEV), torch.from_numpy(wl.row_ke).to(DEV)
+    logits = torch.empty((T, S), dtype=torch.float32, device=DEV)
+    idx.idx_mqa_logits_prefill(q, w, k8, kscale, ks, ke, logits)
+    sel = torch.empty((T, wl.topk), dtype=torch.int32, device=DEV)
+    idx.idx_topk(logits, ks, ke, wl.topk, sel)
+    idx.idx_device_error()
+    ok8, oks = O.k_quant(bf16_decode(k.view(torch.int16).cpu().numpy().view(np.uint16)))
+    assert np.array_equal(k8.cpu().numpy(), ok8) and np.array_equal(kscale.cpu().numpy(), oks)
+    wv = bf16_decode(wl.w)
+    rows = [0, 1, 2, 3, 4, 5, 4095, T - 2, T - 1]
+    lg = logits[rows].cpu().numpy()
+    sl = sel[rows].cpu().numpy()
+    for i, t in enumerate(rows):
+        hi = int(wl.row_ke[t])
+        ref = O.logits_row(wl.q8[t], wv[t], ok8[:hi], oks[:hi])
+        assert_logits_close(lg[i, :hi], ref, f"prefill row {t}")
+        assert np.all(np.isneginf(lg[i, hi:])), f"prefill mask row {t}"
+        assert_topk_row(sl[i], ref, wl.topk, f"prefill top-k row {t}")
+
+
+def _hierarchical(wl, check_rows):
+    pool = wl.pool
+    B = len(pool.ctx_lens)
+    cache = torch.zeros((pool.num_blocks, W.block_stride_bytes()), dtype=torch.uint8, device=DEV)
+    fill_paged_cache(pool, wl.seed, cache, device_k=True)
+    stp = HierarchicalStep(B, wl.cand.shape[1], wl.cand_block_size, wl.sbk, wl.topk)
+    slots = stp.run(torch.from_numpy(wl.q8).to(DEV), torch.from_numpy(wl.w).to(DEV), cache,
+                    torch.from_numpy(pool.block_table).to(DEV), torch.from_numpy(pool.ctx_lens).to(DEV),
+                    torch.from_numpy(wl.cand).to(DEV))
+    idx.idx_device_error()
+    osi, oend = O.expand_candidates(wl.cand, None, pool.ctx_lens, wl.cand_block_size, wl.sbk)
+    assert np.array_equal(stp.sparse_idx.cpu().numpy(), osi)
+    assert np.array_equal(stp.end.cpu().numpy(), oend)
+    assert not stp.ws.any().item()
+    lg = stp.logits.float().cpu().numpy()
+    cols, pos, sl = stp.cols.cpu().numpy(), stp.positions.cpu().numpy(), slots.cpu().numpy()
+    for b in check_rows:
+        e = int(oend[b])
+        kall = _k_host(wl.seed, b, int(pool.ctx_lens[b]))
+        toks = np.array([O.sparse_column_token(osi[b], c, wl.sbk) for c in range(e)], dtype=np.int64)
+        k8, ks = O.k_quant(kall[toks])
+        ref = O.logits_row(wl.q8[b], wl.w[b], k8, ks)
+        assert_logits_close(lg[b, :e], ref, f"sparse row {b}", BF16_REL)
+        assert np.all(np.isneginf(lg[b, e:]))
+        assert_topk_row(cols[b], ref, wl.topk, f"sparse top-k row {b}", BF16_REL)
+        m = min(wl.topk, e)
+        assert pos[b, :m].tolist() == toks[cols[b, :m]].tolist() and np.all(pos[b, m:] == -1)
+        sm = pool.slot_mapping(b)
+        assert np.array_equal(sl[b], np.where(pos[b] >= 0, sm[np.clip(pos[b], 0, None)], -1))
+
+
+def test_hierarchical_b128_128k():
+    wl = W.hierarchical()
+    rng = np.random.default_rng(wl.seed)
+    _hierarchical(wl, sorted(rng.choice(128, size=6, replace=False).tolist()))
+
+
+def test_hierarchical_many_tiles_per_cta_every_row():
+    # 128 rows of 32 sparse tiles each: every CTA walks ~27 tiles across row
+    # boundaries, inactive tails and unpaired commit groups; every row is checked
+    wl = W.hierarchical(seed=2024, batch=128, ctx=16384, n_cand=64)
+    _hierarchical(wl, list(range(0, 128, 1)))
