@@ -151,6 +151,11 @@ def barrier(dist):
         dist.barrier()
 
 
+def rank_seed(base: int, rank: int) -> int:
+    """Seed of rank `rank`'s own batch: ranks work on independent rows (weak scaling)."""
+    return base + 7919 * rank
+
+
 # ----------------------------------------------------------------------------- oracle side
 
 def oracle_decode_rows(wl: W.DecodeWorkload, rows, k_rows, reps: int = 1):
@@ -213,8 +218,8 @@ class DecodeBench:
         from sparse_attention_indexer_fp8_gb300.pipeline import fill_paged_cache
 
         self.idx, self.dev, self.name = idx, dev, name
-        self.wl = wl = (W.long_decode(seed=1003 + 7919 * rank) if name == "long_decode"
-                        else W.paged_decode(seed=1001 + 7919 * rank))
+        self.wl = wl = (W.long_decode(seed=rank_seed(1003, rank)) if name == "long_decode"
+                        else W.paged_decode(seed=rank_seed(1001, rank)))
         pool = wl.pool
         self.B = B = wl.batch
         self.L = L = pool.ctx_lens.astype(np.int64)
@@ -321,7 +326,7 @@ class PrefillBench:
         import sparse_attention_indexer_fp8_gb300 as idx
 
         self.idx, self.dev, self.name = idx, dev, name
-        self.wl = wl = W.prefill_chunk(seed=1002 + 7919 * rank)
+        self.wl = wl = W.prefill_chunk(seed=rank_seed(1002, rank))
         self.T, self.S = T, S = wl.q8.shape[0], wl.S
         self.pool = pool = W.make_pool(wl.seed, [S])
         self.stride = W.block_stride_bytes()
@@ -433,7 +438,7 @@ class HierBench:
         from sparse_attention_indexer_fp8_gb300.pipeline import HierarchicalStep, fill_paged_cache
 
         self.idx, self.dev, self.name = idx, dev, name
-        self.wl = wl = W.hierarchical(seed=1004 + 7919 * rank)
+        self.wl = wl = W.hierarchical(seed=rank_seed(1004, rank))
         pool = wl.pool
         self.B = B = len(pool.ctx_lens)
         self.stride = W.block_stride_bytes()
