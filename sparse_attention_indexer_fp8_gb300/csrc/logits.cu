@@ -311,19 +311,25 @@ __device__ __forceinline__ float hsum2(uint64_t v) {
 // sum_h w[h] * acc[h] over the 64 head columns of one query (a0: heads 0-31,
 // a1: heads 32-63), with the packed two-lane fp32 FMA of sm_100+: half the FMA
 // instructions of the scalar form, four independent two-lane accumulators.
-template <typename WFn>
+// w4(i) returns the weights of heads 4i..4i+3 (registers, or one broadcast
+// 16-byte shared-memory load).
+template <typename W4Fn>
 __device__ __forceinline__ float weighted_head_sum(const uint32_t (&a0)[32], const uint32_t (&a1)[32],
-                                                   WFn w) {
+                                                   W4Fn w4) {
   uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-  for (int h = 0; h < 32; h += 2) {
-    fma2(acc[(h >> 1) & 3], pack2(__uint_as_float(a0[h]), __uint_as_float(a0[h + 1])),
-         pack2(w(h), w(h + 1)));
+  for (int h = 0; h < 32; h += 4) {
+    const float4 w = w4(h >> 2);
+    fma2(acc[(h >> 1) & 3], pack2(__uint_as_float(a0[h]), __uint_as_float(a0[h + 1])), pack2(w.x, w.y));
+    fma2(acc[((h >> 1) + 1) & 3], pack2(__uint_as_float(a0[h + 2]), __uint_as_float(a0[h + 3])),
+         pack2(w.z, w.w));
   }
 #pragma unroll
-  for (int h = 0; h < 32; h += 2) {
-    fma2(acc[(h >> 1) & 3], pack2(__uint_as_float(a1[h]), __uint_as_float(a1[h + 1])),
-         pack2(w(32 + h), w(33 + h)));
+  for (int h = 0; h < 32; h += 4) {
+    const float4 w = w4(8 + (h >> 2));
+    fma2(acc[(h >> 1) & 3], pack2(__uint_as_float(a1[h]), __uint_as_float(a1[h + 1])), pack2(w.x, w.y));
+    fma2(acc[((h >> 1) + 1) & 3], pack2(__uint_as_float(a1[h + 2]), __uint_as_float(a1[h + 3])),
+         pack2(w.z, w.w));
   }
   return (hsum2(acc[0]) + hsum2(acc[1])) + (hsum2(acc[2]) + hsum2(acc[3]));
 }
@@ -739,10 +745,12 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             reg_fence(a1);
             float sum;
             if constexpr (kRegW) {
-              sum = weighted_head_sum(a0, a1, [&](int h) { return wreg[h]; });
+              sum = weighted_head_sum(a0, a1, [&](int i) {
+                return make_float4(wreg[4 * i], wreg[4 * i + 1], wreg[4 * i + 2], wreg[4 * i + 3]);
+              });
             } else {
-              const float* wj = wsm + j * 64;
-              sum = weighted_head_sum(a0, a1, [&](int h) { return wj[h]; });
+              const float4* wj = reinterpret_cast<const float4*>(wsm + j * 64);
+              sum = weighted_head_sum(a0, a1, [&](int i) { return wj[i]; });
             }
             logit[j] = sum * scale;
           }
