@@ -228,6 +228,9 @@ idx_status_t idx_paged_mqa_logits_decode(const uint8_t* q, int64_t ld_q, const v
  *   logits   [rows, ld] of dtype (IDX_F32 or IDX_BF16).
  *   row_ks   int32 [rows] or NULL (all zero); row_ke int32 [rows].
  *   out      int32 [rows, ld_out], ld_out >= k.
+ *   vals     NULL, or float [rows, ld_vals]: the score of each selected entry
+ *            (-inf for -1 slots), e.g. the values a context-parallel rank
+ *            exchanges for idx_dcp_topk_merge.
  *   ws       NULL, or the selection workspace filled by the logits call that
  *            wrote `logits` (consumed and zeroed).
  * Errors: IDX_ERR_INVALID_ARG for NULL pointers, k < 1, ld_out < k;
@@ -235,7 +238,43 @@ idx_status_t idx_paged_mqa_logits_decode(const uint8_t* q, int64_t ld_q, const v
  */
 idx_status_t idx_topk(const void* logits, int dtype, int64_t ld, const int32_t* row_ks,
                       const int32_t* row_ke, int32_t rows, int32_t k, int32_t* out,
-                      int64_t ld_out, void* ws, size_t ws_bytes, cudaStream_t stream);
+                      int64_t ld_out, float* vals, int64_t ld_vals, void* ws, size_t ws_bytes,
+                      cudaStream_t stream);
+
+/*
+ * idx_dcp_topk_merge - merge per-shard top-k lists into the global top-k.
+ *
+ * "DeepSeek V3.2 稀疏注意力 DSA 推理流程图解", section "几个容易踩的点": under
+ * decode context parallelism each rank scores its own shard of the context and
+ * the ranks exchange only their local top-k candidates, not the score matrix;
+ * this is exact because a token of the global top-k is always in the local
+ * top-k of the shard that holds it. Each shard of a row contributes k_local
+ * (value, shard-local index) pairs (idx_topk with `vals`); candidate j of shard
+ * s stands for the global position
+ *     shard_offset[row * ld_off + s] + cand_idx[row, s * k_local + j] * pos_stride
+ * (contiguous shards: pos_stride 1 and each shard's first position; shards that
+ * deal tokens round-robin: offset = shard number, pos_stride = number of shards).
+ * For every row this call takes the n_shards * k_local candidates, laid out
+ * shard after shard, and writes the global positions of the k largest values,
+ * in unspecified order, followed by -1 when fewer than k candidates are valid.
+ *
+ *   cand_vals     float [rows, ld_v]; an empty candidate (index -1) must hold -inf.
+ *   cand_idx      int32 [rows, ld_i], shard-local indices, -1 = empty.
+ *   shard_offset  int32 [rows, ld_off] (device); ld_off = 0 shares one vector of
+ *                 n_shards offsets between all rows; NULL means every offset is 0.
+ *   pos_stride    >= 1. Global positions must fit in int32.
+ *   out           int32 [rows, ld_out], ld_out >= k.
+ *   vals          NULL, or float [rows, ld_vals]: the merged scores (-inf for -1 slots).
+ * Candidates are ranked by value alone, so a valid candidate must score above
+ * -inf to be sure of beating the empty ones (in-range logits are finite).
+ * Errors: IDX_ERR_INVALID_ARG for NULL pointers, too-small strides or counts
+ * below 1; IDX_ERR_UNSUPPORTED for k > 4096.
+ */
+idx_status_t idx_dcp_topk_merge(const float* cand_vals, int64_t ld_v, const int32_t* cand_idx,
+                                int64_t ld_i, const int32_t* shard_offset, int64_t ld_off,
+                                int32_t n_shards, int32_t pos_stride, int32_t k_local,
+                                int32_t rows, int32_t k, int32_t* out, int64_t ld_out,
+                                float* vals, int64_t ld_vals, cudaStream_t stream);
 
 /*
  * idx_expand_candidates - flatten, filter, sort, dedupe and tail-pad candidate blocks.

@@ -232,6 +232,58 @@ def topk(logits, row_ks, row_ke, k: int) -> np.ndarray:
 
 
 # ----------------------------------------------------------------------------
+# context-parallel decode: merge of the ranks' local top-k lists
+# ----------------------------------------------------------------------------
+
+def dcp_topk_merge_row(cand_vals, cand_idx, shard_offset, k_local: int, k: int, pos_stride: int = 1):
+    """Global top-``k`` of one row from every shard's local top-``k`` candidates.
+
+    [DSA] 几个容易踩的点 (context parallelism): each rank selects within its
+    own shard of the context and the ranks exchange only those local lists,
+    never the score matrix. Candidate ``j`` of shard ``s`` (``cand_idx[s *
+    k_local + j]``, shard-local, ``-1`` = empty) stands for global position
+    ``shard_offset[s] + cand_idx * pos_stride`` (``shard_offset`` None: every
+    offset is 0). The merged list is the candidates sorted by value descending,
+    then global position ascending, cut to ``k`` and padded with ``-1`` /
+    ``-inf``; empty candidates never enter it.
+
+    Returns (positions int64 [k], values float64 [k]).
+    """
+    cand_vals = np.asarray(cand_vals, dtype=np.float64)
+    cand_idx = np.asarray(cand_idx, dtype=np.int64)
+    n_shards = len(cand_idx) // k_local if shard_offset is None else len(shard_offset)
+    pos, val = [], []
+    for s in range(n_shards):
+        for j in range(k_local):
+            i = int(cand_idx[s * k_local + j])
+            if i >= 0:
+                pos.append((0 if shard_offset is None else int(shard_offset[s])) + i * pos_stride)
+                val.append(float(cand_vals[s * k_local + j]))
+    pos = np.array(pos, dtype=np.int64)
+    val = np.array(val, dtype=np.float64)
+    order = np.lexsort((pos, -val))[:k]
+    out_p = np.full(k, -1, dtype=np.int64)
+    out_v = np.full(k, -np.inf)
+    out_p[:len(order)] = pos[order]
+    out_v[:len(order)] = val[order]
+    return out_p, out_v
+
+
+def dcp_topk_merge(cand_vals, cand_idx, shard_offset, k_local: int, k: int, pos_stride: int = 1):
+    """``dcp_topk_merge_row`` for every row: (positions [rows, k], values [rows, k]).
+
+    ``shard_offset``: one vector for every row, one row of offsets per row, or None.
+    """
+    rows = np.asarray(cand_idx).shape[0]
+    per_row = shard_offset is not None and np.ndim(shard_offset) == 2
+    res = [dcp_topk_merge_row(cand_vals[r], cand_idx[r], shard_offset[r] if per_row else shard_offset,
+                              k_local, k, pos_stride) for r in range(rows)]
+    if not res:
+        return np.zeros((0, k), dtype=np.int64), np.zeros((0, k))
+    return np.stack([a for a, _ in res]), np.stack([b for _, b in res])
+
+
+# ----------------------------------------------------------------------------
 # a6: request-local index -> physical slot
 # ----------------------------------------------------------------------------
 

@@ -19,7 +19,7 @@ from . import _lib
 __all__ = [
     "IdxError", "idx_k_quant_and_cache", "idx_gather_k", "idx_mqa_logits_prefill",
     "idx_paged_mqa_logits_decode", "idx_topk", "idx_expand_candidates", "idx_sparse_topk_remap",
-    "idx_req_to_global_slots", "idx_block_span", "idx_workspace_bytes", "idx_device_error",
+    "idx_req_to_global_slots", "idx_dcp_topk_merge", "idx_block_span", "idx_workspace_bytes", "idx_device_error",
     "library",
 ]
 
@@ -116,12 +116,32 @@ def idx_paged_mqa_logits_decode(q, w, cache, block_size, block_table, ctx_lens, 
         0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)))
 
 
-def idx_topk(logits, row_ks, row_ke, k, out, ws=None, stream=None):
-    """Per-row top-k indices (request-local), -1 filled; out int32 [rows, >= k]."""
+def idx_topk(logits, row_ks, row_ke, k, out, vals=None, ws=None, stream=None):
+    """Per-row top-k indices (request-local), -1 filled; out int32 [rows, >= k]; optional scores."""
     _check("idx_topk", library().idx_topk(
         _ptr(logits), _dtype_code(logits), _rows(logits), _ptr(row_ks), _ptr(row_ke), logits.shape[0],
-        k, _ptr(out), _rows(out), _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
-        _stream(stream)))
+        k, _ptr(out), _rows(out), _ptr(vals), 0 if vals is None else _rows(vals), _ptr(ws),
+        0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def idx_dcp_topk_merge(cand_vals, cand_idx, shard_offset, k_local, k, out, vals=None, pos_stride=1,
+                       stream=None):
+    """Merge shard-local top-k candidates [rows, n_shards * k_local] into global top-k positions.
+
+    ``shard_offset``: int32 [n_shards] shared by every row, int32 [rows, n_shards]
+    per row, or None (offsets 0). Candidate index i of shard s maps to
+    ``shard_offset[s] + i * pos_stride``.
+    """
+    if shard_offset is None:
+        n_shards, ld_off = cand_vals.shape[1] // k_local, 0
+    elif shard_offset.dim() == 1:
+        n_shards, ld_off = shard_offset.shape[0], 0
+    else:
+        n_shards, ld_off = shard_offset.shape[1], _rows(shard_offset)
+    _check("idx_dcp_topk_merge", library().idx_dcp_topk_merge(
+        _ptr(cand_vals), _rows(cand_vals), _ptr(cand_idx), _rows(cand_idx), _ptr(shard_offset), ld_off,
+        n_shards, pos_stride, k_local, cand_vals.shape[0], k, _ptr(out), _rows(out), _ptr(vals),
+        0 if vals is None else _rows(vals), _stream(stream)))
 
 
 def idx_expand_candidates(cand, row_ks, row_ke, cand_block_size, sbk, sparse_idx, end, stream=None):

@@ -36,8 +36,10 @@ SIGNATURES = {
                                             c_i64, c_ptr, c_i64, c_ptr, c_i32, c_i32, c_ptr, c_i64,
                                             c_i32, c_ptr, c_i32, c_ptr, c_int, c_i64, c_ptr, c_size,
                                             c_ptr]),
-    "idx_topk": (c_int, [c_ptr, c_int, c_i64, c_ptr, c_ptr, c_i32, c_i32, c_ptr, c_i64, c_ptr, c_size,
-                         c_ptr]),
+    "idx_topk": (c_int, [c_ptr, c_int, c_i64, c_ptr, c_ptr, c_i32, c_i32, c_ptr, c_i64, c_ptr, c_i64,
+                         c_ptr, c_size, c_ptr]),
+    "idx_dcp_topk_merge": (c_int, [c_ptr, c_i64, c_ptr, c_i64, c_ptr, c_i64, c_i32, c_i32, c_i32, c_i32,
+                                   c_i32, c_ptr, c_i64, c_ptr, c_i64, c_ptr]),
     "idx_expand_candidates": (c_int, [c_ptr, c_i64, c_i32, c_i32, c_ptr, c_ptr, c_i32, c_i32, c_ptr,
                                       c_i64, c_ptr, c_ptr]),
     "idx_sparse_topk_remap": (c_int, [c_ptr, c_int, c_i64, c_ptr, c_ptr, c_i64, c_ptr, c_i32, c_i32,

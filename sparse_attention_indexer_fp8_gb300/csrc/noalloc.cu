@@ -77,6 +77,6 @@ extern "C" idx_status_t idx_paged_mqa_topk_decode_noalloc(
                                    block_stride_bytes, block_table, ld_bt, ctx_lens, B, 1, nullptr,
                                    0, 0, nullptr, 0, logits, IDX_F32, ld_logits, hist, bytes, stream);
   if (st != IDX_OK) return st;
-  return idx_topk(logits, IDX_F32, ld_logits, nullptr, ctx_lens, B, k, out, ld_out, hist, bytes,
-                  stream);
+  return idx_topk(logits, IDX_F32, ld_logits, nullptr, ctx_lens, B, k, out, ld_out, nullptr, 0, hist,
+                  bytes, stream);
 }

@@ -48,6 +48,22 @@ struct TopkParams {
   int32_t* cols;           // remap: optional chosen columns
   int64_t ld_cols;
   uint32_t* hist;          // optional: precomputed first-digit histogram per row (kBins0 each)
+  float* vals;             // optional: the selected scores (fp32), -inf for empty slots
+  int64_t ld_vals;
+  const int32_t* cand_idx; // merge: shard-local index of every candidate, -1 = empty
+  int64_t ld_ci;
+  const int32_t* shard_off;  // merge: first global position of each shard (NULL = 0)
+  int64_t ld_off;          // merge: row stride of shard_off (0 = one vector for every row)
+  int pos_stride;          // merge: global distance between a shard's consecutive positions
+  int k_local;             // merge: candidates per shard
+  int n_cand;              // merge: candidates per row (shards * k_local)
+};
+
+// What a row selects from and what its outputs mean.
+enum Mode : int {
+  kPlain = 0,   // columns [ks, ke) of a score row -> request-local indices s - ks
+  kRemap = 1,   // sparse columns [0, end) -> request-local positions through the sparse blocks
+  kMerge = 2    // candidate lists of several shards -> global positions, empty entries last
 };
 
 template <bool kBf16>
@@ -94,6 +110,7 @@ struct Shared {
   int n_tie;      // tickets drawn at the last level
   int thr;
   int need;
+  int32_t sel[kMaxK];  // columns chosen so far, in slot order; the outputs are written from them
 };
 
 // Finds the digit `thr` at which the running count of larger digits reaches
@@ -141,24 +158,14 @@ __device__ void find_threshold(Shared& sh, const uint32_t* hist, int nbins) {
   __syncthreads();
 }
 
-template <bool kRemap>
-__device__ __forceinline__ void store_one(const TopkParams& p, int row, int64_t lo, int64_t base_blk,
-                                          int slot, int64_t col) {
-  if constexpr (kRemap) {
-    const int32_t blk = __ldg(p.si + row * p.ld_si + col / p.sbk);
-    p.out[row * p.ld_out + slot] =
-        static_cast<int32_t>((blk - base_blk) * p.sbk + col % p.sbk);
-    if (p.cols) p.cols[row * p.ld_cols + slot] = static_cast<int32_t>(col);
-  } else {
-    p.out[row * p.ld_out + slot] = static_cast<int32_t>(col - lo);
-  }
+__device__ __forceinline__ void store_one(Shared& sh, int slot, int64_t col) {
+  sh.sel[slot] = static_cast<int32_t>(col);
 }
 
 // One selection pass at `level` over a source of (key, column) pairs.
 // Elements matching the prefix with digit > thr are stored; digit == thr are
 // handed to the next level (appended to `next_keys/next_cols` if room, and
 // counted into `next_hist`), or, at the last level, stored while tickets last.
-template <bool kRemap>
 __device__ __forceinline__ void visit(const TopkParams& p, Shared& sh, int row, int64_t lo,
                                       int64_t base_blk, int level, uint32_t prefix, bool valid,
                                       uint32_t key, int64_t col, uint32_t* next_keys,
@@ -172,7 +179,7 @@ __device__ __forceinline__ void visit(const TopkParams& p, Shared& sh, int row, 
   const bool above = in && d > thr;
   const bool tie = in && d == thr;
   const int s = warp_reserve(&sh.n_out, above);
-  if (above && s < p.k) store_one<kRemap>(p, row, lo, base_blk, s, col);
+  if (above && s < p.k) store_one(sh, s, col);
   if (level < 2) {
     if (next_keys) {
       const int t = warp_reserve(next_n, tie);
@@ -186,7 +193,7 @@ __device__ __forceinline__ void visit(const TopkParams& p, Shared& sh, int row, 
     const int t = warp_reserve(&sh.n_tie, tie);
     if (tie && t < sh.need) {
       const int slot = atomicAdd(&sh.n_out, 1);
-      if (slot < p.k) store_one<kRemap>(p, row, lo, base_blk, slot, col);
+      if (slot < p.k) store_one(sh, slot, col);
     }
   }
 }
@@ -260,7 +267,7 @@ __device__ __forceinline__ int warp_excl_scan(int v, int* total) {
 // it, or below), and one warp scan per class reserves output / bucket slots for
 // all of them. Most elements are below the threshold and cost a handful of
 // integer operations; the collectives are paid once per 16 elements.
-template <bool kBf16, bool kRemap>
+template <bool kBf16>
 __device__ __forceinline__ void level0_body(const TopkParams& p, Shared& sh, int row, int64_t lo,
                                             int64_t base_blk, const void* rowp, int64_t a1,
                                             int64_t nvec, uint32_t* keys_a, int32_t* cols_a) {
@@ -318,7 +325,7 @@ __device__ __forceinline__ void level0_body(const TopkParams& p, Shared& sh, int
         const int d = static_cast<int>(k >> 22);
         const int64_t c = a1 + v * kVec + e;
         if (d > thr) {
-          if (base_ab < p.k) store_one<kRemap>(p, row, lo, base_blk, base_ab, c);
+          if (base_ab < p.k) store_one(sh, base_ab, c);
           ++base_ab;
         } else if (d == thr) {
           if (base_tie < kCapA) {
@@ -333,7 +340,102 @@ __device__ __forceinline__ void level0_body(const TopkParams& p, Shared& sh, int
   }
 }
 
-template <bool kBf16, bool kRemap>
+// Score of column c as fp32.
+template <bool kBf16>
+__device__ __forceinline__ float value_at(const void* row, int64_t c) {
+  if constexpr (kBf16) {
+    return __uint_as_float(static_cast<uint32_t>(__ldg(static_cast<const uint16_t*>(row) + c)) << 16);
+  } else {
+    return __ldg(static_cast<const float*>(row) + c);
+  }
+}
+
+// Writes the row's outputs from the chosen columns sh.sel[0, m): mode-specific
+// indices (and optionally columns and scores), -1 / -inf in the unused slots.
+// In merge mode, candidates without a position are dropped and the remaining
+// entries are compacted to the front in slot order.
+template <bool kBf16, int kMode>
+__device__ __forceinline__ void write_outputs(const TopkParams& p, Shared& sh, int row, int64_t lo,
+                                              const void* rowp, int m) {
+  const int tid = threadIdx.x;
+  const int K = p.k;
+  const float ninf = -__int_as_float(0x7f800000);
+  int32_t* out = p.out + row * p.ld_out;
+  float* vals = p.vals ? p.vals + row * p.ld_vals : nullptr;
+  if constexpr (kMode != kMerge) {
+    const int64_t base_blk = (kMode == kRemap && p.row_ks) ? __ldg(p.row_ks + row) / p.sbk : 0;
+    for (int i = tid; i < K; i += kThreads) {
+      int32_t o = -1, cl = -1;
+      float v = ninf;
+      if (i < m) {
+        const int64_t c = sh.sel[i];
+        cl = static_cast<int32_t>(c);
+        if constexpr (kMode == kRemap) {
+          const int32_t blk = __ldg(p.si + row * p.ld_si + c / p.sbk);
+          o = static_cast<int32_t>((blk - base_blk) * p.sbk + c % p.sbk);
+        } else {
+          o = static_cast<int32_t>(c - lo);
+        }
+        if (vals) v = value_at<kBf16>(rowp, c);
+      }
+      out[i] = o;
+      if (kMode == kRemap && p.cols) p.cols[row * p.ld_cols + i] = cl;
+      if (vals) vals[i] = v;
+    }
+  } else {
+    // each thread owns up to 4 consecutive slots; one block scan orders the valid ones
+    constexpr int kPer = kMaxK / kThreads;
+    int32_t g[kPer];
+    float v[kPer];
+    int cnt = 0;
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+      const int i = tid * kPer + e;
+      g[e] = -1;
+      v[e] = ninf;
+      if (i < m) {
+        const int c = sh.sel[i];
+        const int32_t idx = __ldg(p.cand_idx + row * p.ld_ci + c);
+        if (idx >= 0) {
+          const int32_t off = p.shard_off ? __ldg(p.shard_off + row * p.ld_off + c / p.k_local) : 0;
+          g[e] = off + idx * p.pos_stride;
+          v[e] = value_at<false>(rowp, c);
+          ++cnt;
+        }
+      }
+    }
+    const int lane = tid & 31, warp = tid >> 5;
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += n;
+    }
+    __syncthreads();  // sh.warp_tot may still be read by the last threshold search
+    if (lane == 31) sh.warp_tot[warp] = incl;
+    __syncthreads();
+    int before = incl - cnt;
+    for (int w = 0; w < warp; ++w) before += sh.warp_tot[w];
+    int total = 0;
+    for (int w = 0; w < kThreads / 32; ++w) total += sh.warp_tot[w];
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+      if (g[e] >= 0) {
+        if (before < K) {
+          out[before] = g[e];
+          if (vals) vals[before] = v[e];
+        }
+        ++before;
+      }
+    }
+    for (int i = total + tid; i < K; i += kThreads) {
+      out[i] = -1;
+      if (vals) vals[i] = ninf;
+    }
+  }
+}
+
+template <bool kBf16, int kMode>
 __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p) {
   extern __shared__ __align__(16) uint8_t dyn[];
   __shared__ Shared sh;
@@ -344,11 +446,14 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p) {
 
   const int row = blockIdx.x;
   const int tid = threadIdx.x;
-  int64_t lo, hi, base_blk = 0;
-  if constexpr (kRemap) {
+  const int64_t base_blk = 0;
+  int64_t lo, hi;
+  if constexpr (kMode == kRemap) {
     lo = 0;
     hi = __ldg(p.end + row);
-    base_blk = p.row_ks ? __ldg(p.row_ks + row) / p.sbk : 0;
+  } else if constexpr (kMode == kMerge) {
+    lo = 0;
+    hi = p.n_cand;
   } else {
     lo = p.row_ks ? __ldg(p.row_ks + row) : 0;
     hi = __ldg(p.row_ke + row);
@@ -360,20 +465,14 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p) {
       : static_cast<const void*>(static_cast<const float*>(p.logits) + row * p.ld);
 
   if (n <= K) {
+    // every visible column is kept, in column order
     if (p.hist) {
       uint32_t* g = p.hist + static_cast<int64_t>(row) * kBins0;
       for (int i = tid; i < kBins0; i += kThreads) g[i] = 0;
     }
-    for (int i = tid; i < K; i += kThreads) {
-      if (i < n) {
-        store_one<kRemap>(p, row, lo, base_blk, i, lo + i);
-      } else {
-        p.out[row * p.ld_out + i] = -1;
-        if constexpr (kRemap) {
-          if (p.cols) p.cols[row * p.ld_cols + i] = -1;
-        }
-      }
-    }
+    for (int i = tid; i < n; i += kThreads) sh.sel[i] = static_cast<int32_t>(lo + i);
+    __syncthreads();
+    write_outputs<kBf16, kMode>(p, sh, row, lo, rowp, static_cast<int>(n));
     return;
   }
 
@@ -421,9 +520,9 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p) {
     const int nt = static_cast<int>(hi - a2);
     const bool valid = tid < nh + nt;
     const int64_t c = tid < nh ? lo + tid : a2 + (tid - nh);
-    visit<kRemap>(p, sh, row, lo, base_blk, 0, 0u, valid, valid ? key_at<kBf16>(rowp, c) : 0u, c,
+    visit(p, sh, row, lo, base_blk, 0, 0u, valid, valid ? key_at<kBf16>(rowp, c) : 0u, c,
                   keys_a, cols_a, &sh.n_a, kCapA, sh.hist[1]);
-    level0_body<kBf16, kRemap>(p, sh, row, lo, base_blk, rowp, a1, nvec, keys_a, cols_a);
+    level0_body<kBf16>(p, sh, row, lo, base_blk, rowp, a1, nvec, keys_a, cols_a);
   }
   uint32_t prefix = static_cast<uint32_t>(sh.thr) << 22;
   __syncthreads();
@@ -438,12 +537,12 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p) {
     for (int base = 0; base < na; base += kThreads) {
       const int i = base + tid;
       const bool valid = i < na;
-      visit<kRemap>(p, sh, row, lo, base_blk, 1, prefix, valid, valid ? keys_a[i] : 0u,
+      visit(p, sh, row, lo, base_blk, 1, prefix, valid, valid ? keys_a[i] : 0u,
                     valid ? cols_a[i] : 0, keys_b, cols_b, &sh.n_b, kCapB, sh.hist[0]);
     }
   } else {
     sweep_row<kBf16>(rowp, lo, hi, [&](bool valid, int64_t c, uint32_t key) {
-      visit<kRemap>(p, sh, row, lo, base_blk, 1, prefix, valid, key, c, keys_b, cols_b, &sh.n_b,
+      visit(p, sh, row, lo, base_blk, 1, prefix, valid, key, c, keys_b, cols_b, &sh.n_b,
                     kCapB, sh.hist[0]);
     });
   }
@@ -458,31 +557,27 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p) {
     for (int base = 0; base < nb; base += kThreads) {
       const int i = base + tid;
       const bool valid = i < nb;
-      visit<kRemap>(p, sh, row, lo, base_blk, 2, prefix, valid, valid ? keys_b[i] : 0u,
+      visit(p, sh, row, lo, base_blk, 2, prefix, valid, valid ? keys_b[i] : 0u,
                     valid ? cols_b[i] : 0, nullptr, nullptr, nullptr, 0, nullptr);
     }
   } else if (a_ok) {
     for (int base = 0; base < na; base += kThreads) {
       const int i = base + tid;
       const bool valid = i < na;
-      visit<kRemap>(p, sh, row, lo, base_blk, 2, prefix, valid, valid ? keys_a[i] : 0u,
+      visit(p, sh, row, lo, base_blk, 2, prefix, valid, valid ? keys_a[i] : 0u,
                     valid ? cols_a[i] : 0, nullptr, nullptr, nullptr, 0, nullptr);
     }
   } else {
     sweep_row<kBf16>(rowp, lo, hi, [&](bool valid, int64_t c, uint32_t key) {
-      visit<kRemap>(p, sh, row, lo, base_blk, 2, prefix, valid, key, c, nullptr, nullptr, nullptr,
+      visit(p, sh, row, lo, base_blk, 2, prefix, valid, key, c, nullptr, nullptr, nullptr,
                     0, nullptr);
     });
   }
-  // With exact counts exactly k entries were written. A histogram that does not
-  // match the scores (a misused workspace) can leave a short row: complete it.
+  // With exact counts exactly k columns were chosen. A histogram that does not
+  // match the scores (a misused workspace) can leave a short row: it is
+  // completed with -1 by the output pass.
   __syncthreads();
-  for (int i = sh.n_out + tid; i < K; i += kThreads) {
-    p.out[row * p.ld_out + i] = -1;
-    if constexpr (kRemap) {
-      if (p.cols) p.cols[row * p.ld_cols + i] = -1;
-    }
-  }
+  write_outputs<kBf16, kMode>(p, sh, row, lo, rowp, min(sh.n_out, K));
 }
 
 }  // namespace
@@ -505,9 +600,9 @@ idx_status_t attach_hist(const char* fn, TopkParams* p, int rows, void* ws, size
   return IDX_OK;
 }
 
-template <bool kBf16, bool kRemap>
+template <bool kBf16, int kMode>
 idx_status_t launch_topk(const TopkParams& p, int rows, cudaStream_t stream, const char* fn) {
-  auto kern = topk_kernel<kBf16, kRemap>;
+  auto kern = topk_kernel<kBf16, kMode>;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -524,11 +619,12 @@ idx_status_t launch_topk(const TopkParams& p, int rows, cudaStream_t stream, con
 
 extern "C" idx_status_t idx_topk(const void* logits, int dtype, int64_t ld, const int32_t* row_ks,
                                  const int32_t* row_ke, int32_t rows, int32_t k, int32_t* out,
-                                 int64_t ld_out, void* ws, size_t ws_bytes, cudaStream_t stream) {
+                                 int64_t ld_out, float* vals, int64_t ld_vals, void* ws,
+                                 size_t ws_bytes, cudaStream_t stream) {
   const char* fn = "idx_topk";
   if (rows < 0 || k < 1) return fail(IDX_ERR_INVALID_ARG, "%s: rows < 0 or k < 1", fn);
   if (k > kMaxK) return fail(IDX_ERR_UNSUPPORTED, "%s: k %d exceeds %d", fn, k, kMaxK);
-  if (ld_out < k) return fail(IDX_ERR_INVALID_ARG, "%s: ld_out < k", fn);
+  if (ld_out < k || (vals && ld_vals < k)) return fail(IDX_ERR_INVALID_ARG, "%s: output stride < k", fn);
   if (dtype != IDX_F32 && dtype != IDX_BF16) return fail(IDX_ERR_UNSUPPORTED, "%s: dtype %d", fn, dtype);
   if (rows == 0) return IDX_OK;
   if (!logits || !row_ke || !out) return fail(IDX_ERR_INVALID_ARG, "%s: NULL pointer", fn);
@@ -542,8 +638,10 @@ extern "C" idx_status_t idx_topk(const void* logits, int dtype, int64_t ld, cons
   p.k = k;
   p.out = out;
   p.ld_out = ld_out;
-  return dtype == IDX_BF16 ? launch_topk<true, false>(p, rows, stream, fn)
-                           : launch_topk<false, false>(p, rows, stream, fn);
+  p.vals = vals;
+  p.ld_vals = ld_vals;
+  return dtype == IDX_BF16 ? launch_topk<true, kPlain>(p, rows, stream, fn)
+                           : launch_topk<false, kPlain>(p, rows, stream, fn);
 }
 
 extern "C" idx_status_t idx_sparse_topk_remap(const void* sparse_logits, int dtype, int64_t ld,
@@ -574,6 +672,43 @@ extern "C" idx_status_t idx_sparse_topk_remap(const void* sparse_logits, int dty
   p.ld_out = ld_pos;
   p.cols = col_scratch;
   p.ld_cols = ld_col;
-  return dtype == IDX_BF16 ? launch_topk<true, true>(p, rows, stream, fn)
-                           : launch_topk<false, true>(p, rows, stream, fn);
+  return dtype == IDX_BF16 ? launch_topk<true, kRemap>(p, rows, stream, fn)
+                           : launch_topk<false, kRemap>(p, rows, stream, fn);
+}
+
+extern "C" idx_status_t idx_dcp_topk_merge(const float* cand_vals, int64_t ld_v,
+                                           const int32_t* cand_idx, int64_t ld_i,
+                                           const int32_t* shard_offset, int64_t ld_off,
+                                           int32_t n_shards, int32_t pos_stride, int32_t k_local,
+                                           int32_t rows, int32_t k, int32_t* out, int64_t ld_out,
+                                           float* vals, int64_t ld_vals, cudaStream_t stream) {
+  const char* fn = "idx_dcp_topk_merge";
+  if (rows < 0 || k < 1 || n_shards < 1 || k_local < 1 || pos_stride < 1) {
+    return fail(IDX_ERR_INVALID_ARG,
+                "%s: rows < 0, k < 1, n_shards < 1, k_local < 1 or pos_stride < 1", fn);
+  }
+  if (ld_off != 0 && ld_off < n_shards) return fail(IDX_ERR_INVALID_ARG, "%s: 0 < ld_off < n_shards", fn);
+  if (k > kMaxK) return fail(IDX_ERR_UNSUPPORTED, "%s: k %d exceeds %d", fn, k, kMaxK);
+  const int64_t n_cand = static_cast<int64_t>(n_shards) * k_local;
+  if (n_cand > INT32_MAX / 2) return fail(IDX_ERR_UNSUPPORTED, "%s: too many candidates", fn);
+  if (ld_v < n_cand || ld_i < n_cand) return fail(IDX_ERR_INVALID_ARG, "%s: candidate stride < n_shards * k_local", fn);
+  if (ld_out < k || (vals && ld_vals < k)) return fail(IDX_ERR_INVALID_ARG, "%s: output stride < k", fn);
+  if (rows == 0) return IDX_OK;
+  if (!cand_vals || !cand_idx || !out) return fail(IDX_ERR_INVALID_ARG, "%s: NULL pointer", fn);
+  TopkParams p{};
+  p.logits = cand_vals;
+  p.ld = ld_v;
+  p.cand_idx = cand_idx;
+  p.ld_ci = ld_i;
+  p.shard_off = shard_offset;
+  p.ld_off = ld_off;
+  p.pos_stride = pos_stride;
+  p.k_local = k_local;
+  p.n_cand = static_cast<int>(n_cand);
+  p.k = k;
+  p.out = out;
+  p.ld_out = ld_out;
+  p.vals = vals;
+  p.ld_vals = ld_vals;
+  return launch_topk<false, kMerge>(p, rows, stream, fn);
 }

@@ -3,9 +3,12 @@
 ``fill_paged_cache`` inserts a workload's k into a device cache through
 ``idx_k_quant_and_cache``; ``DecodeStep`` owns the device buffers of one dense
 decode step (k insert of the new tokens, paged logits, top-k, slot conversion)
-and ``HierarchicalStep`` those of one V4.1 consumer-layer step (candidate
-expansion, sparse logits, sparse top-k with remap, slot conversion). Buffers are
-allocated once at construction; ``run`` allocates nothing.
+``HierarchicalStep`` those of one V4.1 consumer-layer step (candidate
+expansion, sparse logits, sparse top-k with remap, slot conversion), and
+``DcpDecodeStep`` those of one rank of a context-parallel decode step (scoring
+of the rank's own shard, local top-k with scores, one exchange, merge). Buffers
+are allocated once at construction; ``run`` allocates nothing but the exchange's
+receive lists.
 """
 
 from __future__ import annotations
@@ -13,8 +16,8 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import (idx_expand_candidates, idx_k_quant_and_cache, idx_paged_mqa_logits_decode,
-               idx_req_to_global_slots, idx_sparse_topk_remap, idx_topk)
+from . import (idx_dcp_topk_merge, idx_expand_candidates, idx_k_quant_and_cache,
+               idx_paged_mqa_logits_decode, idx_req_to_global_slots, idx_sparse_topk_remap, idx_topk)
 from . import workloads as W
 
 
@@ -120,3 +123,66 @@ class HierarchicalStep:
         idx_req_to_global_slots(self.positions, None, block_table, self.block_size, self.block_size,
                                 self.slots, stream=stream)
         return self.slots
+
+
+def exchange_candidates(vals: torch.Tensor, idx: torch.Tensor, group=None):
+    """The one exchange of context-parallel decode: every rank's local top-k.
+
+    [DSA] 几个容易踩的点: ranks that each hold a shard of a long context send
+    each other only their local (score, index) lists, never the score matrix.
+    ``vals`` float32 / ``idx`` int32 ``[rows, k_local]`` on each rank become
+    ``[rows, world * k_local]`` on every rank, rank after rank along the row, the
+    candidate layout ``idx_dcp_topk_merge`` reads. Any backend whose tensors
+    these are will do (gloo with host tensors, NCCL with device tensors).
+    """
+    import torch.distributed as dist
+
+    world = dist.get_world_size(group)
+    gv = [torch.empty_like(vals) for _ in range(world)]
+    gi = [torch.empty_like(idx) for _ in range(world)]
+    dist.all_gather(gv, vals.contiguous(), group=group)
+    dist.all_gather(gi, idx.contiguous(), group=group)
+    return torch.cat(gv, dim=1), torch.cat(gi, dim=1)
+
+
+class DcpDecodeStep:
+    """One rank of a context-parallel decode step.
+
+    The rank's paged cache holds only its shard of every request's context
+    (``ctx_lens`` are shard lengths). ``select_local`` scores that shard and keeps
+    its top-k with scores; ``merge`` turns every rank's lists, gathered rank after
+    rank, into global top-k positions; ``run`` chains the two around
+    ``exchange_candidates``. ``shard_offset`` / ``pos_stride`` give each rank's
+    global positions (see ``idx_dcp_topk_merge``): per-request first positions of
+    contiguous shards ([rows, world], stride 1), or ``arange(world)`` with stride
+    ``world`` when tokens are dealt round-robin.
+    """
+
+    def __init__(self, batch: int, max_shard_ctx: int, world: int, topk: int = W.TOPK,
+                 block_size: int = W.BLOCK_SIZE, device="cuda"):
+        self.topk, self.block_size, self.world = topk, block_size, world
+        ld = (max_shard_ctx + 63) // 64 * 64
+        self.logits = torch.empty((batch, ld), dtype=torch.float32, device=device)
+        self.cand_vals = torch.empty((batch, topk), dtype=torch.float32, device=device)
+        self.cand_idx = torch.empty((batch, topk), dtype=torch.int32, device=device)
+        self.positions = torch.empty((batch, topk), dtype=torch.int32, device=device)
+        self.scores = torch.empty((batch, topk), dtype=torch.float32, device=device)
+        self.ws = torch.zeros((batch, 1024), dtype=torch.int32, device=device)
+
+    def select_local(self, q, w, cache, block_table, ctx_lens, stream=None):
+        idx_paged_mqa_logits_decode(q, w, cache, self.block_size, block_table, ctx_lens, self.logits,
+                                    ws=self.ws, stream=stream)
+        idx_topk(self.logits, None, ctx_lens, self.topk, self.cand_idx, vals=self.cand_vals, ws=self.ws,
+                 stream=stream)
+        return self.cand_vals, self.cand_idx
+
+    def merge(self, all_vals, all_idx, shard_offset, pos_stride: int = 1, stream=None):
+        idx_dcp_topk_merge(all_vals, all_idx, shard_offset, self.topk, self.topk, self.positions,
+                           vals=self.scores, pos_stride=pos_stride, stream=stream)
+        return self.positions
+
+    def run(self, q, w, cache, block_table, ctx_lens, shard_offset, pos_stride: int = 1, group=None):
+        """All three stages on torch's current stream, which the exchange also orders on."""
+        self.select_local(q, w, cache, block_table, ctx_lens)
+        all_vals, all_idx = exchange_candidates(self.cand_vals, self.cand_idx, group)
+        return self.merge(all_vals, all_idx, shard_offset, pos_stride)

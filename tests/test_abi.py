@@ -63,8 +63,18 @@ def test_validation_rejects_before_touching_the_device(lib):
     # block stride too small for 64 tokens of 132 bytes
     assert lib.idx_k_quant_and_cache(fake, 1, 128, 4, fake, fake, 8, 64, 8000, 0, None) == 1
     # k above the selection limit, NULL logits
-    assert lib.idx_topk(fake, 0, 4096, None, fake, 4, 5000, fake, 5000, None, 0, None) == 2
-    assert lib.idx_topk(None, 0, 4096, None, fake, 4, 2048, fake, 2048, None, 0, None) == 1
+    assert lib.idx_topk(fake, 0, 4096, None, fake, 4, 5000, fake, 5000, None, 0, None, 0, None) == 2
+    assert lib.idx_topk(None, 0, 4096, None, fake, 4, 2048, fake, 2048, None, 0, None, 0, None) == 1
+    # merge: candidate stride smaller than n_shards * k_local
+    assert lib.idx_dcp_topk_merge(fake, 100, fake, 100, fake, 0, 4, 1, 2048, 2, 2048, fake, 2048, None,
+                                  0, None) == 1
+    # per-row offsets narrower than the shard count; position stride 0
+    assert lib.idx_dcp_topk_merge(fake, 8192, fake, 8192, fake, 2, 4, 1, 2048, 2, 2048, fake, 2048, None,
+                                  0, None) == 1
+    assert lib.idx_dcp_topk_merge(fake, 8192, fake, 8192, fake, 0, 4, 0, 2048, 2, 2048, fake, 2048, None,
+                                  0, None) == 1
+    assert lib.idx_dcp_topk_merge(fake, 8192, fake, 8192, fake, 0, 4, 1, 2048, 2, 5000, fake, 5000, None,
+                                  0, None) == 2
     # candidate count not a power of two
     assert lib.idx_expand_candidates(fake, 64, 4, 48, None, fake, 64, 64, fake, 64, fake, None) == 2
     # block_span smaller than block_size

@@ -17,7 +17,8 @@ import sparse_attention_indexer_fp8_gb300 as idx
 from oracle import indexer as O
 from oracle.codecs import bf16_decode
 from sparse_attention_indexer_fp8_gb300 import workloads as W
-from sparse_attention_indexer_fp8_gb300.pipeline import DecodeStep, HierarchicalStep, fill_paged_cache
+from sparse_attention_indexer_fp8_gb300.pipeline import (DcpDecodeStep, DecodeStep, HierarchicalStep,
+                                                         fill_paged_cache)
 from tests.checks import BF16_REL, assert_logits_close, assert_topk_row
 
 pytestmark = pytest.mark.gpu
@@ -142,3 +143,43 @@ def test_hierarchical_many_tiles_per_cta_every_row():
     # boundaries, inactive tails and unpaired commit groups; every row is checked
     wl = W.hierarchical(seed=2024, batch=128, ctx=16384, n_cand=64)
     _hierarchical(wl, list(range(0, 128, 1)))
+
+
+def test_dcp_four_emulated_ranks_paged_decode():
+    # Context-parallel decode of the paged decode workload (64 requests of 8K-32K
+    # tokens) with four ranks emulated on one GPU: rank r scores the r-th quarter
+    # of every request's blocks through its own block table, keeps its local
+    # top-2048 with scores, the lists are concatenated rank after rank (the
+    # all-gather), and the merge must give the whole context's top-2048.
+    wl, world = W.paged_decode(), 4
+    pool, B, bs = wl.pool, wl.batch, wl.pool.block_size
+    cache = torch.zeros((pool.num_blocks, W.block_stride_bytes()), dtype=torch.uint8, device=DEV)
+    fill_paged_cache(pool, wl.seed, cache, device_k=True)
+    L = pool.ctx_lens.astype(np.int64)
+    nblk = (L + bs - 1) // bs
+    starts = np.stack([np.minimum(nblk * r // world * bs, L) for r in range(world + 1)], axis=1)
+    q, w = torch.from_numpy(wl.q8).to(DEV), torch.from_numpy(wl.w).to(DEV)
+    steps, cv, ci = [], [], []
+    for rank in range(world):
+        lens = (starts[:, rank + 1] - starts[:, rank]).astype(np.int32)
+        bt = np.zeros_like(pool.block_table)
+        for b in range(B):
+            first, cnt = int(starts[b, rank]) // bs, (int(lens[b]) + bs - 1) // bs
+            bt[b, :cnt] = pool.block_table[b, first:first + cnt]
+        stp = DcpDecodeStep(B, int(lens.max()), world)
+        v, i = stp.select_local(q, w, cache, torch.from_numpy(bt).to(DEV), torch.from_numpy(lens).to(DEV))
+        steps.append(stp)
+        cv.append(v)
+        ci.append(i)
+    offs = torch.from_numpy(starts[:, :world].astype(np.int32)).to(DEV)
+    pos = steps[0].merge(torch.cat(cv, 1), torch.cat(ci, 1), offs).cpu().numpy()
+    sc = steps[0].scores.cpu().numpy()
+    idx.idx_device_error()
+    assert all(not s.ws.any().item() for s in steps)
+    rng = np.random.default_rng(wl.seed + 1)
+    for b in sorted(rng.choice(B, size=4, replace=False).tolist()):
+        n = int(L[b])
+        k8, ks = O.k_quant(_k_host(wl.seed, b, n))
+        ref = O.logits_row(wl.q8[b], wl.w[b], k8, ks)
+        assert_topk_row(pos[b], ref, wl.topk, f"dcp top-k row {b}")
+        assert_logits_close(sc[b], ref[pos[b]], f"dcp scores row {b}")

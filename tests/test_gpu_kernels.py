@@ -316,6 +316,167 @@ def test_topk_bf16_and_wide_rows():
         assert set(out[r].tolist()) == set(ref.tolist())
 
 
+@pytest.mark.parametrize("bf16", [False, True])
+def test_topk_values_output(bf16):
+    # the optional score output: the score of every selected column, -inf in -1 slots
+    width, k = 9000, 2048
+    x = W.make_logits(13, 5, width, ties=True)
+    ke = np.array([width, 5000, 2048, 100, 0], dtype=np.int32)
+    if bf16:
+        xb = bf16_encode(x)
+        t, vals = dev_bf16(xb), bf16_decode(xb)
+    else:
+        t, vals = dev(x), x
+    out = torch.full((5, k + 3), -7, dtype=torch.int32, device=DEV)
+    sc = torch.full((5, k + 1), 7.0, dtype=torch.float32, device=DEV)
+    idx.idx_topk(t, None, dev(ke), k, out, vals=sc[:, :k + 1])
+    o, v = out.cpu().numpy(), sc.cpu().numpy()
+    for r in range(5):
+        n = int(ke[r])
+        m = min(n, k)
+        assert_topk_values_exact(o[r], vals[r, :n], k, f"row {r}")
+        assert np.array_equal(v[r, :m], vals[r, o[r, :m]].astype(np.float32)), f"scores row {r}"
+        assert np.all(np.isneginf(v[r, m:k])) and v[r, k] == 7.0
+
+
+def _oracle_candidates(row, bounds, k_local):
+    """Each shard's local top-k by the oracle: (values, shard-local indices), -inf / -1 padded."""
+    n_shards = len(bounds) - 1
+    cv = np.full(n_shards * k_local, -np.inf, dtype=np.float32)
+    ci = np.full(n_shards * k_local, -1, dtype=np.int32)
+    for s in range(n_shards):
+        loc = O.topk_row(row, int(bounds[s]), int(bounds[s + 1]), k_local)
+        ok = loc >= 0
+        ci[s * k_local:(s + 1) * k_local] = loc
+        cv[s * k_local:(s + 1) * k_local][ok] = row[bounds[s] + loc[ok]]
+    return cv, ci
+
+
+def _check_merge(pos, v, cand_pos, cand_val, k, what):
+    """Merged output against the oracle's merge of the same candidates: the value
+    multiset is unique; each position must be a distinct candidate with its value."""
+    ref_p, ref_v = O.dcp_topk_merge_row(cand_val, cand_pos, None, len(cand_pos), k)
+    m = int(np.sum(ref_p >= 0))
+    assert np.all(pos[m:k] == -1) and np.all(np.isneginf(v[m:k])), f"{what}: tail"
+    assert len(np.unique(pos[:m])) == m and np.all(pos[:m] >= 0), f"{what}: positions"
+    assert np.array_equal(np.sort(v[:m].astype(np.float64))[::-1], ref_v[:m]), f"{what}: values"
+    lut = {}
+    for p_, v_ in zip(cand_pos.tolist(), cand_val.tolist()):
+        if p_ >= 0:
+            lut[p_] = v_
+    assert all(lut.get(int(p_)) == float(v_) for p_, v_ in zip(pos[:m], v[:m])), f"{what}: pairs"
+
+
+def _shard_candidates(x_row, n, n_shards, k_local, mode, rng):
+    """Oracle local top-k of one row's shards: (values, local indices, offsets, stride)."""
+    if mode == "interleaved":            # token t lives on shard t % n_shards
+        cv = np.full(n_shards * k_local, -np.inf, dtype=np.float32)
+        ci = np.full(n_shards * k_local, -1, dtype=np.int32)
+        for s in range(n_shards):
+            loc_row = x_row[s:n:n_shards]
+            loc = O.topk_row(loc_row, 0, len(loc_row), k_local)
+            ok = loc >= 0
+            ci[s * k_local:(s + 1) * k_local] = loc
+            cv[s * k_local:(s + 1) * k_local][ok] = loc_row[loc[ok]]
+        return cv, ci, np.arange(n_shards, dtype=np.int32), n_shards
+    cuts = np.sort(rng.integers(0, n + 1, n_shards - 1))
+    b = np.concatenate([[0], cuts, [n]]).astype(np.int64)
+    cv, ci = _oracle_candidates(x_row, b, k_local)
+    return cv, ci, b[:-1].astype(np.int32), 1
+
+
+@pytest.mark.parametrize("mode", ["per_row", "interleaved"])
+@pytest.mark.parametrize("n_shards,k_local,k", [(2, 2048, 2048), (8, 2048, 2048), (3, 700, 2048),
+                                                (4, 512, 1000), (1, 100, 64), (5, 300, 4096)])
+def test_dcp_merge_vs_oracle(n_shards, k_local, k, mode):
+    # candidates from the oracle's local top-k of seeded rows (ties included),
+    # merged by the library and by the oracle
+    rows, width = 6, 20000
+    x = W.make_logits(14 + n_shards, rows, width, ties=True)
+    x[1] = np.float32(0.5)                                  # every candidate ties
+    rng = np.random.default_rng(n_shards * 1000 + k_local)
+    lens = rng.integers(0, width + 1, rows)
+    lens[0], lens[2] = width, 37                            # full row; fewer candidates than k
+    cv = np.zeros((rows, n_shards * k_local), dtype=np.float32)
+    ci = np.zeros((rows, n_shards * k_local), dtype=np.int32)
+    offs = np.zeros((rows, n_shards), dtype=np.int32)
+    for r in range(rows):
+        cv[r], ci[r], offs[r], stride = _shard_candidates(x[r], int(lens[r]), n_shards, k_local, mode, rng)
+    d_offs = dev(offs[0]) if mode == "interleaved" else dev(offs)   # shared vector / one per row
+    out = torch.full((rows, k + 2), -7, dtype=torch.int32, device=DEV)
+    sc = torch.empty((rows, k), dtype=torch.float32, device=DEV)
+    idx.idx_dcp_topk_merge(dev(cv), dev(ci), d_offs, k_local, k, out, vals=sc, pos_stride=stride)
+    o, v = out.cpu().numpy(), sc.cpu().numpy()
+    assert np.all(o[:, k:] == -7)
+    gpos = np.where(ci >= 0, offs.repeat(k_local, axis=1) + ci * stride, -1).astype(np.int32)
+    for r in range(rows):
+        _check_merge(o[r], v[r], gpos[r], cv[r], k, f"row {r}")
+        ref_p, _ = O.dcp_topk_merge_row(cv[r], ci[r], offs[r], k_local, k, stride)
+        m = int(np.sum(ref_p >= 0))
+        if len(np.unique(cv[r][ci[r] >= 0])) == int(np.sum(ci[r] >= 0)):   # no ties: unique set
+            assert set(o[r, :m].tolist()) == set(ref_p[:m].tolist())
+    # indices already global: the same selection without offsets
+    out2 = torch.full((rows, k), -7, dtype=torch.int32, device=DEV)
+    idx.idx_dcp_topk_merge(dev(cv), dev(gpos), None, k_local, k, out2)
+    o2 = out2.cpu().numpy()
+    for r in range(rows):
+        lut = dict(zip(gpos[r].tolist(), cv[r].tolist()))
+        v2 = np.array([lut[p_] if p_ >= 0 else -np.inf for p_ in o2[r].tolist()], dtype=np.float32)
+        _check_merge(o2[r], v2, gpos[r], cv[r], k, f"global-index row {r}")
+
+
+@pytest.mark.parametrize("n_shards", [2, 4, 8])
+def test_dcp_emulated_ranks_equal_whole_row_topk(n_shards):
+    # Every rank selects within its own shard of the row on the device (top-k with
+    # scores, written straight into its part of the exchange buffer); the merge of
+    # the exchanged lists is the whole row's top-k.
+    rows, width, k = 6, 131072, 2048
+    x = W.make_logits(20 + n_shards, rows, width, ties=n_shards == 4)
+    x[3, ::2] = np.float32(1.0)                             # 65536 equal top scores
+    lens = np.array([width, 100000, 3000, width, 2048 * n_shards, 1], dtype=np.int64)
+    bounds = np.linspace(0, width, n_shards + 1).astype(np.int64)
+    bounds[1:-1] = bounds[1:-1] // 16 * 16 + 3              # ragged, unaligned shard starts
+    t = dev(x)
+    cv = torch.empty((rows, n_shards * k), dtype=torch.float32, device=DEV)
+    ci = torch.empty((rows, n_shards * k), dtype=torch.int32, device=DEV)
+    for s in range(n_shards):
+        lo, hi = int(bounds[s]), int(bounds[s + 1])
+        ke = np.clip(lens - lo, 0, hi - lo).astype(np.int32)
+        idx.idx_topk(t[:, lo:], None, dev(ke), k, ci[:, s * k:(s + 1) * k],
+                     vals=cv[:, s * k:(s + 1) * k])
+    out = torch.empty((rows, k), dtype=torch.int32, device=DEV)
+    sc = torch.empty((rows, k), dtype=torch.float32, device=DEV)
+    idx.idx_dcp_topk_merge(cv, ci, dev(bounds[:-1].astype(np.int32)), k, k, out, vals=sc)
+    o, v = out.cpu().numpy(), sc.cpu().numpy()
+    for r in range(rows):
+        n = int(lens[r])
+        assert_topk_values_exact(o[r], x[r, :n], k, f"row {r}")
+        m = min(n, k)
+        assert np.array_equal(v[r, :m], x[r, o[r, :m]]), f"scores row {r}"
+        if len(np.unique(x[r, :n])) == n:
+            assert set(o[r, :m].tolist()) == set(O.topk_row(x[r], 0, n, k)[:m].tolist())
+
+
+def test_dcp_merge_degenerate():
+    # all candidates empty; a single candidate; zero rows; bad strides
+    k_local, k = 16, 8
+    cv = np.full((3, 2 * k_local), -np.inf, dtype=np.float32)
+    ci = np.full((3, 2 * k_local), -1, dtype=np.int32)
+    cv[1, 20], ci[1, 20] = 2.5, 9
+    cv[2, :] = np.arange(2 * k_local, dtype=np.float32)
+    ci[2, :] = np.arange(2 * k_local)
+    out = torch.full((3, k), -7, dtype=torch.int32, device=DEV)
+    idx.idx_dcp_topk_merge(dev(cv), dev(ci), dev(np.array([0, 1000], dtype=np.int32)), k_local, k, out)
+    o = out.cpu().numpy()
+    assert np.all(o[0] == -1)
+    assert o[1].tolist() == [1000 + 9] + [-1] * (k - 1)
+    assert sorted(o[2].tolist()) == [1000 + j for j in range(24, 32)]
+    empty = torch.empty((0, k), dtype=torch.int32, device=DEV)
+    idx.idx_dcp_topk_merge(dev(cv[:0]), dev(ci[:0]), None, k_local, k, empty)
+    with pytest.raises(idx.IdxError):
+        idx.idx_dcp_topk_merge(dev(cv), dev(ci), None, 64, k, out)
+
+
 # ------------------------------------------------------------------ a7 expansion, a6 slots
 
 def test_expand_candidates_random_vs_oracle():

@@ -230,6 +230,103 @@ def test_topk_brute_force_small():
         assert sorted(sel) == min(sorted(s) for s in valid)
 
 
+# ------------------------------------------------- context-parallel merge
+
+def test_dcp_merge_hand_worked():
+    # shard 0 holds positions 0..9, shard 1 positions 10..; three candidates each.
+    # Sorted by value then position: 5@2, 4@11, 3@0, 3@15, 1@7; the empty one is dropped.
+    vals = np.array([5.0, 3.0, 1.0, 4.0, 3.0, -np.inf])
+    idx = np.array([2, 0, 7, 1, 5, -1])
+    pos, v = O.dcp_topk_merge_row(vals, idx, [0, 10], 3, 4)
+    assert pos.tolist() == [2, 11, 0, 15] and v.tolist() == [5.0, 4.0, 3.0, 3.0]
+    pos, v = O.dcp_topk_merge_row(vals, idx, [0, 10], 3, 7)
+    assert pos.tolist() == [2, 11, 0, 15, 7, -1, -1]
+    assert v[:5].tolist() == [5.0, 4.0, 3.0, 3.0, 1.0] and np.all(np.isneginf(v[5:]))
+    # indices already global: no offsets
+    pos, _ = O.dcp_topk_merge_row(vals, np.array([2, 0, 7, 11, 15, -1]), None, 3, 4)
+    assert pos.tolist() == [2, 11, 0, 15]
+
+
+def _shard_bounds(rng, n, n_shards):
+    cuts = np.sort(rng.integers(0, n + 1, n_shards - 1))
+    return np.concatenate([[0], cuts, [n]]).astype(np.int64)
+
+
+def test_dcp_merge_of_local_topk_equals_global_topk():
+    # The exactness claim of the context-parallel merge: every member of the
+    # global top-k is in the local top-k of its own shard, so merging the local
+    # lists reproduces the whole-row selection (same tie rule: lower position).
+    rng = np.random.default_rng(11)
+    for trial in range(300):
+        n = int(rng.integers(1, 60))
+        k = int(rng.integers(1, 12))
+        n_shards = int(rng.integers(1, 6))
+        row = rng.integers(-4, 5, n).astype(np.float64) if trial % 2 else rng.standard_normal(n)
+        b = _shard_bounds(rng, n, n_shards)
+        cv = np.full(n_shards * k, -np.inf)
+        ci = np.full(n_shards * k, -1, dtype=np.int64)
+        for s in range(n_shards):
+            loc = O.topk_row(row, int(b[s]), int(b[s + 1]), k)
+            ci[s * k:(s + 1) * k] = loc
+            ok = loc >= 0
+            cv[s * k:(s + 1) * k][ok] = row[b[s] + loc[ok]]
+        pos, v = O.dcp_topk_merge_row(cv, ci, b[:-1], k, k)
+        ref = O.topk_row(row, 0, n, k)
+        m = min(n, k)
+        assert sorted(pos[:m].tolist()) == sorted(ref[:m].tolist()) and np.all(pos[m:] == -1)
+        assert np.array_equal(v[:m], row[pos[:m]]) and np.all(np.diff(v[:m]) <= 0)
+
+
+def test_dcp_merge_interleaved_shards_equal_global_topk():
+    # tokens dealt round-robin: shard s holds positions s, s + S, s + 2S, ...;
+    # local index j of shard s is global position s + j * S
+    rng = np.random.default_rng(13)
+    pos, _ = O.dcp_topk_merge_row([3.0, 1.0, 2.0, -np.inf], [1, 0, 0, -1], [0, 1], 2, 3, 2)
+    assert pos.tolist() == [2, 1, 0]                       # 3@(0+1*2), 2@(1+0*2), 1@(0+0*2)
+    for trial in range(200):
+        n = int(rng.integers(1, 50))
+        k = int(rng.integers(1, 10))
+        S = int(rng.integers(1, 5))
+        row = rng.integers(-3, 4, n).astype(np.float64)
+        cv = np.full(S * k, -np.inf)
+        ci = np.full(S * k, -1, dtype=np.int64)
+        for s in range(S):
+            loc_row = row[s::S]
+            loc = O.topk_row(loc_row, 0, len(loc_row), k)
+            ci[s * k:(s + 1) * k] = loc
+            ok = loc >= 0
+            cv[s * k:(s + 1) * k][ok] = loc_row[loc[ok]]
+        got, _ = O.dcp_topk_merge(cv[None], ci[None], np.arange(S)[None], k, k, S)
+        m = min(n, k)
+        assert sorted(got[0, :m].tolist()) == sorted(O.topk_row(row, 0, n, k)[:m].tolist())
+
+
+def test_dcp_merge_brute_force_small():
+    # any candidate multiset: the merged set is one of the maximal k-subsets
+    rng = np.random.default_rng(12)
+    for _ in range(200):
+        k_local = int(rng.integers(1, 4))
+        n_shards = int(rng.integers(1, 4))
+        k = int(rng.integers(1, 6))
+        n = n_shards * k_local
+        vals = rng.integers(-2, 3, n).astype(np.float64)
+        idx = rng.permutation(20)[:n]
+        empty = rng.random(n) < 0.25
+        idx[empty] = -1
+        vals[empty] = -np.inf
+        offs = np.arange(n_shards) * 100
+        pos, v = O.dcp_topk_merge_row(vals, idx, offs, k_local, k)
+        glob = [int(offs[j // k_local] + idx[j]) for j in range(n) if idx[j] >= 0]
+        gval = [vals[j] for j in range(n) if idx[j] >= 0]
+        m = min(len(glob), k)
+        assert np.all(pos[m:] == -1) and np.all(np.isneginf(v[m:]))
+        if m == len(glob):
+            assert sorted(pos[:m].tolist()) == sorted(glob)
+            continue
+        chosen = {glob.index(int(p)) for p in pos[:m]}
+        assert chosen in _brute_force_topk_sets(gval, k)
+
+
 def test_topk_values_match_torch_topk():
     x = W.make_logits(8, 4, 5000)
     got = O.topk(x, None, [5000, 4000, 2048, 100], 2048)
