@@ -25,15 +25,16 @@
 // cross-thread traffic and the [rows x 64 heads x tokens] intermediate never
 // leaves the SM.
 //
-// Roles (192 threads, one CTA per SM, persistent):
+// Roles (320 threads, one CTA per SM, persistent):
 //   warp 0     TMA producer: k boxes (one per cache block / sparse block) and
 //              their scales into a ring of shared-memory stages, q per group;
 //              block-table lookups for the next tile are issued before the
 //              wait for a free stage so their latency hides behind it.
 //   warp 1     allocates tensor memory; one lane issues tcgen05.mma and
 //              commits stage / accumulator barriers.
-//   warps 2-5  epilogue: tcgen05.ld of the accumulator, weighted head sum,
-//              scale, causal / range mask, coalesced store (fp32 or bf16).
+//   warps 2-9  epilogue, two warpgroups taking tiles in turn: tcgen05.ld of
+//              the accumulator, weighted head sum, scale, causal / range mask,
+//              coalesced store (fp32 or bf16).
 // The flattened (group, tile) sequence is split evenly over the CTAs; every
 // role walks the same sequence. Every wait is bounded; on expiry the CTA
 // records a device error code and leaves in order.
@@ -52,6 +53,7 @@ constexpr int kTile = 128;
 constexpr int kEpiWG = IDX_EPI_WARPGROUPS;  // epilogue warpgroups, alternating tiles
 constexpr int kEpiWarps = 4 * kEpiWG;
 constexpr int kThreads = 64 + kEpiWarps * 32;
+
 constexpr int kKvStageBytes = kTile * kDim;       // 16 KB
 constexpr int kScaleStageBytes = 2048;            // up to 16 boxes, each in a 128-byte slot
 constexpr uint64_t kTimeoutNs = 2000000000ull;
@@ -334,6 +336,15 @@ __device__ __forceinline__ float weighted_head_sum(const uint32_t (&a0)[32], con
   return (hsum2(acc[0]) + hsum2(acc[1])) + (hsum2(acc[2]) + hsum2(acc[3]));
 }
 
+template <typename T>
+__device__ __forceinline__ void store_logit(T* dst, T v, bool streaming) {
+  if (streaming) {
+    __stcs(dst, v);
+  } else {
+    *dst = v;
+  }
+}
+
 template <int NQ>
 __global__ void __launch_bounds__(kThreads, 1)
 mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_kv,
@@ -444,8 +455,12 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     // lane fetches the sparse-index / block-table entries of its own box. The
     // next batch is fetched before the current one is issued, so those dependent
     // loads overlap with the waits for free stages instead of serialising.
-    const uint64_t pol_stream = l2_policy_evict_first();
-    const uint64_t pol_keep = l2_policy_evict_last();
+    // Decode reads every k box once (evict first) and keeps q; a prefill chunk
+    // re-reads the same k rows for every query group (keep them in L2) while
+    // each group's q is read by one or two CTAs.
+    const bool prefill = p.mode == kPrefillDense || p.mode == kPrefillSparse;
+    const uint64_t pol_kv = prefill ? l2_policy_evict_last() : l2_policy_evict_first();
+    const uint64_t pol_q = prefill ? l2_policy_evict_first() : l2_policy_evict_last();
     const int upt = kTile / p.unit;  // boxes per tile, 1..16
     const int tpb = 32 / upt;        // tiles per batch
     const uint32_t box_bytes = static_cast<uint32_t>(p.unit) * (kDim + 4);
@@ -493,7 +508,7 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
           if (!got) return false;
           if (lane == 0) {
             mbar_arrive_expect_tx(&q_full[qs], C::kQStageBytes);
-            tma_load_3d(q_s + qs * C::kQStageBytes, &map_q, &q_full[qs], 0, 0, tl.z, pol_keep);
+            tma_load_3d(q_s + qs * C::kQStageBytes, &map_q, &q_full[qs], 0, 0, tl.z, pol_q);
           }
           q_group = tl.x;
           if (++qs == 2) {
@@ -512,9 +527,9 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         if (mine) {
           const int u = lane - ti * upt;
           tma_load_3d(kv_s + st * kKvStageBytes + u * p.unit * kDim, &map_kv, &full[st], 0, bx.row,
-                      bx.blk, pol_stream);
+                      bx.blk, pol_kv);
           tma_load_2d(sc_s + st * kScaleStageBytes + u * p.scale_slot, &map_scale, &full[st],
-                      bx.row, bx.blk, pol_stream);
+                      bx.row, bx.blk, pol_kv);
         }
         if (++st == C::kStages) {
           st = 0;
@@ -648,7 +663,6 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       hist_tiles = 0;
     };
     long long ai = 0;  // active tiles seen
-    long long ti = 0;  // tiles seen
     // A warp waits a commit group's accumulator-ready barrier once, at the
     // group's first tile. Waiting again at the second tile would be unsafe: once
     // the first tile's accumulator is released the MMA warp may already commit
@@ -660,16 +674,34 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     // one query per group: its 64 weights live in registers for the whole group
     constexpr bool kRegW = NQ == 1;
     float wreg[kRegW ? 64 : 1];
-    Walker W;
-    W.init(p, s_g0, s_t0, count);
     const float ninf = -__int_as_float(0x7f800000);
-    while (W.left > 0) {
-      const Group& G = W.G;
-      const bool active = tile_active(G, W.t);
-      const bool mine = active ? ((ai / C::kCommit) % kEpiWG) == wg : (ti % kEpiWG) == wg;
-      if (mine && W.g != cur_g) {
+    // a prefill chunk's scores (GBs) stream past L2 so they do not evict the k rows
+    const bool stream_out = p.mode == kPrefillDense || p.mode == kPrefillSparse;
+    // The CTA's (group, tile) range, a group at a time. Active tiles come in
+    // the producer's and MMA warp's order (ordinal ai); this warpgroup visits
+    // only the tiles of its own commit groups, and fills the inactive tiles of
+    // the range (those outside the group's visible columns) whose index is
+    // congruent to it, so every tile costs a warp no bookkeeping unless it is
+    // that warp's to process.
+    int g = s_g0;
+    int tb = s_t0;
+    long long left = count;
+    bool stop = false;
+    while (left > 0 && !stop) {
+      const Group G = load_group(p, g);
+      const int te = static_cast<int>(min(static_cast<long long>(G.tiles), tb + left));
+      left -= te - tb;
+      // active tiles of the group within [tb, te): the tiles that meet [act_lo, act_hi)
+      const int ta0 = max(G.act_lo / kTile, tb);
+      const int ta1 = max(min((G.act_hi + kTile - 1) / kTile, te), ta0);
+      const int nact = ta1 - ta0;
+      // first active tile of this warpgroup's commit groups
+      const long long cg_first = ai / C::kCommit;
+      const int skip = static_cast<int>((wg - cg_first % kEpiWG + kEpiWG) % kEpiWG);
+      int oi = skip == 0 ? 0 : static_cast<int>((cg_first + skip) * C::kCommit - ai);
+      if (oi < nact && g != cur_g) {
         flush_hist();
-        cur_g = W.g;
+        cur_g = g;
         __syncwarp();
         for (int i = lane; i < NQ * 64; i += 32) {
           const int j = i >> 6;
@@ -706,22 +738,51 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
           lim_hi[j] = hi;
         }
       }
-      const int c = W.t * kTile + trow;
-      if (mine && active) {
-        const int st = static_cast<int>(ai % C::kStages);
-        const uint32_t ph = static_cast<uint32_t>((ai / C::kStages) & 1);
-        const int as = static_cast<int>(ai % C::kAccStages);
-        const long long cg = ai / C::kCommit;
+      // inactive tiles of the range: -inf
+      for (int t = tb; t < te; ++t) {
+        if (t >= ta0 && t < ta1) {
+          t = ta1 - 1;
+          continue;
+        }
+        const int c = t * kTile + trow;
+        if (t % kEpiWG != wg || c >= G.ncols) continue;
+#pragma unroll
+        for (int j = 0; j < NQ; ++j) {
+          if (j < G.nq) {
+            const int64_t o = static_cast<int64_t>(G.row0 + j) * p.ld_out + c;
+            if (p.out_bf16) {
+              store_logit(reinterpret_cast<__nv_bfloat16*>(p.out) + o, __float2bfloat16_rn(ninf),
+                          stream_out);
+            } else {
+              store_logit(reinterpret_cast<float*>(p.out) + o, ninf, stream_out);
+            }
+          }
+        }
+      }
+      while (oi < nact && !stop) {
+        const long long a = ai + oi;
+        const int t = ta0 + oi;
+        const int c = t * kTile + trow;
+        const int st = static_cast<int>(a % C::kStages);
+        const uint32_t ph = static_cast<uint32_t>((a / C::kStages) & 1);
+        const int as = static_cast<int>(a % C::kAccStages);
+        const long long cg = a / C::kCommit;
         const int af = static_cast<int>(cg % C::kAccFull);
         const uint32_t afph = static_cast<uint32_t>((cg / C::kAccFull) & 1);
-        bool got = wait_bar(&full[st], ph, abort_flag, 6u, ai, W.g, W.t, st);
-        if (!__all_sync(0xFFFFFFFFu, got)) break;
+        bool got = wait_bar(&full[st], ph, abort_flag, 6u, a, g, t, st);
+        if (!__all_sync(0xFFFFFFFFu, got)) {
+          stop = true;
+          break;
+        }
         const int box = trow / p.unit;
         const float scale = *reinterpret_cast<const float*>(
             sc_s + st * kScaleStageBytes + box * p.scale_slot + (trow - box * p.unit) * 4);
         if (cg != waited_cg) {
-          got = wait_bar(&acc_full[af], afph, abort_flag, 7u, ai, W.g, W.t, af);
-          if (!__all_sync(0xFFFFFFFFu, got)) break;
+          got = wait_bar(&acc_full[af], afph, abort_flag, 7u, a, g, t, af);
+          if (!__all_sync(0xFFFFFFFFu, got)) {
+            stop = true;
+            break;
+          }
           waited_cg = cg;
         }
         tc_fence_after();
@@ -768,10 +829,10 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
               uint32_t bits;
               if (p.out_bf16) {
                 const __nv_bfloat16 b = __float2bfloat16_rn(v);
-                reinterpret_cast<__nv_bfloat16*>(p.out)[o] = b;
+                store_logit(reinterpret_cast<__nv_bfloat16*>(p.out) + o, b, stream_out);
                 bits = static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16;
               } else {
-                reinterpret_cast<float*>(p.out)[o] = v;
+                store_logit(reinterpret_cast<float*>(p.out) + o, v, stream_out);
                 bits = __float_as_uint(v);
               }
               if (do_hist && vis) {
@@ -786,22 +847,13 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
           hist_row = G.row0;  // warp-uniform: every lane of the warp sets it
           if (++hist_tiles == 2047) flush_hist();
         }
-      } else if (mine && c < G.ncols) {
-#pragma unroll
-        for (int j = 0; j < NQ; ++j) {
-          if (j < G.nq) {
-            const int64_t o = static_cast<int64_t>(G.row0 + j) * p.ld_out + c;
-            if (p.out_bf16) {
-              reinterpret_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(ninf);
-            } else {
-              reinterpret_cast<float*>(p.out)[o] = ninf;
-            }
-          }
-        }
+        // next tile: the rest of this commit group, then skip the other warpgroups' groups
+        ++oi;
+        if ((ai + oi) % C::kCommit == 0) oi += C::kCommit * (kEpiWG - 1);
       }
-      ai += active ? 1 : 0;
-      ++ti;
-      W.advance(p);
+      ai += nact;
+      ++g;
+      tb = 0;
     }
     flush_hist();
   }
