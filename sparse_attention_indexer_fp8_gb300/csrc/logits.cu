@@ -336,15 +336,6 @@ __device__ __forceinline__ float weighted_head_sum(const uint32_t (&a0)[32], con
   return (hsum2(acc[0]) + hsum2(acc[1])) + (hsum2(acc[2]) + hsum2(acc[3]));
 }
 
-template <typename T>
-__device__ __forceinline__ void store_logit(T* dst, T v, bool streaming) {
-  if (streaming) {
-    __stcs(dst, v);
-  } else {
-    *dst = v;
-  }
-}
-
 template <int NQ>
 __global__ void __launch_bounds__(kThreads, 1)
 mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_kv,
@@ -675,8 +666,6 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     constexpr bool kRegW = NQ == 1;
     float wreg[kRegW ? 64 : 1];
     const float ninf = -__int_as_float(0x7f800000);
-    // a prefill chunk's scores (GBs) stream past L2 so they do not evict the k rows
-    const bool stream_out = p.mode == kPrefillDense || p.mode == kPrefillSparse;
     // The CTA's (group, tile) range, a group at a time. Active tiles come in
     // the producer's and MMA warp's order (ordinal ai); this warpgroup visits
     // only the tiles of its own commit groups, and fills the inactive tiles of
@@ -751,10 +740,9 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
           if (j < G.nq) {
             const int64_t o = static_cast<int64_t>(G.row0 + j) * p.ld_out + c;
             if (p.out_bf16) {
-              store_logit(reinterpret_cast<__nv_bfloat16*>(p.out) + o, __float2bfloat16_rn(ninf),
-                          stream_out);
+              reinterpret_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(ninf);
             } else {
-              store_logit(reinterpret_cast<float*>(p.out) + o, ninf, stream_out);
+              reinterpret_cast<float*>(p.out)[o] = ninf;
             }
           }
         }
@@ -829,10 +817,10 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
               uint32_t bits;
               if (p.out_bf16) {
                 const __nv_bfloat16 b = __float2bfloat16_rn(v);
-                store_logit(reinterpret_cast<__nv_bfloat16*>(p.out) + o, b, stream_out);
+                reinterpret_cast<__nv_bfloat16*>(p.out)[o] = b;
                 bits = static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16;
               } else {
-                store_logit(reinterpret_cast<float*>(p.out) + o, v, stream_out);
+                reinterpret_cast<float*>(p.out)[o] = v;
                 bits = __float_as_uint(v);
               }
               if (do_hist && vis) {
