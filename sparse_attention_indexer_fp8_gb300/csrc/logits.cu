@@ -40,6 +40,8 @@
 // records a device error code and leaves in order.
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace idx {
@@ -336,7 +338,7 @@ __device__ __forceinline__ float weighted_head_sum(const uint32_t (&a0)[32], con
   return (hsum2(acc[0]) + hsum2(acc[1])) + (hsum2(acc[2]) + hsum2(acc[3]));
 }
 
-template <int NQ>
+template <int NQ, bool kOutBf16>
 __global__ void __launch_bounds__(kThreads, 1)
 mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_kv,
                   const __grid_constant__ CUtensorMap map_scale, const LogitsParams p) {
@@ -653,15 +655,19 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       hist_row = -1;
       hist_tiles = 0;
     };
-    long long ai = 0;  // active tiles seen
+    // Per-CTA tile ordinals fit in int: a CTA's share of any cache or score
+    // matrix that fits in device memory is far below 2^31 tiles.
+    int ai = 0;  // active tiles seen
     // A warp waits a commit group's accumulator-ready barrier once, at the
     // group's first tile. Waiting again at the second tile would be unsafe: once
     // the first tile's accumulator is released the MMA warp may already commit
     // the group two ahead (an unpaired last tile of the range commits at once)
     // to the same barrier, moving it two phases past this wait's parity.
-    long long waited_cg = -1;
+    int waited_cg = -1;
     int cur_g = -1;
     int lim_lo[NQ], lim_hi[NQ];
+    using OutT = typename std::conditional<kOutBf16, __nv_bfloat16, float>::type;
+    OutT* orow[NQ];  // output row of each query of the current group
     // one query per group: its 64 weights live in registers for the whole group
     constexpr bool kRegW = NQ == 1;
     float wreg[kRegW ? 64 : 1];
@@ -685,9 +691,9 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       const int ta1 = max(min((G.act_hi + kTile - 1) / kTile, te), ta0);
       const int nact = ta1 - ta0;
       // first active tile of this warpgroup's commit groups
-      const long long cg_first = ai / C::kCommit;
-      const int skip = static_cast<int>((wg - cg_first % kEpiWG + kEpiWG) % kEpiWG);
-      int oi = skip == 0 ? 0 : static_cast<int>((cg_first + skip) * C::kCommit - ai);
+      const int cg_first = ai / C::kCommit;
+      const int skip = (wg - cg_first % kEpiWG + kEpiWG) % kEpiWG;
+      int oi = skip == 0 ? 0 : (cg_first + skip) * C::kCommit - ai;
       if (oi < nact && g != cur_g) {
         flush_hist();
         cur_g = g;
@@ -725,6 +731,7 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
           }
           lim_lo[j] = lo;
           lim_hi[j] = hi;
+          orow[j] = reinterpret_cast<OutT*>(p.out) + static_cast<int64_t>(G.row0 + j) * p.ld_out;
         }
       }
       // inactive tiles of the range: -inf
@@ -739,7 +746,7 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         for (int j = 0; j < NQ; ++j) {
           if (j < G.nq) {
             const int64_t o = static_cast<int64_t>(G.row0 + j) * p.ld_out + c;
-            if (p.out_bf16) {
+            if constexpr (kOutBf16) {
               reinterpret_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(ninf);
             } else {
               reinterpret_cast<float*>(p.out)[o] = ninf;
@@ -748,14 +755,14 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         }
       }
       while (oi < nact && !stop) {
-        const long long a = ai + oi;
+        const int a = ai + oi;
         const int t = ta0 + oi;
         const int c = t * kTile + trow;
-        const int st = static_cast<int>(a % C::kStages);
+        const int st = a % C::kStages;
         const uint32_t ph = static_cast<uint32_t>((a / C::kStages) & 1);
-        const int as = static_cast<int>(a % C::kAccStages);
-        const long long cg = a / C::kCommit;
-        const int af = static_cast<int>(cg % C::kAccFull);
+        const int as = a % C::kAccStages;
+        const int cg = a / C::kCommit;
+        const int af = cg % C::kAccFull;
         const uint32_t afph = static_cast<uint32_t>((cg / C::kAccFull) & 1);
         bool got = wait_bar(&full[st], ph, abort_flag, 6u, a, g, t, st);
         if (!__all_sync(0xFFFFFFFFu, got)) {
@@ -813,14 +820,13 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             if (j < G.nq) {
               const bool vis = c >= lim_lo[j] && c < lim_hi[j];
               const float v = vis ? logit[j] : ninf;
-              const int64_t o = static_cast<int64_t>(G.row0 + j) * p.ld_out + c;
               uint32_t bits;
-              if (p.out_bf16) {
+              if constexpr (kOutBf16) {
                 const __nv_bfloat16 b = __float2bfloat16_rn(v);
-                reinterpret_cast<__nv_bfloat16*>(p.out)[o] = b;
+                orow[j][c] = b;
                 bits = static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16;
               } else {
-                reinterpret_cast<float*>(p.out)[o] = v;
+                orow[j][c] = v;
                 bits = __float_as_uint(v);
               }
               if (do_hist && vis) {
@@ -852,10 +858,10 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   if (warp == 1) tmem_dealloc(tmem_base, C::kTmemCols);
 }
 
-template <int NQ>
+template <int NQ, bool kOutBf16>
 idx_status_t launch_logits(const CUtensorMap& mq, const CUtensorMap& mkv, const CUtensorMap& msc,
                            const LogitsParams& p, int grid, cudaStream_t stream, const char* fn) {
-  auto kern = mqa_logits_kernel<NQ>;
+  auto kern = mqa_logits_kernel<NQ, kOutBf16>;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -878,9 +884,15 @@ idx_status_t dispatch(int nq_tmpl, const CUtensorMap& mq, const CUtensorMap& mkv
   if (max_tiles >= 0 && max_tiles < grid) grid = max_tiles;
   if (grid <= 0) return IDX_OK;
   switch (nq_tmpl) {
-    case 1: return launch_logits<1>(mq, mkv, msc, p, static_cast<int>(grid), stream, fn);
-    case 2: return launch_logits<2>(mq, mkv, msc, p, static_cast<int>(grid), stream, fn);
-    case 4: return launch_logits<4>(mq, mkv, msc, p, static_cast<int>(grid), stream, fn);
+    case 1:
+      return p.out_bf16 ? launch_logits<1, true>(mq, mkv, msc, p, static_cast<int>(grid), stream, fn)
+                        : launch_logits<1, false>(mq, mkv, msc, p, static_cast<int>(grid), stream, fn);
+    case 2:
+      return p.out_bf16 ? launch_logits<2, true>(mq, mkv, msc, p, static_cast<int>(grid), stream, fn)
+                        : launch_logits<2, false>(mq, mkv, msc, p, static_cast<int>(grid), stream, fn);
+    case 4:
+      return p.out_bf16 ? launch_logits<4, true>(mq, mkv, msc, p, static_cast<int>(grid), stream, fn)
+                        : launch_logits<4, false>(mq, mkv, msc, p, static_cast<int>(grid), stream, fn);
   }
   return fail(IDX_ERR_UNSUPPORTED, "%s: rows per group %d", fn, nq_tmpl);
 }
