@@ -416,7 +416,9 @@ class PrefillBench:
                 "achieved": round(ach, 1), "peak": round(peak, 1), "unit": "TFLOP/s",
                 "frac": round(ach / peak, 4),
                 "peak_source": f"{peak_kind} bf16 burst x 2 (nominal e4m3/bf16 dense ratio 4.5/2.25)",
-                "algorithmic_flop_per_launch": flop, "traffic": None, "kernel_ms": round(kernel_ms, 5)}
+                "algorithmic_flop_per_launch": flop,
+                "traffic": profiled_traffic("mqa_logits_prefill_prefill.md", "logits.cu"),
+                "kernel_ms": round(kernel_ms, 5)}
 
     def config(self, world):
         return {"workload": self.wl.name, "queries": self.T, "ctx": self.S, "topk": self.wl.topk,
