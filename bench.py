@@ -565,8 +565,90 @@ def oracle_hier_row(wl, b, kq):
     return lg, pos, sl[0]
 
 
+class QPrepBench:
+    """q preparation of the prefill chunk: partial RoPE, per-head e4m3 quantisation, folded bf16 weights."""
+
+    launches_per_step = 1
+    dtype = "bf16->e4m3 (f32 arithmetic)"
+    metric = "indexer q preparation query-rows/s (RoPE + e4m3 quant + weight folding, 8192-query chunk)"
+    # per query row: bf16 q in, e4m3 q out, fp32 weights in, bf16 weights out, position, cos/sin row
+    row_bytes = 64 * 128 * 2 + 64 * 128 + 64 * 4 + 64 * 2 + 4 + 64 * 4
+
+    def __init__(self, name, rank, dev):
+        import sparse_attention_indexer_fp8_gb300 as idx
+
+        self.idx, self.dev, self.name = idx, dev, name
+        self.wl = wl = W.q_prep_chunk(seed=rank_seed(1006, rank))
+        self.T = wl.T
+        self.q = W.make_q_raw_device(wl.seed, wl.T, dev)
+        self.pos = torch.from_numpy(wl.positions).to(dev)
+        self.cs = torch.from_numpy(wl.cos_sin).to(dev)
+        self.w = torch.from_numpy(wl.w).to(dev)
+        self.q8 = torch.empty((wl.T, 64 * 128), dtype=torch.uint8, device=dev)
+        self.w_out = torch.empty((wl.T, 64), dtype=torch.bfloat16, device=dev)
+        self.rows_per_step = wl.T
+
+    def step(self, stream, ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        self.idx.idx_q_rope_quant(self.q, self.pos, self.cs, self.w, self.q8, self.w_out, 128 ** -0.5,
+                                  64 ** -0.5, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    def e2e_prepare(self):
+        self.h_q = self.q.cpu().pin_memory()
+        self.h_in = [(self.h_q, self.q), (_pin(self.wl.positions), self.pos), (_pin(self.wl.w), self.w)]
+        self.h_out = [torch.empty(self.q8.shape, dtype=torch.uint8).pin_memory(),
+                      torch.empty(self.w_out.shape, dtype=torch.bfloat16).pin_memory()]
+        return _nbytes(*[h for h, _ in self.h_in]), _nbytes(*self.h_out)
+
+    def e2e_step(self, stream):
+        for h, d in self.h_in:
+            d.copy_(h, non_blocking=True)
+        self.step(stream)
+        self.h_out[0].copy_(self.q8, non_blocking=True)
+        self.h_out[1].copy_(self.w_out, non_blocking=True)
+
+    def verify_and_time_oracle(self, n_rows):
+        from oracle import indexer as O
+        from oracle.codecs import bf16_decode, bf16_encode
+
+        wl = self.wl
+        rng = np.random.default_rng(wl.seed)
+        sample = sorted(rng.choice(wl.T, size=min(max(n_rows, 1) * 64, wl.T), replace=False).tolist())
+        qs = bf16_decode(self.q[sample].view(torch.int16).cpu().numpy().view(np.uint16)).astype(np.float32)
+        g8 = self.q8[sample].cpu().numpy()
+        gw = self.w_out[sample].view(torch.int16).cpu().numpy().view(np.uint16)
+        t0 = time.perf_counter()
+        o8, ow, _ = O.q_rope_quant(qs.reshape(-1, 64, 128), wl.positions[sample], wl.cos_sin, wl.w[sample],
+                                   128 ** -0.5, 64 ** -0.5)
+        cpu_s = time.perf_counter() - t0
+        assert np.array_equal(g8.reshape(-1, 64, 128), o8), "bench q8 bytes differ from the oracle"
+        assert np.array_equal(gw, bf16_encode(ow)), "bench bf16 weights differ from the oracle"
+        cpu = {"value": round(len(sample) / cpu_s, 3), "unit": "rows/s", "cores": os.cpu_count(),
+               "kind": "oracle", "sample": f"{len(sample)} query rows of the chunk (RoPE, quantisation, "
+                                           f"weights), inputs prepared untimed"}
+        return cpu, f"q8 and bf16 weights bit-exact on {len(sample)} sampled rows"
+
+    def roofline(self, kernel_ms, step_ms, peaks, peak_kind):
+        byt = self.T * self.row_bytes
+        ach = byt / (kernel_ms / 1e3) / 1e9
+        return {"kernel": "q_rope_quant_kernel", "bound": "hbm", "achieved": round(ach, 1),
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4),
+                "peak_source": peak_kind, "algorithmic_bytes_per_launch": byt, "traffic": None,
+                "kernel_ms": round(kernel_ms, 5)}
+
+    def config(self, world):
+        return {"workload": self.wl.name, "queries": self.T, "heads": 64, "head_dim": 128, "rope_dims": 64,
+                "rope": "neox", "weights_out": "bf16",
+                "step": "partial RoPE + per-head e4m3 quantisation + folded weights",
+                "l2": "q in (128 MB) + q8 out (64 MB) > L2, no flush",
+                "parallelism": f"rows sharded, {world} independent replica(s)"}
+
+
 BENCHES = {"long_decode": DecodeBench, "paged_decode": DecodeBench, "prefill": PrefillBench,
-           "hierarchical": HierBench}
+           "hierarchical": HierBench, "q_prep": QPrepBench}
 
 
 # ----------------------------------------------------------------------------- harness
@@ -655,6 +737,7 @@ def run_reference(args, rank):
     if rank != 0:
         return None
     name = args.workload
+    rows_per_call = 1
     if name in ("long_decode", "paged_decode"):
         wl = W.long_decode() if name == "long_decode" else W.paged_decode()
         rng = np.random.default_rng(wl.seed)
@@ -680,6 +763,20 @@ def run_reference(args, rank):
             O.topk_row(lg, 0, hi - lo, wl.topk)
             return time.perf_counter() - t0
         metric, cfg = PrefillBench.metric, {"workload": wl.name, "queries": T, "ctx": wl.S, "topk": wl.topk}
+    elif name == "q_prep":
+        from oracle import indexer as O
+
+        wl = W.q_prep_chunk()
+        g = np.random.default_rng(wl.seed)
+        rows = np.arange(64)
+        qh = g.standard_normal((64, 64, 128)).astype(np.float32)
+
+        def one(i):
+            t0 = time.perf_counter()
+            O.q_rope_quant(qh, wl.positions[rows], wl.cos_sin, wl.w[rows], 128 ** -0.5, 64 ** -0.5)
+            return time.perf_counter() - t0
+        metric, cfg = QPrepBench.metric, {"workload": wl.name, "queries": wl.T}
+        rows_per_call = 64
     else:
         from oracle import indexer as O
 
@@ -698,14 +795,16 @@ def run_reference(args, rank):
     for i in range(args.warmup):
         one(i)
     t = sum(one(i) for i in range(args.steps))
-    value = args.steps / t
+    value = args.steps * rows_per_call / t
     return {
         "impl": "reference", "metric": metric, "value": round(value, 3), "unit": "rows/s", "n_gpus": 0,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 3),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32" if name == "q_prep" else "f64",
         "data": "synthetic", "config": cfg,
         "cpu_baseline": {"value": round(value, 3), "unit": "rows/s", "cores": os.cpu_count(), "kind": "oracle",
-                         "sample": "each step one full row of the workload, cache prepared untimed"},
+                         "sample": "each step one full row of the workload (64 query rows of N(0,1) q for "
+                                   "q_prep), cache prepared untimed"},
         "e2e": {"value": round(value, 3), "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 

@@ -122,6 +122,47 @@ idx_status_t idx_k_quant_and_cache(const void* k, int k_dtype, int64_t ld_k, int
                                    int64_t block_stride_bytes, int scale_fmt,
                                    cudaStream_t stream);
 
+enum { IDX_ROPE_NEOX = 0, IDX_ROPE_INTERLEAVED = 1 };  /* pairing of the rotary dims */
+
+/*
+ * idx_q_rope_quant - prepare the indexer's q: partial RoPE, per-head FP8
+ * quantisation, and the weights with every q-side coefficient folded in.
+ *
+ * "DeepSeek V3.2 稀疏注意力 DSA 推理流程图解", "Indexer 内部六步" steps 3-4:
+ * RoPE is applied to the first 64 of the 128 dims of each head; q is quantised
+ * with one scale per 128 values (one per head); the weights absorb
+ * q_scale * softmax_scale * n_head_scale, so the scoring kernels take q8 raw.
+ * "V4.1 索引器接入稀疏 MQA logits", 实现拆解 item 5: the weights may be written
+ * directly as bf16, the fp32 result rounded once.
+ *
+ * Per token t and head h, in IEEE binary32 with every operation rounded (no
+ * fused multiply-add), c = cos_sin[pos, i] and s = cos_sin[pos, 32 + i] for
+ * rotary pair i (pos = positions[t]):
+ *   NeoX pairs (i, i + 32), interleaved pairs (2i, 2i + 1), i < 32:
+ *   y_a = x_a c - x_b s,  y_b = x_b c + x_a s;   dims 64..127 pass through;
+ *   scale = max_d |y_d| / 448;  q8_d = e4m3_rn_satfinite(y_d / scale) (0 if scale 0);
+ *   w_out = ((w * scale) * softmax_scale) * n_head_scale.
+ *
+ *   q          [T, 64, 128] of q_dtype (IDX_BF16 or IDX_F32), ld_q elements
+ *              between tokens (>= 8192); rows 16-byte aligned.
+ *   positions  int32 [T]: a position outside [0, max_pos) writes the token as
+ *              zeros and raises the device flag (idx_device_error).
+ *   cos_sin    float [max_pos, ld_cs] (ld_cs >= 64): cos of the 32 pair angles,
+ *              then their sin.
+ *   w          [T, 64] of w_dtype, row stride ld_w >= 64.
+ *   q8         uint8 [T, 64, 128], ld_q8 bytes between tokens (>= 8192, % 16 == 0).
+ *   w_out      [T, 64] of w_out_dtype, row stride ld_wo >= 64.
+ * Errors: IDX_ERR_INVALID_ARG for NULL pointers with T > 0, T < 0, max_pos < 1
+ * or short strides; IDX_ERR_UNSUPPORTED for another dtype or rope_style, or
+ * misaligned q / q8 rows.
+ */
+idx_status_t idx_q_rope_quant(const void* q, int q_dtype, int64_t ld_q, const int32_t* positions,
+                              const float* cos_sin, int64_t ld_cs, int32_t max_pos,
+                              int32_t rope_style, const void* w, int w_dtype, int64_t ld_w,
+                              float softmax_scale, float n_head_scale, int32_t T, uint8_t* q8,
+                              int64_t ld_q8, void* w_out, int w_out_dtype, int64_t ld_wo,
+                              cudaStream_t stream);
+
 /*
  * idx_gather_k - copy the first n_tok tokens of one request out of the cache.
  *

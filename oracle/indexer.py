@@ -29,6 +29,61 @@ TOKEN_BYTES = D + 4
 
 
 # ----------------------------------------------------------------------------
+# q preparation: partial RoPE, per-head quantisation, folded weights
+# ----------------------------------------------------------------------------
+
+ROPE_DIMS = 64      # [DSA] step ③: RoPE on the first 64 of the 128 dims only
+
+
+def rope_pairs(interleaved: bool):
+    """Indices (a, b) of the 32 rotary pairs: NeoX (i, i + 32) or interleaved (2i, 2i + 1)."""
+    i = np.arange(ROPE_DIMS // 2)
+    return (2 * i, 2 * i + 1) if interleaved else (i, i + ROPE_DIMS // 2)
+
+
+def q_rope_quant(q, positions, cos_sin, w, softmax_scale, n_head_scale, interleaved=False):
+    """Indexer q preparation, [DSA] "Indexer 内部六步" steps ③ and ④.
+
+    ③ RoPE rotates pair i of the first 64 dims of every head by the angle whose
+    cos / sin are ``cos_sin[pos, i]`` / ``cos_sin[pos, 32 + i]``; dims 64-127 pass
+    through. ④ q is quantised with one scale per 128 values (one per head), and
+    the weights absorb ``q_scale * softmax_scale * n_head_scale``.
+
+    Every step that decides a byte runs in IEEE binary32 with each operation
+    rounded (numpy float32 arithmetic, no fused multiply-add), the precision the
+    quantised codes are defined in: ``y_a = x_a c - x_b s``, ``y_b = x_b c + x_a s``;
+    ``scale = amax / 448``; ``q8 = e4m3(y / scale)`` (zero when the scale is 0);
+    ``w_out = ((w * scale) * softmax_scale) * n_head_scale``. A position outside
+    the table gives an all-zero head (scale 0, ``w_out = w * 0``).
+
+    q: [T, 64, 128] values (bf16 inputs widened exactly); positions: [T];
+    cos_sin: [max_pos, >= 64] float32; w: [T, 64].
+    Returns (q8 uint8 [T, 64, 128], w_out float32 [T, 64], scale float32 [T, 64]).
+    """
+    q = np.asarray(q, dtype=np.float32).reshape(-1, H, D)
+    T = q.shape[0]
+    pos = np.asarray(positions, dtype=np.int64)
+    cs = np.asarray(cos_sin, dtype=np.float32)
+    ok = (pos >= 0) & (pos < cs.shape[0])
+    c = cs[np.where(ok, pos, 0), :ROPE_DIMS // 2][:, None, :]                  # [T, 1, 32]
+    s = cs[np.where(ok, pos, 0), ROPE_DIMS // 2:ROPE_DIMS][:, None, :]
+    a, b = rope_pairs(interleaved)
+    y = q.copy()
+    xa, xb = q[:, :, a], q[:, :, b]
+    y[:, :, a] = xa * c - xb * s
+    y[:, :, b] = xb * c + xa * s
+    y[~ok] = 0.0
+    amax = np.max(np.abs(y), axis=2)
+    scale = (amax / np.float32(E4M3_MAX)).astype(np.float32)
+    q8 = np.zeros((T, H, D), dtype=np.uint8)
+    live = scale != 0
+    q8[live] = e4m3_encode(y[live] / scale[live][:, None])
+    w = np.asarray(w, dtype=np.float32).reshape(T, H)
+    w_out = ((w * scale) * np.float32(softmax_scale)) * np.float32(n_head_scale)
+    return q8, w_out.astype(np.float32), scale
+
+
+# ----------------------------------------------------------------------------
 # a1: k quantisation fused with the cache insert
 # ----------------------------------------------------------------------------
 

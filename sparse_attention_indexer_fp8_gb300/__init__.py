@@ -19,8 +19,8 @@ from . import _lib
 __all__ = [
     "IdxError", "idx_k_quant_and_cache", "idx_gather_k", "idx_mqa_logits_prefill",
     "idx_paged_mqa_logits_decode", "idx_topk", "idx_expand_candidates", "idx_sparse_topk_remap",
-    "idx_req_to_global_slots", "idx_dcp_topk_merge", "idx_block_span", "idx_workspace_bytes", "idx_device_error",
-    "library",
+    "idx_req_to_global_slots", "idx_dcp_topk_merge", "idx_q_rope_quant", "idx_block_span",
+    "idx_workspace_bytes", "idx_device_error", "library",
 ]
 
 
@@ -122,6 +122,24 @@ def idx_topk(logits, row_ks, row_ke, k, out, vals=None, ws=None, stream=None):
         _ptr(logits), _dtype_code(logits), _rows(logits), _ptr(row_ks), _ptr(row_ke), logits.shape[0],
         k, _ptr(out), _rows(out), _ptr(vals), 0 if vals is None else _rows(vals), _ptr(ws),
         0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def idx_q_rope_quant(q, positions, cos_sin, w, q8, w_out, softmax_scale, n_head_scale,
+                     interleaved=False, stream=None):
+    """Partial RoPE (dims 0-63), per-head e4m3 quantisation and folded weights.
+
+    q [T, 64, 128] (or [T, 8192]) bf16/fp32, positions int32 [T], cos_sin fp32
+    [max_pos, >= 64] (cos of the 32 pair angles, then sin), w [T, 64] bf16/fp32;
+    writes q8 uint8 [T, 64, 128] and w_out [T, 64] (fp32 or bf16).
+    """
+    T = q.shape[0]
+    q2 = q.reshape(T, -1) if q.dim() == 3 else q
+    q8_2 = q8.reshape(T, -1) if q8.dim() == 3 else q8
+    _check("idx_q_rope_quant", library().idx_q_rope_quant(
+        _ptr(q2), _dtype_code(q2), _rows(q2) if T else 64 * 128, _ptr(positions), _ptr(cos_sin),
+        _rows(cos_sin), cos_sin.shape[0], _lib.IDX_ROPE_INTERLEAVED if interleaved else _lib.IDX_ROPE_NEOX,
+        _ptr(w), _dtype_code(w), _rows(w), float(softmax_scale), float(n_head_scale), T, _ptr(q8_2),
+        _rows(q8_2) if T else 64 * 128, _ptr(w_out), _dtype_code(w_out), _rows(w_out), _stream(stream)))
 
 
 def idx_dcp_topk_merge(cand_vals, cand_idx, shard_offset, k_local, k, out, vals=None, pos_stride=1,

@@ -17,6 +17,8 @@ IDX_OK = 0
 IDX_F32 = 0
 IDX_BF16 = 1
 IDX_SCALE_FP32 = 0
+IDX_ROPE_NEOX = 0
+IDX_ROPE_INTERLEAVED = 1
 
 OPS = {
     "k_quant_and_cache": 1, "gather_k": 2, "mqa_logits_prefill": 3,
@@ -38,6 +40,9 @@ SIGNATURES = {
                                             c_ptr]),
     "idx_topk": (c_int, [c_ptr, c_int, c_i64, c_ptr, c_ptr, c_i32, c_i32, c_ptr, c_i64, c_ptr, c_i64,
                          c_ptr, c_size, c_ptr]),
+    "idx_q_rope_quant": (c_int, [c_ptr, c_int, c_i64, c_ptr, c_ptr, c_i64, c_i32, c_i32, c_ptr, c_int, c_i64,
+                                 ctypes.c_float, ctypes.c_float, c_i32, c_ptr, c_i64, c_ptr, c_int, c_i64,
+                                 c_ptr]),
     "idx_dcp_topk_merge": (c_int, [c_ptr, c_i64, c_ptr, c_i64, c_ptr, c_i64, c_i32, c_i32, c_i32, c_i32,
                                    c_i32, c_ptr, c_i64, c_ptr, c_i64, c_ptr]),
     "idx_expand_candidates": (c_int, [c_ptr, c_i64, c_i32, c_i32, c_ptr, c_ptr, c_i32, c_i32, c_ptr,

@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -31,6 +32,7 @@ idx_status_t encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, int 
 // Per-translation-unit readers of device error flags, registered in api.cu.
 unsigned int logits_read_and_clear_error(cudaStream_t stream, cudaError_t* err, long long* info);
 unsigned int index_ops_read_and_clear_error(cudaStream_t stream, cudaError_t* err);
+unsigned int q_rope_read_and_clear_error(cudaStream_t stream, cudaError_t* err);
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -117,6 +119,38 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2),
       "l"(policy)
       : "memory");
+}
+
+// --- e4m3 quantisation ----------------------------------------------------------
+// e4m3 codes (round to nearest even, saturating to 448) of fl32(x0 / s) and
+// fl32(x1 / s), x0 in the low byte, where fl32 is the correctly rounded
+// binary32 quotient; r must be fl32(1 / s) (__frcp_rn) and s a positive normal.
+//
+// q = fl32(x * r) lies within 1.5 * 2^-23 (relative) of x / s, and fl32(x / s)
+// within a further 2^-24, so both lie strictly inside [q (1 - 2^-21), q (1 + 2^-21)]
+// (the two bounds, rounded to binary32, are still at least 3.5 ulps away from q).
+// The conversion is monotonic: when both bounds convert to the same code, so
+// does fl32(x / s). Otherwise q is within a few ulps of a rounding boundary and
+// the quotient is computed exactly. This keeps the bytes identical to the
+// division-per-element definition at a fraction of its cost.
+__device__ __forceinline__ uint32_t e4m3x2_of_quotients(float x0, float x1, float s, float r) {
+  constexpr float kUp = 1.0f + 0x1p-21f;
+  constexpr float kDown = 1.0f - 0x1p-21f;
+  const float q0 = __fmul_rn(x0, r);
+  const float q1 = __fmul_rn(x1, r);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(__fmul_rn(q0, kUp), __fmul_rn(q1, kUp)),
+                                               __NV_SATFINITE, __NV_E4M3);
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(__fmul_rn(q0, kDown), __fmul_rn(q1, kDown)),
+                                               __NV_SATFINITE, __NV_E4M3);
+  if (hi == lo) return hi;
+  const uint32_t c0 = __nv_cvt_float_to_fp8(__fdiv_rn(x0, s), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t c1 = __nv_cvt_float_to_fp8(__fdiv_rn(x1, s), __NV_SATFINITE, __NV_E4M3);
+  return c0 | (c1 << 8);
+}
+
+// e4m3 code of fl32(x / s) by the division itself (any positive s).
+__device__ __forceinline__ uint32_t e4m3_of_quotient_exact(float x, float s) {
+  return __nv_cvt_float_to_fp8(__fdiv_rn(x, s), __NV_SATFINITE, __NV_E4M3);
 }
 
 // --- tcgen05 -----------------------------------------------------------------

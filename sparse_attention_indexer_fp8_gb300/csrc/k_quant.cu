@@ -62,13 +62,12 @@ k_quant_and_cache_kernel(const void* __restrict__ k, int64_t ld_k, int n_tok, bo
   // IEEE binary32 divisions, correctly rounded, as the scale format fixes.
   const float scale = __fdiv_rn(amax, 448.0f);
   uint32_t packed = 0;
-  if (scale != 0.0f) {
+  if (scale >= 0x1p-126f) {
+    const float r = __frcp_rn(scale);
+    packed = e4m3x2_of_quotients(x[0], x[1], scale, r) | (e4m3x2_of_quotients(x[2], x[3], scale, r) << 16);
+  } else if (scale != 0.0f) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const __nv_fp8_storage_t b =
-          __nv_cvt_float_to_fp8(__fdiv_rn(x[i], scale), __NV_SATFINITE, __NV_E4M3);
-      packed |= static_cast<uint32_t>(b) << (8 * i);
-    }
+    for (int i = 0; i < 4; ++i) packed |= e4m3_of_quotient_exact(x[i], scale) << (8 * i);
   }
   const int64_t blk = slot / block_size;
   const int off = static_cast<int>(slot - blk * block_size);

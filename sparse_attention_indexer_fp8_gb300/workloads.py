@@ -264,3 +264,42 @@ def hierarchical(seed: int = 1004, batch: int = 128, ctx: int = 131072, n_cand: 
     q8, w = make_q(seed, batch)
     cand = make_candidates(seed, batch, n_cand, ctx // 64)
     return HierarchicalWorkload(f"hierarchical-b{batch}-{ctx // 1024}k", seed, pool, q8, w, cand)
+
+
+# ----------------------------------------------------------------------------
+# q preparation (partial RoPE + per-head quantisation + weight folding)
+# ----------------------------------------------------------------------------
+
+ROPE_BASE = 10000.0
+
+
+def rope_cos_sin(max_pos: int, base: float = ROPE_BASE) -> np.ndarray:
+    """cos / sin table [max_pos, 64] float32 of the 32 rotary pair angles pos * base^(-2i/64)."""
+    i = np.arange(32, dtype=np.float64)
+    ang = np.arange(max_pos, dtype=np.float64)[:, None] * base ** (-2.0 * i / 64.0)[None, :]
+    return np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32)
+
+
+@dataclasses.dataclass
+class QPrepWorkload:
+    name: str
+    seed: int
+    T: int
+    positions: np.ndarray   # int32 [T]
+    cos_sin: np.ndarray     # float32 [max_pos, 64]
+    w: np.ndarray           # float32 [T, 64]: the projection's raw head weights
+
+
+def make_q_raw_device(seed: int, T: int, device) -> torch.Tensor:
+    """Pre-RoPE q drawn on the device: bf16 [T, 64 * 128], N(0, 1). Deterministic per seed."""
+    g = torch.Generator(device=device)
+    g.manual_seed((int(seed) * 1_000_003 + 11) % (2**62))
+    return torch.randn(T, H * D, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+
+
+def q_prep_chunk(seed: int = 1006, T: int = 8192, ctx: int = 32768) -> QPrepWorkload:
+    """The prefill chunk's queries (the last T positions of a ctx-token context)."""
+    g = _gen(seed, 12)
+    w = (torch.randn(T, H, generator=g, dtype=torch.float32) / 8.0).numpy()
+    pos = np.arange(ctx - T, ctx, dtype=np.int32)
+    return QPrepWorkload("q-prep-8192-of-32k", seed, T, pos, rope_cos_sin(ctx), w)

@@ -65,6 +65,13 @@ def test_validation_rejects_before_touching_the_device(lib):
     # k above the selection limit, NULL logits
     assert lib.idx_topk(fake, 0, 4096, None, fake, 4, 5000, fake, 5000, None, 0, None, 0, None) == 2
     assert lib.idx_topk(None, 0, 4096, None, fake, 4, 2048, fake, 2048, None, 0, None, 0, None) == 1
+    # q preparation: bad rope style, short stride, bad dtype
+    assert lib.idx_q_rope_quant(fake, 1, 8192, fake, fake, 64, 10, 5, fake, 0, 64, 1.0, 1.0, 4, fake,
+                                8192, fake, 0, 64, None) == 2
+    assert lib.idx_q_rope_quant(fake, 1, 100, fake, fake, 64, 10, 0, fake, 0, 64, 1.0, 1.0, 4, fake,
+                                8192, fake, 0, 64, None) == 1
+    assert lib.idx_q_rope_quant(fake, 7, 8192, fake, fake, 64, 10, 0, fake, 0, 64, 1.0, 1.0, 4, fake,
+                                8192, fake, 0, 64, None) == 2
     # merge: candidate stride smaller than n_shards * k_local
     assert lib.idx_dcp_topk_merge(fake, 100, fake, 100, fake, 0, 4, 1, 2048, 2, 2048, fake, 2048, None,
                                   0, None) == 1

@@ -13,7 +13,7 @@ import torch
 
 import sparse_attention_indexer_fp8_gb300 as idx
 from oracle import indexer as O
-from oracle.codecs import bf16_decode, bf16_encode
+from oracle.codecs import bf16_decode, bf16_encode, e4m3_decode
 from sparse_attention_indexer_fp8_gb300 import workloads as W
 from tests.checks import BF16_REL, assert_logits_close, assert_topk_row, assert_topk_values_exact
 
@@ -475,6 +475,115 @@ def test_dcp_merge_degenerate():
     idx.idx_dcp_topk_merge(dev(cv[:0]), dev(ci[:0]), None, k_local, k, empty)
     with pytest.raises(idx.IdxError):
         idx.idx_dcp_topk_merge(dev(cv), dev(ci), None, 64, k, out)
+
+
+def test_k_quant_rounding_boundaries():
+    # Values whose quotient by the token scale sits on, or a few ulps either side
+    # of, every e4m3 rounding midpoint, for scales that are and are not powers of
+    # two: the bytes must equal the oracle's division-per-element definition.
+    codes = e4m3_decode(np.arange(0, 0x7F, dtype=np.uint8)).astype(np.float64)   # 0 .. 448
+    mids = (codes[:-1] + codes[1:]) / 2.0
+
+    def steps(x, d):
+        x = np.float32(x)
+        to = np.float32(np.inf) if d > 0 else np.float32(-np.inf)
+        for _ in range(abs(d)):
+            x = np.nextafter(x, to)
+        return x
+
+    rows = []
+    for amax in (448.0, 300.0, 1.0, 3.0e-3, 123.456, 7.0e-5):
+        s = np.float32(np.float32(amax) / np.float32(448.0))
+        for sign in (1.0, -1.0):
+            vals = [np.float32(sign) * steps(np.float32(m) * s, d) for m in mids for d in range(-4, 5)]
+            vals = np.array(vals, dtype=np.float32)
+            for a in range(0, len(vals), 127):
+                row = np.zeros(128, dtype=np.float32)
+                row[0] = np.float32(amax)
+                chunk = vals[a:a + 127]
+                chunk = chunk[np.abs(chunk) <= np.float32(amax)]
+                row[1:1 + len(chunk)] = chunk
+                rows.append(row)
+    k = np.stack(rows)
+    n = len(k)
+    slots = np.arange(n, dtype=np.int64)
+    bs = 64
+    nblk = (n + bs - 1) // bs
+    stride = W.block_stride_bytes(bs)
+    gcache = torch.zeros((nblk, stride), dtype=torch.uint8, device=DEV)
+    idx.idx_k_quant_and_cache(dev(k), dev(slots), gcache, bs)
+    ocache = np.zeros((nblk, stride), dtype=np.uint8)
+    O.k_quant_and_cache(k, slots, ocache, bs)
+    assert np.array_equal(gcache.cpu().numpy(), ocache)
+
+
+# ------------------------------------------------------------------ q preparation
+
+def _cos_sin(max_pos, base=10000.0):
+    i = np.arange(32, dtype=np.float64)
+    ang = np.arange(max_pos, dtype=np.float64)[:, None] * base ** (-2.0 * i / 64.0)[None, :]
+    return np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32)
+
+
+@pytest.mark.parametrize("T", [1, 37, 300])
+@pytest.mark.parametrize("interleaved", [False, True])
+@pytest.mark.parametrize("q_bf16,w_bf16,out_bf16", [(True, False, False), (True, True, True),
+                                                    (False, False, True)])
+def test_q_rope_quant_vs_oracle(T, interleaved, q_bf16, w_bf16, out_bf16):
+    rng = np.random.default_rng(T * 7 + interleaved)
+    max_pos = 5000
+    qf = (rng.standard_normal((T, 64, 128)) * rng.uniform(0.01, 30, (T, 64, 1))).astype(np.float32)
+    qf[0, 3] = 0.0                                        # an all-zero head: scale 0
+    wf = rng.standard_normal((T, 64)).astype(np.float32)
+    pos = rng.integers(0, max_pos, T).astype(np.int32)
+    cs = np.zeros((max_pos, 72), dtype=np.float32)        # strided table
+    cs[:, :64] = _cos_sin(max_pos)
+    pad = 64                                              # strided q rows (elements)
+    if q_bf16:
+        qb = bf16_encode(qf)
+        qv = bf16_decode(qb).astype(np.float32)
+        buf = np.zeros((T, 8192 + pad), dtype=np.uint16)
+        buf[:, :8192] = qb.reshape(T, -1)
+        q_dev = dev_bf16(buf)[:, :8192]
+    else:
+        qv = qf
+        buf = np.zeros((T, 8192 + pad), dtype=np.float32)
+        buf[:, :8192] = qf.reshape(T, -1)
+        q_dev = dev(buf)[:, :8192]
+    if w_bf16:
+        wb = bf16_encode(wf)
+        wv, w_dev = bf16_decode(wb).astype(np.float32), dev_bf16(wb)
+    else:
+        wv, w_dev = wf, dev(wf)
+    q8 = torch.full((T, 8192 + 32), 7, dtype=torch.uint8, device=DEV)
+    w_out = torch.empty((T, 64), dtype=torch.bfloat16 if out_bf16 else torch.float32, device=DEV)
+    ss, nhs = 128 ** -0.5, 64 ** -0.5
+    idx.idx_q_rope_quant(q_dev, dev(pos), dev(cs)[:, :], w_dev, q8[:, :8192], w_out, ss, nhs, interleaved)
+    idx.idx_device_error()
+    o8, ow, _ = O.q_rope_quant(qv.reshape(T, 64, 128), pos, cs[:, :64], wv, ss, nhs, interleaved)
+    g8 = q8.cpu().numpy()
+    assert np.array_equal(g8[:, :8192].reshape(T, 64, 128), o8), "q8 bytes"
+    assert np.all(g8[:, 8192:] == 7), "bytes past the row must stay untouched"
+    if out_bf16:
+        assert np.array_equal(host_bf16(w_out), bf16_encode(ow)), "bf16 weights"
+    else:
+        assert np.array_equal(w_out.cpu().numpy(), ow), "fp32 weights"
+
+
+def test_q_rope_quant_flags_bad_positions():
+    T = 4
+    q = dev_bf16(bf16_encode(np.ones((T, 8192), dtype=np.float32)))
+    w = dev(np.ones((T, 64), dtype=np.float32))
+    q8 = torch.empty((T, 8192), dtype=torch.uint8, device=DEV)
+    w_out = torch.empty((T, 64), dtype=torch.float32, device=DEV)
+    cs = dev(_cos_sin(8))
+    idx.idx_q_rope_quant(q, dev(np.array([0, 8, -1, 7], dtype=np.int32)), cs, w, q8, w_out, 1.0, 1.0)
+    with pytest.raises(idx.IdxError, match="q rope 0x00000001"):
+        idx.idx_device_error()
+    g = q8.cpu().numpy()
+    assert np.all(g[1] == 0) and np.all(g[2] == 0) and g[0].any() and g[3].any()
+    assert np.all(w_out.cpu().numpy()[1:3] == 0)
+    idx.idx_device_error()                                 # the flag was cleared
 
 
 # ------------------------------------------------------------------ a7 expansion, a6 slots

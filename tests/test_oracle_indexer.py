@@ -17,7 +17,7 @@ import pytest
 import torch
 
 from oracle import indexer as O
-from oracle.codecs import bf16_decode, e4m3_decode, e4m3_encode
+from oracle.codecs import bf16_decode, bf16_encode, e4m3_decode, e4m3_encode
 from sparse_attention_indexer_fp8_gb300 import workloads as W
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -228,6 +228,119 @@ def test_topk_brute_force_small():
         assert sel in valid
         # tie rule: the lexicographically smallest valid set (lower index wins)
         assert sorted(sel) == min(sorted(s) for s in valid)
+
+
+# ------------------------------------------------- q preparation (RoPE + quant)
+
+def _cos_sin_table(max_pos, base=10000.0):
+    i = np.arange(32, dtype=np.float64)
+    ang = np.arange(max_pos, dtype=np.float64)[:, None] * base ** (-2.0 * i / 64.0)[None, :]
+    return np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32)
+
+
+def test_q_rope_hand_worked():
+    # one head: x_0 = 2, x_32 = 4 (a NeoX pair), c = 0.5, s = 0.75 (exact in binary):
+    # y_0 = 2*0.5 - 4*0.75 = -2, y_32 = 4*0.5 + 2*0.75 = 3.5 (both e4m3 values at
+    # scale 1); dim 100 passes through. Then 4.25 (x_1 = x_33 = ...) checks rounding:
+    # x_1 = 3, x_33 = 4 give y_33 = 4*0.5 + 3*0.75 = 4.25, which e4m3 rounds (tie, even) to 4.
+    q = np.zeros((1, 64, 128), dtype=np.float32)
+    q[0, 0, 0], q[0, 0, 32], q[0, 0, 100] = 2.0, 4.0, 448.0
+    q[0, 0, 1], q[0, 0, 33] = 3.0, 4.0
+    cs = np.zeros((1, 64), dtype=np.float32)
+    cs[0, :32], cs[0, 32:] = 0.5, 0.75
+    w = np.full((1, 64), 2.0, dtype=np.float32)
+    q8, w_out, scale = O.q_rope_quant(q, [0], cs, w, 0.5, 0.25)
+    assert scale[0, 0] == 1.0                      # amax 448 -> scale 1
+    dec = e4m3_decode(q8[0, 0])
+    assert dec[0] == -2.0 and dec[32] == 3.5 and dec[100] == 448.0
+    assert dec[1] == -1.5 and dec[33] == 4.0 and not dec[[2, 34, 64]].any()
+    assert w_out[0, 0] == 2.0 * 1.0 * 0.5 * 0.25   # weights absorb scale * softmax * n_head
+    assert np.all(scale[0, 1:] == 0) and np.all(q8[0, 1:] == 0) and np.all(w_out[0, 1:] == 0)
+
+
+def test_q_rope_quarter_turns_are_exact():
+    # c = 0, s = 1: (x_a, x_b) -> (-x_b, x_a); c = -1, s = 0: negation; identity for c = 1, s = 0
+    rng = np.random.default_rng(21)
+    q = rng.standard_normal((4, 64, 128)).astype(np.float32)
+    w = rng.standard_normal((4, 64)).astype(np.float32)
+    for interleaved in (False, True):
+        a, b = O.rope_pairs(interleaved)
+        for c_val, s_val in [(0.0, 1.0), (-1.0, 0.0), (1.0, 0.0)]:
+            cs = np.zeros((1, 64), dtype=np.float32)
+            cs[0, :32], cs[0, 32:] = c_val, s_val
+            q8, w_out, scale = O.q_rope_quant(q, np.zeros(4, int), cs, w, 1.0, 1.0, interleaved)
+            y = q.copy()
+            y[:, :, a] = c_val * q[:, :, a] - s_val * q[:, :, b]
+            y[:, :, b] = c_val * q[:, :, b] + s_val * q[:, :, a]
+            k8, ks = O.k_quant(y.reshape(-1, 128))          # the pinned per-128 quantiser
+            assert np.array_equal(q8.reshape(-1, 128), k8) and np.array_equal(scale.reshape(-1), ks)
+            assert np.array_equal(w_out, w * ks.reshape(4, 64))
+
+
+def test_q_rope_preserves_pair_norms_and_styles_agree():
+    rng = np.random.default_rng(22)
+    q = rng.standard_normal((6, 64, 128)).astype(np.float32)
+    cs = _cos_sin_table(4096)
+    pos = rng.integers(0, 4096, 6)
+    w = np.ones((6, 64), dtype=np.float32)
+    # rotation of each pair keeps its length (fp32 rounding only)
+    for interleaved in (False, True):
+        a, b = O.rope_pairs(interleaved)
+        q8, _, scale = O.q_rope_quant(q, pos, cs, w, 1.0, 1.0, interleaved)
+        y = e4m3_decode(q8).astype(np.float64) * scale[:, :, None]
+        n_in = np.hypot(q[:, :, a], q[:, :, b])
+        n_out = np.hypot(y[:, :, a], y[:, :, b])
+        assert np.allclose(n_in, n_out, rtol=0.07, atol=0.07 * scale[:, :, None])   # e4m3 error
+    # the interleaved pairing is the NeoX pairing applied to permuted dims
+    perm = np.concatenate([np.arange(0, 64, 2), np.arange(1, 64, 2), np.arange(64, 128)])
+    q8_i, w_i, _ = O.q_rope_quant(q, pos, cs, w, 1.0, 1.0, True)
+    q8_n, w_n, _ = O.q_rope_quant(q[:, :, perm], pos, cs, w, 1.0, 1.0, False)
+    assert np.array_equal(q8_i[:, :, perm], q8_n) and np.array_equal(w_i, w_n)
+
+
+def test_q_rope_quant_folded_weights_reproduce_the_unfolded_score():
+    # [DSA] step ④: with every coefficient in the weights, the scoring formula on
+    # (q8, w_out) equals sum_h w * softmax_scale * n_head_scale * (rope(q)_h . k)
+    # up to the e4m3 rounding of q
+    rng = np.random.default_rng(23)
+    q = rng.standard_normal((3, 64, 128)).astype(np.float32)
+    w = (rng.standard_normal((3, 64)) / 8).astype(np.float32)
+    cs = _cos_sin_table(64)
+    pos = np.array([0, 17, 63])
+    ss, nhs = 128 ** -0.5, 64 ** -0.5
+    q8, w_out, scale = O.q_rope_quant(q, pos, cs, w, ss, nhs)
+    k = rng.standard_normal((50, 128)).astype(np.float32)
+    k8, ks = O.k_quant(k)
+    a, b = O.rope_pairs(False)
+    for t in range(3):
+        c, s = cs[pos[t], :32].astype(np.float64), cs[pos[t], 32:].astype(np.float64)
+        y = q[t].astype(np.float64)
+        ya, yb = y[:, a] * c - y[:, b] * s, y[:, b] * c + y[:, a] * s
+        y[:, a], y[:, b] = ya, yb
+        kd = e4m3_decode(k8).astype(np.float64) * ks[:, None]
+        exact = (w[t].astype(np.float64) * ss * nhs) @ (y @ kd.T)
+        got = O.logits_row(q8[t], w_out[t], k8, ks)
+        err_bound = (np.abs(w[t].astype(np.float64) * ss * nhs) @ np.abs(y @ kd.T)) * 2.0 ** -4 + 1e-9
+        assert np.all(np.abs(got - exact) <= err_bound)
+
+
+def test_q_rope_bf16_weights_are_the_fp32_result_rounded_once():
+    # "V4.1 索引器接入稀疏 MQA logits", 实现拆解 item 5 / test list: bf16 weights equal the
+    # fp32 weights rounded once; the rounding is checked against PyTorch's cast
+    rng = np.random.default_rng(24)
+    q = rng.standard_normal((5, 64, 128)).astype(np.float32)
+    w = rng.standard_normal((5, 64)).astype(np.float32)
+    _, w_out, _ = O.q_rope_quant(q, np.zeros(5, int), _cos_sin_table(1), w, 128 ** -0.5, 64 ** -0.5)
+    ref = torch.from_numpy(w_out).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(bf16_encode(w_out), ref)
+
+
+def test_q_rope_out_of_range_position_zeroes_the_token():
+    q = np.ones((2, 64, 128), dtype=np.float32)
+    w = -np.ones((2, 64), dtype=np.float32)
+    q8, w_out, scale = O.q_rope_quant(q, [0, 5], _cos_sin_table(3), w, 1.0, 1.0)
+    assert np.all(q8[1] == 0) and np.all(scale[1] == 0) and np.all(w_out[1] == 0)
+    assert np.all(scale[0] > 0)
 
 
 # ------------------------------------------------- context-parallel merge
