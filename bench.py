@@ -565,6 +565,137 @@ def oracle_hier_row(wl, b, kq):
     return lg, pos, sl[0]
 
 
+class HierMtpBench:
+    """V4.1 consumer layers with multi-token prediction: one expansion shared by several layers."""
+
+    next_n, layers = 2, 4
+    launches_per_step = 1 + 3 * layers
+    dtype = "e4m3xe4m3->f32 (bf16 logits)"
+    metric = ("hierarchical sparse decode query-row-layers/s @128K ctx incl. top-2048 "
+              "(next_n 2, one expansion per step shared by 4 consumer layers)")
+
+    def __init__(self, name, rank, dev):
+        import sparse_attention_indexer_fp8_gb300 as idx
+        from sparse_attention_indexer_fp8_gb300.pipeline import HierarchicalStep, fill_paged_cache
+
+        self.idx, self.dev, self.name = idx, dev, name
+        self.wl = wl = W.hierarchical_mtp(seed=rank_seed(1005, rank), next_n=self.next_n)
+        pool = wl.pool
+        self.B = B = len(pool.ctx_lens)
+        self.rows = rows = B * self.next_n
+        self.cache = torch.zeros((pool.num_blocks, W.block_stride_bytes()), dtype=torch.uint8, device=dev)
+        fill_paged_cache(pool, wl.seed, self.cache, device_k=True)
+        # layer 0 uses the workload's q / weights, later layers their own draws
+        qw = [(wl.q8, wl.w)] + [W.make_q(wl.seed + 17 * i, rows) for i in range(1, self.layers)]
+        self.h_qw = qw
+        self.q = [torch.from_numpy(a).to(dev) for a, _ in qw]
+        self.w = [torch.from_numpy(b).to(dev) for _, b in qw]
+        self.bt = torch.from_numpy(pool.block_table).to(dev)
+        self.ctx = torch.from_numpy(pool.ctx_lens).to(dev)
+        self.h_row_ke = np.array([int(pool.ctx_lens[r // self.next_n]) - self.next_n + r % self.next_n + 1
+                                  for r in range(rows)], dtype=np.int32)
+        self.row_ke = torch.from_numpy(self.h_row_ke).to(dev)
+        self.cand = torch.from_numpy(wl.cand).to(dev)
+        self.st = HierarchicalStep(rows, wl.cand.shape[1], wl.cand_block_size, wl.sbk, wl.topk, pool.block_size,
+                                   dev, next_n=self.next_n)
+        self.rows_per_step = rows * self.layers
+
+    def step(self, stream, ev=None):
+        self.st.expand(self.cand, self.ctx, self.row_ke, stream=stream)
+        for i in range(self.layers):
+            if ev is not None and i == 0:
+                ev[0].record(stream)
+            idx = self.idx
+            st, wl = self.st, self.wl
+            idx.idx_paged_mqa_logits_decode(self.q[i], self.w[i], self.cache, wl.pool.block_size, self.bt,
+                                            self.ctx, st.logits, next_n=self.next_n, sparse_idx=st.sparse_idx,
+                                            end=st.end, sbk=wl.sbk, ws=st.ws, stream=stream)
+            if ev is not None and i == 0:
+                ev[1].record(stream)
+            idx.idx_sparse_topk_remap(st.logits, st.end, st.sparse_idx, None, wl.sbk, wl.topk, st.positions,
+                                      col_scratch=st.cols, ws=st.ws, stream=stream)
+            idx.idx_req_to_global_slots(st.positions, st.row_to_req, self.bt, wl.pool.block_size,
+                                        wl.pool.block_size, st.slots, stream=stream)
+
+    def e2e_prepare(self):
+        self.h_in = ([(_pin(a), d) for (a, _), d in zip(self.h_qw, self.q)] +
+                     [(_pin(b), d) for (_, b), d in zip(self.h_qw, self.w)] +
+                     [(_pin(self.wl.cand), self.cand), (_pin(self.wl.pool.ctx_lens), self.ctx),
+                      (_pin(self.h_row_ke), self.row_ke)])
+        self.h_out = torch.empty(self.st.slots.shape, dtype=torch.int32).pin_memory()
+        return _nbytes(*[h for h, _ in self.h_in]), _nbytes(self.h_out)
+
+    def e2e_step(self, stream):
+        for h, d in self.h_in:
+            d.copy_(h, non_blocking=True)
+        self.step(stream)
+        self.h_out.copy_(self.st.slots, non_blocking=True)
+
+    def verify_and_time_oracle(self, n_rows):
+        from oracle import indexer as O
+        from tests.checks import BF16_REL, assert_logits_close, assert_topk_row
+
+        wl, st, nn = self.wl, self.st, self.next_n
+        g_si, g_end = st.sparse_idx.cpu().numpy(), st.end.cpu().numpy()
+        o_si, o_end = O.expand_candidates(wl.cand, None, self.h_row_ke, wl.cand_block_size, wl.sbk)
+        assert np.array_equal(g_si, o_si) and np.array_equal(g_end, o_end), "bench expansion differs"
+        q8, w = self.h_qw[-1]          # the buffers hold the last layer's results
+        rng = np.random.default_rng(wl.seed)
+        sample = sorted(rng.choice(self.rows, size=min(n_rows, self.rows), replace=False).tolist())
+        g_lg = st.logits.float().cpu().numpy()
+        g_cols, g_pos, g_slots = st.cols.cpu().numpy(), st.positions.cpu().numpy(), st.slots.cpu().numpy()
+        kq = {r: oracle_sparse_k(wl, r // nn, o_si[r], int(o_end[r]), self.dev) for r in sample}
+        t0 = time.perf_counter()
+        ref = {}
+        for r in sample:
+            k8, ks = kq[r]
+            e = int(o_end[r])
+            lg = O.logits_row(q8[r], w[r], k8[:e], ks[:e])
+            dense = np.full(o_si.shape[1] * wl.sbk, -np.inf)
+            dense[:e] = lg
+            cols, pos = O.sparse_topk_remap_row(dense, e, o_si[r], 0, wl.sbk, wl.topk)
+            sl = O.req_to_global_slots(pos[None], np.array([r // nn]), wl.pool.block_table, wl.pool.block_size,
+                                       wl.pool.block_size)
+            ref[r] = (lg, sl[0])
+        cpu_s = time.perf_counter() - t0
+        for r in sample:
+            lg, _ = ref[r]
+            e = int(o_end[r])
+            assert_logits_close(g_lg[r, :e], lg, f"bench mtp sparse logits row {r}", BF16_REL)
+            assert_topk_row(g_cols[r], lg, wl.topk, f"bench mtp top-k row {r}", BF16_REL)
+            m = min(wl.topk, e)
+            want = [O.sparse_column_token(o_si[r], int(c), wl.sbk) for c in g_cols[r, :m]]
+            assert g_pos[r, :m].tolist() == want and np.all(g_pos[r, m:] == -1), f"bench mtp remap row {r}"
+            sm = wl.pool.slot_mapping(r // nn)
+            assert np.array_equal(g_slots[r], np.where(g_pos[r] >= 0, sm[np.clip(g_pos[r], 0, None)], -1))
+        self.end_sum = int(o_end.sum())
+        cpu = {"value": round(len(sample) / cpu_s, 3), "unit": "rows/s", "cores": os.cpu_count(),
+               "kind": "oracle", "sample": f"{len(sample)} query rows of the last layer (candidate logits, "
+                                           f"top-2048 remap, slots), candidate k prepared untimed"}
+        return cpu, f"ok on {len(sample)} sampled rows; expansion exact on all {self.rows} rows"
+
+    def roofline(self, kernel_ms, step_ms, peaks, peak_kind):
+        end_sum = getattr(self, "end_sum", None)
+        if end_sum is None:
+            end_sum = int(self.st.end.sum().item())
+        ncols = self.st.logits.shape[1]
+        byt = end_sum * W.TOKEN_BYTES + self.rows * (64 * 128 + 64 * 4 + ncols * 2)
+        ach = byt / (kernel_ms / 1e3) / 1e9
+        return {"kernel": "mqa_logits_kernel<1> (sparse decode, bf16 out, one layer)", "bound": "hbm",
+                "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(ach / peaks["hbm_gbs"], 4), "peak_source": peak_kind,
+                "algorithmic_bytes_per_launch": byt, "traffic": None, "kernel_ms": round(kernel_ms, 5)}
+
+    def config(self, world):
+        return {"workload": self.wl.name, "batch": self.B, "next_n": self.next_n, "query_rows": self.rows,
+                "layers_per_step": self.layers, "ctx": int(self.wl.pool.ctx_lens[0]),
+                "candidates": int(self.wl.cand.shape[1]), "sbk": self.wl.sbk, "topk": self.wl.topk,
+                "step": "expand once + per layer: sparse logits (bf16) + top-2048 remap + slot conversion",
+                "l2": "candidate blocks scattered over a 2.2 GB cache, no flush",
+                "e2e_result": "the last layer's slot table",
+                "parallelism": f"rows sharded, {world} independent replica(s)"}
+
+
 class QPrepBench:
     """q preparation of the prefill chunk: partial RoPE, per-head e4m3 quantisation, folded bf16 weights."""
 
@@ -648,7 +779,7 @@ class QPrepBench:
 
 
 BENCHES = {"long_decode": DecodeBench, "paged_decode": DecodeBench, "prefill": PrefillBench,
-           "hierarchical": HierBench, "q_prep": QPrepBench}
+           "hierarchical": HierBench, "hierarchical_mtp": HierMtpBench, "q_prep": QPrepBench}
 
 
 # ----------------------------------------------------------------------------- harness
@@ -777,6 +908,30 @@ def run_reference(args, rank):
             return time.perf_counter() - t0
         metric, cfg = QPrepBench.metric, {"workload": wl.name, "queries": wl.T}
         rows_per_call = 64
+    elif name == "hierarchical_mtp":
+        from oracle import indexer as O
+
+        wl = W.hierarchical_mtp()
+        nn = wl.next_n
+        rows = [0, 1, 2, 3]
+        prep = {}
+        for r in rows:
+            ke = int(wl.pool.ctx_lens[r // nn]) - nn + r % nn + 1
+            si, end = O.expand_candidates_row(wl.cand[r], 0, ke, 64, 64)
+            prep[r] = (si, end, oracle_sparse_k(wl, r // nn, si, end, None))
+
+        def one(i):
+            r = rows[i % 4]
+            si, end, (k8, ks) = prep[r]
+            t0 = time.perf_counter()
+            lg = O.logits_row(wl.q8[r], wl.w[r], k8[:end], ks[:end])
+            dense = np.full(si.shape[0] * wl.sbk, -np.inf)
+            dense[:end] = lg
+            _, pos = O.sparse_topk_remap_row(dense, end, si, 0, wl.sbk, wl.topk)
+            O.req_to_global_slots(pos[None], np.array([r // nn]), wl.pool.block_table, 64, 64)
+            return time.perf_counter() - t0
+        metric, cfg = HierMtpBench.metric, {"workload": wl.name, "batch": len(wl.pool.ctx_lens),
+                                           "next_n": nn, "topk": wl.topk}
     else:
         from oracle import indexer as O
 

@@ -98,12 +98,22 @@ class DecodeStep:
 
 
 class HierarchicalStep:
-    """One V4.1 consumer-layer decode step: expand, sparse score (bf16), select + remap, slots."""
+    """One V4.1 decode step for the consumer layers: expand once, then score, select + remap, slots.
+
+    [V41] 功能与动机 / 实现拆解 item 2: the candidate expansion (and the schedule)
+    is done once per step and shared by every consumer layer of that step;
+    ``expand`` fills ``sparse_idx`` / ``end`` and ``score`` runs one layer on
+    them (any number of times, the expansion buffers are only read). With
+    ``next_n > 1`` (multi-token prediction) every request has ``next_n`` query
+    rows, row ``r`` belonging to request ``r // next_n``, each with its own
+    causal limit (``row_ke``) and candidates.
+    """
 
     def __init__(self, rows: int, n_cand: int, cand_block_size: int = 64, sbk: int = 64,
-                 topk: int = W.TOPK, block_size: int = W.BLOCK_SIZE, device="cuda"):
+                 topk: int = W.TOPK, block_size: int = W.BLOCK_SIZE, device="cuda", next_n: int = 1):
         R = cand_block_size // sbk
         self.cand_block_size, self.sbk, self.topk, self.block_size = cand_block_size, sbk, topk, block_size
+        self.next_n = next_n
         self.sparse_idx = torch.empty((rows, n_cand * R), dtype=torch.int32, device=device)
         self.end = torch.empty(rows, dtype=torch.int32, device=device)
         self.logits = torch.empty((rows, n_cand * R * sbk), dtype=torch.bfloat16, device=device)
@@ -111,18 +121,29 @@ class HierarchicalStep:
         self.positions = torch.empty((rows, topk), dtype=torch.int32, device=device)
         self.slots = torch.empty((rows, topk), dtype=torch.int32, device=device)
         self.ws = torch.zeros((rows, 1024), dtype=torch.int32, device=device)
+        self.row_to_req = (None if next_n == 1 else
+                           torch.arange(rows // next_n, dtype=torch.int32, device=device).repeat_interleave(next_n))
 
-    def run(self, q, w, cache, block_table, ctx_lens, cand, stream=None):
-        idx_expand_candidates(cand, None, ctx_lens, self.cand_block_size, self.sbk, self.sparse_idx,
-                              self.end, stream=stream)
+    def expand(self, cand, ctx_lens, row_ke=None, stream=None):
+        """Once per step. ``row_ke`` (int32 [rows]) is required when ``next_n > 1``."""
+        ke = ctx_lens if row_ke is None else row_ke
+        idx_expand_candidates(cand, None, ke, self.cand_block_size, self.sbk, self.sparse_idx, self.end,
+                              stream=stream)
+
+    def score(self, q, w, cache, block_table, ctx_lens, stream=None):
+        """One consumer layer on the current expansion; returns the slot table."""
         idx_paged_mqa_logits_decode(q, w, cache, self.block_size, block_table, ctx_lens, self.logits,
-                                    sparse_idx=self.sparse_idx, end=self.end, sbk=self.sbk,
-                                    ws=self.ws, stream=stream)
+                                    next_n=self.next_n, sparse_idx=self.sparse_idx, end=self.end,
+                                    sbk=self.sbk, ws=self.ws, stream=stream)
         idx_sparse_topk_remap(self.logits, self.end, self.sparse_idx, None, self.sbk, self.topk,
                               self.positions, col_scratch=self.cols, ws=self.ws, stream=stream)
-        idx_req_to_global_slots(self.positions, None, block_table, self.block_size, self.block_size,
-                                self.slots, stream=stream)
+        idx_req_to_global_slots(self.positions, self.row_to_req, block_table, self.block_size,
+                                self.block_size, self.slots, stream=stream)
         return self.slots
+
+    def run(self, q, w, cache, block_table, ctx_lens, cand, row_ke=None, stream=None):
+        self.expand(cand, ctx_lens, row_ke, stream=stream)
+        return self.score(q, w, cache, block_table, ctx_lens, stream=stream)
 
 
 def exchange_candidates(vals: torch.Tensor, idx: torch.Tensor, group=None):

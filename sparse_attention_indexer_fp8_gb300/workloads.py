@@ -255,6 +255,7 @@ class HierarchicalWorkload:
     cand_block_size: int = 64
     sbk: int = 64
     topk: int = TOPK
+    next_n: int = 1             # query rows per request (rows = batch * next_n)
 
 
 def hierarchical(seed: int = 1004, batch: int = 128, ctx: int = 131072, n_cand: int = 64) -> HierarchicalWorkload:
@@ -264,6 +265,18 @@ def hierarchical(seed: int = 1004, batch: int = 128, ctx: int = 131072, n_cand: 
     q8, w = make_q(seed, batch)
     cand = make_candidates(seed, batch, n_cand, ctx // 64)
     return HierarchicalWorkload(f"hierarchical-b{batch}-{ctx // 1024}k", seed, pool, q8, w, cand)
+
+
+def hierarchical_mtp(seed: int = 1005, batch: int = 128, ctx: int = 131072, n_cand: int = 64,
+                     next_n: int = 2) -> HierarchicalWorkload:
+    """The hierarchical workload with next_n query rows per request, each with its own candidates."""
+    lens = np.full(batch, ctx, dtype=np.int32)
+    pool = make_pool(seed, lens)
+    rows = batch * next_n
+    q8, w = make_q(seed, rows)
+    cand = make_candidates(seed, rows, n_cand, ctx // 64)
+    return HierarchicalWorkload(f"hierarchical-mtp{next_n}-b{batch}-{ctx // 1024}k", seed, pool, q8, w, cand,
+                                next_n=next_n)
 
 
 # ----------------------------------------------------------------------------

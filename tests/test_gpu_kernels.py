@@ -191,6 +191,48 @@ def test_decode_sparse_logits_and_remap(sbk, cbs, out_bf16):
                         BF16_REL if out_bf16 else 0.0)
 
 
+@pytest.mark.parametrize("next_n", [2, 3])
+def test_hierarchical_mtp_rows_and_layer_reuse(next_n):
+    # V4.1 consumer layers with multi-token prediction: each request has next_n
+    # query rows (row r of request r // next_n sees [0, L - next_n + j + 1)); the
+    # expansion is done once and two layers (different q / weights) are scored
+    # on it, each checked against the oracle, and the expansion is untouched.
+    from sparse_attention_indexer_fp8_gb300.pipeline import HierarchicalStep
+
+    ctx = np.array([1000, 777, 4096, 2500, 64, 5], dtype=np.int32)
+    B = len(ctx)
+    rows = B * next_n
+    pool = W.make_pool(300 + next_n, ctx)
+    g, o = build_caches(pool, 300 + next_n)
+    cand = W.make_candidates(310 + next_n, rows, 16, 64, n_dup=3, n_pad=2, n_oob=2)
+    r2r = np.repeat(np.arange(B), next_n).astype(np.int32)
+    row_ke = np.array([O.decode_row_limit(int(ctx[r // next_n]), next_n, r % next_n) for r in range(rows)],
+                      dtype=np.int32)
+    k = 200
+    st = HierarchicalStep(rows, cand.shape[1], 64, 64, k, 64, DEV, next_n=next_n)
+    st.expand(dev(cand), dev(ctx), dev(row_ke))
+    osi, oend = O.expand_candidates(cand, None, row_ke, 64, 64)
+    si0, end0 = st.sparse_idx.clone(), st.end.clone()
+    assert np.array_equal(si0.cpu().numpy(), osi) and np.array_equal(end0.cpu().numpy(), oend)
+    for layer in range(2):
+        q8, w = W.make_q(320 + 10 * layer + next_n, rows)
+        slots = st.score(dev(q8), dev(w), g, dev(pool.block_table), dev(ctx)).cpu().numpy()
+        assert torch.equal(st.sparse_idx, si0) and torch.equal(st.end, end0), "expansion must be reusable"
+        ref = O.sparse_logits_decode(q8, w, o, 64, pool.block_table, r2r, osi, oend, 64)
+        got = st.logits.float().cpu().numpy()
+        assert_logits_close(got, ref, f"layer {layer} sparse logits", BF16_REL)
+        cols, pos = st.cols.cpu().numpy(), st.positions.cpu().numpy()
+        for r in range(rows):
+            e = int(oend[r])
+            assert_topk_values_exact(cols[r], got[r, :e], k, f"layer {layer} row {r}")
+            assert_topk_row(cols[r], ref[r, :e], k, f"layer {layer} row {r} vs oracle", BF16_REL)
+            m = min(k, e)
+            want = [O.sparse_column_token(osi[r], int(c), 64) for c in cols[r, :m]]
+            assert pos[r, :m].tolist() == want and np.all(pos[r, m:] == -1)
+        oslots = O.req_to_global_slots(pos, r2r, pool.block_table, 64, 64)
+        assert np.array_equal(slots, oslots)
+
+
 # ------------------------------------------------------------------ a3 prefill logits
 
 @pytest.mark.parametrize("T,w_bf16,out_bf16,ragged", [(256, False, False, False), (255, True, True, True),
