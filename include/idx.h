@@ -78,7 +78,10 @@ typedef enum idx_status {
 } idx_status_t;
 
 enum { IDX_F32 = 0, IDX_BF16 = 1 };          /* element types of weights, k and logits */
-enum { IDX_SCALE_FP32 = 0 };                 /* k scale format: fp32 amax / 448 */
+enum {                                       /* k scale format, stored as fp32 in the cache */
+  IDX_SCALE_FP32 = 0,                        /*   amax / 448 */
+  IDX_SCALE_UE8M0 = 1                        /*   the smallest power of two >= amax / 448 */
+};
 
 /* operation codes of idx_workspace_bytes */
 enum {
@@ -111,7 +114,9 @@ enum {
  *                 one >= num_blocks * block_size, skips the token.
  *   cache         uint8 [num_blocks, block_stride_bytes], written in place.
  *   block_size    tokens per block, one of 16, 32, 64, 128.
- *   scale_fmt     IDX_SCALE_FP32.
+ *   scale_fmt     IDX_SCALE_FP32, or IDX_SCALE_UE8M0 (step 5's scale_fmt option:
+ *                 the binary32 amax / 448 rounded up to a power of two, so the
+ *                 division by it is exact; same 4-byte slot).
  * Errors: IDX_ERR_INVALID_ARG for NULL pointers with n_tok > 0, n_tok < 0,
  * ld_k < 128, block_stride_bytes < block_size * 132; IDX_ERR_UNSUPPORTED for
  * another block_size, block_stride_bytes % 16 != 0, another dtype or scale_fmt.

@@ -87,7 +87,20 @@ def q_rope_quant(q, positions, cos_sin, w, softmax_scale, n_head_scale, interlea
 # a1: k quantisation fused with the cache insert
 # ----------------------------------------------------------------------------
 
-def k_quant(k) -> tuple[np.ndarray, np.ndarray]:
+def ue8m0_ceil(s) -> np.ndarray:
+    """The smallest power of two >= each positive binary32 ``s`` (0 stays 0).
+
+    The UE8M0 scale format ([DSA] step ⑤'s ``scale_fmt`` option) keeps only an
+    exponent: ``s = m * 2^e`` with ``m`` in [0.5, 1) is already a power of two when
+    ``m == 0.5``, and otherwise rounds up to ``2^e``.
+    """
+    s = np.asarray(s, dtype=np.float32)
+    m, e = np.frexp(s.astype(np.float64))
+    up = np.where(m == 0.5, s.astype(np.float64), np.ldexp(1.0, e))
+    return np.where(s == 0, 0.0, up).astype(np.float32)
+
+
+def k_quant(k, ue8m0: bool = False) -> tuple[np.ndarray, np.ndarray]:
     """Per-token FP8 quantisation of k, one fp32 scale per 128 values.
 
     [DSA] step ⑤: k is quantised and written into the cache in one operation
@@ -98,7 +111,9 @@ def k_quant(k) -> tuple[np.ndarray, np.ndarray]:
     Steps, all in IEEE binary32 as the format fixes: ``amax = max |k_d|``;
     ``scale = amax / 448``; ``k8_d = e4m3(k_d / scale)``. A token whose scale is
     zero (all-zero k, or amax so small the division underflows) stores scale 0
-    and all-zero bytes, so its logits are exactly 0.
+    and all-zero bytes, so its logits are exactly 0. With ``ue8m0`` the binary32
+    ``amax / 448`` is rounded up to a power of two (``ue8m0_ceil``) before the
+    division, which is then exact.
 
     k: [n, 128] array of fp32 values (bf16 inputs widened exactly).
     Returns (k8 uint8 [n, 128], scale float32 [n]).
@@ -111,13 +126,15 @@ def k_quant(k) -> tuple[np.ndarray, np.ndarray]:
         kb = k[a:a + 4096]
         amax = np.max(np.abs(kb), axis=1)
         s = (amax / np.float32(E4M3_MAX)).astype(np.float32)
+        if ue8m0:
+            s = ue8m0_ceil(s)
         scale[a:a + 4096] = s
         live = s != 0
         k8[a:a + 4096][live] = e4m3_encode(kb[live] / s[live, None])
     return k8, scale
 
 
-def k_quant_and_cache(k, slot_mapping, cache: np.ndarray, block_size: int) -> None:
+def k_quant_and_cache(k, slot_mapping, cache: np.ndarray, block_size: int, ue8m0: bool = False) -> None:
     """Quantise each token of ``k`` and write it to its slot of the paged cache.
 
     [DSA] step ⑤ and data-flow item 1 (132 bytes per token). ``slot_mapping[i]``
@@ -126,7 +143,7 @@ def k_quant_and_cache(k, slot_mapping, cache: np.ndarray, block_size: int) -> No
 
     cache: uint8 [num_blocks, block_stride], modified in place.
     """
-    k8, scale = k_quant(k)
+    k8, scale = k_quant(k, ue8m0)
     slots = np.asarray(slot_mapping, dtype=np.int64)
     for i, slot in enumerate(slots):
         if slot < 0:

@@ -68,12 +68,16 @@ def _rows(t: torch.Tensor) -> int:
     return t.stride(0)
 
 
-def idx_k_quant_and_cache(k, slot_mapping, cache, block_size, stream=None):
-    """k [n, 128] bf16/f32, slot_mapping int64 [n], cache uint8 [num_blocks, block_stride]."""
+def idx_k_quant_and_cache(k, slot_mapping, cache, block_size, ue8m0=False, stream=None):
+    """k [n, 128] bf16/f32, slot_mapping int64 [n], cache uint8 [num_blocks, block_stride].
+
+    ``ue8m0``: power-of-two scales (the UE8M0 scale format) instead of amax / 448.
+    """
     ld_k = _rows(k)
     _check("idx_k_quant_and_cache", library().idx_k_quant_and_cache(
         _ptr(k), _dtype_code(k), ld_k, k.shape[0], _ptr(slot_mapping), _ptr(cache),
-        cache.shape[0], block_size, cache.stride(0), _lib.IDX_SCALE_FP32, _stream(stream)))
+        cache.shape[0], block_size, cache.stride(0),
+        _lib.IDX_SCALE_UE8M0 if ue8m0 else _lib.IDX_SCALE_FP32, _stream(stream)))
 
 
 def idx_gather_k(cache, block_size, block_table_row, n_tok, k8_out, kscale_out, stream=None):

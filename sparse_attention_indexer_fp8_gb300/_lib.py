@@ -17,6 +17,7 @@ IDX_OK = 0
 IDX_F32 = 0
 IDX_BF16 = 1
 IDX_SCALE_FP32 = 0
+IDX_SCALE_UE8M0 = 1
 IDX_ROPE_NEOX = 0
 IDX_ROPE_INTERLEAVED = 1
 

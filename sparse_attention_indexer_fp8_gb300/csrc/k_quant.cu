@@ -42,9 +42,23 @@ __device__ __forceinline__ void load4(const void* k, int64_t ld_k, int tok, int 
   }
 }
 
+// The smallest power of two >= s (s a positive binary32 value), the UE8M0
+// scale format: an exact power of two keeps its value, anything else rounds up
+// to the next exponent. 0 stays 0.
+__device__ __forceinline__ float ue8m0_ceil(float s) {
+  const uint32_t b = __float_as_uint(s);
+  if (s == 0.0f) return 0.0f;
+  const uint32_t e = b >> 23;                  // biased exponent (s > 0, finite)
+  if (e == 0) {                                // subnormal: the next power of two above it
+    const int lz = __clz(b);                   // b < 2^23
+    return __uint_as_float(1u << (31 - lz + ((b & (b - 1)) != 0)));
+  }
+  return (b & 0x7FFFFFu) == 0 ? s : __uint_as_float((e + 1) << 23);
+}
+
 template <bool kBf16>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
-k_quant_and_cache_kernel(const void* __restrict__ k, int64_t ld_k, int n_tok, bool vec,
+k_quant_and_cache_kernel(const void* __restrict__ k, int64_t ld_k, int n_tok, bool vec, bool ue8m0,
                          const int64_t* __restrict__ slot_mapping, uint8_t* __restrict__ cache,
                          int64_t n_slots, int block_size, int64_t block_stride) {
   const int tok = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
@@ -59,8 +73,10 @@ k_quant_and_cache_kernel(const void* __restrict__ k, int64_t ld_k, int n_tok, bo
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
 
-  // IEEE binary32 divisions, correctly rounded, as the scale format fixes.
-  const float scale = __fdiv_rn(amax, 448.0f);
+  // IEEE binary32 divisions, correctly rounded, as the scale format fixes;
+  // UE8M0 then rounds the scale up to a power of two (k / scale stays <= 448)
+  float scale = __fdiv_rn(amax, 448.0f);
+  if (ue8m0) scale = ue8m0_ceil(scale);
   uint32_t packed = 0;
   if (scale >= 0x1p-126f) {
     const float r = __frcp_rn(scale);
@@ -127,7 +143,9 @@ extern "C" idx_status_t idx_k_quant_and_cache(const void* k, int k_dtype, int64_
   const char* fn = "idx_k_quant_and_cache";
   if (n_tok < 0 || num_blocks < 0) return fail(IDX_ERR_INVALID_ARG, "%s: negative size", fn);
   if (k_dtype != IDX_BF16 && k_dtype != IDX_F32) return fail(IDX_ERR_UNSUPPORTED, "%s: k_dtype %d", fn, k_dtype);
-  if (scale_fmt != IDX_SCALE_FP32) return fail(IDX_ERR_UNSUPPORTED, "%s: scale_fmt %d", fn, scale_fmt);
+  if (scale_fmt != IDX_SCALE_FP32 && scale_fmt != IDX_SCALE_UE8M0) {
+    return fail(IDX_ERR_UNSUPPORTED, "%s: scale_fmt %d", fn, scale_fmt);
+  }
   if (ld_k < kDim) return fail(IDX_ERR_INVALID_ARG, "%s: ld_k %lld < 128", fn, static_cast<long long>(ld_k));
   if (n_tok == 0) return IDX_OK;
   if (!k || !slot_mapping || !cache) return fail(IDX_ERR_INVALID_ARG, "%s: NULL pointer", fn);
@@ -140,10 +158,12 @@ extern "C" idx_status_t idx_k_quant_and_cache(const void* k, int k_dtype, int64_
   const dim3 grid((n_tok + kWarpsPerBlock - 1) / kWarpsPerBlock);
   if (k_dtype == IDX_BF16) {
     k_quant_and_cache_kernel<true><<<grid, kWarpsPerBlock * 32, 0, stream>>>(
-        k, ld_k, n_tok, vec, slot_mapping, cache, n_slots, block_size, block_stride_bytes);
+        k, ld_k, n_tok, vec, scale_fmt == IDX_SCALE_UE8M0, slot_mapping, cache, n_slots, block_size,
+        block_stride_bytes);
   } else {
     k_quant_and_cache_kernel<false><<<grid, kWarpsPerBlock * 32, 0, stream>>>(
-        k, ld_k, n_tok, vec, slot_mapping, cache, n_slots, block_size, block_stride_bytes);
+        k, ld_k, n_tok, vec, scale_fmt == IDX_SCALE_UE8M0, slot_mapping, cache, n_slots, block_size,
+        block_stride_bytes);
   }
   return check_launch(fn);
 }

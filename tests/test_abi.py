@@ -60,6 +60,7 @@ def test_validation_rejects_before_touching_the_device(lib):
     fake = ctypes.c_void_p(0x1000)   # never dereferenced: every call below fails validation first
     # block size outside {16, 32, 64, 128}
     assert lib.idx_k_quant_and_cache(fake, 1, 128, 4, fake, fake, 8, 48, 8704, 0, None) == 2
+    assert lib.idx_k_quant_and_cache(fake, 1, 128, 4, fake, fake, 8, 64, 8704, 2, None) == 2   # scale_fmt
     # block stride too small for 64 tokens of 132 bytes
     assert lib.idx_k_quant_and_cache(fake, 1, 128, 4, fake, fake, 8, 64, 8000, 0, None) == 1
     # k above the selection limit, NULL logits

@@ -43,7 +43,7 @@ def host_bf16(t):
     return t.view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def build_caches(pool, seed, block_size=64, stride=None):
+def build_caches(pool, seed, block_size=64, stride=None, ue8m0=False):
     """GPU cache filled by the kernel, oracle cache filled by the oracle, same k."""
     stride = stride or W.block_stride_bytes(block_size)
     gcache = torch.zeros((pool.num_blocks, stride), dtype=torch.uint8, device=DEV)
@@ -52,10 +52,10 @@ def build_caches(pool, seed, block_size=64, stride=None):
     for b in range(len(pool.ctx_lens)):
         kb = W.make_k(seed, b, int(pool.ctx_lens[b]))
         ks.append(kb)
-        O.k_quant_and_cache(bf16_decode(kb), pool.slot_mapping(b), ocache, block_size)
+        O.k_quant_and_cache(bf16_decode(kb), pool.slot_mapping(b), ocache, block_size, ue8m0)
     k_all = dev_bf16(np.concatenate(ks))
     slots = dev(np.concatenate([pool.slot_mapping(b) for b in range(len(pool.ctx_lens))]))
-    idx.idx_k_quant_and_cache(k_all, slots, gcache, block_size)
+    idx.idx_k_quant_and_cache(k_all, slots, gcache, block_size, ue8m0=ue8m0)
     return gcache, ocache
 
 
@@ -65,6 +65,24 @@ def test_k_quant_and_cache_bitexact_tiny_pool():
     wl = W.tiny_decode()
     g, o = build_caches(wl.pool, wl.seed)
     assert np.array_equal(g.cpu().numpy(), o)
+
+
+def test_ue8m0_cache_bitexact_and_decode_logits():
+    # power-of-two k scales (the UE8M0 scale format): the cache bytes equal the
+    # oracle's, and the scoring kernels read that cache unchanged
+    wl = W.tiny_decode()
+    pool = wl.pool
+    g, o = build_caches(pool, wl.seed, ue8m0=True)
+    assert np.array_equal(g.cpu().numpy(), o)
+    rows = len(pool.ctx_lens)
+    ld = int(pool.ctx_lens.max())
+    out = torch.empty((rows, ld), dtype=torch.float32, device=DEV)
+    idx.idx_paged_mqa_logits_decode(dev(wl.q8), dev(wl.w), g, 64, dev(pool.block_table), dev(pool.ctx_lens), out)
+    ref = O.paged_decode_logits(wl.q8, wl.w, o, 64, pool.block_table, pool.ctx_lens)
+    got = out.cpu().numpy()
+    for r in range(rows):
+        L = int(pool.ctx_lens[r])
+        assert_logits_close(got[r, :L], ref[r, :L], f"ue8m0 row {r}")
 
 
 def test_k_quant_skips_negative_and_out_of_range_slots_f32_strided_bs16():

@@ -68,6 +68,29 @@ def test_k_quant_bf16_inputs_and_underflow():
     assert s[0] == 0 and not k8.any()
 
 
+def test_ue8m0_scales_hand_worked_and_bounds():
+    # amax 448 -> 1 (already a power of two); 500 -> 500/448 = 1.116 -> 2;
+    # 224 -> 0.5; 300 -> 0.6696 -> 1; 0 -> 0 (zero bytes)
+    k = np.zeros((5, 128), dtype=np.float32)
+    for i, a in enumerate([448.0, 500.0, 224.0, 300.0, 0.0]):
+        k[i, 7] = a
+        k[i, 8] = -a / 2
+    k8, s = O.k_quant(k, ue8m0=True)
+    assert s.tolist() == [1.0, 2.0, 0.5, 1.0, 0.0]
+    assert e4m3_decode(k8[1, 7:9]).tolist() == [256.0, -128.0]      # 500/2 = 250 -> 256 (RNE), -125 -> -128
+    assert e4m3_decode(k8[3, 7:9]).tolist() == [288.0, -144.0]      # 300, -150 rounded to e4m3
+    assert not k8[4].any()
+    # random rows: a power of two in [amax/448, 2 amax/448), every code within range
+    rng = np.random.default_rng(30)
+    kr = (rng.standard_normal((200, 128)) * rng.uniform(1e-3, 1e3, (200, 1))).astype(np.float32)
+    k8, s = O.k_quant(kr, ue8m0=True)
+    base = (np.max(np.abs(kr), axis=1) / np.float32(448)).astype(np.float32)
+    m, _ = np.frexp(s.astype(np.float64))
+    assert np.all(m == 0.5) and np.all(s >= base) and np.all(s < 2 * base)
+    # the division by a power of two is exact: codes are the fp32 scaling's codes
+    assert np.array_equal(k8, e4m3_encode(kr.astype(np.float64) / s[:, None]))
+
+
 def test_cache_layout_hand_worked():
     bs, stride = 64, W.block_stride_bytes(64)
     assert stride == 8704
