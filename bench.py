@@ -784,6 +784,9 @@ BENCHES = {"long_decode": DecodeBench, "paged_decode": DecodeBench, "prefill": P
 
 # ----------------------------------------------------------------------------- harness
 
+GRAPH_STEPS = 10
+
+
 def run_ours(args, rank, world, local, dist):
     import sparse_attention_indexer_fp8_gb300 as idx
 
@@ -801,21 +804,42 @@ def run_ours(args, rank, world, local, dist):
         for _ in range(5):
             bench.step(stream)
         torch.cuda.synchronize(dev)
+    # the dominant kernel's own duration, from events around it in plain launches
+    n_kev = min(args.steps, 100)
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
+           for _ in range(n_kev)]
+    for i in range(n_kev):
+        bench.step(stream, kev[i])
+    torch.cuda.synchronize(dev)
+    kernel_ms = statistics.mean(a.elapsed_time(b) for a, b in kev)
+    # the timed steps: replays of a CUDA graph holding GRAPH_STEPS steps (the
+    # launches of a step are captured once; a replay costs one launch)
+    graph = None
+    if args.graphs:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            cap = torch.cuda.current_stream(dev)
+            for _ in range(GRAPH_STEPS):
+                bench.step(cap)
+        graph.replay()
+        torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(dist)
     torch.cuda.synchronize(dev)
     t0 = time.time()
     e0.record(stream)
-    for i in range(args.steps):
-        bench.step(stream, kev[i])
+    done = 0
+    if graph is not None:
+        for _ in range(args.steps // GRAPH_STEPS):
+            graph.replay()
+        done = args.steps // GRAPH_STEPS * GRAPH_STEPS
+    for _ in range(args.steps - done):
+        bench.step(stream)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     barrier(dist)
     t1 = time.time()
     ms_total = max_over_ranks(dist, e0.elapsed_time(e1), dev)
-    kernel_ms = statistics.mean(a.elapsed_time(b) for a, b in kev)
     idx.idx_device_error(stream)
 
     # end to end through the public API with host buffers: per step H2D of the
@@ -823,11 +847,25 @@ def run_ours(args, rank, world, local, dist):
     h2d, d2h = bench.e2e_prepare()
     for _ in range(args.warmup):
         bench.e2e_step(stream)
+    e2e_graph = None
+    if args.graphs:
+        # the copies from and to pinned host memory are captured with the kernels
+        e2e_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(e2e_graph):
+            cap = torch.cuda.current_stream(dev)
+            for _ in range(GRAPH_STEPS):
+                bench.e2e_step(cap)
+        e2e_graph.replay()
     barrier(dist)
     torch.cuda.synchronize(dev)
     a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a0.record(stream)
-    for _ in range(args.steps):
+    done = 0
+    if e2e_graph is not None:
+        for _ in range(args.steps // GRAPH_STEPS):
+            e2e_graph.replay()
+        done = args.steps // GRAPH_STEPS * GRAPH_STEPS
+    for _ in range(args.steps - done):
         bench.e2e_step(stream)
     a1.record(stream)
     torch.cuda.synchronize(dev)
@@ -858,6 +896,7 @@ def run_ours(args, rank, world, local, dist):
         "e2e": {"value": round(rows_total / (e2e_ms / 1e3 / args.steps), 1), "unit": "rows/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": bench.launches_per_step * args.steps,
+        "launch": (f"CUDA graph of {GRAPH_STEPS} steps, replayed" if args.graphs else "direct launches"),
         "clocks": sampler.summary(t0, t1) if sampler else None,
         "parity": parity,
     }
@@ -972,6 +1011,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="long_decode", choices=sorted(BENCHES))
     ap.add_argument("--cpu-rows", type=int, default=12)
+    ap.add_argument("--no-graphs", dest="graphs", action="store_false",
+                    help="launch every step's kernels directly instead of replaying a CUDA graph")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
