@@ -183,3 +183,67 @@ def test_dcp_four_emulated_ranks_paged_decode():
         ref = O.logits_row(wl.q8[b], wl.w[b], k8, ks)
         assert_topk_row(pos[b], ref, wl.topk, f"dcp top-k row {b}")
         assert_logits_close(sc[b], ref[pos[b]], f"dcp scores row {b}")
+
+
+def test_q_prep_chunk_8192_bitexact_sampled():
+    # the q preparation of the prefill chunk (8192 queries, positions 24576..32767 of
+    # a 32K context) in the benchmark's configuration: bf16 q, fp32 weights in,
+    # bf16 weights out; q8 bytes and weights bit-exact on 256 sampled rows
+    wl = W.q_prep_chunk()
+    q = W.make_q_raw_device(wl.seed, wl.T, DEV)
+    q8 = torch.empty((wl.T, 8192), dtype=torch.uint8, device=DEV)
+    wo = torch.empty((wl.T, 64), dtype=torch.bfloat16, device=DEV)
+    idx.idx_q_rope_quant(q, torch.from_numpy(wl.positions).to(DEV), torch.from_numpy(wl.cos_sin).to(DEV),
+                         torch.from_numpy(wl.w).to(DEV), q8, wo, 128 ** -0.5, 64 ** -0.5)
+    idx.idx_device_error()
+    rows = np.sort(np.random.default_rng(wl.seed).choice(wl.T, 256, replace=False))
+    rows = np.unique(np.concatenate([rows, [0, wl.T - 1]]))
+    qs = bf16_decode(q[rows].view(torch.int16).cpu().numpy().view(np.uint16)).astype(np.float32)
+    o8, ow, _ = O.q_rope_quant(qs.reshape(-1, 64, 128), wl.positions[rows], wl.cos_sin, wl.w[rows],
+                               128 ** -0.5, 64 ** -0.5)
+    assert np.array_equal(q8[rows].cpu().numpy().reshape(-1, 64, 128), o8)
+    from oracle.codecs import bf16_encode
+    assert np.array_equal(wo[rows].view(torch.int16).cpu().numpy().view(np.uint16), bf16_encode(ow))
+
+
+def test_hierarchical_mtp_b128_128k_four_layers():
+    # MTP rows (next_n 2) at 128K with one expansion shared by four layers, as benchmarked
+    wl = W.hierarchical_mtp()
+    pool, nn = wl.pool, wl.next_n
+    B = len(pool.ctx_lens)
+    rows = B * nn
+    cache = torch.zeros((pool.num_blocks, W.block_stride_bytes()), dtype=torch.uint8, device=DEV)
+    fill_paged_cache(pool, wl.seed, cache, device_k=True)
+    row_ke = np.array([int(pool.ctx_lens[r // nn]) - nn + r % nn + 1 for r in range(rows)], dtype=np.int32)
+    stp = HierarchicalStep(rows, wl.cand.shape[1], wl.cand_block_size, wl.sbk, wl.topk, pool.block_size, DEV,
+                           next_n=nn)
+    stp.expand(torch.from_numpy(wl.cand).to(DEV), torch.from_numpy(pool.ctx_lens).to(DEV),
+               torch.from_numpy(row_ke).to(DEV))
+    osi, oend = O.expand_candidates(wl.cand, None, row_ke, wl.cand_block_size, wl.sbk)
+    assert np.array_equal(stp.sparse_idx.cpu().numpy(), osi) and np.array_equal(stp.end.cpu().numpy(), oend)
+    bt = torch.from_numpy(pool.block_table).to(DEV)
+    ctx = torch.from_numpy(pool.ctx_lens).to(DEV)
+    rng = np.random.default_rng(wl.seed)
+    check = sorted(rng.choice(rows, size=3, replace=False).tolist())
+    for layer in range(4):
+        q8, w = (wl.q8, wl.w) if layer == 0 else W.make_q(wl.seed + 17 * layer, rows)
+        slots = stp.score(torch.from_numpy(q8).to(DEV), torch.from_numpy(w).to(DEV), cache, bt, ctx)
+        idx.idx_device_error()
+        if layer not in (0, 3):
+            continue
+        lg = stp.logits.float().cpu().numpy()
+        cols, pos, sl = stp.cols.cpu().numpy(), stp.positions.cpu().numpy(), slots.cpu().numpy()
+        for r in check:
+            e = int(oend[r])
+            b = r // nn
+            kall = _k_host(wl.seed, b, int(pool.ctx_lens[b]))
+            toks = np.array([O.sparse_column_token(osi[r], c, wl.sbk) for c in range(e)], dtype=np.int64)
+            k8, ks = O.k_quant(kall[toks])
+            ref = O.logits_row(q8[r], w[r], k8, ks)
+            assert_logits_close(lg[r, :e], ref, f"layer {layer} mtp row {r}", BF16_REL)
+            assert_topk_row(cols[r], ref, wl.topk, f"layer {layer} mtp top-k row {r}", BF16_REL)
+            m = min(wl.topk, e)
+            assert pos[r, :m].tolist() == toks[cols[r, :m]].tolist() and np.all(pos[r, m:] == -1)
+            sm = pool.slot_mapping(b)
+            assert np.array_equal(sl[r], np.where(pos[r] >= 0, sm[np.clip(pos[r], 0, None)], -1))
+    assert not stp.ws.any().item()
