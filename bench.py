@@ -696,6 +696,118 @@ class HierMtpBench:
                 "parallelism": f"rows sharded, {world} independent replica(s)"}
 
 
+class DcpBench:
+    """Context-parallel decode of the 128K workload, four ranks emulated on one GPU.
+
+    Rank r owns the r-th quarter of every request's blocks (its block table and
+    shard lengths); each rank scores its shard and keeps its local top-2048 with
+    scores, written straight into its part of the all-gather buffer (on one GPU the
+    exchange is the identity), and the merge selects the global top-2048.
+    """
+
+    world = 4
+    launches_per_step = 2 * world + 1
+    dtype = "e4m3xe4m3->f32"
+    metric = "context-parallel decode indexer query-rows/s @128K ctx incl. top-2048 (4 ranks emulated)"
+
+    def __init__(self, name, rank, dev):
+        import sparse_attention_indexer_fp8_gb300 as idx
+        from sparse_attention_indexer_fp8_gb300.pipeline import fill_paged_cache
+
+        self.idx, self.dev, self.name = idx, dev, name
+        self.wl = wl = W.long_decode(seed=rank_seed(1003, rank))
+        pool = wl.pool
+        self.B = B = wl.batch
+        bs, W_ = pool.block_size, self.world
+        self.cache = torch.zeros((pool.num_blocks, W.block_stride_bytes()), dtype=torch.uint8, device=dev)
+        fill_paged_cache(pool, wl.seed, self.cache, device_k=True)
+        self.q = torch.from_numpy(wl.q8).to(dev)
+        self.w = torch.from_numpy(wl.w).to(dev)
+        L = pool.ctx_lens.astype(np.int64)
+        nblk = (L + bs - 1) // bs
+        starts = np.stack([np.minimum(nblk * r // W_ * bs, L) for r in range(W_ + 1)], axis=1)
+        self.starts = starts
+        self.shards = []
+        for r in range(W_):
+            lens = (starts[:, r + 1] - starts[:, r]).astype(np.int32)
+            bt = np.zeros_like(pool.block_table)
+            for b in range(B):
+                first, cnt = int(starts[b, r]) // bs, (int(lens[b]) + bs - 1) // bs
+                bt[b, :cnt] = pool.block_table[b, first:first + cnt]
+            ld = (int(lens.max()) + 63) // 64 * 64
+            self.shards.append({
+                "lens": torch.from_numpy(lens).to(dev), "bt": torch.from_numpy(bt).to(dev),
+                "logits": torch.empty((B, ld), dtype=torch.float32, device=dev),
+                "ws": torch.zeros((B, 1024), dtype=torch.int32, device=dev), "h_lens": lens})
+        k = wl.topk
+        self.all_vals = torch.empty((B, W_ * k), dtype=torch.float32, device=dev)
+        self.all_idx = torch.empty((B, W_ * k), dtype=torch.int32, device=dev)
+        self.offs = torch.from_numpy(starts[:, :W_].astype(np.int32)).to(dev)
+        self.positions = torch.empty((B, k), dtype=torch.int32, device=dev)
+        self.scores = torch.empty((B, k), dtype=torch.float32, device=dev)
+        self.rows_per_step = B
+
+    def step(self, stream, ev=None):
+        idx, wl, k = self.idx, self.wl, self.wl.topk
+        for r, sh in enumerate(self.shards):
+            if ev is not None and r == 0:
+                ev[0].record(stream)
+            idx.idx_paged_mqa_logits_decode(self.q, self.w, self.cache, wl.pool.block_size, sh["bt"], sh["lens"],
+                                            sh["logits"], ws=sh["ws"], stream=stream)
+            if ev is not None and r == 0:
+                ev[1].record(stream)
+            idx.idx_topk(sh["logits"], None, sh["lens"], k, self.all_idx[:, r * k:(r + 1) * k],
+                         vals=self.all_vals[:, r * k:(r + 1) * k], ws=sh["ws"], stream=stream)
+        idx.idx_dcp_topk_merge(self.all_vals, self.all_idx, self.offs, k, k, self.positions, vals=self.scores,
+                               stream=stream)
+
+    def e2e_prepare(self):
+        self.h_in = [(_pin(self.wl.q8), self.q), (_pin(self.wl.w), self.w)] + \
+                    [(_pin(sh["h_lens"]), sh["lens"]) for sh in self.shards]
+        self.h_out = torch.empty(self.positions.shape, dtype=torch.int32).pin_memory()
+        return _nbytes(*[h for h, _ in self.h_in]), _nbytes(self.h_out)
+
+    def e2e_step(self, stream):
+        for h, d in self.h_in:
+            d.copy_(h, non_blocking=True)
+        self.step(stream)
+        self.h_out.copy_(self.positions, non_blocking=True)
+
+    def verify_and_time_oracle(self, n_rows):
+        from tests.checks import assert_logits_close, assert_topk_row
+
+        wl = self.wl
+        rng = np.random.default_rng(wl.seed)
+        rows = sorted(rng.choice(self.B, size=min(n_rows, self.B), replace=False).tolist())
+        k_rows = oracle_k_rows(wl, rows, self.dev)
+        cpu_s, ref = oracle_decode_rows(wl, rows, k_rows)
+        pos, sc = self.positions.cpu().numpy(), self.scores.cpu().numpy()
+        for b in rows:
+            lg = ref[b][0]
+            assert_topk_row(pos[b], lg, wl.topk, f"bench dcp top-k row {b}")
+            assert_logits_close(sc[b], lg[pos[b]], f"bench dcp scores row {b}")
+        cpu = {"value": round(len(rows) / cpu_s, 3), "unit": "rows/s", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"{len(rows)} full rows of this workload (logits over the whole context, top-2048), "
+                         f"cache prepared untimed"}
+        return cpu, f"merged top-2048 and scores ok on {len(rows)} sampled rows"
+
+    def roofline(self, kernel_ms, step_ms, peaks, peak_kind):
+        lens = self.shards[0]["h_lens"].astype(np.int64)
+        byt = int(lens.sum()) * 136 + self.B * (8192 + 256)
+        ach = byt / (kernel_ms / 1e3) / 1e9
+        return {"kernel": "mqa_logits_kernel<1> (rank 0's quarter of every context)", "bound": "hbm",
+                "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(ach / peaks["hbm_gbs"], 4), "peak_source": peak_kind,
+                "algorithmic_bytes_per_launch": byt, "traffic": None, "kernel_ms": round(kernel_ms, 5)}
+
+    def config(self, world):
+        return {"workload": self.wl.name + "-dcp4", "batch": self.B, "ranks_emulated": self.world,
+                "sharding": "contiguous block-aligned quarters of every context", "topk": self.wl.topk,
+                "step": "per rank: paged logits + local top-2048 with scores; merge of the 4 lists",
+                "l2": "inputs larger than L2 (k cache > 129 MB), no flush",
+                "parallelism": f"ranks emulated on one GPU, {world} independent replica(s)"}
+
+
 class QPrepBench:
     """q preparation of the prefill chunk: partial RoPE, per-head e4m3 quantisation, folded bf16 weights."""
 
@@ -779,7 +891,8 @@ class QPrepBench:
 
 
 BENCHES = {"long_decode": DecodeBench, "paged_decode": DecodeBench, "prefill": PrefillBench,
-           "hierarchical": HierBench, "hierarchical_mtp": HierMtpBench, "q_prep": QPrepBench}
+           "hierarchical": HierBench, "hierarchical_mtp": HierMtpBench, "q_prep": QPrepBench,
+           "dcp_decode": DcpBench}
 
 
 # ----------------------------------------------------------------------------- harness
@@ -908,13 +1021,14 @@ def run_reference(args, rank):
         return None
     name = args.workload
     rows_per_call = 1
-    if name in ("long_decode", "paged_decode"):
-        wl = W.long_decode() if name == "long_decode" else W.paged_decode()
+    if name in ("long_decode", "paged_decode", "dcp_decode"):
+        wl = W.paged_decode() if name == "paged_decode" else W.long_decode()
         rng = np.random.default_rng(wl.seed)
         rows = sorted(rng.choice(wl.batch, size=min(4, wl.batch), replace=False).tolist())
         k_rows = oracle_k_rows(wl, rows, None)
         one = lambda i: oracle_decode_rows(wl, [rows[i % len(rows)]], k_rows)[0]  # noqa: E731
-        metric = DecodeBench.metric.fget(type("X", (), {"name": name})())
+        metric = (DcpBench.metric if name == "dcp_decode"
+                  else DecodeBench.metric.fget(type("X", (), {"name": name})()))
         cfg = {"workload": wl.name, "batch": wl.batch, "topk": wl.topk}
     elif name == "prefill":
         from oracle import indexer as O
