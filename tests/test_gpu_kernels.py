@@ -797,13 +797,21 @@ def test_selection_workspace_sparse_paths():
     pa = torch.empty((rows, k), dtype=torch.int32, device=DEV)
     pb = torch.empty((rows, k), dtype=torch.int32, device=DEV)
     ca = torch.empty((rows, k), dtype=torch.int32, device=DEV)
+    cb = torch.empty((rows, k), dtype=torch.int32, device=DEV)
     idx.idx_sparse_topk_remap(out, end, si, None, 64, k, pa, col_scratch=ca, ws=ws)
     assert not ws.any().item()
-    idx.idx_sparse_topk_remap(out, end, si, None, 64, k, pb)
-    ca = ca.cpu().numpy()
+    idx.idx_sparse_topk_remap(out, end, si, None, 64, k, pb, col_scratch=cb)
+    ca, cb, pa, pb = ca.cpu().numpy(), cb.cpu().numpy(), pa.cpu().numpy(), pb.cpu().numpy()
+    sih = si.cpu().numpy()
     for r in range(rows):
         assert_topk_values_exact(ca[r], lg[r, :e[r]], k, f"sparse ws row {r}")
-    assert np.array_equal(np.sort(pa.cpu().numpy(), axis=1), np.sort(pb.cpu().numpy(), axis=1)) or True
+        # with or without the fused histogram: the same multiset of chosen scores,
+        # and every position is its column's token
+        m = min(k, int(e[r]))
+        assert np.array_equal(np.sort(lg[r, ca[r, :m]]), np.sort(lg[r, cb[r, :m]])), r
+        for c_, p_ in ((ca, pa), (cb, pb)):
+            assert [O.sparse_column_token(sih[r], int(c), 64) for c in c_[r, :m]] == p_[r, :m].tolist(), r
+            assert np.all(p_[r, m:] == -1), r
     # dense prefill runs four queries per group: the workspace is refused there
     k8, ks = W.make_random_cache_tokens(3, 256)
     q2, w2 = W.make_q(4, 8)
