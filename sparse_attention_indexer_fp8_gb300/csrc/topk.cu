@@ -9,15 +9,16 @@
 // selection's store step.
 //
 // Design: one 1024-thread block per row. Scores are mapped to order-preserving
-// 32-bit keys and selected by three radix digits (11, 11 and 10 bits). Level 0
-// histograms the row from global memory; each later level histograms only the
-// elements that tie with the threshold digit of the level above, and those
-// elements are also compacted into shared memory, so normally the row is read
-// from global memory exactly twice. When a tie bucket overflows its
-// shared-memory buffer the next level re-reads global memory with a prefix
-// filter instead (correct for any input, slower). Elements above the threshold
-// are written as soon as their digit decides them; at the last level exactly
-// the number still missing is taken from the fully tied bucket. Writes use
+// 32-bit keys and selected by three radix digits (10, 11 and 11 bits). Level 0
+// histograms the row from global memory (or takes the histogram the scoring
+// kernel accumulated); a second pass over the row keeps only the elements at or
+// above the threshold digit, compacted into shared memory, where they are split
+// into the chosen and the tied. Each later level histograms only the elements
+// that tie with the threshold digit of the level above, so normally the row is
+// read from global memory once or twice. When a bucket overflows its
+// shared-memory buffer the level re-reads global memory with a prefix filter
+// instead (correct for any input, slower). At the last level exactly the
+// number still missing is taken from the fully tied bucket. Writes use
 // warp-aggregated shared-memory counters, so the output is a set in no
 // particular order.
 #include "common.cuh"
@@ -28,9 +29,10 @@ namespace {
 constexpr int kThreads = 1024;
 constexpr int kBins = 2048;      // bins of the second and third digits (11 bits each)
 constexpr int kBins0 = 1024;     // bins of the first digit (the top 10 key bits)
-constexpr int kCapA = 12288;  // tie bucket of level 0 (collected from global memory)
+constexpr int kCapA = 12288;  // level-0 hits, above or tied (collected from global memory)
 constexpr int kCapB = 4096;   // tie bucket of level 1 (collected from bucket A)
-constexpr int kSmemDyn = (kCapA + kCapB) * 8;
+constexpr int kStageBytes = kThreads * 16 * 4;  // level-0 staging: 16 keys per thread
+constexpr int kSmemDyn = (kCapA + kCapB) * 8 + kStageBytes;
 constexpr int kMaxK = 4096;
 
 struct TopkParams {
@@ -262,30 +264,35 @@ __device__ __forceinline__ int warp_excl_scan(int v, int* total) {
   return incl - v;
 }
 
-// The level-0 pass over the aligned body of the row, batched: every thread
-// classifies the 16 elements it loaded (above the threshold digit, tied with
-// it, or below), and one warp scan per class reserves output / bucket slots for
-// all of them. Most elements are below the threshold and cost a handful of
-// integer operations; the collectives are paid once per 16 elements.
+// The level-0 pass over the aligned body of the row. A key is a hit when it is
+// at least the smallest key of the threshold digit (so above it or tied with
+// it); only hits are kept, appended to bucket A with their columns, and sorted
+// into "above" and "tied" afterwards from shared memory. Each thread tests the
+// 16 elements it loaded with one compare each into a bit mask and parks the
+// keys in its own slots of the warp's staging area; one warp scan reserves
+// bucket slots for all hits, and each thread then walks only its own set bits
+// (a few per warp at the usual hit rate of a few per cent), so the per-element
+// cost is the load, the key transform and the compare.
 template <bool kBf16>
-__device__ __forceinline__ void level0_body(const TopkParams& p, Shared& sh, int row, int64_t lo,
-                                            int64_t base_blk, const void* rowp, int64_t a1,
-                                            int64_t nvec, uint32_t* keys_a, int32_t* cols_a) {
+__device__ __forceinline__ void level0_collect(Shared& sh, const void* rowp, int64_t a1, int64_t nvec,
+                                               uint32_t tie_lo, uint32_t* keys_a, int32_t* cols_a,
+                                               uint4* stage) {
   constexpr int kVec = kBf16 ? 8 : 4;
   constexpr int kEsz = kBf16 ? 2 : 4;
   constexpr int kUnroll = kBf16 ? 2 : 4;
   constexpr int kPer = kVec * kUnroll;  // 16 elements per thread per step
   const int tid = threadIdx.x;
   const int lane = tid & 31;
-  const int thr = sh.thr;
+  uint4* mine = stage + (tid >> 5) * (kPer / 4) * 32 + lane;  // slot m of this lane: mine[32 * m]
   const uint4* vp = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(rowp) + a1 * kEsz);
   for (int64_t v0 = 0; v0 < nvec; v0 += static_cast<int64_t>(kThreads) * kUnroll) {
     uint32_t key[kPer];
-    int n_ab = 0, n_tie = 0;
+    uint32_t hit = 0;
 #pragma unroll
     for (int j = 0; j < kUnroll; ++j) {
       const int64_t v = v0 + j * kThreads + tid;
-      const uint4 r = v < nvec ? __ldg(vp + v) : make_uint4(0, 0, 0, 0);
+      const bool ok = v < nvec;
+      const uint4 r = ok ? __ldg(vp + v) : make_uint4(0, 0, 0, 0);
       const uint32_t w[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
       for (int e = 0; e < kVec; ++e) {
@@ -295,47 +302,30 @@ __device__ __forceinline__ void level0_body(const TopkParams& p, Shared& sh, int
         } else {
           k = f32_key(w[e]);
         }
-        // out-of-range vectors get key 0, whose digit 0 is never above any threshold
-        // and is only a tie when the threshold digit itself is 0 (guarded below)
-        key[j * kVec + e] = v < nvec ? k : 0u;
-        const int d = static_cast<int>(key[j * kVec + e] >> 22);
-        n_ab += (v < nvec && d > thr) ? 1 : 0;
-        n_tie += (v < nvec && d == thr) ? 1 : 0;
+        key[j * kVec + e] = k;
+        hit |= (ok && k >= tie_lo) ? (1u << (j * kVec + e)) : 0u;
       }
     }
-    int tot_ab, tot_tie;
-    int off_ab = warp_excl_scan(n_ab, &tot_ab);
-    int off_tie = warp_excl_scan(n_tie, &tot_tie);
-    if (tot_ab == 0 && tot_tie == 0) continue;
-    int base_ab = 0, base_tie = 0;
-    if (lane == 0) {
-      if (tot_ab) base_ab = atomicAdd(&sh.n_out, tot_ab);
-      if (tot_tie) base_tie = atomicAdd(&sh.n_a, tot_tie);
+    int tot;
+    int slot = warp_excl_scan(__popc(hit), &tot);
+    if (tot == 0) continue;
+#pragma unroll
+    for (int m = 0; m < kPer / 4; ++m) {
+      mine[32 * m] = make_uint4(key[4 * m], key[4 * m + 1], key[4 * m + 2], key[4 * m + 3]);
     }
-    base_ab = __shfl_sync(0xFFFFFFFFu, base_ab, 0) + off_ab;
-    base_tie = __shfl_sync(0xFFFFFFFFu, base_tie, 0) + off_tie;
-    if (n_ab == 0 && n_tie == 0) continue;
-#pragma unroll
-    for (int j = 0; j < kUnroll; ++j) {
-      const int64_t v = v0 + j * kThreads + tid;
-      if (v >= nvec) continue;
-#pragma unroll
-      for (int e = 0; e < kVec; ++e) {
-        const uint32_t k = key[j * kVec + e];
-        const int d = static_cast<int>(k >> 22);
-        const int64_t c = a1 + v * kVec + e;
-        if (d > thr) {
-          if (base_ab < p.k) store_one(sh, base_ab, c);
-          ++base_ab;
-        } else if (d == thr) {
-          if (base_tie < kCapA) {
-            keys_a[base_tie] = k;
-            cols_a[base_tie] = static_cast<int32_t>(c);
-          }
-          ++base_tie;
-          atomicAdd(&sh.hist[1][digit(k, 1)], 1u);
-        }
+    int base = 0;
+    if (lane == 0) base = atomicAdd(&sh.n_a, tot);
+    slot += __shfl_sync(0xFFFFFFFFu, base, 0);
+    // the staged keys are this thread's own: program order is the only ordering needed
+    const uint32_t* mk = reinterpret_cast<const uint32_t*>(mine);
+    while (hit) {
+      const int i = __ffs(hit) - 1;
+      hit &= hit - 1;
+      if (slot < kCapA) {
+        keys_a[slot] = mk[(i >> 2) * 128 + (i & 3)];
+        cols_a[slot] = static_cast<int32_t>(a1 + (v0 + (i / kVec) * kThreads + tid) * kVec + i % kVec);
       }
+      ++slot;
     }
   }
 }
@@ -443,6 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p) {
   int32_t* cols_a = reinterpret_cast<int32_t*>(dyn + kCapA * 4);
   uint32_t* keys_b = reinterpret_cast<uint32_t*>(dyn + kCapA * 8);
   int32_t* cols_b = reinterpret_cast<int32_t*>(dyn + kCapA * 8 + kCapB * 4);
+  uint4* stage = reinterpret_cast<uint4*>(dyn + (kCapA + kCapB) * 8);
 
   const int row = blockIdx.x;
   const int tid = threadIdx.x;
@@ -506,23 +497,57 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p) {
   __syncthreads();
   find_threshold(sh, sh.hist[0], kBins0);
 
-  // level 0: store digit > thr, collect the tie bucket into A, histogram its next digit
+  // level 0: every key at or above the threshold digit goes to bucket A; A is
+  // then split into the chosen (digit above the threshold) and the tied, whose
+  // next digit is histogrammed
   {
     constexpr int kVec = kBf16 ? 8 : 4;
     constexpr int kEsz = kBf16 ? 2 : 4;
+    const uint32_t tie_lo = static_cast<uint32_t>(sh.thr) << 22;
     const uintptr_t base = reinterpret_cast<uintptr_t>(rowp);
     int64_t a1 = lo + (kVec - static_cast<int64_t>(((base / kEsz) + lo) % kVec)) % kVec;
     if (a1 > hi) a1 = hi;
     const int64_t nvec = (hi - a1) / kVec;
     const int64_t a2 = a1 + nvec * kVec;
     // unaligned head [lo, a1) and tail [a2, hi), element by element
-    const int nh = static_cast<int>(a1 - lo);
-    const int nt = static_cast<int>(hi - a2);
-    const bool valid = tid < nh + nt;
-    const int64_t c = tid < nh ? lo + tid : a2 + (tid - nh);
-    visit(p, sh, row, lo, base_blk, 0, 0u, valid, valid ? key_at<kBf16>(rowp, c) : 0u, c,
-                  keys_a, cols_a, &sh.n_a, kCapA, sh.hist[1]);
-    level0_body<kBf16>(p, sh, row, lo, base_blk, rowp, a1, nvec, keys_a, cols_a);
+    {
+      const int nh = static_cast<int>(a1 - lo);
+      const int nt = static_cast<int>(hi - a2);
+      const bool valid = tid < nh + nt;
+      const int64_t c = tid < nh ? lo + tid : a2 + (tid - nh);
+      const uint32_t key = valid ? key_at<kBf16>(rowp, c) : 0u;
+      const bool h = valid && key >= tie_lo;
+      const int s = warp_reserve(&sh.n_a, h);
+      if (h && s < kCapA) {
+        keys_a[s] = key;
+        cols_a[s] = static_cast<int32_t>(c);
+      }
+    }
+    level0_collect<kBf16>(sh, rowp, a1, nvec, tie_lo, keys_a, cols_a, stage);
+    __syncthreads();
+    const int na = sh.n_a;
+    if (na <= kCapA) {
+      const int thr = sh.thr;
+      for (int b = 0; b < na; b += kThreads) {
+        const int i = b + tid;
+        const bool valid = i < na;
+        const uint32_t key = valid ? keys_a[i] : 0u;
+        const bool above = valid && static_cast<int>(key >> 22) > thr;
+        const int s = warp_reserve(&sh.n_out, above);
+        if (above && s < K) store_one(sh, s, cols_a[i]);
+        if (valid && !above) atomicAdd(&sh.hist[1][digit(key, 1)], 1u);
+      }
+    } else {
+      // more hits than bucket A holds: classify the row again from global memory,
+      // storing the chosen directly and keeping as many ties as fit
+      __syncthreads();
+      if (tid == 0) sh.n_a = 0;
+      __syncthreads();
+      sweep_row<kBf16>(rowp, lo, hi, [&](bool valid, int64_t c, uint32_t key) {
+        visit(p, sh, row, lo, base_blk, 0, 0u, valid, key, c, keys_a, cols_a, &sh.n_a, kCapA,
+              sh.hist[1]);
+      });
+    }
   }
   uint32_t prefix = static_cast<uint32_t>(sh.thr) << 22;
   __syncthreads();
