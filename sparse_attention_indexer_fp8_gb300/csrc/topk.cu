@@ -138,18 +138,16 @@ __device__ void find_threshold(Shared& sh, const uint32_t* hist, int nbins) {
   }
   if (lane == 31) sh.warp_tot[warp] = incl;
   __syncthreads();
-  if (warp == 0) {
-    const int v = sh.warp_tot[lane];
-    int wi = v;
+  // every warp scans the 32 warp totals itself (no second barrier)
+  const int wt = sh.warp_tot[lane];
+  int wi = wt;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int n = __shfl_up_sync(0xFFFFFFFFu, wi, o);
-      if (lane >= o) wi += n;
-    }
-    sh.warp_tot[lane] = wi - v;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xFFFFFFFFu, wi, o);
+    if (lane >= o) wi += n;
   }
-  __syncthreads();
-  int before = sh.warp_tot[warp] + incl - local;
+  const int warp_before = __shfl_sync(0xFFFFFFFFu, wi - wt, warp);
+  int before = warp_before + incl - local;
   for (int j = 0; j < per; ++j) {
     if (before < need && before + c[j] >= need) {
       sh.thr = nbins - 1 - (tid * per + j);
