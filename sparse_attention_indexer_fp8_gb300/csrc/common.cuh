@@ -98,6 +98,13 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   return pol;
 }
 
+// Asks the memory system to bring [ptr, ptr + bytes) into L2 (a bulk
+// asynchronous prefetch: no destination, nothing to wait for). ptr 16-byte
+// aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* ptr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

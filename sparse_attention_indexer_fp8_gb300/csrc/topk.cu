@@ -59,6 +59,9 @@ struct TopkParams {
   int pos_stride;          // merge: global distance between a shard's consecutive positions
   int k_local;             // merge: candidates per shard
   int n_cand;              // merge: candidates per row (shards * k_local)
+  int rows;
+  int ahead;               // rows in flight at once (one per SM): the row a wave later is
+                           // moved into L2 while this one is selected (0 = off)
 };
 
 // What a row selects from and what its outputs mean.
@@ -67,6 +70,21 @@ enum Mode : int {
   kRemap = 1,   // sparse columns [0, end) -> request-local positions through the sparse blocks
   kMerge = 2    // candidate lists of several shards -> global positions, empty entries last
 };
+
+// The columns [lo, hi) that row `row` selects from.
+template <int kMode>
+__device__ __forceinline__ void row_range(const TopkParams& p, int row, int64_t& lo, int64_t& hi) {
+  if constexpr (kMode == kRemap) {
+    lo = 0;
+    hi = __ldg(p.end + row);
+  } else if constexpr (kMode == kMerge) {
+    lo = 0;
+    hi = p.n_cand;
+  } else {
+    lo = p.row_ks ? __ldg(p.row_ks + row) : 0;
+    hi = __ldg(p.row_ke + row);
+  }
+}
 
 template <bool kBf16>
 __device__ __forceinline__ uint32_t key_at(const void* row, int64_t c) {
@@ -437,17 +455,27 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p) {
   const int tid = threadIdx.x;
   const int64_t base_blk = 0;
   int64_t lo, hi;
-  if constexpr (kMode == kRemap) {
-    lo = 0;
-    hi = __ldg(p.end + row);
-  } else if constexpr (kMode == kMerge) {
-    lo = 0;
-    hi = p.n_cand;
-  } else {
-    lo = p.row_ks ? __ldg(p.row_ks + row) : 0;
-    hi = __ldg(p.row_ke + row);
-  }
+  row_range<kMode>(p, row, lo, hi);
   const int64_t n = hi > lo ? hi - lo : 0;
+  // More rows than SMs: the row that will most likely run on this SM next (one
+  // wave later) is moved into L2 now, by the lanes of warp 0 in 16 KB pieces,
+  // so its passes read L2 instead of waiting on DRAM.
+  if (p.ahead > 0 && tid < 32 && row + p.ahead < p.rows) {
+    constexpr int kEsz = kBf16 ? 2 : 4;
+    const int nr = row + p.ahead;
+    int64_t nlo, nhi;
+    row_range<kMode>(p, nr, nlo, nhi);
+    if (nhi > nlo) {
+      const uint8_t* nb = static_cast<const uint8_t*>(p.logits) + (static_cast<int64_t>(nr) * p.ld + nlo) * kEsz;
+      const uint8_t* b0 = reinterpret_cast<const uint8_t*>((reinterpret_cast<uintptr_t>(nb) + 15) & ~uintptr_t(15));
+      const uint8_t* b1 = reinterpret_cast<const uint8_t*>(
+          (reinterpret_cast<uintptr_t>(nb) + (nhi - nlo) * kEsz) & ~uintptr_t(15));
+      for (const uint8_t* q = b0 + tid * 16384; q < b1; q += 32 * 16384) {
+        const int64_t left = b1 - q;
+        bulk_prefetch_l2(q, static_cast<uint32_t>(left < 16384 ? left : 16384));
+      }
+    }
+  }
   const int K = p.k;
   const void* rowp = kBf16
       ? static_cast<const void*>(static_cast<const uint16_t*>(p.logits) + row * p.ld)
@@ -624,9 +652,10 @@ idx_status_t attach_hist(const char* fn, TopkParams* p, int rows, void* ws, size
 }
 
 template <bool kBf16, int kMode>
-idx_status_t launch_topk(const TopkParams& p, int rows, cudaStream_t stream, const char* fn) {
+idx_status_t launch_topk(TopkParams p, int rows, cudaStream_t stream, const char* fn) {
   auto kern = topk_kernel<kBf16, kMode>;
   static bool attr_set[64] = {false};
+  static int sm_count[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
@@ -634,6 +663,15 @@ idx_status_t launch_topk(const TopkParams& p, int rows, cudaStream_t stream, con
     if (e != cudaSuccess) return fail(IDX_ERR_CUDA, "%s: cudaFuncSetAttribute: %s", fn, cudaGetErrorString(e));
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
+  int sms = dev >= 0 && dev < 64 ? sm_count[dev] : 0;
+  if (sms == 0) {
+    cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return fail(IDX_ERR_CUDA, "%s: cudaDeviceGetAttribute: %s", fn, cudaGetErrorString(e));
+    if (dev >= 0 && dev < 64) sm_count[dev] = sms;
+  }
+  // one block per SM at a time (1024 threads, 64 registers each)
+  p.rows = rows;
+  p.ahead = rows > sms ? sms : 0;
   kern<<<rows, kThreads, kSmemDyn, stream>>>(p);
   return check_launch(fn);
 }
