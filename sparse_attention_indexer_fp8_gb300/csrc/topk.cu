@@ -655,7 +655,6 @@ template <bool kBf16, int kMode>
 idx_status_t launch_topk(TopkParams p, int rows, cudaStream_t stream, const char* fn) {
   auto kern = topk_kernel<kBf16, kMode>;
   static bool attr_set[64] = {false};
-  static int sm_count[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
@@ -663,15 +662,10 @@ idx_status_t launch_topk(TopkParams p, int rows, cudaStream_t stream, const char
     if (e != cudaSuccess) return fail(IDX_ERR_CUDA, "%s: cudaFuncSetAttribute: %s", fn, cudaGetErrorString(e));
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  int sms = dev >= 0 && dev < 64 ? sm_count[dev] : 0;
-  if (sms == 0) {
-    cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return fail(IDX_ERR_CUDA, "%s: cudaDeviceGetAttribute: %s", fn, cudaGetErrorString(e));
-    if (dev >= 0 && dev < 64) sm_count[dev] = sms;
-  }
   // one block per SM at a time (1024 threads, 64 registers each)
+  const int sms = device_sm_count();
   p.rows = rows;
-  p.ahead = rows > sms ? sms : 0;
+  p.ahead = sms > 0 && rows > sms ? sms : 0;
   kern<<<rows, kThreads, kSmemDyn, stream>>>(p);
   return check_launch(fn);
 }
