@@ -377,6 +377,25 @@ def test_topk_bf16_and_wide_rows():
 
 
 @pytest.mark.parametrize("bf16", [False, True])
+def test_topk_more_rows_than_sms(bf16):
+    # more rows than SMs: blocks run in waves and each asks for the row one wave
+    # ahead to be staged in L2; ragged causal ranges, odd row stride, empty rows
+    rows, width, k = 700, 6000, 512
+    x = W.make_logits(31 + bf16, rows, width, ties=True)
+    rng = np.random.default_rng(31)
+    ks = rng.integers(0, 1500, rows).astype(np.int32)
+    ke = np.minimum(ks + rng.integers(0, width, rows), width).astype(np.int32)
+    ke[5], ks[5] = 0, 0                       # empty row
+    ke[6] = ks[6] + 300                       # fewer visible columns than k
+    out, vals = _run_topk(x, ks, ke, k, bf16=bf16, ld_pad=3)
+    for r in range(rows):
+        seg = vals[r, ks[r]:ke[r]]
+        assert_topk_values_exact(out[r], seg, k, f"row {r}")
+        if r % 50 == 0 and len(np.unique(seg)) == len(seg):
+            assert set(out[r].tolist()) == set(O.topk_row(vals[r], ks[r], ke[r], k).tolist())
+
+
+@pytest.mark.parametrize("bf16", [False, True])
 def test_topk_values_output(bf16):
     # the optional score output: the score of every selected column, -inf in -1 slots
     width, k = 9000, 2048
