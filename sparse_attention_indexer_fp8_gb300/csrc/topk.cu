@@ -26,13 +26,20 @@
 namespace idx {
 namespace {
 
-constexpr int kThreads = 1024;
 constexpr int kBins = 2048;      // bins of the second and third digits (11 bits each)
 constexpr int kBins0 = 1024;     // bins of the first digit (the top 10 key bits)
-constexpr int kCapA = 12288;  // level-0 hits, above or tied (collected from global memory)
-constexpr int kCapB = 4096;   // tie bucket of level 1 (collected from bucket A)
-constexpr int kStageBytes = kThreads * 16 * 4;  // level-0 staging: 16 keys per thread
-constexpr int kSmemDyn = (kCapA + kCapB) * 8 + kStageBytes;
+// Block configurations: 1024 threads and one block per SM for rows of any
+// length; 512 threads and two blocks per SM for many shorter rows (prefill
+// chunks), so one block's barrier-bound phases overlap the other's passes.
+template <int kT>
+struct TopkCfg {
+  static constexpr int kCapA = kT == 1024 ? 12288 : 6144;  // level-0 hits, above or tied
+  static constexpr int kCapB = 4096;                        // level-1 ties (from bucket A)
+  static constexpr int kStageBytes = kT * 16 * 4;           // level-0 staging: 16 keys per thread
+  // bucket B is first written at level 1, after the staging area's last use
+  static constexpr int kUnionBytes = kCapB * 8 > kStageBytes ? kCapB * 8 : kStageBytes;
+  static constexpr int kSmemDyn = kCapA * 8 + kUnionBytes;
+};
 constexpr int kMaxK = 4096;
 
 struct TopkParams {
@@ -135,12 +142,15 @@ struct Shared {
 
 // Finds the digit `thr` at which the running count of larger digits reaches
 // `need`; sets sh.thr and reduces sh.need to what must come from bucket `thr`.
-__device__ void find_threshold(Shared& sh, const uint32_t* hist, int nbins) {
-  const int need = sh.need;          // read before any thread can update it
-  const int per = nbins / kThreads;  // 1 or 2 (nbins is 1024 or 2048)
+template <int kThreads, int nbins>
+__device__ void find_threshold(Shared& sh, const uint32_t* hist) {
+  const int need = sh.need;                // read before any thread can update it
+  constexpr int per = nbins / kThreads;    // 1, 2 or 4 (nbins is 1024 or 2048)
+  static_assert(per >= 1 && per * kThreads == nbins, "bins per thread");
   const int tid = threadIdx.x;
-  int c[2] = {0, 0};
+  int c[per];
   int local = 0;
+#pragma unroll
   for (int j = 0; j < per; ++j) {
     c[j] = static_cast<int>(hist[nbins - 1 - (tid * per + j)]);
     local += c[j];
@@ -157,7 +167,7 @@ __device__ void find_threshold(Shared& sh, const uint32_t* hist, int nbins) {
   if (lane == 31) sh.warp_tot[warp] = incl;
   __syncthreads();
   // every warp scans the 32 warp totals itself (no second barrier)
-  const int wt = sh.warp_tot[lane];
+  const int wt = lane < kThreads / 32 ? sh.warp_tot[lane] : 0;
   int wi = wt;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -166,6 +176,7 @@ __device__ void find_threshold(Shared& sh, const uint32_t* hist, int nbins) {
   }
   const int warp_before = __shfl_sync(0xFFFFFFFFu, wi - wt, warp);
   int before = warp_before + incl - local;
+#pragma unroll
   for (int j = 0; j < per; ++j) {
     if (before < need && before + c[j] >= need) {
       sh.thr = nbins - 1 - (tid * per + j);
@@ -220,7 +231,7 @@ __device__ __forceinline__ void visit(const TopkParams& p, Shared& sh, int row, 
 // every warp of the block (f may use warp collectives). The aligned middle is
 // read with 16-byte loads, four per thread in flight; the unaligned head and
 // tail (fewer than one vector each) are read element by element.
-template <bool kBf16, typename F>
+template <int kThreads, bool kBf16, typename F>
 __device__ __forceinline__ void sweep_row(const void* rowp, int64_t lo, int64_t hi, F&& f) {
   constexpr int kVec = kBf16 ? 8 : 4;
   constexpr int kEsz = kBf16 ? 2 : 4;
@@ -289,7 +300,7 @@ __device__ __forceinline__ int warp_excl_scan(int v, int* total) {
 // bucket slots for all hits, and each thread then walks only its own set bits
 // (a few per warp at the usual hit rate of a few per cent), so the per-element
 // cost is the load, the key transform and the compare.
-template <bool kBf16>
+template <int kThreads, bool kBf16>
 __device__ __forceinline__ void level0_collect(Shared& sh, const void* rowp, int64_t a1, int64_t nvec,
                                                uint32_t tie_lo, uint32_t* keys_a, int32_t* cols_a,
                                                uint4* stage) {
@@ -337,7 +348,7 @@ __device__ __forceinline__ void level0_collect(Shared& sh, const void* rowp, int
     while (hit) {
       const int i = __ffs(hit) - 1;
       hit &= hit - 1;
-      if (slot < kCapA) {
+      if (slot < TopkCfg<kThreads>::kCapA) {
         keys_a[slot] = mk[(i >> 2) * 128 + (i & 3)];
         cols_a[slot] = static_cast<int32_t>(a1 + (v0 + (i / kVec) * kThreads + tid) * kVec + i % kVec);
       }
@@ -360,7 +371,7 @@ __device__ __forceinline__ float value_at(const void* row, int64_t c) {
 // indices (and optionally columns and scores), -1 / -inf in the unused slots.
 // In merge mode, candidates without a position are dropped and the remaining
 // entries are compacted to the front in slot order.
-template <bool kBf16, int kMode>
+template <int kThreads, bool kBf16, int kMode>
 __device__ __forceinline__ void write_outputs(const TopkParams& p, Shared& sh, int row, int64_t lo,
                                               const void* rowp, int m) {
   const int tid = threadIdx.x;
@@ -389,7 +400,7 @@ __device__ __forceinline__ void write_outputs(const TopkParams& p, Shared& sh, i
       if (vals) vals[i] = v;
     }
   } else {
-    // each thread owns up to 4 consecutive slots; one block scan orders the valid ones
+    // each thread owns kMaxK / kThreads consecutive slots; one block scan orders the valid ones
     constexpr int kPer = kMaxK / kThreads;
     int32_t g[kPer];
     float v[kPer];
@@ -441,15 +452,18 @@ __device__ __forceinline__ void write_outputs(const TopkParams& p, Shared& sh, i
   }
 }
 
-template <bool kBf16, int kMode>
-__global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p) {
+template <bool kBf16, int kMode, int kThreads>
+__global__ void __launch_bounds__(kThreads, 1024 / kThreads) topk_kernel(const TopkParams p) {
+  constexpr int kCapA = TopkCfg<kThreads>::kCapA;
+  constexpr int kCapB = TopkCfg<kThreads>::kCapB;
   extern __shared__ __align__(16) uint8_t dyn[];
   __shared__ Shared sh;
   uint32_t* keys_a = reinterpret_cast<uint32_t*>(dyn);
   int32_t* cols_a = reinterpret_cast<int32_t*>(dyn + kCapA * 4);
+  // bucket B and the level-0 staging area share one region (used one after the other)
   uint32_t* keys_b = reinterpret_cast<uint32_t*>(dyn + kCapA * 8);
   int32_t* cols_b = reinterpret_cast<int32_t*>(dyn + kCapA * 8 + kCapB * 4);
-  uint4* stage = reinterpret_cast<uint4*>(dyn + (kCapA + kCapB) * 8);
+  uint4* stage = reinterpret_cast<uint4*>(dyn + kCapA * 8);
 
   const int row = blockIdx.x;
   const int tid = threadIdx.x;
@@ -489,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p) {
     }
     for (int i = tid; i < n; i += kThreads) sh.sel[i] = static_cast<int32_t>(lo + i);
     __syncthreads();
-    write_outputs<kBf16, kMode>(p, sh, row, lo, rowp, static_cast<int>(n));
+    write_outputs<kThreads, kBf16, kMode>(p, sh, row, lo, rowp, static_cast<int>(n));
     return;
   }
 
@@ -516,12 +530,12 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p) {
       g[i] = 0;
     }
   } else {
-    sweep_row<kBf16>(rowp, lo, hi, [&](bool valid, int64_t, uint32_t key) {
+    sweep_row<kThreads, kBf16>(rowp, lo, hi, [&](bool valid, int64_t, uint32_t key) {
       if (valid) atomicAdd(&sh.hist[0][key >> 22], 1u);
     });
   }
   __syncthreads();
-  find_threshold(sh, sh.hist[0], kBins0);
+  find_threshold<kThreads, kBins0>(sh, sh.hist[0]);
 
   // level 0: every key at or above the threshold digit goes to bucket A; A is
   // then split into the chosen (digit above the threshold) and the tied, whose
@@ -549,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p) {
         cols_a[s] = static_cast<int32_t>(c);
       }
     }
-    level0_collect<kBf16>(sh, rowp, a1, nvec, tie_lo, keys_a, cols_a, stage);
+    level0_collect<kThreads, kBf16>(sh, rowp, a1, nvec, tie_lo, keys_a, cols_a, stage);
     __syncthreads();
     const int na = sh.n_a;
     if (na <= kCapA) {
@@ -569,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p) {
       __syncthreads();
       if (tid == 0) sh.n_a = 0;
       __syncthreads();
-      sweep_row<kBf16>(rowp, lo, hi, [&](bool valid, int64_t c, uint32_t key) {
+      sweep_row<kThreads, kBf16>(rowp, lo, hi, [&](bool valid, int64_t c, uint32_t key) {
         visit(p, sh, row, lo, base_blk, 0, 0u, valid, key, c, keys_a, cols_a, &sh.n_a, kCapA,
               sh.hist[1]);
       });
@@ -578,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p) {
   uint32_t prefix = static_cast<uint32_t>(sh.thr) << 22;
   __syncthreads();
   for (int i = tid; i < kBins; i += kThreads) sh.hist[0][i] = 0;  // free since level 0 is done
-  find_threshold(sh, sh.hist[1], kBins);
+  find_threshold<kThreads, kBins>(sh, sh.hist[1]);
   prefix |= static_cast<uint32_t>(sh.thr) << 11;
 
   // level 1: from bucket A when it held every tie, else global memory with a prefix filter
@@ -592,13 +606,13 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p) {
                     valid ? cols_a[i] : 0, keys_b, cols_b, &sh.n_b, kCapB, sh.hist[0]);
     }
   } else {
-    sweep_row<kBf16>(rowp, lo, hi, [&](bool valid, int64_t c, uint32_t key) {
+    sweep_row<kThreads, kBf16>(rowp, lo, hi, [&](bool valid, int64_t c, uint32_t key) {
       visit(p, sh, row, lo, base_blk, 1, prefix, valid, key, c, keys_b, cols_b, &sh.n_b,
                     kCapB, sh.hist[0]);
     });
   }
   __syncthreads();
-  find_threshold(sh, sh.hist[0], kBins);
+  find_threshold<kThreads, kBins>(sh, sh.hist[0]);
   prefix |= static_cast<uint32_t>(sh.thr);
 
   // level 2: every remaining candidate shares the full key prefix; take the bucket
@@ -619,7 +633,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p) {
                     valid ? cols_a[i] : 0, nullptr, nullptr, nullptr, 0, nullptr);
     }
   } else {
-    sweep_row<kBf16>(rowp, lo, hi, [&](bool valid, int64_t c, uint32_t key) {
+    sweep_row<kThreads, kBf16>(rowp, lo, hi, [&](bool valid, int64_t c, uint32_t key) {
       visit(p, sh, row, lo, base_blk, 2, prefix, valid, key, c, nullptr, nullptr, nullptr,
                     0, nullptr);
     });
@@ -628,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p) {
   // match the scores (a misused workspace) can leave a short row: it is
   // completed with -1 by the output pass.
   __syncthreads();
-  write_outputs<kBf16, kMode>(p, sh, row, lo, rowp, min(sh.n_out, K));
+  write_outputs<kThreads, kBf16, kMode>(p, sh, row, lo, rowp, min(sh.n_out, K));
 }
 
 }  // namespace
@@ -651,23 +665,35 @@ idx_status_t attach_hist(const char* fn, TopkParams* p, int rows, void* ws, size
   return IDX_OK;
 }
 
-template <bool kBf16, int kMode>
-idx_status_t launch_topk(TopkParams p, int rows, cudaStream_t stream, const char* fn) {
-  auto kern = topk_kernel<kBf16, kMode>;
+template <bool kBf16, int kMode, int kThreads>
+idx_status_t launch_topk_cfg(TopkParams p, int rows, int sms, cudaStream_t stream, const char* fn) {
+  auto kern = topk_kernel<kBf16, kMode, kThreads>;
+  constexpr int smem = TopkCfg<kThreads>::kSmemDyn;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemDyn);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return fail(IDX_ERR_CUDA, "%s: cudaFuncSetAttribute: %s", fn, cudaGetErrorString(e));
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  // one block per SM at a time (1024 threads, 64 registers each)
-  const int sms = device_sm_count();
+  const int resident = sms * (1024 / kThreads);  // blocks in flight at once
   p.rows = rows;
-  p.ahead = sms > 0 && rows > sms ? sms : 0;
-  kern<<<rows, kThreads, kSmemDyn, stream>>>(p);
+  p.ahead = sms > 0 && rows > resident ? resident : 0;
+  kern<<<rows, kThreads, smem, stream>>>(p);
   return check_launch(fn);
+}
+
+// Many rows of at most 64K columns (prefill chunks) take the two-blocks-per-SM
+// configuration; anything else one 1024-thread block per SM.
+template <bool kBf16, int kMode>
+idx_status_t launch_topk(const TopkParams& p, int rows, int64_t max_cols, cudaStream_t stream,
+                         const char* fn) {
+  const int sms = device_sm_count();
+  if (sms > 0 && rows > 2 * sms && max_cols <= 65536) {
+    return launch_topk_cfg<kBf16, kMode, 512>(p, rows, sms, stream, fn);
+  }
+  return launch_topk_cfg<kBf16, kMode, 1024>(p, rows, sms, stream, fn);
 }
 
 }  // namespace
@@ -695,8 +721,8 @@ extern "C" idx_status_t idx_topk(const void* logits, int dtype, int64_t ld, cons
   p.ld_out = ld_out;
   p.vals = vals;
   p.ld_vals = ld_vals;
-  return dtype == IDX_BF16 ? launch_topk<true, kPlain>(p, rows, stream, fn)
-                           : launch_topk<false, kPlain>(p, rows, stream, fn);
+  return dtype == IDX_BF16 ? launch_topk<true, kPlain>(p, rows, ld, stream, fn)
+                           : launch_topk<false, kPlain>(p, rows, ld, stream, fn);
 }
 
 extern "C" idx_status_t idx_sparse_topk_remap(const void* sparse_logits, int dtype, int64_t ld,
@@ -727,8 +753,8 @@ extern "C" idx_status_t idx_sparse_topk_remap(const void* sparse_logits, int dty
   p.ld_out = ld_pos;
   p.cols = col_scratch;
   p.ld_cols = ld_col;
-  return dtype == IDX_BF16 ? launch_topk<true, kRemap>(p, rows, stream, fn)
-                           : launch_topk<false, kRemap>(p, rows, stream, fn);
+  return dtype == IDX_BF16 ? launch_topk<true, kRemap>(p, rows, ld, stream, fn)
+                           : launch_topk<false, kRemap>(p, rows, ld, stream, fn);
 }
 
 extern "C" idx_status_t idx_dcp_topk_merge(const float* cand_vals, int64_t ld_v,
@@ -765,5 +791,5 @@ extern "C" idx_status_t idx_dcp_topk_merge(const float* cand_vals, int64_t ld_v,
   p.ld_out = ld_out;
   p.vals = vals;
   p.ld_vals = ld_vals;
-  return launch_topk<false, kMerge>(p, rows, stream, fn);
+  return launch_topk<false, kMerge>(p, rows, n_cand, stream, fn);
 }
