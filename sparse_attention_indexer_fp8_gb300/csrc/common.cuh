@@ -51,7 +51,8 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 
 // Order-preserving map of an fp32 bit pattern onto uint32 (larger value -> larger key).
 __device__ __forceinline__ uint32_t f32_key(uint32_t u) {
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  // negative: all bits flipped; positive: the sign bit set
+  return u ^ (static_cast<uint32_t>(static_cast<int32_t>(u) >> 31) | 0x80000000u);
 }
 
 // --- mbarrier --------------------------------------------------------------

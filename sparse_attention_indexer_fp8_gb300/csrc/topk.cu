@@ -21,6 +21,8 @@
 // number still missing is taken from the fully tied bucket. Writes use
 // warp-aggregated shared-memory counters, so the output is a set in no
 // particular order.
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace idx {
@@ -308,17 +310,23 @@ __device__ __forceinline__ void level0_collect(Shared& sh, const void* rowp, int
   constexpr int kEsz = kBf16 ? 2 : 4;
   constexpr int kUnroll = kBf16 ? 2 : 4;
   constexpr int kPer = kVec * kUnroll;  // 16 elements per thread per step
+  constexpr int kStep = kThreads * kUnroll;  // vectors per step
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   uint4* mine = stage + (tid >> 5) * (kPer / 4) * 32 + lane;  // slot m of this lane: mine[32 * m]
   const uint4* vp = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(rowp) + a1 * kEsz);
-  for (int64_t v0 = 0; v0 < nvec; v0 += static_cast<int64_t>(kThreads) * kUnroll) {
+  // columns and vector indices fit in int32 (rows hold fewer than 2^31 columns)
+  const int nv = static_cast<int>(nvec);
+  const int col0 = static_cast<int>(a1);
+  // one step: kUnroll vectors per thread; kCheck only for the last, partial step
+  auto step = [&](int v0, auto check) {
+    constexpr bool kCheck = decltype(check)::value;
     uint32_t key[kPer];
     uint32_t hit = 0;
 #pragma unroll
     for (int j = 0; j < kUnroll; ++j) {
-      const int64_t v = v0 + j * kThreads + tid;
-      const bool ok = v < nvec;
+      const int v = v0 + j * kThreads + tid;
+      const bool ok = !kCheck || v < nv;
       const uint4 r = ok ? __ldg(vp + v) : make_uint4(0, 0, 0, 0);
       const uint32_t w[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
@@ -330,12 +338,12 @@ __device__ __forceinline__ void level0_collect(Shared& sh, const void* rowp, int
           k = f32_key(w[e]);
         }
         key[j * kVec + e] = k;
-        hit |= (ok && k >= tie_lo) ? (1u << (j * kVec + e)) : 0u;
+        if (ok && k >= tie_lo) hit |= 1u << (j * kVec + e);
       }
     }
     int tot;
     int slot = warp_excl_scan(__popc(hit), &tot);
-    if (tot == 0) continue;
+    if (tot == 0) return;
 #pragma unroll
     for (int m = 0; m < kPer / 4; ++m) {
       mine[32 * m] = make_uint4(key[4 * m], key[4 * m + 1], key[4 * m + 2], key[4 * m + 3]);
@@ -345,16 +353,20 @@ __device__ __forceinline__ void level0_collect(Shared& sh, const void* rowp, int
     slot += __shfl_sync(0xFFFFFFFFu, base, 0);
     // the staged keys are this thread's own: program order is the only ordering needed
     const uint32_t* mk = reinterpret_cast<const uint32_t*>(mine);
+    const int cbase = col0 + (v0 + tid) * kVec;  // column of this thread's first element
     while (hit) {
       const int i = __ffs(hit) - 1;
       hit &= hit - 1;
       if (slot < TopkCfg<kThreads>::kCapA) {
         keys_a[slot] = mk[(i >> 2) * 128 + (i & 3)];
-        cols_a[slot] = static_cast<int32_t>(a1 + (v0 + (i / kVec) * kThreads + tid) * kVec + i % kVec);
+        cols_a[slot] = cbase + (i / kVec) * (kThreads * kVec) + i % kVec;
       }
       ++slot;
     }
-  }
+  };
+  const int nfull = nv / kStep * kStep;
+  for (int v0 = 0; v0 < nfull; v0 += kStep) step(v0, std::false_type{});
+  if (nfull < nv) step(nfull, std::true_type{});
 }
 
 // Score of column c as fp32.

@@ -395,6 +395,26 @@ def test_topk_more_rows_than_sms(bf16):
             assert set(out[r].tolist()) == set(O.topk_row(vals[r], ks[r], ke[r], k).tolist())
 
 
+def test_topk_more_rows_than_sms_ties_and_overflow():
+    # the two-blocks-per-SM configuration (many rows, at most 64K columns) with the
+    # rows that overflow its smaller buckets and force the global re-read paths
+    rows, width, k = 400, 40000, 2048
+    x = W.make_logits(33, rows, width, ties=True)
+    x[1::8, :] = 0.5                                                  # every bucket ties
+    x[2::8, :] = (1.0 + np.arange(width) * 2.0 ** -22).astype(np.float32)  # one first-digit bucket
+    x[3::8, ::3] = -np.inf
+    x[4::8, :30000] = 0.25                                            # level-0 bucket overflows
+    x[4::8, 30000:] = (0.25 + np.arange(10000) * 2.0 ** -24).astype(np.float32)
+    x[5::8, :] = np.float32(-3.0)
+    x[5::8, 123] = np.float32(3.0)
+    ke = np.full(rows, width, dtype=np.int32)
+    ke[6::8] = 1000                                                   # fewer columns than k
+    out, vals = _run_topk(x, None, ke, k)
+    for r in range(rows):
+        assert_topk_values_exact(out[r], vals[r, :ke[r]], k, f"row {r}")
+    assert all(123 in set(out[r].tolist()) for r in range(5, rows, 8))
+
+
 @pytest.mark.parametrize("bf16", [False, True])
 def test_topk_values_output(bf16):
     # the optional score output: the score of every selected column, -inf in -1 slots
