@@ -253,18 +253,23 @@ __device__ __forceinline__ void sweep_row(const void* rowp, int64_t lo, int64_t 
     f(valid, c, valid ? key_at<kBf16>(rowp, c) : 0u);
   }
   const uint4* vp = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(rowp) + a1 * kEsz);
-  for (int64_t v0 = 0; v0 < nvec; v0 += static_cast<int64_t>(kThreads) * kUnroll) {
+  // columns and vector indices fit in int32 (rows hold fewer than 2^31 columns)
+  constexpr int kStep = kThreads * kUnroll;
+  const int nv = static_cast<int>(nvec);
+  const int col0 = static_cast<int>(a1);
+  auto step = [&](int v0, auto check) {
+    constexpr bool kCheck = decltype(check)::value;
     uint4 r[kUnroll];
 #pragma unroll
     for (int j = 0; j < kUnroll; ++j) {
-      const int64_t v = v0 + j * kThreads + tid;
-      r[j] = v < nvec ? __ldg(vp + v) : make_uint4(0, 0, 0, 0);
+      const int v = v0 + j * kThreads + tid;
+      r[j] = (!kCheck || v < nv) ? __ldg(vp + v) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int j = 0; j < kUnroll; ++j) {
-      const int64_t v = v0 + j * kThreads + tid;
-      const bool valid = v < nvec;
-      const int64_t c = a1 + v * kVec;
+      const int v = v0 + j * kThreads + tid;
+      const bool valid = !kCheck || v < nv;
+      const int c = col0 + v * kVec;
       const uint32_t w[4] = {r[j].x, r[j].y, r[j].z, r[j].w};
 #pragma unroll
       for (int e = 0; e < kVec; ++e) {
@@ -277,7 +282,10 @@ __device__ __forceinline__ void sweep_row(const void* rowp, int64_t lo, int64_t 
         f(valid, c + e, key);
       }
     }
-  }
+  };
+  const int nfull = nv / kStep * kStep;
+  for (int v0 = 0; v0 < nfull; v0 += kStep) step(v0, std::false_type{});
+  if (nfull < nv) step(nfull, std::true_type{});
 }
 
 // Exclusive prefix sum of v over the warp; *total receives the warp's sum.
