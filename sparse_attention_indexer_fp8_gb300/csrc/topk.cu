@@ -8,8 +8,12 @@
 // sparse column back to its request-local position; here that remap is the
 // selection's store step.
 //
-// Design: one 1024-thread block per row. Scores are mapped to order-preserving
-// 32-bit keys and selected by three radix digits (10, 11 and 11 bits). Level 0
+// Design: one block per row (1024 threads, one block per SM; or 512 threads and
+// two blocks per SM when there are many rows of at most 64K columns, so one
+// block's barrier-bound phases overlap the other's passes). Scores are mapped to
+// order-preserving 32-bit keys and selected by three radix digits (10, 11 and 11
+// bits). With more rows than blocks in flight, each block asks for the row one
+// wave ahead to be staged in L2. Level 0
 // histograms the row from global memory (or takes the histogram the scoring
 // kernel accumulated); a second pass over the row keeps only the elements at or
 // above the threshold digit, compacted into shared memory, where they are split
