@@ -25,14 +25,18 @@
 // cross-thread traffic and the [rows x 64 heads x tokens] intermediate never
 // leaves the SM.
 //
-// Roles (320 threads, one CTA per SM, persistent):
+// Roles (persistent CTAs; with one query per group, decode and the sparse
+// modes, two 192-thread CTAs per SM with one epilogue warpgroup each: two
+// independent pipelines per SM stream the cache at a markedly higher rate than
+// one; with two or four queries per group, one 320-thread CTA per SM with two
+// epilogue warpgroups):
 //   warp 0     TMA producer: k boxes (one per cache block / sparse block) and
 //              their scales into a ring of shared-memory stages, q per group;
 //              block-table lookups for the next tile are issued before the
 //              wait for a free stage so their latency hides behind it.
 //   warp 1     allocates tensor memory; one lane issues tcgen05.mma and
 //              commits stage / accumulator barriers.
-//   warps 2-9  epilogue, two warpgroups taking tiles in turn: tcgen05.ld of
+//   warps 2-   epilogue, warpgroups taking tiles in turn: tcgen05.ld of
 //              the accumulator, weighted head sum, scale, causal / range mask,
 //              coalesced store (fp32 or bf16).
 // The flattened (group, tile) sequence is split evenly over the CTAs; every
@@ -49,12 +53,6 @@ namespace idx {
 namespace {
 
 constexpr int kTile = 128;
-#ifndef IDX_EPI_WARPGROUPS
-#define IDX_EPI_WARPGROUPS 2
-#endif
-constexpr int kEpiWG = IDX_EPI_WARPGROUPS;  // epilogue warpgroups, alternating tiles
-constexpr int kEpiWarps = 4 * kEpiWG;
-constexpr int kThreads = 64 + kEpiWarps * 32;
 
 constexpr int kKvStageBytes = kTile * kDim;       // 16 KB
 constexpr int kScaleStageBytes = 2048;            // up to 16 boxes, each in a 128-byte slot
@@ -109,14 +107,19 @@ constexpr int kHistBins = 1024;  // first selection digit: the top 10 bits of th
 template <int NQ>
 struct Cfg {
   static constexpr int N = 64 * NQ;
-  static constexpr int kStages = NQ == 1 ? 10 : (NQ == 2 ? 10 : 8);
+  // CTAs per SM and epilogue warpgroups per CTA (taking tiles in turn)
+  static constexpr int kCtasPerSm = NQ == 1 ? 2 : 1;
+  static constexpr int kEpiWG = NQ == 1 ? 1 : 2;
+  static constexpr int kEpiWarps = 4 * kEpiWG;
+  static constexpr int kThreads = 64 + kEpiWarps * 32;
+  static constexpr int kStages = NQ == 1 ? 4 : (NQ == 2 ? 10 : 8);
   static constexpr int kAccStages = NQ == 4 ? 2 : 4;
   // tiles per tcgen05.commit: one commit covers the MMAs of kCommit consecutive
   // tiles (commits are costly next to a 4-MMA tile); one accumulator-ready
   // barrier per commit group
   static constexpr int kCommit = NQ == 4 ? 1 : 2;
   static constexpr int kAccFull = kAccStages / kCommit;
-  static constexpr int kTmemCols = kAccStages * N;  // 256 or 512
+  static constexpr int kTmemCols = kAccStages * N;  // 256 or 512 per CTA, 512 per SM
   static constexpr int kQStageBytes = NQ * 64 * kDim;
   static constexpr int kOffKv = 0;
   static constexpr int kOffQ = kOffKv + kStages * kKvStageBytes;
@@ -128,7 +131,8 @@ struct Cfg {
   static constexpr int kOffBar = kOffHist + kEpiWarps * kHistWords * 4;
   static constexpr int kNumBars = 2 * kStages + kAccFull + kAccStages + 4;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 1024;  // + alignment slack
-  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(kSmemBytes <= 232448 / kCtasPerSm - 2048, "shared memory budget per CTA");
+  static_assert(kTmemCols * kCtasPerSm <= 512, "tensor memory columns per SM");
 };
 
 struct Group {
@@ -245,6 +249,7 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
 }
 
 // Block-wide inclusive scan of one int per thread (blockDim.x = kThreads).
+template <int kThreads>
 __device__ __forceinline__ long long block_scan(long long v, long long* warp_tot, long long* total) {
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
@@ -339,10 +344,12 @@ __device__ __forceinline__ float weighted_head_sum(const uint32_t (&a0)[32], con
 }
 
 template <int NQ, bool kOutBf16>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<NQ>::kThreads, Cfg<NQ>::kCtasPerSm)
 mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_kv,
                   const __grid_constant__ CUtensorMap map_scale, const LogitsParams p) {
   using C = Cfg<NQ>;
+  constexpr int kThreads = C::kThreads;
+  constexpr int kEpiWG = C::kEpiWG;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* kv_s = smem + C::kOffKv;
@@ -403,7 +410,7 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       const int g = base + threadIdx.x;
       const long long v = g < p.n_groups ? (max(__ldg(p.ctx_lens + g), 0) + kTile - 1) / kTile : 0;
       long long chunk;
-      block_scan(v, s_warp_tot, &chunk);
+      block_scan<kThreads>(v, s_warp_tot, &chunk);
       running += chunk;
     }
     total = running;
@@ -423,7 +430,7 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       const int g = base + threadIdx.x;
       const long long v = g < p.n_groups ? (max(__ldg(p.ctx_lens + g), 0) + kTile - 1) / kTile : 0;
       long long chunk;
-      const long long incl = block_scan(v, s_warp_tot, &chunk) + running;
+      const long long incl = block_scan<kThreads>(v, s_warp_tot, &chunk) + running;
       if (g < p.n_groups && v > 0 && incl - v <= u0 && u0 < incl) {
         s_g0 = g;
         s_t0 = static_cast<int>(u0 - (incl - v));
@@ -868,10 +875,15 @@ idx_status_t launch_logits(const CUtensorMap& mq, const CUtensorMap& mkv, const 
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cfg<NQ>::kSmemBytes);
+    // all of the unified L1 / shared memory as shared memory, so kCtasPerSm CTAs fit
+    if (e == cudaSuccess) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
+    }
     if (e != cudaSuccess) return fail(IDX_ERR_CUDA, "%s: cudaFuncSetAttribute: %s", fn, cudaGetErrorString(e));
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  kern<<<grid, kThreads, Cfg<NQ>::kSmemBytes, stream>>>(mq, mkv, msc, p);
+  kern<<<grid, Cfg<NQ>::kThreads, Cfg<NQ>::kSmemBytes, stream>>>(mq, mkv, msc, p);
   return check_launch(fn);
 }
 
@@ -880,7 +892,9 @@ idx_status_t dispatch(int nq_tmpl, const CUtensorMap& mq, const CUtensorMap& mkv
                       cudaStream_t stream, const char* fn) {
   const int sms = device_sm_count();
   if (sms <= 0) return fail(IDX_ERR_CUDA, "%s: cannot query the SM count", fn);
-  long long grid = sms;
+  // persistent: kCtasPerSm CTAs on every SM (fewer when there are fewer tiles)
+  const int per_sm = nq_tmpl == 1 ? Cfg<1>::kCtasPerSm : (nq_tmpl == 2 ? Cfg<2>::kCtasPerSm : Cfg<4>::kCtasPerSm);
+  long long grid = static_cast<long long>(sms) * per_sm;
   if (max_tiles >= 0 && max_tiles < grid) grid = max_tiles;
   if (grid <= 0) return IDX_OK;
   switch (nq_tmpl) {
