@@ -25,10 +25,10 @@
 // cross-thread traffic and the [rows x 64 heads x tokens] intermediate never
 // leaves the SM.
 //
-// Roles (persistent CTAs; with one query per group, decode and the sparse
-// modes, two 192-thread CTAs per SM with one epilogue warpgroup each: two
+// Roles (persistent CTAs; with one or two queries per group, decode and the
+// sparse modes, two 192-thread CTAs per SM with one epilogue warpgroup each: two
 // independent pipelines per SM stream the cache at a markedly higher rate than
-// one; with two or four queries per group, one 320-thread CTA per SM with two
+// one; with four queries per group, prefill, one 320-thread CTA per SM with two
 // epilogue warpgroups):
 //   warp 0     TMA producer: k boxes (one per cache block / sparse block) and
 //              their scales into a ring of shared-memory stages, q per group;
@@ -108,16 +108,16 @@ template <int NQ>
 struct Cfg {
   static constexpr int N = 64 * NQ;
   // CTAs per SM and epilogue warpgroups per CTA (taking tiles in turn)
-  static constexpr int kCtasPerSm = NQ == 1 ? 2 : 1;
-  static constexpr int kEpiWG = NQ == 1 ? 1 : 2;
+  static constexpr int kCtasPerSm = NQ == 4 ? 1 : 2;
+  static constexpr int kEpiWG = NQ == 4 ? 2 : 1;
   static constexpr int kEpiWarps = 4 * kEpiWG;
   static constexpr int kThreads = 64 + kEpiWarps * 32;
-  static constexpr int kStages = NQ == 1 ? 4 : (NQ == 2 ? 10 : 8);
-  static constexpr int kAccStages = NQ == 4 ? 2 : 4;
+  static constexpr int kStages = NQ == 4 ? 8 : 4;
+  static constexpr int kAccStages = NQ == 1 ? 4 : 2;
   // tiles per tcgen05.commit: one commit covers the MMAs of kCommit consecutive
   // tiles (commits are costly next to a 4-MMA tile); one accumulator-ready
   // barrier per commit group
-  static constexpr int kCommit = NQ == 4 ? 1 : 2;
+  static constexpr int kCommit = NQ == 1 ? 2 : 1;
   static constexpr int kAccFull = kAccStages / kCommit;
   static constexpr int kTmemCols = kAccStages * N;  // 256 or 512 per CTA, 512 per SM
   static constexpr int kQStageBytes = NQ * 64 * kDim;
