@@ -208,6 +208,79 @@ def _nbytes(*ts):
     return int(sum(t.numel() * t.element_size() for t in ts))
 
 
+def _pin_like(d):
+    return torch.empty(d.shape, dtype=d.dtype).pin_memory()
+
+
+class E2EPipeline:
+    """End-to-end steps through the public API with host buffers, two steps in flight.
+
+    Every step copies all of its inputs from pinned host memory to the device and
+    its result back. The host-to-device copy of step i + 1 (on its own stream, into
+    the second of two device buffer sets) and the device-to-host copy of step i - 1
+    (on a third stream) overlap step i's kernels; events order each copy against
+    the kernels that read or write the same buffer set. The bench's own device
+    tensors are re-pointed (``Tensor.set_``) at the set a step uses, so its ``step``
+    runs unchanged."""
+
+    def __init__(self, bench, dev):
+        self.bench = bench
+        self.inputs, self.outputs = bench.e2e_io()
+        self.sets_in = [[d.clone() for _, d in self.inputs] for _ in range(2)]
+        self.sets_out = [[d.clone() for _, d in self.outputs] for _ in range(2)]
+        self.h2d = torch.cuda.Stream(dev)
+        self.d2h = torch.cuda.Stream(dev)
+        self.ev = {k: [torch.cuda.Event() for _ in range(2)]
+                   for k in ("in_ready", "in_free", "out_ready", "out_free")}
+        self.used = [False, False]
+        self.i = 0
+
+    def bytes_per_step(self):
+        return _nbytes(*[h for h, _ in self.inputs]), _nbytes(*[h for h, _ in self.outputs])
+
+    def begin(self, stream):
+        """Forks the copy streams from ``stream`` (required inside a graph capture)."""
+        fork = torch.cuda.Event()
+        fork.record(stream)
+        self.h2d.wait_event(fork)
+        self.d2h.wait_event(fork)
+        self.used = [False, False]
+        self.i = 0
+
+    def step(self, stream):
+        s, ev = self.i % 2, self.ev
+        with torch.cuda.stream(self.h2d):
+            if self.used[s]:
+                self.h2d.wait_event(ev["in_free"][s])      # the kernels of step i - 2 are done with set s
+            for (h, _), buf in zip(self.inputs, self.sets_in[s]):
+                buf.copy_(h, non_blocking=True)
+            ev["in_ready"][s].record(self.h2d)
+        stream.wait_event(ev["in_ready"][s])
+        if self.used[s]:
+            stream.wait_event(ev["out_free"][s])          # step i - 2's result has left set s
+        for (_, d), buf in zip(self.inputs, self.sets_in[s]):
+            d.set_(buf)
+        for (_, d), buf in zip(self.outputs, self.sets_out[s]):
+            d.set_(buf)
+        self.bench.step(stream)
+        ev["in_free"][s].record(stream)
+        ev["out_ready"][s].record(stream)
+        with torch.cuda.stream(self.d2h):
+            self.d2h.wait_event(ev["out_ready"][s])
+            for (h, _), buf in zip(self.outputs, self.sets_out[s]):
+                h.copy_(buf, non_blocking=True)
+            ev["out_free"][s].record(self.d2h)
+        self.used[s] = True
+        self.i += 1
+
+    def end(self, stream):
+        """Joins the copy streams back into ``stream``."""
+        for side in (self.h2d, self.d2h):
+            j = torch.cuda.Event()
+            j.record(side)
+            stream.wait_event(j)
+
+
 class DecodeBench:
     """Dense paged decode: k insert of the new token, logits, top-2048, slot conversion."""
 
@@ -258,18 +331,12 @@ class DecodeBench:
         idx.idx_req_to_global_slots(self.local, None, self.bt, wl.pool.block_size, wl.block_span, self.slots,
                                     stream=stream)
 
-    def e2e_prepare(self):
-        self.h_in = [(_pin(self.wl.q8), self.q), (_pin(self.wl.w), self.w), (self.new_k.cpu().pin_memory(),
-                     self.new_k), (self.new_slots.cpu().pin_memory(), self.new_slots),
-                     (_pin(self.wl.pool.ctx_lens), self.ctx)]
-        self.h_out = torch.empty(self.slots.shape, dtype=torch.int32).pin_memory()
-        return _nbytes(*[h for h, _ in self.h_in]), _nbytes(self.h_out)
-
-    def e2e_step(self, stream):
-        for h, d in self.h_in:
-            d.copy_(h, non_blocking=True)
-        self.step(stream)
-        self.h_out.copy_(self.slots, non_blocking=True)
+    def e2e_io(self):
+        """(pinned host, device) pairs of a step's inputs and of its result."""
+        inputs = [(_pin(self.wl.q8), self.q), (_pin(self.wl.w), self.w), (self.new_k.cpu().pin_memory(),
+                  self.new_k), (self.new_slots.cpu().pin_memory(), self.new_slots),
+                  (_pin(self.wl.pool.ctx_lens), self.ctx)]
+        return inputs, [(_pin_like(self.slots), self.slots)]
 
     def verify_and_time_oracle(self, n_rows):
         from tests.checks import assert_logits_close, assert_topk_row
@@ -359,18 +426,11 @@ class PrefillBench:
             ev[1].record(stream)
         idx.idx_topk(self.logits, self.ks, self.ke, self.wl.topk, self.local, stream=stream)
 
-    def e2e_prepare(self):
-        self.h_in = [(_pin(self.wl.q8), self.q), (self.w.cpu().pin_memory(), self.w),
-                     (self.chunk_k.cpu().pin_memory(), self.chunk_k),
-                     (self.chunk_slots.cpu().pin_memory(), self.chunk_slots)]
-        self.h_out = torch.empty(self.local.shape, dtype=torch.int32).pin_memory()
-        return _nbytes(*[h for h, _ in self.h_in]), _nbytes(self.h_out)
-
-    def e2e_step(self, stream):
-        for h, d in self.h_in:
-            d.copy_(h, non_blocking=True)
-        self.step(stream)
-        self.h_out.copy_(self.local, non_blocking=True)
+    def e2e_io(self):
+        inputs = [(_pin(self.wl.q8), self.q), (self.w.cpu().pin_memory(), self.w),
+                  (self.chunk_k.cpu().pin_memory(), self.chunk_k),
+                  (self.chunk_slots.cpu().pin_memory(), self.chunk_slots)]
+        return inputs, [(_pin_like(self.local), self.local)]
 
     def _oracle_k(self):
         from oracle import indexer as O
@@ -470,17 +530,10 @@ class HierBench:
         idx.idx_req_to_global_slots(st.positions, None, self.bt, wl.pool.block_size, wl.pool.block_size,
                                     st.slots, stream=stream)
 
-    def e2e_prepare(self):
-        self.h_in = [(_pin(self.wl.q8), self.q), (_pin(self.wl.w), self.w), (_pin(self.wl.cand), self.cand),
-                     (_pin(self.wl.pool.ctx_lens), self.ctx)]
-        self.h_out = torch.empty(self.st.slots.shape, dtype=torch.int32).pin_memory()
-        return _nbytes(*[h for h, _ in self.h_in]), _nbytes(self.h_out)
-
-    def e2e_step(self, stream):
-        for h, d in self.h_in:
-            d.copy_(h, non_blocking=True)
-        self.step(stream)
-        self.h_out.copy_(self.st.slots, non_blocking=True)
+    def e2e_io(self):
+        inputs = [(_pin(self.wl.q8), self.q), (_pin(self.wl.w), self.w), (_pin(self.wl.cand), self.cand),
+                  (_pin(self.wl.pool.ctx_lens), self.ctx)]
+        return inputs, [(_pin_like(self.st.slots), self.st.slots)]
 
     def verify_and_time_oracle(self, n_rows):
         from oracle import indexer as O
@@ -617,19 +670,12 @@ class HierMtpBench:
             idx.idx_req_to_global_slots(st.positions, st.row_to_req, self.bt, wl.pool.block_size,
                                         wl.pool.block_size, st.slots, stream=stream)
 
-    def e2e_prepare(self):
-        self.h_in = ([(_pin(a), d) for (a, _), d in zip(self.h_qw, self.q)] +
-                     [(_pin(b), d) for (_, b), d in zip(self.h_qw, self.w)] +
-                     [(_pin(self.wl.cand), self.cand), (_pin(self.wl.pool.ctx_lens), self.ctx),
-                      (_pin(self.h_row_ke), self.row_ke)])
-        self.h_out = torch.empty(self.st.slots.shape, dtype=torch.int32).pin_memory()
-        return _nbytes(*[h for h, _ in self.h_in]), _nbytes(self.h_out)
-
-    def e2e_step(self, stream):
-        for h, d in self.h_in:
-            d.copy_(h, non_blocking=True)
-        self.step(stream)
-        self.h_out.copy_(self.st.slots, non_blocking=True)
+    def e2e_io(self):
+        inputs = ([(_pin(a), d) for (a, _), d in zip(self.h_qw, self.q)] +
+                  [(_pin(b), d) for (_, b), d in zip(self.h_qw, self.w)] +
+                  [(_pin(self.wl.cand), self.cand), (_pin(self.wl.pool.ctx_lens), self.ctx),
+                   (_pin(self.h_row_ke), self.row_ke)])
+        return inputs, [(_pin_like(self.st.slots), self.st.slots)]
 
     def verify_and_time_oracle(self, n_rows):
         from oracle import indexer as O
@@ -761,17 +807,10 @@ class DcpBench:
         idx.idx_dcp_topk_merge(self.all_vals, self.all_idx, self.offs, k, k, self.positions, vals=self.scores,
                                stream=stream)
 
-    def e2e_prepare(self):
-        self.h_in = [(_pin(self.wl.q8), self.q), (_pin(self.wl.w), self.w)] + \
-                    [(_pin(sh["h_lens"]), sh["lens"]) for sh in self.shards]
-        self.h_out = torch.empty(self.positions.shape, dtype=torch.int32).pin_memory()
-        return _nbytes(*[h for h, _ in self.h_in]), _nbytes(self.h_out)
-
-    def e2e_step(self, stream):
-        for h, d in self.h_in:
-            d.copy_(h, non_blocking=True)
-        self.step(stream)
-        self.h_out.copy_(self.positions, non_blocking=True)
+    def e2e_io(self):
+        inputs = [(_pin(self.wl.q8), self.q), (_pin(self.wl.w), self.w)] + \
+                 [(_pin(sh["h_lens"]), sh["lens"]) for sh in self.shards]
+        return inputs, [(_pin_like(self.positions), self.positions)]
 
     def verify_and_time_oracle(self, n_rows):
         from tests.checks import assert_logits_close, assert_topk_row
@@ -839,19 +878,9 @@ class QPrepBench:
         if ev is not None:
             ev[1].record(stream)
 
-    def e2e_prepare(self):
-        self.h_q = self.q.cpu().pin_memory()
-        self.h_in = [(self.h_q, self.q), (_pin(self.wl.positions), self.pos), (_pin(self.wl.w), self.w)]
-        self.h_out = [torch.empty(self.q8.shape, dtype=torch.uint8).pin_memory(),
-                      torch.empty(self.w_out.shape, dtype=torch.bfloat16).pin_memory()]
-        return _nbytes(*[h for h, _ in self.h_in]), _nbytes(*self.h_out)
-
-    def e2e_step(self, stream):
-        for h, d in self.h_in:
-            d.copy_(h, non_blocking=True)
-        self.step(stream)
-        self.h_out[0].copy_(self.q8, non_blocking=True)
-        self.h_out[1].copy_(self.w_out, non_blocking=True)
+    def e2e_io(self):
+        inputs = [(self.q.cpu().pin_memory(), self.q), (_pin(self.wl.positions), self.pos), (_pin(self.wl.w), self.w)]
+        return inputs, [(_pin_like(self.q8), self.q8), (_pin_like(self.w_out), self.w_out)]
 
     def verify_and_time_oracle(self, n_rows):
         from oracle import indexer as O
@@ -955,19 +984,25 @@ def run_ours(args, rank, world, local, dist):
     ms_total = max_over_ranks(dist, e0.elapsed_time(e1), dev)
     idx.idx_device_error(stream)
 
-    # end to end through the public API with host buffers: per step H2D of the
-    # step's inputs from pinned memory, the step, D2H of the result table
-    h2d, d2h = bench.e2e_prepare()
+    # end to end through the public API with host buffers: every step copies its
+    # inputs in from pinned memory and its result table out; two steps are in
+    # flight, so step i + 1's inputs and step i - 1's result move during step i
+    pipe = E2EPipeline(bench, dev)
+    h2d, d2h = pipe.bytes_per_step()
+    pipe.begin(stream)
     for _ in range(args.warmup):
-        bench.e2e_step(stream)
+        pipe.step(stream)
+    pipe.end(stream)
     e2e_graph = None
     if args.graphs:
         # the copies from and to pinned host memory are captured with the kernels
         e2e_graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(e2e_graph):
             cap = torch.cuda.current_stream(dev)
+            pipe.begin(cap)
             for _ in range(GRAPH_STEPS):
-                bench.e2e_step(cap)
+                pipe.step(cap)
+            pipe.end(cap)
         e2e_graph.replay()
     barrier(dist)
     torch.cuda.synchronize(dev)
@@ -978,8 +1013,11 @@ def run_ours(args, rank, world, local, dist):
         for _ in range(args.steps // GRAPH_STEPS):
             e2e_graph.replay()
         done = args.steps // GRAPH_STEPS * GRAPH_STEPS
-    for _ in range(args.steps - done):
-        bench.e2e_step(stream)
+    if args.steps > done:
+        pipe.begin(stream)
+        for _ in range(args.steps - done):
+            pipe.step(stream)
+        pipe.end(stream)
     a1.record(stream)
     torch.cuda.synchronize(dev)
     barrier(dist)
@@ -1007,7 +1045,9 @@ def run_ours(args, rank, world, local, dist):
         "roofline": bench.roofline(kernel_ms, step_ms, peaks, peak_kind),
         "cpu_baseline": cpu,
         "e2e": {"value": round(rows_total / (e2e_ms / 1e3 / args.steps), 1), "unit": "rows/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "copies": "every step: inputs in from pinned host memory, result out; two steps in "
+                          "flight (step i+1's inputs and step i-1's result move during step i)"},
         "gpu_launches": bench.launches_per_step * args.steps,
         "launch": (f"CUDA graph of {GRAPH_STEPS} steps, replayed" if args.graphs else "direct launches"),
         "clocks": sampler.summary(t0, t1) if sampler else None,
