@@ -282,9 +282,9 @@ class E2EPipeline:
 
 
 class DecodeBench:
-    """Dense paged decode: k insert of the new token, logits, top-2048, slot conversion."""
+    """Dense paged decode: k insert of the new token, logits, top-2048 with the slot conversion."""
 
-    launches_per_step = 4
+    launches_per_step = 3
 
     def __init__(self, name, rank, dev):
         import sparse_attention_indexer_fp8_gb300 as idx
@@ -327,9 +327,10 @@ class DecodeBench:
                                         self.logits, ws=self.ws, stream=stream)
         if ev is not None:
             ev[1].record(stream)
-        idx.idx_topk(self.logits, None, self.ctx, wl.topk, self.local, ws=self.ws, stream=stream)
-        idx.idx_req_to_global_slots(self.local, None, self.bt, wl.pool.block_size, wl.block_span, self.slots,
-                                    stream=stream)
+        # top-2048 with the slot conversion fused into the selection's output pass
+        idx.idx_topk(self.logits, None, self.ctx, wl.topk, self.local, ws=self.ws, stream=stream,
+                     slots=self.slots, block_table=self.bt, block_size=wl.pool.block_size,
+                     block_span=wl.block_span)
 
     def e2e_io(self):
         """(pinned host, device) pairs of a step's inputs and of its result."""
@@ -375,7 +376,7 @@ class DecodeBench:
         return {"workload": self.wl.name, "batch": self.B, "ctx_min": int(L.min()), "ctx_max": int(L.max()),
                 "ctx_mean": float(L.mean()), "topk": self.wl.topk, "block_size": pool.block_size,
                 "block_stride_bytes": self.stride, "cache_gb": round(pool.num_blocks * self.stride / 1e9, 3),
-                "step": "k insert + paged logits + top-2048 + slot conversion",
+                "step": "k insert + paged logits + top-2048 with the slot conversion fused",
                 "l2": "inputs larger than L2 (k cache > 129 MB), no flush",
                 "parallelism": f"rows sharded, {world} independent replica(s)"}
 
@@ -489,9 +490,9 @@ class PrefillBench:
 
 
 class HierBench:
-    """V4.1 consumer-layer decode: expand candidates, sparse logits (bf16), top-2048 + remap, slots."""
+    """V4.1 consumer-layer decode: expand candidates, sparse logits (bf16), top-2048 + remap + slots."""
 
-    launches_per_step = 4
+    launches_per_step = 3
     dtype = "e4m3xe4m3->f32 (bf16 logits)"
     metric = "hierarchical sparse decode indexer query-rows/s @128K ctx incl. top-2048"
 
@@ -526,9 +527,9 @@ class HierBench:
         if ev is not None:
             ev[1].record(stream)
         idx.idx_sparse_topk_remap(st.logits, st.end, st.sparse_idx, None, wl.sbk, wl.topk, st.positions,
-                                  col_scratch=st.cols, ws=st.ws, stream=stream)
-        idx.idx_req_to_global_slots(st.positions, None, self.bt, wl.pool.block_size, wl.pool.block_size,
-                                    st.slots, stream=stream)
+                                  col_scratch=st.cols, ws=st.ws, stream=stream, slots=st.slots,
+                                  block_table=self.bt, block_size=wl.pool.block_size,
+                                  block_span=wl.pool.block_size)
 
     def e2e_io(self):
         inputs = [(_pin(self.wl.q8), self.q), (_pin(self.wl.w), self.w), (_pin(self.wl.cand), self.cand),
@@ -584,7 +585,7 @@ class HierBench:
         return {"workload": self.wl.name, "batch": self.B, "ctx": int(self.wl.pool.ctx_lens[0]),
                 "candidates": int(self.wl.cand.shape[1]), "cand_block_size": self.wl.cand_block_size,
                 "sbk": self.wl.sbk, "topk": self.wl.topk,
-                "step": "expand + sparse logits (bf16) + top-2048 remap + slot conversion",
+                "step": "expand + sparse logits (bf16) + top-2048 remap with the slot conversion fused",
                 "l2": "candidate blocks scattered over a 2.2 GB cache, no flush",
                 "parallelism": f"rows sharded, {world} independent replica(s)"}
 
@@ -622,7 +623,7 @@ class HierMtpBench:
     """V4.1 consumer layers with multi-token prediction: one expansion shared by several layers."""
 
     next_n, layers = 2, 4
-    launches_per_step = 1 + 3 * layers
+    launches_per_step = 1 + 2 * layers
     dtype = "e4m3xe4m3->f32 (bf16 logits)"
     metric = ("hierarchical sparse decode query-row-layers/s @128K ctx incl. top-2048 "
               "(next_n 2, one expansion per step shared by 4 consumer layers)")
@@ -666,9 +667,9 @@ class HierMtpBench:
             if ev is not None and i == 0:
                 ev[1].record(stream)
             idx.idx_sparse_topk_remap(st.logits, st.end, st.sparse_idx, None, wl.sbk, wl.topk, st.positions,
-                                      col_scratch=st.cols, ws=st.ws, stream=stream)
-            idx.idx_req_to_global_slots(st.positions, st.row_to_req, self.bt, wl.pool.block_size,
-                                        wl.pool.block_size, st.slots, stream=stream)
+                                      col_scratch=st.cols, ws=st.ws, stream=stream, slots=st.slots,
+                                      block_table=self.bt, block_size=wl.pool.block_size,
+                                      block_span=wl.pool.block_size, row_to_req=st.row_to_req)
 
     def e2e_io(self):
         inputs = ([(_pin(a), d) for (a, _), d in zip(self.h_qw, self.q)] +
@@ -736,7 +737,7 @@ class HierMtpBench:
         return {"workload": self.wl.name, "batch": self.B, "next_n": self.next_n, "query_rows": self.rows,
                 "layers_per_step": self.layers, "ctx": int(self.wl.pool.ctx_lens[0]),
                 "candidates": int(self.wl.cand.shape[1]), "sbk": self.wl.sbk, "topk": self.wl.topk,
-                "step": "expand once + per layer: sparse logits (bf16) + top-2048 remap + slot conversion",
+                "step": "expand once + per layer: sparse logits (bf16) + top-2048 remap with the slot conversion fused",
                 "l2": "candidate blocks scattered over a 2.2 GB cache, no flush",
                 "e2e_result": "the last layer's slot table",
                 "parallelism": f"rows sharded, {world} independent replica(s)"}

@@ -396,6 +396,35 @@ idx_status_t idx_req_to_global_slots(const int32_t* local, int64_t ld_l, int32_t
                                      int32_t* slots, int64_t ld_s, cudaStream_t stream);
 
 /*
+ * idx_topk_slots / idx_sparse_topk_remap_slots - the selection with the slot
+ * conversion fused into its output pass.
+ *
+ * Same selection and outputs as idx_topk (without `vals`) and
+ * idx_sparse_topk_remap, and in addition every request-local entry v of row r
+ * converted exactly as idx_req_to_global_slots does with the same row_to_req,
+ * block_table, ld_bt, block_size and block_span, written to slots[r, i]
+ * (int32 [rows, ld_slots], ld_slots >= k; -1 where the entry is -1). One launch
+ * instead of two; the results equal the two-call sequence. A slot beyond int32
+ * is written as -1 and raises the device flag (idx_device_error).
+ * Errors: those of the two calls it replaces.
+ */
+idx_status_t idx_topk_slots(const void* logits, int dtype, int64_t ld, const int32_t* row_ks,
+                            const int32_t* row_ke, int32_t rows, int32_t k, int32_t* out,
+                            int64_t ld_out, const int32_t* row_to_req, const int32_t* block_table,
+                            int64_t ld_bt, int32_t block_size, int32_t block_span, int32_t* slots,
+                            int64_t ld_slots, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+idx_status_t idx_sparse_topk_remap_slots(const void* sparse_logits, int dtype, int64_t ld,
+                                         const int32_t* end, const int32_t* sparse_idx,
+                                         int64_t ld_si, const int32_t* row_ks, int32_t sbk,
+                                         int32_t rows, int32_t k, int32_t* col_scratch,
+                                         int64_t ld_col, int32_t* positions, int64_t ld_pos,
+                                         const int32_t* row_to_req, const int32_t* block_table,
+                                         int64_t ld_bt, int32_t block_size, int32_t block_span,
+                                         int32_t* slots, int64_t ld_slots, void* ws,
+                                         size_t ws_bytes, cudaStream_t stream);
+
+/*
  * idx_paged_mqa_topk_decode_noalloc - decode scoring and top-k for callers that
  * cannot allocate device memory.
  *

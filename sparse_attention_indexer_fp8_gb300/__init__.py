@@ -120,12 +120,26 @@ def idx_paged_mqa_logits_decode(q, w, cache, block_size, block_table, ctx_lens, 
         0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)))
 
 
-def idx_topk(logits, row_ks, row_ke, k, out, vals=None, ws=None, stream=None):
-    """Per-row top-k indices (request-local), -1 filled; out int32 [rows, >= k]; optional scores."""
-    _check("idx_topk", library().idx_topk(
+def idx_topk(logits, row_ks, row_ke, k, out, vals=None, ws=None, stream=None, slots=None,
+             block_table=None, block_size=None, block_span=None, row_to_req=None):
+    """Per-row top-k indices (request-local), -1 filled; out int32 [rows, >= k]; optional scores.
+
+    With ``slots`` (int32 [rows, >= k]) the slot conversion of idx_req_to_global_slots
+    (``block_table``, ``block_size``, ``block_span``, ``row_to_req``) is fused into the
+    selection's output pass (idx_topk_slots; no ``vals`` then)."""
+    wsb = 0 if ws is None else ws.numel() * ws.element_size()
+    if slots is None:
+        _check("idx_topk", library().idx_topk(
+            _ptr(logits), _dtype_code(logits), _rows(logits), _ptr(row_ks), _ptr(row_ke), logits.shape[0],
+            k, _ptr(out), _rows(out), _ptr(vals), 0 if vals is None else _rows(vals), _ptr(ws), wsb,
+            _stream(stream)))
+        return
+    if vals is not None:
+        raise ValueError("idx_topk: the fused slot conversion has no score output")
+    _check("idx_topk_slots", library().idx_topk_slots(
         _ptr(logits), _dtype_code(logits), _rows(logits), _ptr(row_ks), _ptr(row_ke), logits.shape[0],
-        k, _ptr(out), _rows(out), _ptr(vals), 0 if vals is None else _rows(vals), _ptr(ws),
-        0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)))
+        k, _ptr(out), _rows(out), _ptr(row_to_req), _ptr(block_table), _rows(block_table), block_size,
+        block_span, _ptr(slots), _rows(slots), _ptr(ws), wsb, _stream(stream)))
 
 
 def idx_q_rope_quant(q, positions, cos_sin, w, q8, w_out, softmax_scale, n_head_scale,
@@ -174,14 +188,26 @@ def idx_expand_candidates(cand, row_ks, row_ke, cand_block_size, sbk, sparse_idx
 
 
 def idx_sparse_topk_remap(sparse_logits, end, sparse_idx, row_ks, sbk, k, positions, col_scratch=None,
-                          ws=None, stream=None):
-    """Top-k over sparse columns [0, end) then column -> request-local position."""
-    _check("idx_sparse_topk_remap", library().idx_sparse_topk_remap(
+                          ws=None, stream=None, slots=None, block_table=None, block_size=None,
+                          block_span=None, row_to_req=None):
+    """Top-k over sparse columns [0, end) then column -> request-local position.
+
+    With ``slots`` the slot conversion is fused into the output pass
+    (idx_sparse_topk_remap_slots), as for idx_topk."""
+    wsb = 0 if ws is None else ws.numel() * ws.element_size()
+    if slots is None:
+        _check("idx_sparse_topk_remap", library().idx_sparse_topk_remap(
+            _ptr(sparse_logits), _dtype_code(sparse_logits), _rows(sparse_logits), _ptr(end),
+            _ptr(sparse_idx), _rows(sparse_idx), _ptr(row_ks), sbk, sparse_logits.shape[0], k,
+            _ptr(col_scratch), 0 if col_scratch is None else _rows(col_scratch), _ptr(positions),
+            _rows(positions), _ptr(ws), wsb, _stream(stream)))
+        return
+    _check("idx_sparse_topk_remap_slots", library().idx_sparse_topk_remap_slots(
         _ptr(sparse_logits), _dtype_code(sparse_logits), _rows(sparse_logits), _ptr(end),
         _ptr(sparse_idx), _rows(sparse_idx), _ptr(row_ks), sbk, sparse_logits.shape[0], k,
         _ptr(col_scratch), 0 if col_scratch is None else _rows(col_scratch), _ptr(positions),
-        _rows(positions), _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
-        _stream(stream)))
+        _rows(positions), _ptr(row_to_req), _ptr(block_table), _rows(block_table), block_size,
+        block_span, _ptr(slots), _rows(slots), _ptr(ws), wsb, _stream(stream)))
 
 
 def idx_req_to_global_slots(local, row_to_req, block_table, block_size, block_span, slots, k=None,

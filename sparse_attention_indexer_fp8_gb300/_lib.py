@@ -52,6 +52,11 @@ SIGNATURES = {
                                       c_i32, c_ptr, c_i64, c_ptr, c_i64, c_ptr, c_size, c_ptr]),
     "idx_req_to_global_slots": (c_int, [c_ptr, c_i64, c_i32, c_i32, c_ptr, c_ptr, c_i64, c_i32, c_i32,
                                         c_ptr, c_i64, c_ptr]),
+    "idx_topk_slots": (c_int, [c_ptr, c_int, c_i64, c_ptr, c_ptr, c_i32, c_i32, c_ptr, c_i64, c_ptr, c_ptr,
+                               c_i64, c_i32, c_i32, c_ptr, c_i64, c_ptr, c_size, c_ptr]),
+    "idx_sparse_topk_remap_slots": (c_int, [c_ptr, c_int, c_i64, c_ptr, c_ptr, c_i64, c_ptr, c_i32, c_i32,
+                                            c_i32, c_ptr, c_i64, c_ptr, c_i64, c_ptr, c_ptr, c_i64, c_i32,
+                                            c_i32, c_ptr, c_i64, c_ptr, c_size, c_ptr]),
     "idx_paged_mqa_topk_decode_noalloc": (c_int, [c_ptr, c_i64, c_ptr, c_int, c_i64, c_ptr, c_i32,
                                                   c_i32, c_i64, c_ptr, c_i64, c_ptr, c_i32, c_ptr,
                                                   c_i64, c_i32, c_ptr, c_i64, c_ptr]),

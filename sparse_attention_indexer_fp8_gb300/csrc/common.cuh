@@ -33,6 +33,7 @@ idx_status_t encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, int 
 unsigned int logits_read_and_clear_error(cudaStream_t stream, cudaError_t* err, long long* info);
 unsigned int index_ops_read_and_clear_error(cudaStream_t stream, cudaError_t* err);
 unsigned int q_rope_read_and_clear_error(cudaStream_t stream, cudaError_t* err);
+unsigned int topk_read_and_clear_error(cudaStream_t stream, cudaError_t* err);
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 

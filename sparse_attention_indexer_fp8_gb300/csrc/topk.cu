@@ -30,6 +30,10 @@
 #include "common.cuh"
 
 namespace idx {
+
+// bit 1: a fused slot conversion produced a slot beyond int32 (written as -1)
+__device__ unsigned int g_topk_error = 0;
+
 namespace {
 
 constexpr int kBins = 2048;      // bins of the second and third digits (11 bits each)
@@ -72,6 +76,15 @@ struct TopkParams {
   int pos_stride;          // merge: global distance between a shard's consecutive positions
   int k_local;             // merge: candidates per shard
   int n_cand;              // merge: candidates per row (shards * k_local)
+  // optional slot conversion of the request-local outputs (plain and remap modes):
+  // slot = block_table[req(r), v / block_size] * block_span + v % block_size
+  int32_t* slots;          // NULL = none
+  int64_t ld_slots;
+  const int32_t* row_to_req;  // NULL: row r belongs to request r
+  const int32_t* bt;
+  int64_t ld_bt;
+  int block_size;
+  int block_span;
   int rows;
   int ahead;               // rows in flight at once (one per SM): the row a wave later is
                            // moved into L2 while this one is selected (0 = off)
@@ -391,6 +404,21 @@ __device__ __forceinline__ float value_at(const void* row, int64_t c) {
   }
 }
 
+// The physical slot of request-local position v of row `row` (the conversion of
+// idx_req_to_global_slots), -1 for v < 0 or a block index past the table row.
+__device__ __forceinline__ int32_t slot_of(const TopkParams& p, int row, int32_t v) {
+  if (v < 0) return -1;
+  const int64_t lb = v / p.block_size;
+  if (lb >= p.ld_bt) return -1;
+  const int64_t req = p.row_to_req ? __ldg(p.row_to_req + row) : row;
+  const int64_t s = static_cast<int64_t>(__ldg(p.bt + req * p.ld_bt + lb)) * p.block_span + v % p.block_size;
+  if (s < 0 || s > INT32_MAX) {
+    atomicOr(&g_topk_error, 2u);
+    return -1;
+  }
+  return static_cast<int32_t>(s);
+}
+
 // Writes the row's outputs from the chosen columns sh.sel[0, m): mode-specific
 // indices (and optionally columns and scores), -1 / -inf in the unused slots.
 // In merge mode, candidates without a position are dropped and the remaining
@@ -420,6 +448,7 @@ __device__ __forceinline__ void write_outputs(const TopkParams& p, Shared& sh, i
         if (vals) v = value_at<kBf16>(rowp, c);
       }
       out[i] = o;
+      if (p.slots) p.slots[row * p.ld_slots + i] = slot_of(p, row, o);
       if (kMode == kRemap && p.cols) p.cols[row * p.ld_cols + i] = cl;
       if (vals) vals[i] = v;
     }
@@ -670,6 +699,18 @@ __global__ void __launch_bounds__(kThreads, 1024 / kThreads) topk_kernel(const T
 }
 
 }  // namespace
+
+unsigned int topk_read_and_clear_error(cudaStream_t stream, cudaError_t* err) {
+  unsigned int v = 0;
+  const unsigned int zero = 0;
+  *err = cudaStreamSynchronize(stream);
+  if (*err != cudaSuccess) return 0;
+  *err = cudaMemcpyFromSymbol(&v, g_topk_error, sizeof(v));
+  if (*err != cudaSuccess) return 0;
+  if (v) *err = cudaMemcpyToSymbol(g_topk_error, &zero, sizeof(zero));
+  return v;
+}
+
 }  // namespace idx
 
 using namespace idx;
@@ -686,6 +727,27 @@ idx_status_t attach_hist(const char* fn, TopkParams* p, int rows, void* ws, size
   }
   if (!aligned(ws, 16)) return fail(IDX_ERR_UNSUPPORTED, "%s: workspace must be 16-byte aligned", fn);
   p->hist = static_cast<uint32_t*>(ws);
+  return IDX_OK;
+}
+
+// The optional fused slot conversion (the checks of idx_req_to_global_slots).
+idx_status_t attach_slots(const char* fn, TopkParams* p, int32_t k, const int32_t* row_to_req,
+                          const int32_t* block_table, int64_t ld_bt, int32_t block_size,
+                          int32_t block_span, int32_t* slots, int64_t ld_slots) {
+  if (!slots) return fail(IDX_ERR_INVALID_ARG, "%s: NULL slots", fn);
+  if (!block_table) return fail(IDX_ERR_INVALID_ARG, "%s: NULL block_table", fn);
+  if (block_size < 1 || ld_bt < 1) return fail(IDX_ERR_INVALID_ARG, "%s: block_size and ld_bt must be positive", fn);
+  if (block_span < block_size) {
+    return fail(IDX_ERR_UNSUPPORTED, "%s: block_span %d < block_size %d", fn, block_span, block_size);
+  }
+  if (ld_slots < k) return fail(IDX_ERR_INVALID_ARG, "%s: ld_slots < k", fn);
+  p->slots = slots;
+  p->ld_slots = ld_slots;
+  p->row_to_req = row_to_req;
+  p->bt = block_table;
+  p->ld_bt = ld_bt;
+  p->block_size = block_size;
+  p->block_span = block_span;
   return IDX_OK;
 }
 
@@ -722,18 +784,18 @@ idx_status_t launch_topk(const TopkParams& p, int rows, int64_t max_cols, cudaSt
 
 }  // namespace
 
-extern "C" idx_status_t idx_topk(const void* logits, int dtype, int64_t ld, const int32_t* row_ks,
-                                 const int32_t* row_ke, int32_t rows, int32_t k, int32_t* out,
-                                 int64_t ld_out, float* vals, int64_t ld_vals, void* ws,
-                                 size_t ws_bytes, cudaStream_t stream) {
-  const char* fn = "idx_topk";
+namespace {
+
+idx_status_t topk_common(const char* fn, const void* logits, int dtype, int64_t ld,
+                         const int32_t* row_ks, const int32_t* row_ke, int32_t rows, int32_t k,
+                         int32_t* out, int64_t ld_out, float* vals, int64_t ld_vals, void* ws,
+                         size_t ws_bytes, TopkParams& p, cudaStream_t stream) {
   if (rows < 0 || k < 1) return fail(IDX_ERR_INVALID_ARG, "%s: rows < 0 or k < 1", fn);
   if (k > kMaxK) return fail(IDX_ERR_UNSUPPORTED, "%s: k %d exceeds %d", fn, k, kMaxK);
   if (ld_out < k || (vals && ld_vals < k)) return fail(IDX_ERR_INVALID_ARG, "%s: output stride < k", fn);
   if (dtype != IDX_F32 && dtype != IDX_BF16) return fail(IDX_ERR_UNSUPPORTED, "%s: dtype %d", fn, dtype);
   if (rows == 0) return IDX_OK;
   if (!logits || !row_ke || !out) return fail(IDX_ERR_INVALID_ARG, "%s: NULL pointer", fn);
-  TopkParams p{};
   idx_status_t st = attach_hist(fn, &p, rows, ws, ws_bytes);
   if (st != IDX_OK) return st;
   p.logits = logits;
@@ -749,20 +811,48 @@ extern "C" idx_status_t idx_topk(const void* logits, int dtype, int64_t ld, cons
                            : launch_topk<false, kPlain>(p, rows, ld, stream, fn);
 }
 
-extern "C" idx_status_t idx_sparse_topk_remap(const void* sparse_logits, int dtype, int64_t ld,
-                                              const int32_t* end, const int32_t* sparse_idx,
-                                              int64_t ld_si, const int32_t* row_ks, int32_t sbk,
-                                              int32_t rows, int32_t k, int32_t* col_scratch,
-                                              int64_t ld_col, int32_t* positions, int64_t ld_pos,
-                                              void* ws, size_t ws_bytes, cudaStream_t stream) {
-  const char* fn = "idx_sparse_topk_remap";
+}  // namespace
+
+extern "C" idx_status_t idx_topk(const void* logits, int dtype, int64_t ld, const int32_t* row_ks,
+                                 const int32_t* row_ke, int32_t rows, int32_t k, int32_t* out,
+                                 int64_t ld_out, float* vals, int64_t ld_vals, void* ws,
+                                 size_t ws_bytes, cudaStream_t stream) {
+  TopkParams p{};
+  return topk_common("idx_topk", logits, dtype, ld, row_ks, row_ke, rows, k, out, ld_out, vals,
+                     ld_vals, ws, ws_bytes, p, stream);
+}
+
+extern "C" idx_status_t idx_topk_slots(const void* logits, int dtype, int64_t ld,
+                                       const int32_t* row_ks, const int32_t* row_ke, int32_t rows,
+                                       int32_t k, int32_t* out, int64_t ld_out,
+                                       const int32_t* row_to_req, const int32_t* block_table,
+                                       int64_t ld_bt, int32_t block_size, int32_t block_span,
+                                       int32_t* slots, int64_t ld_slots, void* ws, size_t ws_bytes,
+                                       cudaStream_t stream) {
+  const char* fn = "idx_topk_slots";
+  TopkParams p{};
+  if (rows > 0) {
+    idx_status_t st = attach_slots(fn, &p, k, row_to_req, block_table, ld_bt, block_size, block_span,
+                                   slots, ld_slots);
+    if (st != IDX_OK) return st;
+  }
+  return topk_common(fn, logits, dtype, ld, row_ks, row_ke, rows, k, out, ld_out, nullptr, 0, ws,
+                     ws_bytes, p, stream);
+}
+
+namespace {
+
+idx_status_t remap_common(const char* fn, const void* sparse_logits, int dtype, int64_t ld,
+                          const int32_t* end, const int32_t* sparse_idx, int64_t ld_si,
+                          const int32_t* row_ks, int32_t sbk, int32_t rows, int32_t k,
+                          int32_t* col_scratch, int64_t ld_col, int32_t* positions, int64_t ld_pos,
+                          void* ws, size_t ws_bytes, TopkParams& p, cudaStream_t stream) {
   if (rows < 0 || k < 1 || sbk < 1) return fail(IDX_ERR_INVALID_ARG, "%s: rows < 0, k < 1 or sbk < 1", fn);
   if (k > kMaxK) return fail(IDX_ERR_UNSUPPORTED, "%s: k %d exceeds %d", fn, k, kMaxK);
   if (ld_pos < k || (col_scratch && ld_col < k)) return fail(IDX_ERR_INVALID_ARG, "%s: output stride < k", fn);
   if (dtype != IDX_F32 && dtype != IDX_BF16) return fail(IDX_ERR_UNSUPPORTED, "%s: dtype %d", fn, dtype);
   if (rows == 0) return IDX_OK;
   if (!sparse_logits || !end || !sparse_idx || !positions) return fail(IDX_ERR_INVALID_ARG, "%s: NULL pointer", fn);
-  TopkParams p{};
   idx_status_t st = attach_hist(fn, &p, rows, ws, ws_bytes);
   if (st != IDX_OK) return st;
   p.logits = sparse_logits;
@@ -779,6 +869,37 @@ extern "C" idx_status_t idx_sparse_topk_remap(const void* sparse_logits, int dty
   p.ld_cols = ld_col;
   return dtype == IDX_BF16 ? launch_topk<true, kRemap>(p, rows, ld, stream, fn)
                            : launch_topk<false, kRemap>(p, rows, ld, stream, fn);
+}
+
+}  // namespace
+
+extern "C" idx_status_t idx_sparse_topk_remap(const void* sparse_logits, int dtype, int64_t ld,
+                                              const int32_t* end, const int32_t* sparse_idx,
+                                              int64_t ld_si, const int32_t* row_ks, int32_t sbk,
+                                              int32_t rows, int32_t k, int32_t* col_scratch,
+                                              int64_t ld_col, int32_t* positions, int64_t ld_pos,
+                                              void* ws, size_t ws_bytes, cudaStream_t stream) {
+  TopkParams p{};
+  return remap_common("idx_sparse_topk_remap", sparse_logits, dtype, ld, end, sparse_idx, ld_si,
+                      row_ks, sbk, rows, k, col_scratch, ld_col, positions, ld_pos, ws, ws_bytes, p,
+                      stream);
+}
+
+extern "C" idx_status_t idx_sparse_topk_remap_slots(
+    const void* sparse_logits, int dtype, int64_t ld, const int32_t* end, const int32_t* sparse_idx,
+    int64_t ld_si, const int32_t* row_ks, int32_t sbk, int32_t rows, int32_t k, int32_t* col_scratch,
+    int64_t ld_col, int32_t* positions, int64_t ld_pos, const int32_t* row_to_req,
+    const int32_t* block_table, int64_t ld_bt, int32_t block_size, int32_t block_span,
+    int32_t* slots, int64_t ld_slots, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  const char* fn = "idx_sparse_topk_remap_slots";
+  TopkParams p{};
+  if (rows > 0) {
+    idx_status_t st = attach_slots(fn, &p, k, row_to_req, block_table, ld_bt, block_size, block_span,
+                                   slots, ld_slots);
+    if (st != IDX_OK) return st;
+  }
+  return remap_common(fn, sparse_logits, dtype, ld, end, sparse_idx, ld_si, row_ks, sbk, rows, k,
+                      col_scratch, ld_col, positions, ld_pos, ws, ws_bytes, p, stream);
 }
 
 extern "C" idx_status_t idx_dcp_topk_merge(const float* cand_vals, int64_t ld_v,

@@ -84,10 +84,11 @@ class DecodeStep:
         idx_paged_mqa_logits_decode(q, w, cache, self.block_size, block_table, ctx_lens, self.logits,
                                     next_n=self.next_n, ws=self.ws, stream=stream)
         ke = ctx_lens if (row_ke is None and self.next_n == 1) else row_ke
-        idx_topk(self.logits, None, ke, self.topk, self.local, ws=self.ws, stream=stream)
-        idx_req_to_global_slots(self.local, None if self.next_n == 1 else self._row_to_req(ctx_lens),
-                                block_table, self.block_size, self.block_span, self.slots,
-                                stream=stream)
+        # selection with the slot conversion fused into its output pass
+        idx_topk(self.logits, None, ke, self.topk, self.local, ws=self.ws, stream=stream,
+                 slots=self.slots, block_table=block_table, block_size=self.block_size,
+                 block_span=self.block_span,
+                 row_to_req=None if self.next_n == 1 else self._row_to_req(ctx_lens))
         return self.slots
 
     def _row_to_req(self, ctx_lens):
@@ -136,9 +137,9 @@ class HierarchicalStep:
                                     next_n=self.next_n, sparse_idx=self.sparse_idx, end=self.end,
                                     sbk=self.sbk, ws=self.ws, stream=stream)
         idx_sparse_topk_remap(self.logits, self.end, self.sparse_idx, None, self.sbk, self.topk,
-                              self.positions, col_scratch=self.cols, ws=self.ws, stream=stream)
-        idx_req_to_global_slots(self.positions, self.row_to_req, block_table, self.block_size,
-                                self.block_size, self.slots, stream=stream)
+                              self.positions, col_scratch=self.cols, ws=self.ws, stream=stream,
+                              slots=self.slots, block_table=block_table, block_size=self.block_size,
+                              block_span=self.block_size, row_to_req=self.row_to_req)
         return self.slots
 
     def run(self, q, w, cache, block_table, ctx_lens, cand, row_ke=None, stream=None):

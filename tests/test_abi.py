@@ -87,6 +87,14 @@ def test_validation_rejects_before_touching_the_device(lib):
     assert lib.idx_expand_candidates(fake, 64, 4, 48, None, fake, 64, 64, fake, 64, fake, None) == 2
     # block_span smaller than block_size
     assert lib.idx_req_to_global_slots(fake, 8, 1, 8, None, fake, 8, 64, 32, fake, 8, None) == 2
+    # fused slot conversion: the same checks (span, NULL slots, slot stride)
+    assert lib.idx_topk_slots(fake, 0, 4096, None, fake, 4, 2048, fake, 2048, None, fake, 8, 64, 32,
+                              fake, 2048, None, 0, None) == 2
+    assert lib.idx_topk_slots(fake, 0, 4096, None, fake, 4, 2048, fake, 2048, None, fake, 8, 64, 64,
+                              None, 2048, None, 0, None) == 1
+    assert lib.idx_sparse_topk_remap_slots(fake, 1, 4096, fake, fake, 64, None, 64, 4, 2048, None, 0,
+                                           fake, 2048, None, fake, 8, 64, 64, fake, 100, None, 0,
+                                           None) == 1
     # dense decode with next_n = 3
     assert lib.idx_paged_mqa_logits_decode(fake, 8192, fake, 0, 64, fake, 16, 64, 8704, fake, 8, fake,
                                            2, 3, None, 0, 0, None, 0, fake, 0, 4096, None, 0, None) == 2

@@ -174,6 +174,70 @@ def _hier_inputs(seed, block_size=64):
     return ctx, pool, g, o, q8, w, cand
 
 
+def _slots_closed_form(v, bt, req, block_size, block_span):
+    """Slot of request-local position v of a row of request req (-1 passes through)."""
+    if v < 0 or v // block_size >= bt.shape[1]:
+        return -1
+    return int(bt[req, v // block_size]) * block_span + v % block_size
+
+
+@pytest.mark.parametrize("with_ws", [False, True])
+def test_topk_with_fused_slots(with_ws):
+    # the fused conversion writes, for the same selection, exactly the slots of the
+    # closed form (a wider block span and an explicit, permuted row -> request map)
+    ctx, pool, g, o, q8, w, cand = _hier_inputs(83)
+    rows, k, span = len(ctx), 2048, 96
+    L = int(ctx.max())
+    logits = torch.empty((rows, (L + 63) // 64 * 64), dtype=torch.float32, device=DEV)
+    ws = torch.zeros((rows, 1024), dtype=torch.int32, device=DEV) if with_ws else None
+    bt = dev(pool.block_table)
+    idx.idx_paged_mqa_logits_decode(dev(q8), dev(w), g, 64, bt, dev(ctx), logits, ws=ws)
+    sel = torch.empty((rows, k), dtype=torch.int32, device=DEV)
+    slots = torch.full((rows, k + 2), -7, dtype=torch.int32, device=DEV)
+    r2q = np.arange(rows, dtype=np.int32)[::-1].copy()
+    # rows see the columns of their own request; the slots go through the mapped request's table
+    idx.idx_topk(logits, None, dev(ctx), k, sel, ws=ws, slots=slots[:, :k], block_table=bt, block_size=64,
+                 block_span=span, row_to_req=dev(r2q))
+    idx.idx_device_error()
+    sel, sl = sel.cpu().numpy(), slots.cpu().numpy()
+    lg = logits.cpu().numpy()
+    for r in range(rows):
+        assert_topk_values_exact(sel[r], lg[r, :ctx[r]], k, f"row {r}")
+        want = [_slots_closed_form(int(v), pool.block_table, int(r2q[r]), 64, span) for v in sel[r]]
+        assert sl[r, :k].tolist() == want, r
+        assert np.all(sl[r, k:] == -7)
+
+
+def test_sparse_remap_with_fused_slots():
+    ctx, pool, g, o, q8, w, cand = _hier_inputs(84)
+    rows, k, sbk = len(ctx), 256, 64
+    si = torch.empty((rows, 16), dtype=torch.int32, device=DEV)
+    end = torch.empty(rows, dtype=torch.int32, device=DEV)
+    idx.idx_expand_candidates(dev(cand), None, dev(ctx), 64, sbk, si, end)
+    bt = dev(pool.block_table)
+    out = torch.empty((rows, 16 * sbk), dtype=torch.bfloat16, device=DEV)
+    ws = torch.zeros((rows, 1024), dtype=torch.int32, device=DEV)
+    idx.idx_paged_mqa_logits_decode(dev(q8), dev(w), g, 64, bt, dev(ctx), out, sparse_idx=si, end=end,
+                                    sbk=sbk, ws=ws)
+    pos = torch.empty((rows, k), dtype=torch.int32, device=DEV)
+    cols = torch.empty((rows, k), dtype=torch.int32, device=DEV)
+    slots = torch.empty((rows, k), dtype=torch.int32, device=DEV)
+    idx.idx_sparse_topk_remap(out, end, si, None, sbk, k, pos, col_scratch=cols, ws=ws, slots=slots,
+                              block_table=bt, block_size=64, block_span=64)
+    # the two-call sequence on the same positions gives the same slots
+    ref = torch.empty((rows, k), dtype=torch.int32, device=DEV)
+    idx.idx_req_to_global_slots(pos, None, bt, 64, 64, ref)
+    idx.idx_device_error()
+    assert torch.equal(slots, ref)
+    pos, cols, sih = pos.cpu().numpy(), cols.cpu().numpy(), si.cpu().numpy()
+    e = end.cpu().numpy()
+    lg = out.float().cpu().numpy()
+    for r in range(rows):
+        m = min(k, int(e[r]))
+        assert_topk_values_exact(cols[r], lg[r, :e[r]], k, f"row {r}")
+        assert [O.sparse_column_token(sih[r], int(c), sbk) for c in cols[r, :m]] == pos[r, :m].tolist()
+
+
 @pytest.mark.parametrize("sbk,cbs,out_bf16", [(64, 64, True), (16, 64, True), (8, 16, False),
                                               (32, 64, False)])
 def test_decode_sparse_logits_and_remap(sbk, cbs, out_bf16):
