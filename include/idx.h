@@ -40,7 +40,7 @@
  * while they write the scores, so the selection does not read the scores twice:
  * pass the same device buffer of idx_workspace_bytes(op, rows, 0, 0) bytes
  * (1024 uint32 per row, 16-byte aligned) as `ws` to a logits call and then to
- * idx_topk / idx_sparse_topk_remap over the same rows and the same visible
+ * idx_topk / idx_sparse_topk_remap (or their _slots forms) over the same rows and the same visible
  * columns (decode with next_n = 1: columns [0, ctx_len); sparse modes: [0, end)).
  * The buffer must be all zero before the logits call (clear it once after
  * allocating it); the selection zeroes every row it consumes, so the buffer is
