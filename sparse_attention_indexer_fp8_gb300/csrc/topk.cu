@@ -755,6 +755,9 @@ template <bool kBf16, int kMode, int kThreads>
 idx_status_t launch_topk_cfg(TopkParams p, int rows, int sms, cudaStream_t stream, const char* fn) {
   auto kern = topk_kernel<kBf16, kMode, kThreads>;
   constexpr int smem = TopkCfg<kThreads>::kSmemDyn;
+  // 1024 / kThreads blocks per SM: 228 KB of shared memory per SM, 1 KB reserved per block
+  static_assert((smem + sizeof(Shared) + 1024) * (1024 / kThreads) <= 233472, "blocks per SM");
+  static_assert(smem + sizeof(Shared) <= 232448, "shared memory per block");
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
