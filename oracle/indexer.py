@@ -528,13 +528,22 @@ def sparse_topk_remap_row(values, end: int, si_row, ks: int, sbk: int, k: int):
     Returns (cols int64 [k], positions int64 [k]).
     """
     cols = topk_row(values, 0, end, k)
-    pos = np.full(k, -1, dtype=np.int64)
+    return cols, sparse_remap_columns(cols, si_row, ks, sbk)
+
+
+def sparse_remap_columns(cols, si_row, ks: int, sbk: int) -> np.ndarray:
+    """The remap step alone: sparse column ``c`` -> ``(si[c // sbk] - ks // sbk) * sbk + c % sbk``.
+
+    [V41] 实现拆解 item 3 (the remap kernel after the sparse top-k); ``-1`` stays ``-1``.
+    """
+    cols = np.asarray(cols, dtype=np.int64)
+    pos = np.full(cols.shape, -1, dtype=np.int64)
     base = ks // sbk
     for i, c in enumerate(cols):
         if c < 0:
             continue
         pos[i] = (int(si_row[c // sbk]) - base) * sbk + int(c) % sbk
-    return cols, pos
+    return pos
 
 
 def dense_masked_topk_row(sparse_values, end: int, si_row, ks: int, ke: int, sbk: int, k: int):

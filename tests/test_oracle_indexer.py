@@ -583,3 +583,89 @@ def test_sparse_topk_equals_dense_masked_topk():
             assert set(pos[:m].tolist()) == set(ref[:m].tolist())
             for c, p in zip(cols[:m], pos[:m]):
                 assert O.sparse_column_token(si[r], int(c), 64) == p
+
+
+def test_sparse_remap_golden_with_ks():
+    # hand-worked rows whose request starts at ks = 2 SBK and 3 SBK ([V41] 实现拆解 item 3, rows metadata)
+    with open(os.path.join(GOLDEN, "sparse_remap.json")) as f:
+        spec = json.load(f)
+    for c in spec["cases"]:
+        si, end = O.expand_candidates_row(c["cand"], c["ks"], c["ke"], c["cand_block_size"], c["sbk"])
+        assert list(si) == c["sparse_idx"] and end == c["end"], c["note"]
+        vals = np.zeros(len(si) * c["sbk"])
+        for col, v in c["scores"].items():
+            vals[int(col)] = v
+        cols, pos = O.sparse_topk_remap_row(vals, end, si, c["ks"], c["sbk"], c["k"])
+        assert list(cols) == c["cols"], c["note"]
+        assert list(pos) == c["positions"], c["note"]
+
+
+def test_sparse_logits_prefill_one_hot_closed_form():
+    # one live head / dim / token: the only finite non-zero column is the one that maps onto the token
+    sbk, S = 8, 64
+    q8 = np.zeros((1, 64, 128), dtype=np.uint8)
+    w = np.zeros((1, 64), dtype=np.float32)
+    k8 = np.zeros((S, 128), dtype=np.uint8)
+    ks = np.ones(S, dtype=np.float32)
+    q8[0, 9, 17] = e4m3_encode(3.0)[()]
+    w[0, 9] = 0.5
+    k8[43, 17] = e4m3_encode(-1.5)[()]
+    ks[43] = 0.25
+    si = np.array([[5, 2, 6, 6]])         # sparse blocks of 8 tokens: column 3 -> token 43
+    out = O.sparse_logits_prefill(q8, w, k8, ks, si, np.array([20]), sbk)
+    want = np.full(32, -np.inf)
+    want[:20] = 0.0
+    want[3] = 0.5 * 3.0 * -1.5 * 0.25
+    assert np.array_equal(out[0], want)
+    # the same token through another column: block 5 at column 11 when listed second
+    out = O.sparse_logits_prefill(q8, w, k8, ks, np.array([[2, 5, 6, 6]]), np.array([32]), sbk)
+    assert out[0, 11] == want[3] and np.count_nonzero(out[0]) == 1
+
+
+def test_sparse_logits_prefill_equal_dense_at_mapped_positions():
+    # rows of a prefill chunk whose requests start at ks > 0: every valid sparse column equals the
+    # dense prefill logit of its absolute token; columns past end are -inf
+    rng = np.random.default_rng(8)
+    S, T = 700, 6
+    k = rng.standard_normal((S, 128)).astype(np.float32)
+    k8, kscale = O.k_quant(k)
+    q8, w = W.make_q(8, T)
+    for sbk, cbs in ((64, 64), (16, 64), (8, 32)):
+        row_ks = np.array([0, sbk, 3 * sbk, 128, 2 * sbk, 5 * sbk])
+        row_ke = np.array([700, 650, 400, 300, 2 * sbk + 1, 700])
+        cand = rng.integers(-1, 12, (T, 8))
+        si, end = O.expand_candidates(cand, row_ks, row_ke, cbs, sbk)
+        sp = O.sparse_logits_prefill(q8, w, k8, kscale, si, end, sbk)
+        dense = O.mqa_logits(q8, w, k8, kscale, row_ks, row_ke)
+        assert np.count_nonzero(end) >= T // 2
+        for r in range(T):
+            for c in range(sp.shape[1]):
+                if c < end[r]:
+                    tok = O.sparse_column_token(si[r], c, sbk)
+                    assert row_ks[r] <= tok < row_ke[r]
+                    assert sp[r, c] == dense[r, tok]
+                else:
+                    assert sp[r, c] == -np.inf
+
+
+def test_sparse_topk_equals_dense_masked_topk_with_ks():
+    # prefill rows with ks > 0: the remapped selection equals the dense-masked selection over [ks, ke)
+    rng = np.random.default_rng(9)
+    S, T = 900, 4
+    k = rng.standard_normal((S, 128)).astype(np.float32)
+    k8, kscale = O.k_quant(k)
+    q8, w = W.make_q(9, T)
+    row_ks = np.array([64, 192, 320, 128])
+    row_ke = np.array([900, 700, 899, 129])
+    cand = rng.integers(-1, 14, (T, 8))
+    si, end = O.expand_candidates(cand, row_ks, row_ke, 64, 64)
+    sp = O.sparse_logits_prefill(q8, w, k8, kscale, si, end, 64)
+    for kk in (16, 100, 600):
+        for r in range(T):
+            cols, pos = O.sparse_topk_remap_row(sp[r], int(end[r]), si[r], int(row_ks[r]), 64, kk)
+            ref = O.dense_masked_topk_row(sp[r], int(end[r]), si[r], int(row_ks[r]), int(row_ke[r]), 64, kk)
+            m = min(kk, int(end[r]))
+            assert np.all(pos[m:] == -1) and np.all(ref[m:] == -1)
+            assert set(pos[:m].tolist()) == set(ref[:m].tolist())
+            for c, p in zip(cols[:m], pos[:m]):
+                assert O.sparse_column_token(si[r], int(c), 64) - row_ks[r] == p
