@@ -15,7 +15,7 @@ import sparse_attention_indexer_fp8_gb300 as idx
 from oracle import indexer as O
 from oracle.codecs import bf16_decode, bf16_encode, e4m3_decode
 from sparse_attention_indexer_fp8_gb300 import workloads as W
-from tests.checks import BF16_REL, assert_logits_close, assert_topk_row, assert_topk_values_exact
+from tests.checks import assert_logits_close, assert_topk_row, assert_topk_values_exact
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -161,7 +161,7 @@ def test_decode_dense_logits(next_n, block_size, out_bf16, w_bf16):
     got = out.float().cpu().numpy()
     for r in range(rows):
         L = int(ctx[r // next_n])
-        assert_logits_close(got[r, :L], ref[r, :L], f"row {r}", BF16_REL if out_bf16 else 0.0)
+        assert_logits_close(got[r, :L], ref[r, :L], f"row {r}", bf16=out_bf16)
         assert np.all(got[r, L:] == 7.0), "columns beyond the context must stay untouched"
 
 
@@ -255,7 +255,7 @@ def test_decode_sparse_logits_and_remap(sbk, cbs, out_bf16):
                                     sparse_idx=si, end=end, sbk=sbk)
     ref = O.sparse_logits_decode(q8, w, o, 64, pool.block_table, None, osi, oend, sbk)
     got = out.float().cpu().numpy()
-    assert_logits_close(got, ref, "sparse logits", BF16_REL if out_bf16 else 0.0)
+    assert_logits_close(got, ref, "sparse logits", bf16=out_bf16)
     # selection + remap on the kernel's own sparse scores
     k = 300
     pos = torch.empty((rows, k), dtype=torch.int32, device=DEV)
@@ -270,7 +270,7 @@ def test_decode_sparse_logits_and_remap(sbk, cbs, out_bf16):
             assert O.sparse_column_token(osi[r], int(c), sbk) == p_
         assert np.all(pos[r, m:] == -1)
         assert_topk_row(cols[r], ref[r, :e], k, f"sparse top-k vs oracle row {r}",
-                        BF16_REL if out_bf16 else 0.0)
+                        bf16=out_bf16)
 
 
 @pytest.mark.parametrize("next_n", [2, 3])
@@ -302,12 +302,12 @@ def test_hierarchical_mtp_rows_and_layer_reuse(next_n):
         assert torch.equal(st.sparse_idx, si0) and torch.equal(st.end, end0), "expansion must be reusable"
         ref = O.sparse_logits_decode(q8, w, o, 64, pool.block_table, r2r, osi, oend, 64)
         got = st.logits.float().cpu().numpy()
-        assert_logits_close(got, ref, f"layer {layer} sparse logits", BF16_REL)
+        assert_logits_close(got, ref, f"layer {layer} sparse logits", bf16=True)
         cols, pos = st.cols.cpu().numpy(), st.positions.cpu().numpy()
         for r in range(rows):
             e = int(oend[r])
             assert_topk_values_exact(cols[r], got[r, :e], k, f"layer {layer} row {r}")
-            assert_topk_row(cols[r], ref[r, :e], k, f"layer {layer} row {r} vs oracle", BF16_REL)
+            assert_topk_row(cols[r], ref[r, :e], k, f"layer {layer} row {r} vs oracle", bf16=True)
             m = min(k, e)
             want = [O.sparse_column_token(osi[r], int(c), 64) for c in cols[r, :m]]
             assert pos[r, :m].tolist() == want and np.all(pos[r, m:] == -1)
@@ -337,7 +337,7 @@ def test_prefill_dense_logits(T, w_bf16, out_bf16, ragged):
     wv = bf16_decode(w) if w_bf16 else w
     ref = O.mqa_logits(q8, wv, k8, kscale, ks, ke)
     assert_logits_close(out.float().cpu().numpy()[:, :S], ref, "prefill logits",
-                        BF16_REL if out_bf16 else 0.0)
+                        bf16=out_bf16)
 
 
 def test_prefill_sparse_logits():
@@ -367,10 +367,12 @@ def test_prefill_sparse_logits():
         e = int(oend[r])
         # the chosen sparse columns against the oracle's sparse scores (tie-tolerant) ...
         assert_topk_row(cols[r], ref[r, :e], k, f"sparse prefill top-k row {r}")
-        # ... and each position is its column's token, relative to the row start
+        # ... and each position is the oracle's remap of its column (ks > 0 rows included)
         m = min(k, e)
-        expect = [O.sparse_column_token(osi[r], int(c), sbk) - int(ks[r]) for c in cols[r, :m]]
-        assert pos[r, :m].tolist() == expect and np.all(pos[r, m:] == -1)
+        expect = O.sparse_remap_columns(cols[r, :m], osi[r], int(ks[r]), sbk)
+        assert np.array_equal(pos[r, :m], expect) and np.all(pos[r, m:] == -1)
+        assert np.all(pos[r, :m] == np.array([O.sparse_column_token(osi[r], int(c), sbk) for c in cols[r, :m]],
+                                             dtype=np.int64) - int(ks[r]))
 
 
 # ------------------------------------------------------------------ a5 top-k
