@@ -76,6 +76,23 @@ def profiled_traffic(profile: str, kernel_src: str):
         return None
 
 
+def hbm_roofline(kernel: str, alg_bytes: int, out_bytes: int, kernel_ms: float, peaks, peak_kind: str,
+                 traffic=None, **extra):
+    """Roofline of an HBM-bound scoring launch.
+
+    ``frac`` counts the bytes the method has to read (the k cache records, q and
+    the weights); the score write, which a fused selection would not need, is
+    reported beside it (``output_bytes_per_launch``, ``frac_incl_output``).
+    """
+    sec = kernel_ms / 1e3
+    ach = alg_bytes / sec / 1e9
+    return {"kernel": kernel, "bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4), "peak_source": peak_kind,
+            "algorithmic_bytes_per_launch": int(alg_bytes), "output_bytes_per_launch": int(out_bytes),
+            "frac_incl_output": round((alg_bytes + out_bytes) / sec / 1e9 / peaks["hbm_gbs"], 4),
+            "traffic": traffic, "kernel_ms": round(kernel_ms, 5), **extra}
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle-reason samples taken while the GPU works."""
 
@@ -362,14 +379,10 @@ class DecodeBench:
 
     def roofline(self, kernel_ms, step_ms, peaks, peak_kind):
         tok = int(self.L.sum())
-        byt = tok * (W.TOKEN_BYTES + 4) + self.B * (64 * 128 + 64 * 4)
-        ach = byt / (kernel_ms / 1e3) / 1e9
-        return {"kernel": "mqa_logits_kernel<1> (paged decode)", "bound": "hbm", "achieved": round(ach, 1),
-                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4),
-                "peak_source": peak_kind, "algorithmic_bytes_per_launch": byt,
-                "traffic": profiled_traffic(f"mqa_logits_decode_{self.name}.md", "logits.cu"),
-                "kernel_ms": round(kernel_ms, 5),
-                "step_kcache_frac": round(tok * W.TOKEN_BYTES / (step_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4)}
+        return hbm_roofline("mqa_logits_kernel<1> (paged decode)", tok * W.TOKEN_BYTES + self.B * (64 * 128 + 64 * 4),
+                            tok * 4, kernel_ms, peaks, peak_kind,
+                            traffic=profiled_traffic(f"mqa_logits_decode_{self.name}.md", "logits.cu"),
+                            step_kcache_frac=round(tok * W.TOKEN_BYTES / (step_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4))
 
     def config(self, world):
         L, pool = self.L, self.wl.pool
@@ -538,7 +551,7 @@ class HierBench:
 
     def verify_and_time_oracle(self, n_rows):
         from oracle import indexer as O
-        from tests.checks import BF16_REL, assert_logits_close, assert_topk_row
+        from tests.checks import assert_logits_close, assert_topk_row
 
         wl, st = self.wl, self.st
         g_si, g_end = st.sparse_idx.cpu().numpy(), st.end.cpu().numpy()
@@ -555,9 +568,9 @@ class HierBench:
         for b in sample:
             lg, _, _ = ref[b]
             e = int(o_end[b])
-            assert_logits_close(g_lg[b, :e], lg, f"bench sparse logits row {b}", BF16_REL)
+            assert_logits_close(g_lg[b, :e], lg, f"bench sparse logits row {b}", bf16=True)
             assert np.all(np.isneginf(g_lg[b, e:])), f"bench sparse mask row {b}"
-            assert_topk_row(g_cols[b], lg, wl.topk, f"bench sparse top-k row {b}", BF16_REL)
+            assert_topk_row(g_cols[b], lg, wl.topk, f"bench sparse top-k row {b}", bf16=True)
             m = min(wl.topk, e)
             want = [O.sparse_column_token(o_si[b], int(c), wl.sbk) for c in g_cols[b, :m]]
             assert g_pos[b, :m].tolist() == want and np.all(g_pos[b, m:] == -1), f"bench remap row {b}"
@@ -574,12 +587,8 @@ class HierBench:
         if end_sum is None:
             end_sum = int(self.st.end.sum().item())
         ncols = self.st.logits.shape[1]
-        byt = end_sum * W.TOKEN_BYTES + self.B * (64 * 128 + 64 * 4 + ncols * 2)
-        ach = byt / (kernel_ms / 1e3) / 1e9
-        return {"kernel": "mqa_logits_kernel<1> (sparse decode, bf16 out)", "bound": "hbm",
-                "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(ach / peaks["hbm_gbs"], 4), "peak_source": peak_kind,
-                "algorithmic_bytes_per_launch": byt, "traffic": None, "kernel_ms": round(kernel_ms, 5)}
+        return hbm_roofline("mqa_logits_kernel<1> (sparse decode, bf16 out)", end_sum * W.TOKEN_BYTES + self.B * (64 * 128 + 64 * 4),
+                            self.B * ncols * 2, kernel_ms, peaks, peak_kind)
 
     def config(self, world):
         return {"workload": self.wl.name, "batch": self.B, "ctx": int(self.wl.pool.ctx_lens[0]),
@@ -680,7 +689,7 @@ class HierMtpBench:
 
     def verify_and_time_oracle(self, n_rows):
         from oracle import indexer as O
-        from tests.checks import BF16_REL, assert_logits_close, assert_topk_row
+        from tests.checks import assert_logits_close, assert_topk_row
 
         wl, st, nn = self.wl, self.st, self.next_n
         g_si, g_end = st.sparse_idx.cpu().numpy(), st.end.cpu().numpy()
@@ -708,8 +717,8 @@ class HierMtpBench:
         for r in sample:
             lg, _ = ref[r]
             e = int(o_end[r])
-            assert_logits_close(g_lg[r, :e], lg, f"bench mtp sparse logits row {r}", BF16_REL)
-            assert_topk_row(g_cols[r], lg, wl.topk, f"bench mtp top-k row {r}", BF16_REL)
+            assert_logits_close(g_lg[r, :e], lg, f"bench mtp sparse logits row {r}", bf16=True)
+            assert_topk_row(g_cols[r], lg, wl.topk, f"bench mtp top-k row {r}", bf16=True)
             m = min(wl.topk, e)
             want = [O.sparse_column_token(o_si[r], int(c), wl.sbk) for c in g_cols[r, :m]]
             assert g_pos[r, :m].tolist() == want and np.all(g_pos[r, m:] == -1), f"bench mtp remap row {r}"
@@ -726,12 +735,8 @@ class HierMtpBench:
         if end_sum is None:
             end_sum = int(self.st.end.sum().item())
         ncols = self.st.logits.shape[1]
-        byt = end_sum * W.TOKEN_BYTES + self.rows * (64 * 128 + 64 * 4 + ncols * 2)
-        ach = byt / (kernel_ms / 1e3) / 1e9
-        return {"kernel": "mqa_logits_kernel<1> (sparse decode, bf16 out, one layer)", "bound": "hbm",
-                "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(ach / peaks["hbm_gbs"], 4), "peak_source": peak_kind,
-                "algorithmic_bytes_per_launch": byt, "traffic": None, "kernel_ms": round(kernel_ms, 5)}
+        return hbm_roofline("mqa_logits_kernel<1> (sparse decode, bf16 out, one layer)", end_sum * W.TOKEN_BYTES + self.rows * (64 * 128 + 64 * 4),
+                            self.rows * ncols * 2, kernel_ms, peaks, peak_kind)
 
     def config(self, world):
         return {"workload": self.wl.name, "batch": self.B, "next_n": self.next_n, "query_rows": self.rows,
@@ -833,12 +838,9 @@ class DcpBench:
 
     def roofline(self, kernel_ms, step_ms, peaks, peak_kind):
         lens = self.shards[0]["h_lens"].astype(np.int64)
-        byt = int(lens.sum()) * 136 + self.B * (8192 + 256)
-        ach = byt / (kernel_ms / 1e3) / 1e9
-        return {"kernel": "mqa_logits_kernel<1> (rank 0's quarter of every context)", "bound": "hbm",
-                "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(ach / peaks["hbm_gbs"], 4), "peak_source": peak_kind,
-                "algorithmic_bytes_per_launch": byt, "traffic": None, "kernel_ms": round(kernel_ms, 5)}
+        tok = int(lens.sum())
+        return hbm_roofline("mqa_logits_kernel<1> (rank 0's quarter of every context)",
+                            tok * W.TOKEN_BYTES + self.B * (8192 + 256), tok * 4, kernel_ms, peaks, peak_kind)
 
     def config(self, world):
         return {"workload": self.wl.name + "-dcp4", "batch": self.B, "ranks_emulated": self.world,
