@@ -443,14 +443,17 @@ idx_status_t idx_sparse_topk_remap_slots(const void* sparse_logits, int dtype, i
  * indices (-1 filled) to `out` [B, ld_out]; the other arguments are as for
  * idx_paged_mqa_logits_decode.
  *
- * The first call on a device looks up the scratch array's device address (a
- * runtime query, no allocation); make that first call before any stream
- * capture. Every call clears the scratch rows it uses before scoring. All
- * calls on a device share the one array, so calls whose work overlaps on the
- * GPU (other streams, other host threads) race on it and must be serialised
- * by the caller.
- * Errors: IDX_ERR_UNSUPPORTED when B > IDX_NOALLOC_MAX_ROWS; otherwise those of
- * the two entry points it runs.
+ * Every call asks the runtime for the scratch array's device address on the
+ * current device (a host-side query, no allocation; asked anew each time, so
+ * a context destroyed and re-created, e.g. by cudaDeviceReset, is followed
+ * correctly). The first call on a device is also where the runtime sets the
+ * array up there: make that first call before any stream capture. Every call
+ * clears the scratch rows it uses before scoring. All calls on a device share
+ * the one array, so calls whose work overlaps on the GPU (other streams, other
+ * host threads) race on it and must be serialised by the caller.
+ * Errors: IDX_ERR_UNSUPPORTED when B > IDX_NOALLOC_MAX_ROWS or k > 4096;
+ * IDX_ERR_INVALID_ARG for k < 1, ld_out < k or NULL out / logits, all checked
+ * before any work is enqueued; otherwise those of the two entry points it runs.
  */
 #define IDX_NOALLOC_MAX_ROWS 1024
 idx_status_t idx_paged_mqa_topk_decode_noalloc(const uint8_t* q, int64_t ld_q, const void* w,

@@ -6,8 +6,6 @@
 // is part of the library image: it exists on every device that loads the
 // library, for as long as the library stays loaded, and it is never allocated
 // or freed by a call.
-#include <mutex>
-
 #include "common.cuh"
 
 namespace idx {
@@ -21,29 +19,20 @@ constexpr int kHistWordsPerRow = 1024;  // first-digit bins of the selection
 // contents from an earlier (possibly failed) call are never read.
 static __device__ __align__(256) uint32_t g_noalloc_hist[kNoAllocMaxRows * kHistWordsPerRow];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_setup_mutex;
-uint32_t* g_hist_ptr[kMaxDevices] = {nullptr};
-
-// Device address of the scratch array for the current device. In host code the
+// Device address of the scratch array on the current device. In host code the
 // array's name only stands in for the symbol; the address the kernels need is
-// looked up once per device, with that device current.
+// asked of the runtime with the device current. It is asked on every call, not
+// cached: a context torn down and created again (cudaDeviceReset) places the
+// array at a new address, and the query is a host-side lookup that allocates
+// nothing.
 idx_status_t scratch_for_current_device(const char* fn, uint32_t** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return fail(IDX_ERR_CUDA, "%s: cudaGetDevice: %s", fn, cudaGetErrorString(e));
-  if (dev < 0 || dev >= kMaxDevices) return fail(IDX_ERR_UNSUPPORTED, "%s: device ordinal %d", fn, dev);
-  std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (!g_hist_ptr[dev]) {
-    void* ptr = nullptr;
-    e = cudaGetSymbolAddress(&ptr, g_noalloc_hist);
-    if (e != cudaSuccess || !ptr) {
-      return fail(IDX_ERR_CUDA, "%s: cudaGetSymbolAddress of the scratch array: %s", fn,
-                  cudaGetErrorString(e));
-    }
-    g_hist_ptr[dev] = static_cast<uint32_t*>(ptr);
+  void* ptr = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_hist);
+  if (e != cudaSuccess || !ptr) {
+    return fail(IDX_ERR_CUDA, "%s: cudaGetSymbolAddress of the scratch array: %s", fn,
+                cudaGetErrorString(e));
   }
-  *out = g_hist_ptr[dev];
+  *out = static_cast<uint32_t*>(ptr);
   return IDX_OK;
 }
 
@@ -65,7 +54,14 @@ extern "C" idx_status_t idx_paged_mqa_topk_decode_noalloc(
                 "idx_paged_mqa_logits_decode + idx_topk with a caller workspace instead",
                 fn, B, kNoAllocMaxRows);
   }
+  // the selection's own checks, made before any work is enqueued so that a bad
+  // k or output never leaves a call half done (scores written, no selection)
+  if (k < 1 || k > 4096) {
+    return fail(k < 1 ? IDX_ERR_INVALID_ARG : IDX_ERR_UNSUPPORTED, "%s: k %d outside [1, 4096]", fn, k);
+  }
+  if (ld_out < k) return fail(IDX_ERR_INVALID_ARG, "%s: ld_out < k", fn);
   if (B == 0) return IDX_OK;
+  if (!out || !logits) return fail(IDX_ERR_INVALID_ARG, "%s: NULL out or logits", fn);
   uint32_t* hist = nullptr;
   idx_status_t st = scratch_for_current_device(fn, &hist);
   if (st != IDX_OK) return st;
