@@ -99,3 +99,68 @@ def bf16_encode(x) -> np.ndarray:
     nan_bits = (upper & 0x8000) | 0x7FC0
     out = np.where(np.isnan(f), nan_bits, out)
     return out.astype(np.uint16)
+
+
+# ----------------------------------------------------------------------------
+# OCP Microscaling (MX) formats: FP4 E2M1 elements and E8M0 shared scales
+# ----------------------------------------------------------------------------
+#
+# The V4.1 review names an MXFP4 indexer cache ("功能与动机"; the
+# indexer_kv_dtype "mxfp4" switch of "风险与影响") without printing the format;
+# MXFP4 is the OCP Microscaling format with FP4 E2M1 elements. For a 4-bit code
+# ``s ee m``: ``ee == 0`` is subnormal, value ``(-1)^s * 0.5 * m``; otherwise
+# ``(-1)^s * 2^(ee - 1) * (1 + m/2)``. The eight magnitudes are 0, 0.5, 1, 1.5, 2,
+# 3, 4, 6; there is no infinity or NaN. E8M0 is an unsigned exponent: code c is
+# ``2^(c - 127)``, code 255 is NaN.
+
+E2M1_MAX = 6.0
+
+
+def _e2m1_value(code: int) -> float:
+    sign = (code >> 3) & 1
+    exp = (code >> 1) & 0x3
+    man = code & 0x1
+    mag = 0.5 * man if exp == 0 else 2.0 ** (exp - 1) * (1.0 + man / 2.0)
+    return -mag if sign else mag
+
+
+#: value of every 4-bit code 0..15 as fp64
+E2M1_TABLE = np.array([_e2m1_value(c) for c in range(16)], dtype=np.float64)
+
+
+def e2m1_decode(codes) -> np.ndarray:
+    """4-bit e2m1 codes (any integer array; the low nibble is used) -> fp64 values."""
+    return E2M1_TABLE[np.asarray(codes, dtype=np.int64) & 0xF]
+
+
+def e2m1_encode(x) -> np.ndarray:
+    """Values -> e2m1 codes, round to nearest with ties to the even code, saturating to +-6.
+
+    From the field layout: magnitudes below 1 are subnormal, multiples of 0.5
+    rounded half-to-even (0.25 -> 0, 0.75 -> 1.0 whose mantissa bit is even);
+    otherwise ``|x| = 2^e (1 + f)`` with the 1-bit mantissa ``2 f`` rounded
+    half-to-even (a carry bumps the exponent). Magnitudes of 6 and above
+    saturate to 6 (code 0b0111). The sign bit is copied. NaN is not accepted.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    if np.isnan(x).any():
+        raise ValueError("e2m1 has no NaN")
+    mag = np.minimum(np.abs(x), E2M1_MAX)
+    sub = mag < 1.0
+    m_sub = np.rint(mag * 2.0)                   # 0, 1 or 2 (2 = the smallest normal, 1.0)
+    code_sub = np.where(m_sub == 2.0, 0b010, m_sub.astype(np.int64))
+    frac, exp2 = np.frexp(np.where(sub, 1.0, mag))   # mag = frac * 2^exp2, frac in [0.5, 1)
+    e = exp2 - 1                                  # 0, 1 or 2
+    man = np.rint((2.0 * frac - 1.0) * 2.0)       # 0, 1 or 2 (carry)
+    carry = man == 2.0
+    e = np.where(carry, e + 1, e)
+    man = np.where(carry, 0.0, man)
+    code_norm = ((e + 1) << 1) + man.astype(np.int64)
+    code = np.where(sub, code_sub, np.minimum(code_norm, 0b0111))
+    return (code | (np.signbit(x).astype(np.int64) << 3)).astype(np.uint8)
+
+
+def e8m0_decode(codes) -> np.ndarray:
+    """E8M0 scale codes -> fp64 values ``2^(c - 127)``; 255 -> NaN."""
+    c = np.asarray(codes, dtype=np.int64) & 0xFF
+    return np.where(c == 255, np.nan, np.ldexp(1.0, c - 127))

@@ -21,7 +21,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from .codecs import E4M3_MAX, e4m3_decode, e4m3_encode
+from .codecs import E4M3_MAX, e2m1_decode, e2m1_encode, e4m3_decode, e4m3_encode, e8m0_decode
 
 H = 64
 D = 128
@@ -189,6 +189,17 @@ def _dequant_k(k8, kscale) -> np.ndarray:
     return e4m3_decode(k8) * np.asarray(kscale, dtype=np.float64)[:, None]
 
 
+def logits_row_values(q8_row, w_row, k) -> np.ndarray:
+    """Scores of one query row against k given as fp64 values ``[S, 128]``.
+
+    [DSA] step ⑥: ``sum_h weights[h] * (q[h] . k[s])``, q as raw e4m3 values
+    (step ④ folds every q-side coefficient into the weights).
+    """
+    q = e4m3_decode(q8_row)                       # [64, 128]
+    per_head = q @ np.asarray(k, dtype=np.float64).T    # [64, S]: q[t,h] . k[s]
+    return np.asarray(w_row, dtype=np.float64) @ per_head
+
+
 def logits_row(q8_row, w_row, k8, kscale) -> np.ndarray:
     """Scores of one query row against tokens ``k8``/``kscale`` (fp64).
 
@@ -199,11 +210,7 @@ def logits_row(q8_row, w_row, k8, kscale) -> np.ndarray:
 
     q8_row [64, 128] uint8, w_row [64] values, k8 [S, 128] uint8, kscale [S].
     """
-    q = e4m3_decode(q8_row)                       # [64, 128]
-    k = _dequant_k(k8, kscale)                    # [S, 128]
-    per_head = q @ k.T                            # [64, S]: q[t,h] . k[s]
-    w = np.asarray(w_row, dtype=np.float64)
-    return w @ per_head                           # sum_h w[h] * (q[h] . k[s])
+    return logits_row_values(q8_row, w_row, _dequant_k(k8, kscale))
 
 
 def mqa_logits(q8, w, k8, kscale, row_ks, row_ke) -> np.ndarray:
@@ -563,4 +570,145 @@ def dense_masked_topk_row(sparse_values, end: int, si_row, ks: int, ke: int, sbk
     keep = [int(i) for i in sel if i >= 0 and np.isfinite(dense[ks + int(i)])]
     out = np.full(k, -1, dtype=np.int64)
     out[:len(keep)] = keep
+    return out
+
+
+# ----------------------------------------------------------------------------
+# f2: the MXFP4 indexer cache (V4.1 path)
+# ----------------------------------------------------------------------------
+#
+# [V41] 功能与动机 / 实现拆解 items 1-2 and 风险与影响: the V4.1 consumer layers
+# read an MXFP4 indexer cache (indexer_kv_dtype "mxfp4") through an
+# fp8 x fp4 sparse MQA-logits kernel. The pages print neither the layout nor
+# the quantiser. Readings used here (and by the library):
+#
+# * the format is OCP MXFP4: the 128 dims of a token form four blocks of 32
+#   consecutive elements; each element is FP4 E2M1 and each block shares one
+#   E8M0 scale, so a token is 64 bytes of elements plus 4 scale bytes = 68 bytes;
+# * quantisation follows the OCP MX conversion: per block, shared exponent
+#   ``floor(log2(amax)) - 2`` (2 = the largest E2M1 exponent), clamped to the
+#   E8M0 range [-127, 127] (an all-zero block gets -127), elements
+#   ``e2m1(V / 2^shared)`` rounded to nearest even and saturated to +-6;
+# * split block layout: block ``b`` at ``b * block_stride``; token ``i`` keeps its
+#   64 element bytes at ``i * 64`` (dim ``d`` in byte ``d // 2``, even ``d`` in the
+#   low nibble) and its four scale codes at ``block_size * 64 + 4 * i`` (byte ``j``
+#   scales dims ``32 j .. 32 j + 31``);
+# * q stays FP8 e4m3 with its scale folded into the weights ([DSA] step ④), so
+#   a score is ``sum_h w[h] * sum_d q8[h, d] * e2m1(k[d]) * 2^(E[d // 32] - 127)``
+#   with no per-token fp32 factor.
+
+MX_BLOCK = 32
+MXFP4_TOKEN_BYTES = D // 2 + D // MX_BLOCK     # 64 + 4 = 68
+
+
+def mxfp4_quant(k) -> tuple[np.ndarray, np.ndarray]:
+    """OCP MX conversion of k to MXFP4, one shared scale per 32 dims.
+
+    k: [n, 128] fp32 values (bf16 inputs widened exactly).
+    Returns (codes uint8 [n, 128], one e2m1 code per dim; scales uint8 [n, 4], E8M0 codes).
+    Every step is exact in fp64: ``frexp`` gives ``floor(log2(amax))`` and the
+    division is by a power of two.
+    """
+    k = np.asarray(k, dtype=np.float64).reshape(-1, D)
+    n = k.shape[0]
+    blocks = k.reshape(n, D // MX_BLOCK, MX_BLOCK)
+    amax = np.max(np.abs(blocks), axis=2)                       # [n, 4]
+    _, e = np.frexp(amax)                                       # amax = m 2^e, m in [0.5, 1): floor(log2) = e - 1
+    shared = np.where(amax > 0, e - 1 - 2, -127)
+    shared = np.clip(shared, -127, 127)
+    q = blocks / np.ldexp(1.0, shared)[:, :, None]
+    codes = e2m1_encode(q).reshape(n, D)
+    return codes, (shared + 127).astype(np.uint8)
+
+
+def mxfp4_values(codes, scales) -> np.ndarray:
+    """k as the MXFP4 cache represents it: fp64 ``[n, 128]``."""
+    codes = np.asarray(codes).reshape(-1, D)
+    s = e8m0_decode(np.asarray(scales).reshape(-1, D // MX_BLOCK))
+    return e2m1_decode(codes) * np.repeat(s, MX_BLOCK, axis=1)
+
+
+def mxfp4_pack(codes) -> np.ndarray:
+    """[n, 128] e2m1 codes -> [n, 64] bytes, dim 2i in the low nibble of byte i."""
+    c = np.asarray(codes, dtype=np.uint8).reshape(-1, D)
+    return (c[:, 0::2] & 0xF) | ((c[:, 1::2] & 0xF) << 4)
+
+
+def mxfp4_unpack(packed) -> np.ndarray:
+    """[n, 64] bytes -> [n, 128] e2m1 codes (inverse of ``mxfp4_pack``)."""
+    b = np.asarray(packed, dtype=np.uint8).reshape(-1, D // 2)
+    out = np.empty((b.shape[0], D), dtype=np.uint8)
+    out[:, 0::2] = b & 0xF
+    out[:, 1::2] = b >> 4
+    return out
+
+
+def mxfp4_block_stride(block_size: int, align: int = 512) -> int:
+    """Bytes per cache block: ``block_size * 68`` rounded up to ``align`` ([V41] 512 B stride rule)."""
+    return (block_size * MXFP4_TOKEN_BYTES + align - 1) // align * align
+
+
+def mxfp4_k_quant_and_cache(k, slot_mapping, cache: np.ndarray, block_size: int) -> None:
+    """Quantise each token of ``k`` to MXFP4 and write it to its slot (negative slot: skipped).
+
+    The MXFP4 counterpart of ``k_quant_and_cache`` ([DSA] step ⑤: quantisation
+    fused with the insert), in the split block layout described above.
+    """
+    codes, scales = mxfp4_quant(k)
+    packed = mxfp4_pack(codes)
+    for i, slot in enumerate(np.asarray(slot_mapping, dtype=np.int64)):
+        if slot < 0:
+            continue
+        blk, off = divmod(int(slot), block_size)
+        cache[blk, off * (D // 2):(off + 1) * (D // 2)] = packed[i]
+        base = block_size * (D // 2) + 4 * off
+        cache[blk, base:base + 4] = scales[i]
+
+
+def mxfp4_cache_token(cache: np.ndarray, block_size: int, block: int, offset: int):
+    """(codes uint8 [128], scale codes uint8 [4]) of one token of an MXFP4 cache."""
+    packed = cache[block, offset * (D // 2):(offset + 1) * (D // 2)]
+    base = block_size * (D // 2) + 4 * offset
+    return mxfp4_unpack(packed)[0], cache[block, base:base + 4].copy()
+
+
+def mxfp4_gather_values(cache: np.ndarray, block_size: int, block_table_row, positions) -> np.ndarray:
+    """fp64 k values ``[len(positions), 128]`` of request positions read through the block table."""
+    out = np.zeros((len(positions), D))
+    for i, p in enumerate(positions):
+        blk = int(block_table_row[int(p) // block_size])
+        c, s = mxfp4_cache_token(cache, block_size, blk, int(p) % block_size)
+        out[i] = mxfp4_values(c, s)[0]
+    return out
+
+
+def paged_decode_logits_mxfp4(q8, w, cache, block_size, block_table, ctx_lens, next_n=1) -> np.ndarray:
+    """``paged_decode_logits`` over an MXFP4 cache (same row limits and fill values)."""
+    ctx_lens = np.asarray(ctx_lens, dtype=np.int64)
+    B = len(ctx_lens)
+    out = np.full((B * next_n, int(ctx_lens.max()) if B else 0), np.nan)
+    for b in range(B):
+        L = int(ctx_lens[b])
+        kv = mxfp4_gather_values(cache, block_size, block_table[b], range(L))
+        for j in range(next_n):
+            r = b * next_n + j
+            lim = max(min(decode_row_limit(L, next_n, j), L), 0)
+            out[r, :L] = -np.inf
+            if lim > 0:
+                out[r, :lim] = logits_row_values(q8[r], w[r], kv[:lim])
+    return out
+
+
+def sparse_logits_decode_mxfp4(q8, w, cache, block_size, block_table, row_to_req, si, end, sbk) -> np.ndarray:
+    """``sparse_logits_decode`` over an MXFP4 cache: column ``c < end`` scores its mapped token."""
+    si = np.asarray(si)
+    rows, n_si = si.shape
+    out = np.full((rows, n_si * sbk), -np.inf)
+    for r in range(rows):
+        req = r if row_to_req is None else int(row_to_req[r])
+        e = int(end[r])
+        if e <= 0:
+            continue
+        toks = [sparse_column_token(si[r], c, sbk) for c in range(e)]
+        out[r, :e] = logits_row_values(q8[r], w[r], mxfp4_gather_values(cache, block_size, block_table[req], toks))
     return out
