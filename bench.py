@@ -175,11 +175,11 @@ def rank_seed(base: int, rank: int) -> int:
 
 # ----------------------------------------------------------------------------- oracle side
 
-def oracle_decode_rows(wl: W.DecodeWorkload, rows, k_rows, reps: int = 1):
+def oracle_decode_rows(wl: W.DecodeWorkload, rows, k_rows, reps: int = 1, kv: str = "fp8"):
     """Time the oracle's decode step (new-token insert, logits, top-k, slots) on sample rows.
 
-    ``k_rows[b]`` = (k8, kscale) of request b, prepared beforehand (the cache is
-    state, not per-step work). Returns (seconds, per-row results).
+    ``k_rows[b]`` = (k8, kscale) of request b, or its MXFP4 k values, prepared
+    beforehand (the cache is state, not per-step work). Returns (seconds, per-row results).
     """
     from oracle import indexer as O
 
@@ -188,9 +188,13 @@ def oracle_decode_rows(wl: W.DecodeWorkload, rows, k_rows, reps: int = 1):
     for _ in range(reps):
         for b in rows:
             L = int(wl.pool.ctx_lens[b])
-            k8, ks = k_rows[b]
-            O.k_quant(np.zeros((1, 128), dtype=np.float32))          # the new token's insert
-            lg = O.logits_row(wl.q8[b], wl.w[b], k8, ks)
+            if kv == "mxfp4":
+                O.mxfp4_quant(np.zeros((1, 128), dtype=np.float32))  # the new token's insert
+                lg = O.logits_row_values(wl.q8[b], wl.w[b], k_rows[b])
+            else:
+                k8, ks = k_rows[b]
+                O.k_quant(np.zeros((1, 128), dtype=np.float32))      # the new token's insert
+                lg = O.logits_row(wl.q8[b], wl.w[b], k8, ks)
             sel = O.topk_row(lg, 0, L, wl.topk)
             sl = O.req_to_global_slots(sel[None], None, wl.pool.block_table[b:b + 1],
                                        wl.pool.block_size, wl.block_span)
@@ -198,7 +202,7 @@ def oracle_decode_rows(wl: W.DecodeWorkload, rows, k_rows, reps: int = 1):
     return time.perf_counter() - t0, out
 
 
-def oracle_k_rows(wl: W.DecodeWorkload, rows, device):
+def oracle_k_rows(wl: W.DecodeWorkload, rows, device, kv: str = "fp8"):
     """Quantised k of sample requests, from the same generator the GPU arm drew them with."""
     from oracle import indexer as O
     from oracle.codecs import bf16_decode
@@ -210,7 +214,8 @@ def oracle_k_rows(wl: W.DecodeWorkload, rows, device):
             kb = W.make_k_device(wl.seed, b, L, device).view(torch.int16).cpu().numpy().view(np.uint16)
         else:
             kb = W.make_k(wl.seed, b, L)
-        res[b] = O.k_quant(bf16_decode(kb))
+        kf = bf16_decode(kb)
+        res[b] = O.mxfp4_values(*O.mxfp4_quant(kf)) if kv == "mxfp4" else O.k_quant(kf)
     return res
 
 
@@ -308,14 +313,20 @@ class DecodeBench:
         from sparse_attention_indexer_fp8_gb300.pipeline import fill_paged_cache
 
         self.idx, self.dev, self.name = idx, dev, name
-        self.wl = wl = (W.long_decode(seed=rank_seed(1003, rank)) if name == "long_decode"
+        # the MXFP4 line runs the same long-context workload (same k) on the MXFP4 indexer cache
+        self.kv = "mxfp4" if name.endswith("_mxfp4") else "fp8"
+        self.wl = wl = (W.long_decode(seed=rank_seed(1003, rank)) if name.startswith("long_decode")
                         else W.paged_decode(seed=rank_seed(1001, rank)))
         pool = wl.pool
         self.B = B = wl.batch
         self.L = L = pool.ctx_lens.astype(np.int64)
-        self.stride = W.block_stride_bytes()
+        self.token_bytes = W.MXFP4_TOKEN_BYTES if self.kv == "mxfp4" else W.TOKEN_BYTES
+        self.stride = W.mxfp4_block_stride_bytes() if self.kv == "mxfp4" else W.block_stride_bytes()
         self.cache = torch.zeros((pool.num_blocks, self.stride), dtype=torch.uint8, device=dev)
-        fill_paged_cache(pool, wl.seed, self.cache, device_k=True)
+        fill_paged_cache(pool, wl.seed, self.cache, device_k=True, kv=self.kv)
+        self.insert = idx.idx_k_quant_and_cache_mxfp4 if self.kv == "mxfp4" else idx.idx_k_quant_and_cache
+        self.scorer = (idx.idx_paged_mqa_logits_decode_mxfp4 if self.kv == "mxfp4"
+                       else idx.idx_paged_mqa_logits_decode)
         self.q = torch.from_numpy(wl.q8).to(dev)
         self.w = torch.from_numpy(wl.w).to(dev)
         self.bt = torch.from_numpy(pool.block_table).to(dev)
@@ -333,15 +344,17 @@ class DecodeBench:
         self.rows_per_step = B
 
     metric = property(lambda self: "decode indexer query-rows/s @128K ctx incl. top-2048; % of HBM roofline"
-                      if self.name == "long_decode" else "paged decode indexer query-rows/s incl. top-2048")
+                      if self.name == "long_decode" else
+                      ("decode indexer query-rows/s @128K ctx incl. top-2048, MXFP4 indexer cache"
+                       if self.name == "long_decode_mxfp4" else "paged decode indexer query-rows/s incl. top-2048"))
 
     def step(self, stream, ev=None):
         idx, wl = self.idx, self.wl
-        idx.idx_k_quant_and_cache(self.new_k, self.new_slots, self.cache, wl.pool.block_size, stream=stream)
+        self.insert(self.new_k, self.new_slots, self.cache, wl.pool.block_size, stream=stream)
         if ev is not None:
             ev[0].record(stream)
-        idx.idx_paged_mqa_logits_decode(self.q, self.w, self.cache, wl.pool.block_size, self.bt, self.ctx,
-                                        self.logits, ws=self.ws, stream=stream)
+        self.scorer(self.q, self.w, self.cache, wl.pool.block_size, self.bt, self.ctx, self.logits, ws=self.ws,
+                    stream=stream)
         if ev is not None:
             ev[1].record(stream)
         # top-2048 with the slot conversion fused into the selection's output pass
@@ -362,8 +375,8 @@ class DecodeBench:
         wl, L = self.wl, self.L
         rng = np.random.default_rng(wl.seed)
         sample = sorted(rng.choice(self.B, size=min(n_rows, self.B), replace=False).tolist())
-        k_rows = oracle_k_rows(wl, sample, self.dev)
-        cpu_s, ref = oracle_decode_rows(wl, sample, k_rows)
+        k_rows = oracle_k_rows(wl, sample, self.dev, self.kv)
+        cpu_s, ref = oracle_decode_rows(wl, sample, k_rows, kv=self.kv)
         g_logits, g_sel, g_slots = self.logits.cpu().numpy(), self.local.cpu().numpy(), self.slots.cpu().numpy()
         for b in sample:
             lg = ref[b][0]
@@ -379,21 +392,26 @@ class DecodeBench:
 
     def roofline(self, kernel_ms, step_ms, peaks, peak_kind):
         tok = int(self.L.sum())
-        return hbm_roofline("mqa_logits_kernel<1> (paged decode)", tok * W.TOKEN_BYTES + self.B * (64 * 128 + 64 * 4),
+        tb = self.token_bytes
+        return hbm_roofline("mqa_logits_kernel<1, MXFP4 k> (paged decode)" if self.kv == "mxfp4"
+                            else "mqa_logits_kernel<1> (paged decode)", tok * tb + self.B * (64 * 128 + 64 * 4),
                             tok * 4, kernel_ms, peaks, peak_kind,
                             traffic=profiled_traffic(f"mqa_logits_decode_{self.name}.md", "logits.cu"),
-                            step_kcache_frac=round(tok * W.TOKEN_BYTES / (step_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4))
+                            step_kcache_frac=round(tok * tb / (step_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4))
 
     def config(self, world):
         L, pool = self.L, self.wl.pool
-        return {"workload": self.wl.name, "batch": self.B, "ctx_min": int(L.min()), "ctx_max": int(L.max()),
+        return {"workload": self.wl.name + ("-mxfp4-cache" if self.kv == "mxfp4" else ""), "batch": self.B,
+                "ctx_min": int(L.min()), "ctx_max": int(L.max()),
                 "ctx_mean": float(L.mean()), "topk": self.wl.topk, "block_size": pool.block_size,
+                "kv_cache": "MXFP4 (e2m1 + E8M0 per 32, 68 B/token)" if self.kv == "mxfp4"
+                else "e4m3 + fp32 scale (132 B/token)",
                 "block_stride_bytes": self.stride, "cache_gb": round(pool.num_blocks * self.stride / 1e9, 3),
                 "step": "k insert + paged logits + top-2048 with the slot conversion fused",
                 "l2": "inputs larger than L2 (k cache > 129 MB), no flush",
                 "parallelism": f"rows sharded, {world} independent replica(s)"}
 
-    dtype = "e4m3xe4m3->f32"
+    dtype = property(lambda self: "e4m3xe2m1(mx)->f32" if self.kv == "mxfp4" else "e4m3xe4m3->f32")
 
 
 class PrefillBench:
@@ -922,7 +940,8 @@ class QPrepBench:
                 "parallelism": f"rows sharded, {world} independent replica(s)"}
 
 
-BENCHES = {"long_decode": DecodeBench, "paged_decode": DecodeBench, "prefill": PrefillBench,
+BENCHES = {"long_decode": DecodeBench, "long_decode_mxfp4": DecodeBench, "paged_decode": DecodeBench,
+           "prefill": PrefillBench,
            "hierarchical": HierBench, "hierarchical_mtp": HierMtpBench, "q_prep": QPrepBench,
            "dcp_decode": DcpBench}
 
@@ -1064,12 +1083,13 @@ def run_reference(args, rank):
         return None
     name = args.workload
     rows_per_call = 1
-    if name in ("long_decode", "paged_decode", "dcp_decode"):
+    if name in ("long_decode", "long_decode_mxfp4", "paged_decode", "dcp_decode"):
         wl = W.paged_decode() if name == "paged_decode" else W.long_decode()
+        kv = "mxfp4" if name == "long_decode_mxfp4" else "fp8"
         rng = np.random.default_rng(wl.seed)
         rows = sorted(rng.choice(wl.batch, size=min(4, wl.batch), replace=False).tolist())
-        k_rows = oracle_k_rows(wl, rows, None)
-        one = lambda i: oracle_decode_rows(wl, [rows[i % len(rows)]], k_rows)[0]  # noqa: E731
+        k_rows = oracle_k_rows(wl, rows, None, kv)
+        one = lambda i: oracle_decode_rows(wl, [rows[i % len(rows)]], k_rows, kv=kv)[0]  # noqa: E731
         metric = (DcpBench.metric if name == "dcp_decode"
                   else DecodeBench.metric.fget(type("X", (), {"name": name})()))
         cfg = {"workload": wl.name, "batch": wl.batch, "topk": wl.topk}

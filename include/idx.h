@@ -98,6 +98,7 @@ enum {
 #define IDX_HEADS 64
 #define IDX_HEAD_DIM 128
 #define IDX_TOKEN_BYTES 132
+#define IDX_MXFP4_TOKEN_BYTES 68
 
 /*
  * idx_k_quant_and_cache - quantise k to e4m3 and insert it into the paged cache.
@@ -126,6 +127,49 @@ idx_status_t idx_k_quant_and_cache(const void* k, int k_dtype, int64_t ld_k, int
                                    int32_t num_blocks, int32_t block_size,
                                    int64_t block_stride_bytes, int scale_fmt,
                                    cudaStream_t stream);
+
+/*
+ * The MXFP4 indexer cache (the V4.1 path)
+ * ---------------------------------------
+ * "V4.1 索引器接入稀疏 MQA logits", 功能与动机 and 实现拆解 items 1-2: the V4.1
+ * consumer layers read an MXFP4 indexer cache (风险与影响: indexer_kv_dtype
+ * "mxfp4") through an fp8 x fp4 MQA-logits kernel. The page prints neither the
+ * format nor the layout; this library reads it as OCP MXFP4 over the 128 dims
+ * of a token: four blocks of 32 dims, each element FP4 E2M1 (magnitudes 0, 0.5,
+ * 1, 1.5, 2, 3, 4, 6), each block one E8M0 scale 2^(code - 127). A token takes
+ * 64 element bytes plus 4 scale bytes = IDX_MXFP4_TOKEN_BYTES, about half the
+ * 132 bytes of the e4m3 cache. Split block layout: block b starts at
+ * b * block_stride_bytes; token i keeps its elements at i * 64 (dim d in byte
+ * d / 2, even d in the low nibble) and its four scale codes at
+ * block_size * 64 + 4 * i (byte j scales dims 32 j .. 32 j + 31).
+ * block_stride_bytes must be at least block_size * 68 and a multiple of 32, the
+ * cache 32-byte aligned; rounding the stride up to 512 (4608 bytes for 64
+ * tokens) follows the V4.1 stride rule. q stays e4m3 with its scale folded into
+ * the weights, so a score is
+ *     sum_h w[h] * sum_d q8[h, d] * e2m1(k[d]) * 2^(E[d / 32] - 127).
+ */
+
+/*
+ * idx_k_quant_and_cache_mxfp4 - quantise k to MXFP4 and insert it into an MXFP4 cache.
+ *
+ * "DeepSeek V3.2 稀疏注意力 DSA 推理流程图解", "Indexer 内部六步" step 5 (the
+ * quantisation is fused with the insert), for the MXFP4 cache above. Per token
+ * and 32-dim block, the OCP MX conversion: amax = max |k_d| in binary32; shared
+ * exponent floor(log2(amax)) - 2, clamped to [-127, 127] (zero or tiny blocks get
+ * -127); element = e2m1 of k_d / 2^shared, rounded to nearest even and saturated
+ * to +-6 (the sign of a zero result is kept). Inputs must be finite.
+ *
+ *   k, ld_k, n_tok, slot_mapping, num_blocks, block_size: as idx_k_quant_and_cache.
+ *   cache  uint8 [num_blocks, block_stride_bytes], written in place.
+ * Errors: IDX_ERR_INVALID_ARG for NULL pointers with n_tok > 0, negative sizes,
+ * ld_k < 128, block_stride_bytes < block_size * 68; IDX_ERR_UNSUPPORTED for
+ * another block_size or dtype, block_stride_bytes % 32 != 0, or a cache that is
+ * not 32-byte aligned.
+ */
+idx_status_t idx_k_quant_and_cache_mxfp4(const void* k, int k_dtype, int64_t ld_k, int32_t n_tok,
+                                         const int64_t* slot_mapping, uint8_t* cache,
+                                         int32_t num_blocks, int32_t block_size,
+                                         int64_t block_stride_bytes, cudaStream_t stream);
 
 enum { IDX_ROPE_NEOX = 0, IDX_ROPE_INTERLEAVED = 1 };  /* pairing of the rotary dims */
 
@@ -258,6 +302,32 @@ idx_status_t idx_paged_mqa_logits_decode(const uint8_t* q, int64_t ld_q, const v
                                          int32_t sbk, void* logits, int out_dtype,
                                          int64_t ld_out, void* ws, size_t ws_bytes,
                                          cudaStream_t stream);
+
+/*
+ * idx_paged_mqa_logits_decode_mxfp4 - decode logits read from an MXFP4 cache.
+ *
+ * The fp8 x fp4 scoring of the V4.1 path ("V4.1 索引器接入稀疏 MQA logits",
+ * 实现拆解 item 2): the same rows, modes, outputs and workspace as
+ * idx_paged_mqa_logits_decode, with k read from the MXFP4 cache described
+ * above (block scales applied by the tensor core, no per-token factor).
+ * Dense mode supports next_n = 1; sparse mode any next_n.
+ *
+ *   cache   uint8 [num_blocks, block_stride_bytes] in the MXFP4 layout
+ *           (32-byte aligned, stride a multiple of 32 and >= block_size * 68).
+ *   other arguments as idx_paged_mqa_logits_decode.
+ * Errors: as idx_paged_mqa_logits_decode; IDX_ERR_UNSUPPORTED for dense next_n
+ * other than 1 or a cache layout outside the rules above.
+ */
+idx_status_t idx_paged_mqa_logits_decode_mxfp4(const uint8_t* q, int64_t ld_q, const void* w,
+                                               int w_dtype, int64_t ld_w, const uint8_t* cache,
+                                               int32_t num_blocks, int32_t block_size,
+                                               int64_t block_stride_bytes,
+                                               const int32_t* block_table, int64_t ld_bt,
+                                               const int32_t* ctx_lens, int32_t B, int32_t next_n,
+                                               const int32_t* sparse_idx, int64_t ld_si,
+                                               int32_t n_si, const int32_t* end, int32_t sbk,
+                                               void* logits, int out_dtype, int64_t ld_out,
+                                               void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
  * idx_topk - per-row top-k with -1 fill.

@@ -673,13 +673,19 @@ def mxfp4_cache_token(cache: np.ndarray, block_size: int, block: int, offset: in
 
 
 def mxfp4_gather_values(cache: np.ndarray, block_size: int, block_table_row, positions) -> np.ndarray:
-    """fp64 k values ``[len(positions), 128]`` of request positions read through the block table."""
-    out = np.zeros((len(positions), D))
-    for i, p in enumerate(positions):
-        blk = int(block_table_row[int(p) // block_size])
-        c, s = mxfp4_cache_token(cache, block_size, blk, int(p) % block_size)
-        out[i] = mxfp4_values(c, s)[0]
-    return out
+    """fp64 k values ``[len(positions), 128]`` of request positions read through the block table.
+
+    Position ``p`` lives in block ``block_table_row[p // block_size]`` at offset
+    ``p % block_size``; the bytes are picked with array indexing, then decoded
+    exactly as ``mxfp4_cache_token`` + ``mxfp4_values`` decode one token.
+    """
+    pos = np.asarray(list(positions), dtype=np.int64)
+    blk = np.asarray(block_table_row, dtype=np.int64)[pos // block_size]
+    off = pos % block_size
+    half = D // 2
+    packed = cache[blk[:, None], off[:, None] * half + np.arange(half)[None, :]]
+    scales = cache[blk[:, None], block_size * half + 4 * off[:, None] + np.arange(4)[None, :]]
+    return mxfp4_values(mxfp4_unpack(packed), scales)
 
 
 def paged_decode_logits_mxfp4(q8, w, cache, block_size, block_table, ctx_lens, next_n=1) -> np.ndarray:

@@ -17,8 +17,8 @@ import torch
 from . import _lib
 
 __all__ = [
-    "IdxError", "idx_k_quant_and_cache", "idx_gather_k", "idx_mqa_logits_prefill",
-    "idx_paged_mqa_logits_decode", "idx_topk", "idx_expand_candidates", "idx_sparse_topk_remap",
+    "IdxError", "idx_k_quant_and_cache", "idx_k_quant_and_cache_mxfp4", "idx_gather_k",
+    "idx_mqa_logits_prefill", "idx_paged_mqa_logits_decode", "idx_paged_mqa_logits_decode_mxfp4", "idx_topk", "idx_expand_candidates", "idx_sparse_topk_remap",
     "idx_req_to_global_slots", "idx_dcp_topk_merge", "idx_q_rope_quant", "idx_block_span",
     "idx_workspace_bytes", "idx_device_error", "library",
 ]
@@ -80,6 +80,13 @@ def idx_k_quant_and_cache(k, slot_mapping, cache, block_size, ue8m0=False, strea
         _lib.IDX_SCALE_UE8M0 if ue8m0 else _lib.IDX_SCALE_FP32, _stream(stream)))
 
 
+def idx_k_quant_and_cache_mxfp4(k, slot_mapping, cache, block_size, stream=None):
+    """k [n, 128] bf16/f32 -> MXFP4 cache uint8 [num_blocks, block_stride] (68 bytes per token)."""
+    _check("idx_k_quant_and_cache_mxfp4", library().idx_k_quant_and_cache_mxfp4(
+        _ptr(k), _dtype_code(k), _rows(k), k.shape[0], _ptr(slot_mapping), _ptr(cache),
+        cache.shape[0], block_size, cache.stride(0), _stream(stream)))
+
+
 def idx_gather_k(cache, block_size, block_table_row, n_tok, k8_out, kscale_out, stream=None):
     """Copy n_tok tokens of one request (block_table_row int32) into k8_out [n, 128] / kscale_out [n]."""
     _check("idx_gather_k", library().idx_gather_k(
@@ -113,6 +120,20 @@ def idx_paged_mqa_logits_decode(q, w, cache, block_size, block_table, ctx_lens, 
     if n_si is None:
         n_si = sparse_idx.shape[1] if sparse_idx is not None else 0
     _check("idx_paged_mqa_logits_decode", library().idx_paged_mqa_logits_decode(
+        _ptr(q), _q_stride(q), _ptr(w), _dtype_code(w), _rows(w), _ptr(cache), cache.shape[0],
+        block_size, cache.stride(0), _ptr(block_table), _rows(block_table), _ptr(ctx_lens),
+        ctx_lens.shape[0], next_n, _ptr(sparse_idx), ld_si, n_si, _ptr(end), sbk, _ptr(logits),
+        _dtype_code(logits), _rows(logits), _ptr(ws),
+        0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def idx_paged_mqa_logits_decode_mxfp4(q, w, cache, block_size, block_table, ctx_lens, logits, next_n=1,
+                                      sparse_idx=None, end=None, sbk=0, n_si=None, ws=None, stream=None):
+    """idx_paged_mqa_logits_decode over an MXFP4 cache (dense next_n 1, or sparse)."""
+    ld_si = sparse_idx.stride(0) if sparse_idx is not None else 0
+    if n_si is None:
+        n_si = sparse_idx.shape[1] if sparse_idx is not None else 0
+    _check("idx_paged_mqa_logits_decode_mxfp4", library().idx_paged_mqa_logits_decode_mxfp4(
         _ptr(q), _q_stride(q), _ptr(w), _dtype_code(w), _rows(w), _ptr(cache), cache.shape[0],
         block_size, cache.stride(0), _ptr(block_table), _rows(block_table), _ptr(ctx_lens),
         ctx_lens.shape[0], next_n, _ptr(sparse_idx), ld_si, n_si, _ptr(end), sbk, _ptr(logits),

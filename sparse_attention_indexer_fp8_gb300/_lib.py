@@ -31,6 +31,8 @@ OPS = {
 SIGNATURES = {
     "idx_k_quant_and_cache": (c_int, [c_ptr, c_int, c_i64, c_i32, c_ptr, c_ptr, c_i32, c_i32, c_i64,
                                       c_int, c_ptr]),
+    "idx_k_quant_and_cache_mxfp4": (c_int, [c_ptr, c_int, c_i64, c_i32, c_ptr, c_ptr, c_i32, c_i32, c_i64,
+                                            c_ptr]),
     "idx_gather_k": (c_int, [c_ptr, c_i32, c_i64, c_ptr, c_i32, c_ptr, c_ptr, c_ptr]),
     "idx_mqa_logits_prefill": (c_int, [c_ptr, c_i64, c_ptr, c_int, c_i64, c_ptr, c_ptr, c_i32, c_ptr,
                                        c_ptr, c_i32, c_ptr, c_i64, c_i32, c_ptr, c_i32, c_ptr, c_int,
@@ -39,6 +41,10 @@ SIGNATURES = {
                                             c_i64, c_ptr, c_i64, c_ptr, c_i32, c_i32, c_ptr, c_i64,
                                             c_i32, c_ptr, c_i32, c_ptr, c_int, c_i64, c_ptr, c_size,
                                             c_ptr]),
+    "idx_paged_mqa_logits_decode_mxfp4": (c_int, [c_ptr, c_i64, c_ptr, c_int, c_i64, c_ptr, c_i32, c_i32,
+                                                  c_i64, c_ptr, c_i64, c_ptr, c_i32, c_i32, c_ptr, c_i64,
+                                                  c_i32, c_ptr, c_i32, c_ptr, c_int, c_i64, c_ptr, c_size,
+                                                  c_ptr]),
     "idx_topk": (c_int, [c_ptr, c_int, c_i64, c_ptr, c_ptr, c_i32, c_i32, c_ptr, c_i64, c_ptr, c_i64,
                          c_ptr, c_size, c_ptr]),
     "idx_q_rope_quant": (c_int, [c_ptr, c_int, c_i64, c_ptr, c_ptr, c_i64, c_i32, c_i32, c_ptr, c_int, c_i64,

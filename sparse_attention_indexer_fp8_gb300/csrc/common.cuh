@@ -15,6 +15,7 @@ namespace idx {
 constexpr int kHeads = 64;
 constexpr int kDim = 128;
 constexpr int kTokenBytes = 132;
+constexpr int kMxTokenBytes = 68;  // MXFP4 cache: 64 bytes of e2m1 elements + 4 E8M0 scale codes
 
 // ---------------------------------------------------------------------------
 // host-side status helpers (defined in api.cu)
@@ -219,6 +220,77 @@ __device__ __forceinline__ void umma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint
       "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// Instruction descriptor of the block-scaled tcgen05.mma kind::mxf8f6f4 with FP4
+// e2m1 A (k) and e4m3 B (q), fp32 accumulation, both operands K-major: B's
+// scale-factor id in bits 4-5, A/B formats in bits 7-9 / 10-12 (e2m1 = 5,
+// e4m3 = 0), N >> 3 in bits 17-22, scale type UE8M0 (1) in bit 23, M >> 4 in
+// bits 24-28, A's scale-factor id in bits 29-30. The ids pick the byte of each
+// 32-bit scale word that the instruction's K block (32 elements) uses.
+__host__ __device__ constexpr uint32_t idesc_mx_e2m1_e4m3(int M, int N) {
+  return (5u << 7) | (0u << 10) | (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__host__ __device__ constexpr uint32_t idesc_with_scale_ids(uint32_t idesc, uint32_t a_id, uint32_t b_id) {
+  return idesc | (b_id << 4) | (a_id << 29);
+}
+
+// D += (A * scale_A) x (B * scale_B)^T over one K block of 32, scale_vec::1X: one
+// E8M0 scale per row and K block. For M = 128 the scale of A's row r is read
+// from tensor-memory lane r, column sfa + r / 32 (byte = the A id); B's from
+// sfb likewise.
+__device__ __forceinline__ void umma_mx_e2m1_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                  uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                  uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Orders this thread's generic-proxy shared-memory writes before later
+// async-proxy reads of them (a tensor-memory copy or an MMA operand).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Shared-memory descriptor of 32 consecutive 16-byte lines (no swizzle: 8-line
+// core matrices of 128 bytes, the next one 128 bytes on), the source of a
+// tcgen05.cp of shape 32x128b. Fields as in sw128_kmajor_desc, swizzle mode 0.
+__device__ __forceinline__ uint64_t lines_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(128 >> 4) << 16;
+  d |= static_cast<uint64_t>(128 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  return d;
+}
+
+// Copies 32 lines of 16 bytes from shared memory into tensor memory, line m into
+// lane m of each of the four lane quarters, four 32-bit columns from taddr.
+// Asynchronous, in issue order with this thread's later tcgen05.mma.
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t src_desc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(src_desc) : "memory");
+}
+
+// Each thread of the warp writes 32-bit words to its own TMEM lane: one column,
+// or four consecutive columns. Complete with tmem_wait_st() before signalling.
+__device__ __forceinline__ void tmem_st_x1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_x4(uint32_t taddr, uint32_t v0, uint32_t v1, uint32_t v2, uint32_t v3) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v0),
+               "r"(v1), "r"(v2), "r"(v3)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // Arrive on `bar` once every tcgen05 operation this thread issued so far has completed.

@@ -6,6 +6,7 @@
 // handles one token: lane l owns dims 4l..4l+3, the warp reduces |k| to amax, and
 // the lane writes its four e4m3 bytes as one 32-bit store, so a token's 128-byte
 // value row leaves as one coalesced 128-byte transaction.
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 
 #include "common.cuh"
@@ -92,6 +93,50 @@ k_quant_and_cache_kernel(const void* __restrict__ k, int64_t ld_k, int n_tok, bo
   if (lane == 0) *reinterpret_cast<float*>(base + block_size * kDim + 4 * off) = scale;
 }
 
+// MXFP4 insert (the V4.1 cache format): the OCP MX conversion per 32-dim block.
+// One warp per token, lane l owns dims 4l..4l+3, so block j is lanes 8j..8j+7.
+// Shared exponent floor(log2(amax)) - 2, clamped to the E8M0 range: for a
+// binary32 amax with biased exponent E that is E - 129, and its E8M0 code is
+// max(E - 2, 0) (E = 0 for zero or subnormal amax, which clamps to 2^-127).
+// The quotient by the power of two is a multiplication by 2^(127 - code),
+// exact except where it underflows to a magnitude far below the smallest e2m1
+// step, which rounds to 0 either way; cvt.rn.satfinite.e2m1x2 rounds to nearest
+// even and saturates to +-6. The lane's four codes leave as one 16-bit store
+// (dim 2i in the low nibble), the warp's 64 bytes as one transaction, and lane
+// 0 writes the four scale codes of the token as one 32-bit word.
+template <bool kBf16>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+k_quant_and_cache_mxfp4_kernel(const void* __restrict__ k, int64_t ld_k, int n_tok, bool vec,
+                               const int64_t* __restrict__ slot_mapping, uint8_t* __restrict__ cache,
+                               int64_t n_slots, int block_size, int64_t block_stride) {
+  const int tok = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (tok >= n_tok) return;
+  const int64_t slot = __ldg(slot_mapping + tok);
+  if (slot < 0 || slot >= n_slots) return;
+
+  float x[4];
+  load4<kBf16>(k, ld_k, tok, lane, vec, x);
+  float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+  const int e = static_cast<int>(__float_as_uint(amax) >> 23);   // amax >= 0
+  const uint32_t code = static_cast<uint32_t>(max(e - 2, 0));   // 0..252
+  const float inv = __uint_as_float((254u - code) << 23);      // 2^(127 - code), a normal float
+  const uint32_t lo = __nv_cvt_float2_to_fp4x2(make_float2(x[0] * inv, x[1] * inv), __NV_E2M1, cudaRoundNearest);
+  const uint32_t hi = __nv_cvt_float2_to_fp4x2(make_float2(x[2] * inv, x[3] * inv), __NV_E2M1, cudaRoundNearest);
+  // the four block codes, byte j from lane 8j
+  const uint32_t c0 = __shfl_sync(0xFFFFFFFFu, code, 0), c1 = __shfl_sync(0xFFFFFFFFu, code, 8);
+  const uint32_t c2 = __shfl_sync(0xFFFFFFFFu, code, 16), c3 = __shfl_sync(0xFFFFFFFFu, code, 24);
+  const int64_t blk = slot / block_size;
+  const int off = static_cast<int>(slot - blk * block_size);
+  uint8_t* base = cache + blk * block_stride;
+  *reinterpret_cast<uint16_t*>(base + off * (kDim / 2) + 2 * lane) = static_cast<uint16_t>(lo | (hi << 8));
+  if (lane == 0) {
+    *reinterpret_cast<uint32_t*>(base + block_size * (kDim / 2) + 4 * off) = c0 | (c1 << 8) | (c2 << 16) | (c3 << 24);
+  }
+}
+
 // One thread per 16-byte chunk: eight threads move one token's value row.
 __global__ void gather_k_kernel(const uint8_t* __restrict__ cache, int block_size,
                                 int64_t block_stride, const int32_t* __restrict__ block_table,
@@ -127,6 +172,23 @@ idx_status_t check_cache(const char* fn, const void* cache, int32_t block_size,
                 static_cast<long long>(block_stride));
   }
   if (!aligned(cache, 16)) return fail(IDX_ERR_UNSUPPORTED, "%s: cache is not 16-byte aligned", fn);
+  return IDX_OK;
+}
+
+idx_status_t check_cache_mxfp4(const char* fn, const void* cache, int32_t block_size,
+                               int64_t block_stride) {
+  if (!block_size_ok(block_size)) {
+    return fail(IDX_ERR_UNSUPPORTED, "%s: block_size %d is not one of 16, 32, 64, 128", fn, block_size);
+  }
+  if (block_stride < static_cast<int64_t>(block_size) * IDX_MXFP4_TOKEN_BYTES) {
+    return fail(IDX_ERR_INVALID_ARG, "%s: block_stride_bytes %lld < block_size * 68", fn,
+                static_cast<long long>(block_stride));
+  }
+  if (block_stride % 32 != 0) {
+    return fail(IDX_ERR_UNSUPPORTED, "%s: block_stride_bytes %lld is not a multiple of 32", fn,
+                static_cast<long long>(block_stride));
+  }
+  if (!aligned(cache, 32)) return fail(IDX_ERR_UNSUPPORTED, "%s: cache is not 32-byte aligned", fn);
   return IDX_OK;
 }
 
@@ -186,5 +248,33 @@ extern "C" idx_status_t idx_gather_k(const uint8_t* cache, int32_t block_size,
   const dim3 grid(static_cast<unsigned>((threads + block - 1) / block));
   gather_k_kernel<<<grid, block, 0, stream>>>(cache, block_size, block_stride_bytes, block_table,
                                               n_tok, k8_out, kscale_out);
+  return check_launch(fn);
+}
+
+extern "C" idx_status_t idx_k_quant_and_cache_mxfp4(const void* k, int k_dtype, int64_t ld_k,
+                                                    int32_t n_tok, const int64_t* slot_mapping,
+                                                    uint8_t* cache, int32_t num_blocks,
+                                                    int32_t block_size, int64_t block_stride_bytes,
+                                                    cudaStream_t stream) {
+  const char* fn = "idx_k_quant_and_cache_mxfp4";
+  if (n_tok < 0 || num_blocks < 0) return fail(IDX_ERR_INVALID_ARG, "%s: negative size", fn);
+  if (k_dtype != IDX_BF16 && k_dtype != IDX_F32) return fail(IDX_ERR_UNSUPPORTED, "%s: k_dtype %d", fn, k_dtype);
+  if (ld_k < kDim) return fail(IDX_ERR_INVALID_ARG, "%s: ld_k %lld < 128", fn, static_cast<long long>(ld_k));
+  if (n_tok == 0) return IDX_OK;
+  if (!k || !slot_mapping || !cache) return fail(IDX_ERR_INVALID_ARG, "%s: NULL pointer", fn);
+  idx_status_t st = check_cache_mxfp4(fn, cache, block_size, block_stride_bytes);
+  if (st != IDX_OK) return st;
+  const size_t esz = k_dtype == IDX_BF16 ? 2 : 4;
+  const size_t vec_bytes = 4 * esz;
+  const bool vec = aligned(k, vec_bytes) && (static_cast<size_t>(ld_k) * esz) % vec_bytes == 0;
+  const int64_t n_slots = static_cast<int64_t>(num_blocks) * block_size;
+  const dim3 grid((n_tok + kWarpsPerBlock - 1) / kWarpsPerBlock);
+  if (k_dtype == IDX_BF16) {
+    k_quant_and_cache_mxfp4_kernel<true><<<grid, kWarpsPerBlock * 32, 0, stream>>>(
+        k, ld_k, n_tok, vec, slot_mapping, cache, n_slots, block_size, block_stride_bytes);
+  } else {
+    k_quant_and_cache_mxfp4_kernel<false><<<grid, kWarpsPerBlock * 32, 0, stream>>>(
+        k, ld_k, n_tok, vec, slot_mapping, cache, n_slots, block_size, block_stride_bytes);
+  }
   return check_launch(fn);
 }

@@ -35,7 +35,9 @@
 //              block-table lookups for the next tile are issued before the
 //              wait for a free stage so their latency hides behind it.
 //   warp 1     allocates tensor memory; one lane issues tcgen05.mma and
-//              commits stage / accumulator barriers.
+//              commits stage / accumulator barriers (MXFP4 k: the warp first
+//              stages the tile's block scales and copies them into tensor
+//              memory with tcgen05.cp).
 //   warps 2-   epilogue, warpgroups taking tiles in turn: tcgen05.ld of
 //              the accumulator, weighted head sum, scale, causal / range mask,
 //              coalesced store (fp32 or bf16).
@@ -82,6 +84,8 @@ struct LogitsParams {
   int64_t kv_block_stride;    // bytes between cache blocks (paged)
   int unit;             // tokens per k box (cache block, sparse block or 128)
   int scale_slot;       // bytes between the scale boxes of one stage (>= 128)
+  int unit_shift;       // log2(unit) (a power of two)
+  int slot_shift;       // log2(scale_slot)
   int block_size;
   const int32_t* block_table;
   int64_t ld_bt;
@@ -104,8 +108,13 @@ struct LogitsParams {
 
 constexpr int kHistBins = 1024;  // first selection digit: the top 10 bits of the order-preserving key
 
-template <int NQ>
+// kFp4: k read from the MXFP4 cache (one query per group only). The MMA warp
+// copies each tile's block scales into tensor memory ahead of its MMAs; they
+// take columns from the accumulators: three accumulator stages, a commit per
+// tile, then one 4-column scale slot per k stage and one for q.
+template <int NQ, bool kFp4 = false>
 struct Cfg {
+  static_assert(!kFp4 || NQ == 1, "the MXFP4 path serves one query per group");
   static constexpr int N = 64 * NQ;
   // CTAs per SM and epilogue warpgroups per CTA (taking tiles in turn)
   static constexpr int kCtasPerSm = NQ == 4 ? 1 : 2;
@@ -113,13 +122,18 @@ struct Cfg {
   static constexpr int kEpiWarps = 4 * kEpiWG;
   static constexpr int kThreads = 64 + kEpiWarps * 32;
   static constexpr int kStages = NQ == 4 ? 8 : 4;
-  static constexpr int kAccStages = NQ == 1 ? 4 : 2;
+  static constexpr int kAccStages = NQ == 1 ? (kFp4 ? 3 : 4) : 2;
   // tiles per tcgen05.commit: one commit covers the MMAs of kCommit consecutive
   // tiles (commits are costly next to a 4-MMA tile); one accumulator-ready
   // barrier per commit group
-  static constexpr int kCommit = NQ == 1 ? 2 : 1;
+  static constexpr int kCommit = NQ == 1 && !kFp4 ? 2 : 1;
   static constexpr int kAccFull = kAccStages / kCommit;
-  static constexpr int kTmemCols = kAccStages * N;  // 256 or 512 per CTA, 512 per SM
+  // MXFP4: the scale words of k stage s at columns kSfaCol + 4 s .. + 3 (row r of
+  // the tile in lane r, column + r / 32), q's (all 1.0) at kSfbCol .. + 3
+  static constexpr int kSfaCol = kAccStages * N;
+  static constexpr int kSfbCol = kSfaCol + 4 * kStages;
+  static constexpr int kTmemCols = kFp4 ? 256 : kAccStages * N;  // 256 or 512 per CTA, 512 per SM
+  static_assert(!kFp4 || kSfbCol + 4 <= kTmemCols, "scale columns fit the allocation");
   static constexpr int kQStageBytes = NQ * 64 * kDim;
   static constexpr int kOffKv = 0;
   static constexpr int kOffQ = kOffKv + kStages * kKvStageBytes;
@@ -128,7 +142,13 @@ struct Cfg {
   // per epilogue warp, one query per group: 1024 bins of 16-bit counts
   static constexpr int kHistWords = NQ == 1 ? kHistBins / 2 : 0;
   static constexpr int kOffHist = kOffW + kEpiWarps * NQ * 64 * 4;
-  static constexpr int kOffBar = kOffHist + kEpiWarps * kHistWords * 4;
+  static constexpr int kOffSf = kOffHist + kEpiWarps * kHistWords * 4;
+  // MXFP4: per k stage the tile's 128 scale words as 32 lines of 16 bytes (line m
+  // holds rows m, m + 32, m + 64, m + 96), the layout the 32x128b.warpx4
+  // tensor-memory copy spreads over the four lane quarters; then one such block
+  // of 1.0 scales for q
+  static constexpr int kSfLineBytes = kFp4 ? 512 * (kStages + 1) : 0;
+  static constexpr int kOffBar = kOffSf + kSfLineBytes;
   static constexpr int kNumBars = 2 * kStages + kAccFull + kAccStages + 4;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 1024;  // + alignment slack
   static_assert(kSmemBytes <= 232448 / kCtasPerSm - 2048, "shared memory budget per CTA");
@@ -343,11 +363,11 @@ __device__ __forceinline__ float weighted_head_sum(const uint32_t (&a0)[32], con
   return (hsum2(acc[0]) + hsum2(acc[1])) + (hsum2(acc[2]) + hsum2(acc[3]));
 }
 
-template <int NQ, bool kOutBf16>
-__global__ void __launch_bounds__(Cfg<NQ>::kThreads, Cfg<NQ>::kCtasPerSm)
+template <int NQ, bool kOutBf16, bool kFp4>
+__global__ void __launch_bounds__(Cfg<NQ, kFp4>::kThreads, Cfg<NQ, kFp4>::kCtasPerSm)
 mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_kv,
                   const __grid_constant__ CUtensorMap map_scale, const LogitsParams p) {
-  using C = Cfg<NQ>;
+  using C = Cfg<NQ, kFp4>;
   constexpr int kThreads = C::kThreads;
   constexpr int kEpiWG = C::kEpiWG;
   extern __shared__ uint8_t smem_raw[];
@@ -364,6 +384,7 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   uint64_t* acc_empty = acc_full + C::kAccFull;
   uint64_t* q_full = acc_empty + C::kAccStages;
   uint64_t* q_empty = q_full + 2;
+  uint8_t* sf_lines = smem + C::kOffSf;  // MXFP4 (see Cfg::kSfLineBytes)
 
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
@@ -463,7 +484,9 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     const uint64_t pol_q = prefill ? l2_policy_evict_first() : l2_policy_evict_last();
     const int upt = kTile / p.unit;  // boxes per tile, 1..16
     const int tpb = 32 / upt;        // tiles per batch
-    const uint32_t box_bytes = static_cast<uint32_t>(p.unit) * (kDim + 4);
+    // bytes a box moves from global memory (the FP4 tensor map counts the packed
+    // bytes it reads, not the padded bytes it writes to shared memory)
+    const uint32_t box_bytes = static_cast<uint32_t>(p.unit) * (kFp4 ? kMxTokenBytes : kTokenBytes);
     int st = 0;
     uint32_t ph = 0;
     int qs = 0;
@@ -569,56 +592,122 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     }
   } else if (warp == 1) {
     // =========================== MMA issuer ===========================
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_e4m3_f32(kTile, C::N);
-      int st = 0, as = 0, qs = 0;
-      uint32_t ph = 0, aph = 0, qph = 0;
-      int q_group = -1;
-      long long ai = 0;  // active tiles issued
-      Walker W;
-      W.init(p, s_g0, s_t0, count);
-      bool ok = true;
-      while (W.left > 0 && ok) {
-        if (tile_active(W.G, W.t)) {
-          if (W.g != q_group) {
-            if (q_group >= 0) {
-              umma_commit(&q_empty[qs]);
-              if (++qs == 2) {
-                qs = 0;
-                qph ^= 1u;
-              }
+    // One lane issues the tensor-core work. For MXFP4 tiles the whole warp
+    // first moves the tile's scale words into the copy layout: lane m gathers
+    // the words of rows m, m + 32, m + 64, m + 96 into one 16-byte line, and the
+    // issuing lane then copies the 32 lines into tensor memory
+    // (tcgen05.cp.32x128b.warpx4: line m lands in lane m of every lane quarter,
+    // so row r finds its word in lane r, column r / 32, where the block-scaled
+    // MMA reads it) ahead of the tile's MMAs. Copy and MMAs are issued by one
+    // thread and execute in issue order.
+    constexpr uint32_t idesc = idesc_e4m3_f32(kTile, C::N);
+    int st = 0, as = 0, qs = 0;
+    uint32_t ph = 0, aph = 0, qph = 0;
+    int q_group = -1;
+    long long ai = 0;  // active tiles issued
+    Walker W;
+    W.init(p, s_g0, s_t0, count);
+    // e4m3 k: only lane 0 runs the loop. MXFP4 k: the whole warp does (it stages
+    // the scales); lane 0 waits and the answer is shared with the warp.
+    auto wait0 = [&](uint64_t* bar, uint32_t par, unsigned site, int idx) -> bool {
+      if constexpr (!kFp4) {
+        return wait_bar(bar, par, abort_flag, site, ai, W.g, W.t, idx);
+      } else {
+        bool got = true;
+        if (lane == 0) got = wait_bar(bar, par, abort_flag, site, ai, W.g, W.t, idx);
+        return __shfl_sync(0xFFFFFFFFu, got, 0);
+      }
+    };
+    if constexpr (kFp4) {
+      // q's scales: 1.0 (E8M0 code 127) everywhere, copied once before the first MMA
+      *reinterpret_cast<uint4*>(sf_lines + C::kStages * 512 + lane * 16) =
+          make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tmem_cp_32x128b_warpx4(tmem_base + static_cast<uint32_t>(C::kSfbCol),
+                               lines_desc(smem_u32(sf_lines + C::kStages * 512)));
+      }
+    }
+    bool ok = kFp4 || lane == 0;
+    while (W.left > 0 && ok) {
+      if (tile_active(W.G, W.t)) {
+        if (W.g != q_group) {
+          if (q_group >= 0) {
+            if (lane == 0) umma_commit(&q_empty[qs]);
+            if (++qs == 2) {
+              qs = 0;
+              qph ^= 1u;
             }
-            if (!wait_bar(&q_full[qs], qph, abort_flag, 3u, ai, W.g, W.t, qs)) break;
-            q_group = W.g;
           }
-          if (!wait_bar(&full[st], ph, abort_flag, 4u, ai, W.g, W.t, st)) break;
-          if (!wait_bar(&acc_empty[as], aph ^ 1u, abort_flag, 5u, ai, W.g, W.t, as)) break;
+          if (!wait0(&q_full[qs], qph, 3u, qs)) break;
+          q_group = W.g;
+        }
+        if constexpr (kFp4) {
+          // every lane reads the loaded scale words, so every lane waits for the stage
+          const bool got = wait_bar(&full[st], ph, abort_flag, 4u, ai, W.g, W.t, st);
+          if (!__all_sync(0xFFFFFFFFu, got)) break;
+          const uint8_t* sc = sc_s + st * kScaleStageBytes;
+          uint32_t v[4];
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            // row r is word r % unit of scale box r / unit (powers of two: shifts, no division)
+            const int r = lane + 32 * q4;
+            v[q4] = *reinterpret_cast<const uint32_t*>(sc + ((r >> p.unit_shift) << p.slot_shift) +
+                                                       ((r & (p.unit - 1)) << 2));
+          }
+          *reinterpret_cast<uint4*>(sf_lines + st * 512 + lane * 16) = make_uint4(v[0], v[1], v[2], v[3]);
+          fence_proxy_async_smem();  // the copy reads these lines through the async proxy
+          __syncwarp();
+        } else {
+          if (!wait0(&full[st], ph, 4u, st)) break;
+        }
+        if (!wait0(&acc_empty[as], aph ^ 1u, 5u, as)) break;
+        if (lane == 0) {
           tc_fence_after();
           const uint64_t a_desc = sw128_kmajor_desc(smem_u32(kv_s + st * kKvStageBytes));
           const uint64_t b_desc = sw128_kmajor_desc(smem_u32(q_s + qs * C::kQStageBytes));
           const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(as * C::N);
+          if constexpr (kFp4) {
+            // the FP4 tile sits in shared memory as 16-element groups padded to 16
+            // bytes, so a K block of 32 elements spans 32 bytes exactly as e4m3 does;
+            // K block k takes byte k of every scale word
+            constexpr uint32_t mx = idesc_mx_e2m1_e4m3(kTile, C::N);
+            const uint32_t sfa = tmem_base + static_cast<uint32_t>(C::kSfaCol + 4 * st);
+            const uint32_t sfb = tmem_base + static_cast<uint32_t>(C::kSfbCol);
+            tmem_cp_32x128b_warpx4(sfa, lines_desc(smem_u32(sf_lines + st * 512)));
 #pragma unroll
-          for (int k = 0; k < kDim / 32; ++k) {
-            // +32 bytes along K inside the 128-byte swizzled rows = +2 in the >>4 address field
-            umma_e4m3(d_tmem, a_desc + 2 * k, b_desc + 2 * k, idesc, k > 0 ? 1u : 0u);
+            for (int k = 0; k < kDim / 32; ++k) {
+              umma_mx_e2m1_e4m3(d_tmem, a_desc + 2 * k, b_desc + 2 * k,
+                                idesc_with_scale_ids(mx, static_cast<uint32_t>(k), static_cast<uint32_t>(k)),
+                                sfa, sfb, k > 0 ? 1u : 0u);
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < kDim / 32; ++k) {
+              // +32 bytes along K inside the 128-byte swizzled rows = +2 in the >>4 address field
+              umma_e4m3(d_tmem, a_desc + 2 * k, b_desc + 2 * k, idesc, k > 0 ? 1u : 0u);
+            }
           }
           if ((ai + 1) % C::kCommit == 0) umma_commit(&acc_full[(ai / C::kCommit) % C::kAccFull]);
-          ++ai;
-          if (++st == C::kStages) {
-            st = 0;
-            ph ^= 1u;
-          }
-          if (++as == C::kAccStages) {
-            as = 0;
-            aph ^= 1u;
-          }
         }
-        W.advance(p);
+        if constexpr (kFp4) __syncwarp();
+        ++ai;
+        if (++st == C::kStages) {
+          st = 0;
+          ph ^= 1u;
+        }
+        if (++as == C::kAccStages) {
+          as = 0;
+          aph ^= 1u;
+        }
       }
+      W.advance(p);
+    }
+    if (lane == 0) {
       // an unfinished commit group (odd tile count) still needs its commit
       if (ai % C::kCommit != 0) umma_commit(&acc_full[((ai - 1) / C::kCommit) % C::kAccFull]);
       if (q_group >= 0) umma_commit(&q_empty[qs]);
-      (void)ok;
     }
     __syncwarp();
   } else {
@@ -635,6 +724,8 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     const int wg = ew / 4;
     const int quarter = warp & 3;  // tensor-memory lanes this warp may read
     const int trow = quarter * 32 + lane;
+    // this thread's token row inside a stage's scale boxes: word trow % unit of box trow / unit
+    const int sc_off = ((trow >> p.unit_shift) << p.slot_shift) + ((trow & (p.unit - 1)) << 2);
     float* wsm = w_s + ew * NQ * 64;
     // private histogram of this warp's visible logits for the current group;
     // flushed to the row's global histogram when the warp moves to another group
@@ -776,9 +867,8 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
           stop = true;
           break;
         }
-        const int box = trow / p.unit;
-        const float scale = *reinterpret_cast<const float*>(
-            sc_s + st * kScaleStageBytes + box * p.scale_slot + (trow - box * p.unit) * 4);
+        // the token's fp32 scale (the MXFP4 block scales were applied by the MMA)
+        const float scale = kFp4 ? 1.0f : *reinterpret_cast<const float*>(sc_s + st * kScaleStageBytes + sc_off);
         if (cg != waited_cg) {
           got = wait_bar(&acc_full[af], afph, abort_flag, 7u, a, g, t, af);
           if (!__all_sync(0xFFFFFFFFu, got)) {
@@ -865,16 +955,17 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   if (warp == 1) tmem_dealloc(tmem_base, C::kTmemCols);
 }
 
-template <int NQ, bool kOutBf16>
+template <int NQ, bool kOutBf16, bool kFp4 = false>
 idx_status_t launch_logits(const CUtensorMap& mq, const CUtensorMap& mkv, const CUtensorMap& msc,
                            const LogitsParams& p, int grid, cudaStream_t stream, const char* fn) {
-  auto kern = mqa_logits_kernel<NQ, kOutBf16>;
+  using C = Cfg<NQ, kFp4>;
+  auto kern = mqa_logits_kernel<NQ, kOutBf16, kFp4>;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cfg<NQ>::kSmemBytes);
+                                         C::kSmemBytes);
     // all of the unified L1 / shared memory as shared memory, so kCtasPerSm CTAs fit
     if (e == cudaSuccess) {
       e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -883,20 +974,27 @@ idx_status_t launch_logits(const CUtensorMap& mq, const CUtensorMap& mkv, const 
     if (e != cudaSuccess) return fail(IDX_ERR_CUDA, "%s: cudaFuncSetAttribute: %s", fn, cudaGetErrorString(e));
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  kern<<<grid, Cfg<NQ>::kThreads, Cfg<NQ>::kSmemBytes, stream>>>(mq, mkv, msc, p);
+  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(mq, mkv, msc, p);
   return check_launch(fn);
 }
 
 idx_status_t dispatch(int nq_tmpl, const CUtensorMap& mq, const CUtensorMap& mkv,
                       const CUtensorMap& msc, const LogitsParams& p, long long max_tiles,
-                      cudaStream_t stream, const char* fn) {
+                      cudaStream_t stream, const char* fn, bool fp4 = false) {
   const int sms = device_sm_count();
   if (sms <= 0) return fail(IDX_ERR_CUDA, "%s: cannot query the SM count", fn);
   // persistent: kCtasPerSm CTAs on every SM (fewer when there are fewer tiles)
-  const int per_sm = nq_tmpl == 1 ? Cfg<1>::kCtasPerSm : (nq_tmpl == 2 ? Cfg<2>::kCtasPerSm : Cfg<4>::kCtasPerSm);
+  const int per_sm = fp4 ? Cfg<1, true>::kCtasPerSm
+                         : (nq_tmpl == 1 ? Cfg<1>::kCtasPerSm
+                                         : (nq_tmpl == 2 ? Cfg<2>::kCtasPerSm : Cfg<4>::kCtasPerSm));
   long long grid = static_cast<long long>(sms) * per_sm;
   if (max_tiles >= 0 && max_tiles < grid) grid = max_tiles;
   if (grid <= 0) return IDX_OK;
+  if (fp4) {
+    if (nq_tmpl != 1) return fail(IDX_ERR_UNSUPPORTED, "%s: the MXFP4 path serves one query per group", fn);
+    return p.out_bf16 ? launch_logits<1, true, true>(mq, mkv, msc, p, static_cast<int>(grid), stream, fn)
+                      : launch_logits<1, false, true>(mq, mkv, msc, p, static_cast<int>(grid), stream, fn);
+  }
   switch (nq_tmpl) {
     case 1:
       return p.out_bf16 ? launch_logits<1, true>(mq, mkv, msc, p, static_cast<int>(grid), stream, fn)
@@ -982,13 +1080,17 @@ unsigned int logits_read_and_clear_error(cudaStream_t stream, cudaError_t* err, 
 
 using namespace idx;
 
-extern "C" idx_status_t idx_paged_mqa_logits_decode(
-    const uint8_t* q, int64_t ld_q, const void* w, int w_dtype, int64_t ld_w, const uint8_t* cache,
-    int32_t num_blocks, int32_t block_size, int64_t block_stride_bytes, const int32_t* block_table,
-    int64_t ld_bt, const int32_t* ctx_lens, int32_t B, int32_t next_n, const int32_t* sparse_idx,
-    int64_t ld_si, int32_t n_si, const int32_t* end, int32_t sbk, void* logits, int out_dtype,
-    int64_t ld_out, void* ws, size_t ws_bytes, cudaStream_t stream) {
-  const char* fn = "idx_paged_mqa_logits_decode";
+namespace {
+
+// Both paged decode entry points: the e4m3 cache (132 bytes per token, fp32
+// token scale) and the MXFP4 cache (68 bytes per token, E8M0 block scales).
+idx_status_t paged_decode(const char* fn, bool fp4, const uint8_t* q, int64_t ld_q, const void* w,
+                          int w_dtype, int64_t ld_w, const uint8_t* cache, int32_t num_blocks,
+                          int32_t block_size, int64_t block_stride_bytes, const int32_t* block_table,
+                          int64_t ld_bt, const int32_t* ctx_lens, int32_t B, int32_t next_n,
+                          const int32_t* sparse_idx, int64_t ld_si, int32_t n_si, const int32_t* end,
+                          int32_t sbk, void* logits, int out_dtype, int64_t ld_out, void* ws,
+                          size_t ws_bytes, cudaStream_t stream) {
   if (B < 0 || next_n < 1) return fail(IDX_ERR_INVALID_ARG, "%s: B < 0 or next_n < 1", fn);
   if (B == 0) return IDX_OK;
   const int64_t rows64 = static_cast<int64_t>(B) * next_n;
@@ -1001,11 +1103,16 @@ extern "C" idx_status_t idx_paged_mqa_logits_decode(
   if (!(block_size == 16 || block_size == 32 || block_size == 64 || block_size == 128)) {
     return fail(IDX_ERR_UNSUPPORTED, "%s: block_size %d is not one of 16, 32, 64, 128", fn, block_size);
   }
-  if (block_stride_bytes < static_cast<int64_t>(block_size) * kTokenBytes) {
-    return fail(IDX_ERR_INVALID_ARG, "%s: block_stride_bytes < block_size * 132", fn);
+  const int token_bytes = fp4 ? kMxTokenBytes : kTokenBytes;
+  const int row_bytes = fp4 ? kDim / 2 : kDim;  // element bytes of one token
+  if (block_stride_bytes < static_cast<int64_t>(block_size) * token_bytes) {
+    return fail(IDX_ERR_INVALID_ARG, "%s: block_stride_bytes < block_size * %d", fn, token_bytes);
   }
-  if (block_stride_bytes % 16 != 0 || !aligned(cache, 16)) {
-    return fail(IDX_ERR_UNSUPPORTED, "%s: cache must be 16-byte aligned with a stride multiple of 16", fn);
+  // the FP4 tensor map reads 32-byte aligned packed rows
+  const int align = fp4 ? 32 : 16;
+  if (block_stride_bytes % align != 0 || !aligned(cache, align)) {
+    return fail(IDX_ERR_UNSUPPORTED, "%s: cache must be %d-byte aligned with a stride multiple of %d", fn,
+                align, align);
   }
   if (ld_bt < 1) return fail(IDX_ERR_INVALID_ARG, "%s: ld_bt < 1", fn);
 
@@ -1047,8 +1154,9 @@ extern "C" idx_status_t idx_paged_mqa_logits_decode(
     p.sbk = sbk;
     max_tiles = static_cast<long long>(p.n_groups) * p.tiles_per_group;
   } else {
-    if (!(next_n == 1 || next_n == 2 || next_n == 4)) {
-      return fail(IDX_ERR_UNSUPPORTED, "%s: dense decode supports next_n 1, 2 or 4 (got %d)", fn, next_n);
+    if (!(next_n == 1 || next_n == 2 || next_n == 4) || (fp4 && next_n != 1)) {
+      return fail(IDX_ERR_UNSUPPORTED, "%s: dense decode supports next_n %s (got %d)", fn,
+                  fp4 ? "1" : "1, 2 or 4", next_n);
     }
     p.mode = kDecodeDense;
     p.n_groups = B;
@@ -1057,6 +1165,8 @@ extern "C" idx_status_t idx_paged_mqa_logits_decode(
     nq_tmpl = next_n;
   }
   p.scale_slot = p.unit * 4 < 128 ? 128 : p.unit * 4;
+  p.unit_shift = __builtin_ctz(static_cast<unsigned>(p.unit));
+  p.slot_shift = __builtin_ctz(static_cast<unsigned>(p.scale_slot));
   st = attach_histogram(fn, &p, nq_tmpl, rows, ws, ws_bytes);
   if (st != IDX_OK) return st;
 
@@ -1064,24 +1174,52 @@ extern "C" idx_status_t idx_paged_mqa_logits_decode(
   st = make_q_map(&mq, q, ld_q, rows, nq_tmpl);
   if (st != IDX_OK) return st;
   {
+    // MXFP4: 128 four-bit elements per row (64 packed bytes) that the copy spreads
+    // into 16-byte groups of 16 elements, giving the same 128-byte shared-memory
+    // rows and swizzle as e4m3
     const uint64_t dims[3] = {static_cast<uint64_t>(kDim), static_cast<uint64_t>(block_size),
                               static_cast<uint64_t>(num_blocks)};
-    const uint64_t strides[2] = {static_cast<uint64_t>(kDim), static_cast<uint64_t>(block_stride_bytes)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(row_bytes), static_cast<uint64_t>(block_stride_bytes)};
     const uint32_t box[3] = {static_cast<uint32_t>(kDim), static_cast<uint32_t>(p.unit), 1u};
-    st = encode_tensor_map(&mkv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, cache, dims, strides, box,
-                           CU_TENSOR_MAP_SWIZZLE_128B);
+    st = encode_tensor_map(&mkv, fp4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                           3, cache, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != IDX_OK) return st;
   }
   {
     const uint64_t dims[2] = {static_cast<uint64_t>(block_size), static_cast<uint64_t>(num_blocks)};
     const uint64_t strides[1] = {static_cast<uint64_t>(block_stride_bytes)};
     const uint32_t box[2] = {static_cast<uint32_t>(p.unit), 1u};
+    // one 4-byte word per token: the fp32 scale, or the four E8M0 block codes
     st = encode_tensor_map(&msc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
-                           cache + static_cast<int64_t>(block_size) * kDim, dims, strides, box,
+                           cache + static_cast<int64_t>(block_size) * row_bytes, dims, strides, box,
                            CU_TENSOR_MAP_SWIZZLE_NONE);
     if (st != IDX_OK) return st;
   }
-  return dispatch(nq_tmpl, mq, mkv, msc, p, max_tiles, stream, fn);
+  return dispatch(nq_tmpl, mq, mkv, msc, p, max_tiles, stream, fn, fp4);
+}
+
+}  // namespace
+
+extern "C" idx_status_t idx_paged_mqa_logits_decode(
+    const uint8_t* q, int64_t ld_q, const void* w, int w_dtype, int64_t ld_w, const uint8_t* cache,
+    int32_t num_blocks, int32_t block_size, int64_t block_stride_bytes, const int32_t* block_table,
+    int64_t ld_bt, const int32_t* ctx_lens, int32_t B, int32_t next_n, const int32_t* sparse_idx,
+    int64_t ld_si, int32_t n_si, const int32_t* end, int32_t sbk, void* logits, int out_dtype,
+    int64_t ld_out, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  return paged_decode("idx_paged_mqa_logits_decode", false, q, ld_q, w, w_dtype, ld_w, cache, num_blocks,
+                      block_size, block_stride_bytes, block_table, ld_bt, ctx_lens, B, next_n, sparse_idx,
+                      ld_si, n_si, end, sbk, logits, out_dtype, ld_out, ws, ws_bytes, stream);
+}
+
+extern "C" idx_status_t idx_paged_mqa_logits_decode_mxfp4(
+    const uint8_t* q, int64_t ld_q, const void* w, int w_dtype, int64_t ld_w, const uint8_t* cache,
+    int32_t num_blocks, int32_t block_size, int64_t block_stride_bytes, const int32_t* block_table,
+    int64_t ld_bt, const int32_t* ctx_lens, int32_t B, int32_t next_n, const int32_t* sparse_idx,
+    int64_t ld_si, int32_t n_si, const int32_t* end, int32_t sbk, void* logits, int out_dtype,
+    int64_t ld_out, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  return paged_decode("idx_paged_mqa_logits_decode_mxfp4", true, q, ld_q, w, w_dtype, ld_w, cache,
+                      num_blocks, block_size, block_stride_bytes, block_table, ld_bt, ctx_lens, B, next_n,
+                      sparse_idx, ld_si, n_si, end, sbk, logits, out_dtype, ld_out, ws, ws_bytes, stream);
 }
 
 extern "C" idx_status_t idx_mqa_logits_prefill(const uint8_t* q, int64_t ld_q, const void* w,
@@ -1147,6 +1285,8 @@ extern "C" idx_status_t idx_mqa_logits_prefill(const uint8_t* q, int64_t ld_q, c
     nq_tmpl = 4;
   }
   p.scale_slot = p.unit * 4 < 128 ? 128 : p.unit * 4;
+  p.unit_shift = __builtin_ctz(static_cast<unsigned>(p.unit));
+  p.slot_shift = __builtin_ctz(static_cast<unsigned>(p.scale_slot));
   st = attach_histogram(fn, &p, nq_tmpl, T, ws, ws_bytes);
   if (st != IDX_OK) return st;
   CUtensorMap mq, mkv, msc;

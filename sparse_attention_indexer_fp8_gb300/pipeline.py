@@ -8,7 +8,8 @@ expansion, sparse logits, sparse top-k with remap, slot conversion), and
 ``DcpDecodeStep`` those of one rank of a context-parallel decode step (scoring
 of the rank's own shard, local top-k with scores, one exchange, merge). Buffers
 are allocated once at construction; ``run`` allocates nothing but the exchange's
-receive lists.
+receive lists. ``kv="mxfp4"`` selects the MXFP4 indexer cache (the V4.1 format)
+for the cache fill and the decode and hierarchical steps.
 """
 
 from __future__ import annotations
@@ -16,18 +17,33 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import (idx_dcp_topk_merge, idx_expand_candidates, idx_k_quant_and_cache,
-               idx_paged_mqa_logits_decode, idx_req_to_global_slots, idx_sparse_topk_remap, idx_topk)
+from . import (idx_dcp_topk_merge, idx_expand_candidates, idx_k_quant_and_cache, idx_k_quant_and_cache_mxfp4,
+               idx_paged_mqa_logits_decode, idx_paged_mqa_logits_decode_mxfp4, idx_req_to_global_slots,
+               idx_sparse_topk_remap, idx_topk)
 from . import workloads as W
 
 
+def _insert(kv: str):
+    return idx_k_quant_and_cache_mxfp4 if kv == "mxfp4" else idx_k_quant_and_cache
+
+
+def _decode_logits(kv: str):
+    return idx_paged_mqa_logits_decode_mxfp4 if kv == "mxfp4" else idx_paged_mqa_logits_decode
+
+
+def cache_block_stride(kv: str = "fp8", block_size: int = W.BLOCK_SIZE) -> int:
+    """Bytes per block of the cache format (512-byte aligned): 8704 (e4m3) or 4608 (MXFP4) for 64 tokens."""
+    return W.mxfp4_block_stride_bytes(block_size) if kv == "mxfp4" else W.block_stride_bytes(block_size)
+
+
 def fill_paged_cache(pool: W.PagedPool, seed: int, cache: torch.Tensor, device_k: bool = False,
-                     chunk_tokens: int = 1 << 21, stream=None) -> None:
-    """Quantise and insert every request's k into ``cache`` through ``idx_k_quant_and_cache``.
+                     chunk_tokens: int = 1 << 21, stream=None, kv: str = "fp8") -> None:
+    """Quantise and insert every request's k into ``cache`` through the cache format's insert.
 
     k comes from ``workloads.make_k`` (host generator) or, with ``device_k``,
     from ``workloads.make_k_device`` (for pools too large to draw on the host).
     """
+    idx_k_quant_and_cache = _insert(kv)
     dev = cache.device
     if device_k:
         for b in range(len(pool.ctx_lens)):
@@ -63,9 +79,11 @@ class DecodeStep:
     """One dense decode step of the indexer for a fixed batch shape."""
 
     def __init__(self, batch: int, max_ctx: int, topk: int = W.TOPK, next_n: int = 1,
-                 block_size: int = W.BLOCK_SIZE, block_span: int | None = None, device="cuda"):
+                 block_size: int = W.BLOCK_SIZE, block_span: int | None = None, device="cuda",
+                 kv: str = "fp8"):
         rows = batch * next_n
         self.batch, self.next_n, self.topk = batch, next_n, topk
+        self.insert, self.logits_call = _insert(kv), _decode_logits(kv)
         self.block_size = block_size
         self.block_span = block_size if block_span is None else block_span
         ld = (max_ctx + 63) // 64 * 64   # 256-byte aligned rows: vector loads in the selection
@@ -80,9 +98,9 @@ class DecodeStep:
             stream=None):
         """Insert new k (optional), score, select, convert; returns the slot table."""
         if new_k is not None:
-            idx_k_quant_and_cache(new_k, new_slots, cache, self.block_size, stream=stream)
-        idx_paged_mqa_logits_decode(q, w, cache, self.block_size, block_table, ctx_lens, self.logits,
-                                    next_n=self.next_n, ws=self.ws, stream=stream)
+            self.insert(new_k, new_slots, cache, self.block_size, stream=stream)
+        self.logits_call(q, w, cache, self.block_size, block_table, ctx_lens, self.logits,
+                         next_n=self.next_n, ws=self.ws, stream=stream)
         ke = ctx_lens if (row_ke is None and self.next_n == 1) else row_ke
         # selection with the slot conversion fused into its output pass
         idx_topk(self.logits, None, ke, self.topk, self.local, ws=self.ws, stream=stream,
@@ -111,8 +129,10 @@ class HierarchicalStep:
     """
 
     def __init__(self, rows: int, n_cand: int, cand_block_size: int = 64, sbk: int = 64,
-                 topk: int = W.TOPK, block_size: int = W.BLOCK_SIZE, device="cuda", next_n: int = 1):
+                 topk: int = W.TOPK, block_size: int = W.BLOCK_SIZE, device="cuda", next_n: int = 1,
+                 kv: str = "fp8"):
         R = cand_block_size // sbk
+        self.logits_call = _decode_logits(kv)
         self.cand_block_size, self.sbk, self.topk, self.block_size = cand_block_size, sbk, topk, block_size
         self.next_n = next_n
         self.sparse_idx = torch.empty((rows, n_cand * R), dtype=torch.int32, device=device)
@@ -133,9 +153,9 @@ class HierarchicalStep:
 
     def score(self, q, w, cache, block_table, ctx_lens, stream=None):
         """One consumer layer on the current expansion; returns the slot table."""
-        idx_paged_mqa_logits_decode(q, w, cache, self.block_size, block_table, ctx_lens, self.logits,
-                                    next_n=self.next_n, sparse_idx=self.sparse_idx, end=self.end,
-                                    sbk=self.sbk, ws=self.ws, stream=stream)
+        self.logits_call(q, w, cache, self.block_size, block_table, ctx_lens, self.logits,
+                         next_n=self.next_n, sparse_idx=self.sparse_idx, end=self.end,
+                         sbk=self.sbk, ws=self.ws, stream=stream)
         idx_sparse_topk_remap(self.logits, self.end, self.sparse_idx, None, self.sbk, self.topk,
                               self.positions, col_scratch=self.cols, ws=self.ws, stream=stream,
                               slots=self.slots, block_table=block_table, block_size=self.block_size,

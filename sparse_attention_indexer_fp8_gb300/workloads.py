@@ -36,6 +36,15 @@ def block_stride_bytes(block_size: int = BLOCK_SIZE, align: int = BLOCK_ALIGN) -
     return (raw + align - 1) // align * align
 
 
+MXFP4_TOKEN_BYTES = 68      # MXFP4 cache: 64 bytes of e2m1 elements + 4 E8M0 block scales
+
+
+def mxfp4_block_stride_bytes(block_size: int = BLOCK_SIZE, align: int = BLOCK_ALIGN) -> int:
+    """Bytes per MXFP4 cache block: ``block_size * 68`` rounded up to ``align`` (4608 for 64 tokens)."""
+    raw = block_size * MXFP4_TOKEN_BYTES
+    return (raw + align - 1) // align * align
+
+
 def _gen(seed: int, *stream: int) -> torch.Generator:
     g = torch.Generator()
     s = int(seed)

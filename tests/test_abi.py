@@ -98,6 +98,19 @@ def test_validation_rejects_before_touching_the_device(lib):
     # dense decode with next_n = 3
     assert lib.idx_paged_mqa_logits_decode(fake, 8192, fake, 0, 64, fake, 16, 64, 8704, fake, 8, fake,
                                            2, 3, None, 0, 0, None, 0, fake, 0, 4096, None, 0, None) == 2
+    # MXFP4 cache: stride below 64 * 68, stride not a multiple of 32, block size, misaligned cache
+    assert lib.idx_k_quant_and_cache_mxfp4(fake, 1, 128, 4, fake, fake, 8, 64, 4350, None) == 1
+    assert lib.idx_k_quant_and_cache_mxfp4(fake, 1, 128, 4, fake, fake, 8, 64, 4368, None) == 2
+    assert lib.idx_k_quant_and_cache_mxfp4(fake, 1, 128, 4, fake, fake, 8, 48, 4608, None) == 2
+    assert lib.idx_k_quant_and_cache_mxfp4(fake, 1, 128, 4, fake, ctypes.c_void_p(0x1010), 8, 64, 4608,
+                                           None) == 2
+    # MXFP4 decode: dense next_n 2, a stride that is not a multiple of 32, too small a stride
+    assert lib.idx_paged_mqa_logits_decode_mxfp4(fake, 8192, fake, 0, 64, fake, 16, 64, 4608, fake, 8, fake,
+                                                 2, 2, None, 0, 0, None, 0, fake, 0, 4096, None, 0, None) == 2
+    assert lib.idx_paged_mqa_logits_decode_mxfp4(fake, 8192, fake, 0, 64, fake, 16, 64, 4368, fake, 8, fake,
+                                                 2, 1, None, 0, 0, None, 0, fake, 0, 4096, None, 0, None) == 2
+    assert lib.idx_paged_mqa_logits_decode_mxfp4(fake, 8192, fake, 0, 64, fake, 16, 64, 4096, fake, 8, fake,
+                                                 2, 1, None, 0, 0, None, 0, fake, 0, 4096, None, 0, None) == 1
     # misaligned q stride
     assert lib.idx_mqa_logits_prefill(fake, 8200, fake, 0, 64, fake, fake, 64, None, fake, 4, None, 0,
                                       0, None, 0, fake, 0, 64, None, 0, None) == 2

@@ -18,7 +18,7 @@ from oracle import indexer as O
 from oracle.codecs import bf16_decode
 from sparse_attention_indexer_fp8_gb300 import workloads as W
 from sparse_attention_indexer_fp8_gb300.pipeline import (DcpDecodeStep, DecodeStep, HierarchicalStep,
-                                                         fill_paged_cache)
+                                                         cache_block_stride, fill_paged_cache)
 from tests.checks import assert_logits_close, assert_topk_row
 
 pytestmark = pytest.mark.gpu
@@ -75,11 +75,11 @@ def _k_host(seed, b, n):
     return bf16_decode(W.make_k_device(seed, b, n, DEV).view(torch.int16).cpu().numpy().view(np.uint16))
 
 
-def _decode(wl, n_rows):
+def _decode(wl, n_rows, kv="fp8"):
     pool = wl.pool
-    cache = torch.zeros((pool.num_blocks, W.block_stride_bytes()), dtype=torch.uint8, device=DEV)
-    fill_paged_cache(pool, wl.seed, cache, device_k=True)
-    stp = DecodeStep(wl.batch, int(pool.ctx_lens.max()))
+    cache = torch.zeros((pool.num_blocks, cache_block_stride(kv)), dtype=torch.uint8, device=DEV)
+    fill_paged_cache(pool, wl.seed, cache, device_k=True, kv=kv)
+    stp = DecodeStep(wl.batch, int(pool.ctx_lens.max()), kv=kv)
     bt = torch.from_numpy(pool.block_table).to(DEV)
     ctx = torch.from_numpy(pool.ctx_lens).to(DEV)
     slots = stp.run(torch.from_numpy(wl.q8).to(DEV), torch.from_numpy(wl.w).to(DEV), cache, bt, ctx)
@@ -98,10 +98,18 @@ def _decode(wl, n_rows):
     rest = [b for b in range(wl.batch) if b not in ends]
     for b in sorted(ends | set(rng.choice(rest, size=n_rows - len(ends), replace=False).tolist())):
         L = int(pool.ctx_lens[b])
-        k8, ks = O.k_quant(_k_host(wl.seed, b, L))
-        ref = O.logits_row(wl.q8[b], wl.w[b], k8, ks)
+        if kv == "mxfp4":
+            ref = O.logits_row_values(wl.q8[b], wl.w[b], O.mxfp4_values(*O.mxfp4_quant(_k_host(wl.seed, b, L))))
+        else:
+            k8, ks = O.k_quant(_k_host(wl.seed, b, L))
+            ref = O.logits_row(wl.q8[b], wl.w[b], k8, ks)
         assert_logits_close(lg[b, :L], ref, f"row {b}")
         assert_topk_row(loc[b], ref, wl.topk, f"top-k row {b}")
+
+
+def test_long_decode_mxfp4_b128_64k_128k():
+    # the long-context decode workload on the MXFP4 indexer cache (the V4.1 format)
+    _decode(W.long_decode(), 12, kv="mxfp4")
 
 
 def test_paged_decode_b64_8k_32k():

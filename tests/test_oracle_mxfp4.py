@@ -201,3 +201,14 @@ def test_mxfp4_sparse_logits_equal_dense_at_mapped_positions():
                     assert sp[r, c] == dense[r, O.sparse_column_token(si[r], c, sbk)]
                 else:
                     assert sp[r, c] == -np.inf
+
+
+def test_mxfp4_gather_equals_token_by_token_reads():
+    ctx = np.array([300, 129])
+    pool, cache, _ = _mx_pool(8, ctx, bs=64)
+    for b in range(2):
+        pos = np.random.default_rng(b).permutation(int(ctx[b]))[:50]
+        got = O.mxfp4_gather_values(cache, 64, pool.block_table[b], pos)
+        for i, p in enumerate(pos):
+            c, s = O.mxfp4_cache_token(cache, 64, int(pool.block_table[b][p // 64]), int(p) % 64)
+            assert np.array_equal(got[i], O.mxfp4_values(c, s)[0])
