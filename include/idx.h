@@ -545,6 +545,24 @@ idx_status_t idx_paged_mqa_topk_decode_noalloc(const uint8_t* q, int64_t ld_q, c
  */
 idx_status_t idx_block_span(int64_t block_stride, int64_t token_stride, int32_t* span);
 
+/*
+ * idx_diag_mma_peak - diagnostic: keep every SM's tensor core busy with dense MMAs.
+ *
+ * Not part of the indexer's path: a measurement aid for the roofline of the
+ * tensor-bound prefill scoring, whose denominator is this GPU's dense FP8
+ * tensor-core rate. Launches `ctas` persistent CTAs (<= 0: one per SM), each
+ * issuing `iters` back-to-back tcgen05.mma of shape 128 x 256 x K from fixed
+ * shared-memory operands into tensor memory (kind IDX_DIAG_E4M3: e4m3 x e4m3,
+ * K = 32; IDX_DIAG_BF16: bf16 x bf16, K = 16; fp32 accumulation). The caller
+ * times the launch on `stream`; *flop_out (if not NULL) receives the FLOP it
+ * performs, 2 * 128 * 256 * K * iters * ctas. Allocates nothing; every wait is
+ * bounded (idx_device_error reports an expired one).
+ * Errors: IDX_ERR_UNSUPPORTED for another kind; IDX_ERR_INVALID_ARG for
+ * iters < 1 or more CTAs than SMs.
+ */
+enum { IDX_DIAG_E4M3 = 0, IDX_DIAG_BF16 = 1 };
+idx_status_t idx_diag_mma_peak(int kind, int32_t iters, int32_t ctas, double* flop_out, cudaStream_t stream);
+
 /* Bytes of the optional selection workspace of an operation for `rows` rows (host only). */
 size_t idx_workspace_bytes(int op, int32_t rows, int32_t max_cols, int32_t k);
 

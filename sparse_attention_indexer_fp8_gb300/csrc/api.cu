@@ -141,14 +141,17 @@ idx_status_t idx_device_error(cudaStream_t stream) {
   if (e != cudaSuccess) return idx::fail(IDX_ERR_CUDA, "idx_device_error: %s", cudaGetErrorString(e));
   unsigned int d = idx::topk_read_and_clear_error(stream, &e);
   if (e != cudaSuccess) return idx::fail(IDX_ERR_CUDA, "idx_device_error: %s", cudaGetErrorString(e));
-  if (a || b || c || d) {
+  unsigned int f = idx::diag_read_and_clear_error(stream, &e);
+  if (e != cudaSuccess) return idx::fail(IDX_ERR_CUDA, "idx_device_error: %s", cudaGetErrorString(e));
+  if (a || b || c || d || f) {
     return idx::fail(IDX_ERR_DEVICE,
                      "device error flags: logits 0x%08x (bit w: wait site w expired; first: site %lld "
                      "block %lld tile-ordinal %lld group %lld tile %lld barrier %lld parity %lld), "
                      "index ops 0x%08x (1 = a row's ks is not a multiple of sbk, 2 = a slot "
                      "beyond int32), q rope 0x%08x (1 = a position outside the cos/sin table), "
-                     "top-k 0x%08x (2 = a fused slot beyond int32)",
-                     a, info[0], info[1], info[2], info[3], info[4], info[5], info[6], b, c, d);
+                     "top-k 0x%08x (2 = a fused slot beyond int32), diagnostics 0x%08x (1 = a wait "
+                     "for the tensor core expired)",
+                     a, info[0], info[1], info[2], info[3], info[4], info[5], info[6], b, c, d, f);
   }
   return IDX_OK;
 }

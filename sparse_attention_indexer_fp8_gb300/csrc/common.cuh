@@ -35,6 +35,7 @@ unsigned int logits_read_and_clear_error(cudaStream_t stream, cudaError_t* err, 
 unsigned int index_ops_read_and_clear_error(cudaStream_t stream, cudaError_t* err);
 unsigned int q_rope_read_and_clear_error(cudaStream_t stream, cudaError_t* err);
 unsigned int topk_read_and_clear_error(cudaStream_t stream, cudaError_t* err);
+unsigned int diag_read_and_clear_error(cudaStream_t stream, cudaError_t* err);
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 

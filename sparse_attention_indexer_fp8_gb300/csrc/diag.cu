@@ -1,0 +1,156 @@
+// Diagnostic: the dense tensor-core issue rate of this GPU, for the roofline of
+// the tensor-bound prefill scoring.
+//
+// One persistent CTA per SM (or `ctas`) keeps its SM's tensor core busy with
+// back-to-back tcgen05.mma of the largest single-CTA shape, M = 128, N = 256,
+// K = 32 (e4m3 x e4m3, kind::f8f6f4) or K = 16 (bf16 x bf16, kind::f16), fp32
+// accumulation into two 256-column tensor-memory accumulators used in turn.
+// Operands are fixed tiles in shared memory (128-byte swizzled, K-major), filled
+// with finite non-zero values, so the run measures the tensor pipe and not the
+// memory system. One commit per 64 MMAs bounds the work in flight; every wait is
+// bounded. FLOP per MMA: 2 * 128 * 256 * K.
+#include "common.cuh"
+
+namespace idx {
+namespace {
+
+constexpr int kDiagM = 128;
+constexpr int kDiagN = 256;
+constexpr int kDiagABytes = kDiagM * 128;   // one 128-byte K row per M row
+constexpr int kDiagBBytes = kDiagN * 128;
+constexpr int kDiagBatch = 64;              // MMAs per commit
+
+__device__ unsigned int g_diag_error = 0;
+
+// Instruction descriptor of kind::f16 with bf16 A and B, fp32 accumulation,
+// K-major: D format 1 (f32) in bits 4-5, A/B formats 1 (bf16) in bits 7-9 / 10-12.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+template <bool kBf16>
+__global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint8_t* a_s = smem;
+  uint8_t* b_s = smem + kDiagABytes;
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t s_tmem;
+  const int tid = threadIdx.x;
+  // finite, non-zero operand bytes: e4m3 codes 0x30..0x4F, or bf16 values near 1
+  for (int i = tid; i < (kDiagABytes + kDiagBBytes) / 4; i += blockDim.x) {
+    const uint32_t b = 0x30u + static_cast<uint32_t>((i * 7) & 31);
+    const uint32_t h = 0x3F80u + static_cast<uint32_t>(i & 7);
+    reinterpret_cast<uint32_t*>(smem)[i] = kBf16 ? (h | (h << 16)) : b * 0x01010101u;
+  }
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  if (tid < 32) {
+    tmem_alloc(&s_tmem, 512);
+    tmem_relinquish();
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  if (tid == 0) {
+    const uint64_t a_desc = sw128_kmajor_desc(smem_u32(a_s));
+    const uint64_t b_desc = sw128_kmajor_desc(smem_u32(b_s));
+    const uint32_t idesc = kBf16 ? idesc_bf16_f32(kDiagM, kDiagN) : idesc_e4m3_f32(kDiagM, kDiagN);
+    uint32_t phase = 0;
+    bool pending = false;
+    for (int i = 0; i < iters; ++i) {
+      const uint32_t d = tmem + static_cast<uint32_t>((i / kDiagBatch) & 1) * kDiagN;
+      const int k = i & 3;   // walk the four 32-byte K steps of the 128-byte rows
+      if constexpr (kBf16) {
+        umma_bf16(d, a_desc + 2 * k, b_desc + 2 * k, idesc, i % kDiagBatch != 0);
+      } else {
+        umma_e4m3(d, a_desc + 2 * k, b_desc + 2 * k, idesc, i % kDiagBatch != 0);
+      }
+      if ((i + 1) % kDiagBatch == 0 || i + 1 == iters) {
+        // wait for the previous batch before queueing more (bounded)
+        if (pending) {
+          const uint64_t t0 = global_timer_ns();
+          while (!mbar_try_wait(&bar, phase)) {
+            if (global_timer_ns() - t0 > 2000000000ull) {
+              atomicOr(&g_diag_error, 1u);
+              break;
+            }
+          }
+          phase ^= 1u;
+        }
+        umma_commit(&bar);
+        pending = true;
+      }
+    }
+    if (pending) {
+      const uint64_t t0 = global_timer_ns();
+      while (!mbar_try_wait(&bar, phase)) {
+        if (global_timer_ns() - t0 > 2000000000ull) {
+          atomicOr(&g_diag_error, 1u);
+          break;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (tid < 32) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+unsigned int diag_read_and_clear_error(cudaStream_t stream, cudaError_t* err) {
+  unsigned int v = 0;
+  const unsigned int zero = 0;
+  *err = cudaStreamSynchronize(stream);
+  if (*err != cudaSuccess) return 0;
+  *err = cudaMemcpyFromSymbol(&v, g_diag_error, sizeof(v));
+  if (*err != cudaSuccess) return 0;
+  if (v) *err = cudaMemcpyToSymbol(g_diag_error, &zero, sizeof(zero));
+  return v;
+}
+
+}  // namespace idx
+
+using namespace idx;
+
+extern "C" idx_status_t idx_diag_mma_peak(int kind, int32_t iters, int32_t ctas, double* flop_out,
+                                          cudaStream_t stream) {
+  const char* fn = "idx_diag_mma_peak";
+  if (kind != IDX_DIAG_E4M3 && kind != IDX_DIAG_BF16) return fail(IDX_ERR_UNSUPPORTED, "%s: kind %d", fn, kind);
+  if (iters < 1) return fail(IDX_ERR_INVALID_ARG, "%s: iters < 1", fn);
+  const int sms = device_sm_count();
+  if (sms <= 0) return fail(IDX_ERR_CUDA, "%s: cannot query the SM count", fn);
+  if (ctas <= 0) ctas = sms;
+  if (ctas > sms) return fail(IDX_ERR_INVALID_ARG, "%s: %d CTAs for %d SMs", fn, ctas, sms);
+  // more than half of an SM's shared memory, so no two CTAs share an SM's tensor core
+  const int smem = 120 * 1024;
+  const int k = kind == IDX_DIAG_BF16 ? 16 : 32;
+  if (flop_out) *flop_out = 2.0 * kDiagM * kDiagN * k * static_cast<double>(iters) * ctas;
+  cudaError_t e;
+  if (kind == IDX_DIAG_BF16) {
+    e = cudaFuncSetAttribute(mma_peak_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess) mma_peak_kernel<true><<<ctas, 128, smem, stream>>>(iters);
+  } else {
+    e = cudaFuncSetAttribute(mma_peak_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess) mma_peak_kernel<false><<<ctas, 128, smem, stream>>>(iters);
+  }
+  if (e != cudaSuccess) return fail(IDX_ERR_CUDA, "%s: cudaFuncSetAttribute: %s", fn, cudaGetErrorString(e));
+  return check_launch(fn);
+}

@@ -268,29 +268,6 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
   }
 }
 
-// Block-wide inclusive scan of one int per thread (blockDim.x = kThreads).
-template <int kThreads>
-__device__ __forceinline__ long long block_scan(long long v, long long* warp_tot, long long* total) {
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  long long incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const long long n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-    if (lane >= o) incl += n;
-  }
-  if (lane == 31) warp_tot[warp] = incl;
-  __syncthreads();
-  long long before = 0, all = 0;
-  for (int w = 0; w < kThreads / 32; ++w) {
-    if (w < warp) before += warp_tot[w];
-    all += warp_tot[w];
-  }
-  *total = all;
-  __syncthreads();
-  return before + incl;
-}
-
 // Coordinates of one k box: cache block (0 when contiguous) and row inside it.
 struct Box {
   int blk;
@@ -390,7 +367,6 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   __shared__ int s_abort;
   __shared__ int s_g0, s_t0;
   __shared__ long long s_count;
-  __shared__ long long s_warp_tot[kThreads / 32];
   __shared__ int4 s_tile[2][32];   // producer batches: (group, tile, row0, req)
   __shared__ int2 s_act[2][32];    //                   (act_lo, act_hi)
   __shared__ int s_ntile[2];
@@ -423,44 +399,60 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   }
 
   // ---- this CTA's share of the (group, tile) sequence ----
-  long long total;
+  // Split evenly over the CTAs: [total * b / grid, total * (b + 1) / grid). In
+  // dense decode the tile count of a group follows its context length: the last
+  // warp walks the lengths 32 groups at a time (the total, then the group that
+  // holds this CTA's first tile) while warps 0 and 1 set up the barriers and
+  // tensor memory.
   if (p.mode == kDecodeDense) {
-    long long running = 0;
-    // pass 1: total tile count
-    for (int base = 0; base < p.n_groups; base += kThreads) {
-      const int g = base + threadIdx.x;
-      const long long v = g < p.n_groups ? (max(__ldg(p.ctx_lens + g), 0) + kTile - 1) / kTile : 0;
-      long long chunk;
-      block_scan<kThreads>(v, s_warp_tot, &chunk);
-      running += chunk;
-    }
-    total = running;
-  } else {
-    total = static_cast<long long>(p.n_groups) * p.tiles_per_group;
-  }
-  const long long u0 = total * blockIdx.x / gridDim.x;
-  const long long u1 = total * (blockIdx.x + 1) / gridDim.x;
-  if (threadIdx.x == 0) {
-    s_count = u1 - u0;
-    s_g0 = 0;
-    s_t0 = 0;
-  }
-  if (p.mode == kDecodeDense) {
-    long long running = 0;
-    for (int base = 0; base < p.n_groups && running <= u0; base += kThreads) {
-      const int g = base + threadIdx.x;
-      const long long v = g < p.n_groups ? (max(__ldg(p.ctx_lens + g), 0) + kTile - 1) / kTile : 0;
-      long long chunk;
-      const long long incl = block_scan<kThreads>(v, s_warp_tot, &chunk) + running;
-      if (g < p.n_groups && v > 0 && incl - v <= u0 && u0 < incl) {
-        s_g0 = g;
-        s_t0 = static_cast<int>(u0 - (incl - v));
+    if (warp == kThreads / 32 - 1) {
+      auto tiles_of = [&](int g) -> int {
+        return g < p.n_groups ? (max(__ldg(p.ctx_lens + g), 0) + kTile - 1) / kTile : 0;
+      };
+      long long total = 0;
+      for (int base = 0; base < p.n_groups; base += 32) {
+        int v = tiles_of(base + lane);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+        total += v;
       }
-      running += chunk;
+      const long long u0 = total * blockIdx.x / gridDim.x;
+      const long long u1 = total * (blockIdx.x + 1) / gridDim.x;
+      if (lane == 0) {
+        s_count = u1 - u0;
+        s_g0 = 0;
+        s_t0 = 0;
+      }
+      __syncwarp();
+      long long run = 0;
+      for (int base = 0; base < p.n_groups && u1 > u0; base += 32) {
+        const int v = tiles_of(base + lane);
+        int incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+          if (lane >= o) incl += n;
+        }
+        const long long hi = run + incl;
+        const bool hit = v > 0 && hi - v <= u0 && u0 < hi;
+        const unsigned m = __ballot_sync(0xFFFFFFFFu, hit);
+        if (m) {
+          if (lane == __ffs(m) - 1) {
+            s_g0 = base + lane;
+            s_t0 = static_cast<int>(u0 - (hi - v));
+          }
+          break;
+        }
+        run += __shfl_sync(0xFFFFFFFFu, incl, 31);
+      }
     }
-  } else if (threadIdx.x == 0 && p.tiles_per_group > 0) {
-    s_g0 = static_cast<int>(u0 / p.tiles_per_group);
-    s_t0 = static_cast<int>(u0 % p.tiles_per_group);
+  } else if (threadIdx.x == 0) {
+    const long long total = static_cast<long long>(p.n_groups) * p.tiles_per_group;
+    const long long u0 = total * blockIdx.x / gridDim.x;
+    const long long u1 = total * (blockIdx.x + 1) / gridDim.x;
+    s_count = u1 - u0;
+    s_g0 = p.tiles_per_group > 0 ? static_cast<int>(u0 / p.tiles_per_group) : 0;
+    s_t0 = p.tiles_per_group > 0 ? static_cast<int>(u0 % p.tiles_per_group) : 0;
   }
   tc_fence_before();
   __syncthreads();

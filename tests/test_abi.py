@@ -111,6 +111,9 @@ def test_validation_rejects_before_touching_the_device(lib):
                                                  2, 1, None, 0, 0, None, 0, fake, 0, 4096, None, 0, None) == 2
     assert lib.idx_paged_mqa_logits_decode_mxfp4(fake, 8192, fake, 0, 64, fake, 16, 64, 4096, fake, 8, fake,
                                                  2, 1, None, 0, 0, None, 0, fake, 0, 4096, None, 0, None) == 1
+    # tensor-rate diagnostic: unknown kind, no iterations
+    assert lib.idx_diag_mma_peak(7, 100, 0, None, None) == 2
+    assert lib.idx_diag_mma_peak(0, 0, 0, None, None) == 1
     # misaligned q stride
     assert lib.idx_mqa_logits_prefill(fake, 8200, fake, 0, 64, fake, fake, 64, None, fake, 4, None, 0,
                                       0, None, 0, fake, 0, 64, None, 0, None) == 2
