@@ -322,11 +322,16 @@ __device__ __forceinline__ int warp_excl_scan(int v, int* total) {
 // at least the smallest key of the threshold digit (so above it or tied with
 // it); only hits are kept, appended to bucket A with their columns, and sorted
 // into "above" and "tied" afterwards from shared memory. Each thread tests the
-// 16 elements it loaded with one compare each into a bit mask and parks the
-// keys in its own slots of the warp's staging area; one warp scan reserves
-// bucket slots for all hits, and each thread then walks only its own set bits
-// (a few per warp at the usual hit rate of a few per cent), so the per-element
-// cost is the load, the key transform and the compare.
+// 16 elements it loaded into a bit mask and parks the loaded words in its own
+// slots of the warp's staging area; one warp scan reserves bucket slots for all
+// hits, and each thread then walks only its own set bits (a few per warp at the
+// usual hit rate of a few per cent), turning just those into keys.
+// The test: when the threshold is a non-negative value (the usual case: the
+// 2048 best of thousands of scores) the order-preserving key of a bit pattern u
+// is at least tie_lo exactly when u, read as a signed integer, is at least
+// tie_lo without its sign bit (negative values and negative NaNs fall below,
+// positive NaNs above +inf, as in the key order), so an element costs one
+// integer compare; otherwise the key itself is compared.
 template <int kThreads, bool kBf16>
 __device__ __forceinline__ void level0_collect(Shared& sh, const void* rowp, int64_t a1, int64_t nvec,
                                                uint32_t tie_lo, uint32_t* keys_a, int32_t* cols_a,
@@ -343,55 +348,70 @@ __device__ __forceinline__ void level0_collect(Shared& sh, const void* rowp, int
   // columns and vector indices fit in int32 (rows hold fewer than 2^31 columns)
   const int nv = static_cast<int>(nvec);
   const int col0 = static_cast<int>(a1);
+  const int32_t t_raw = static_cast<int32_t>(tie_lo & 0x7FFFFFFFu);
+  // element e of a loaded vector as fp32 bits (bf16: the 16-bit pattern in the upper half)
+  auto bits_of = [](const uint32_t (&w)[4], int e) -> uint32_t {
+    if constexpr (kBf16) {
+      return (e & 1) ? (w[e >> 1] & 0xFFFF0000u) : (w[e >> 1] << 16);
+    } else {
+      return w[e];
+    }
+  };
   // one step: kUnroll vectors per thread; kCheck only for the last, partial step
-  auto step = [&](int v0, auto check) {
+  auto step = [&](int v0, auto check, auto fast) {
     constexpr bool kCheck = decltype(check)::value;
-    uint32_t key[kPer];
+    constexpr bool kFast = decltype(fast)::value;
+    uint4 r[kUnroll];
     uint32_t hit = 0;
 #pragma unroll
     for (int j = 0; j < kUnroll; ++j) {
       const int v = v0 + j * kThreads + tid;
       const bool ok = !kCheck || v < nv;
-      const uint4 r = ok ? __ldg(vp + v) : make_uint4(0, 0, 0, 0);
-      const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+      r[j] = ok ? __ldg(vp + v) : make_uint4(0, 0, 0, 0);
+      const uint32_t w[4] = {r[j].x, r[j].y, r[j].z, r[j].w};
 #pragma unroll
       for (int e = 0; e < kVec; ++e) {
-        uint32_t k;
-        if constexpr (kBf16) {
-          k = f32_key(((w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu) << 16);
-        } else {
-          k = f32_key(w[e]);
-        }
-        key[j * kVec + e] = k;
-        if (ok && k >= tie_lo) hit |= 1u << (j * kVec + e);
+        const uint32_t u = bits_of(w, e);
+        const bool is_hit = kFast ? static_cast<int32_t>(u) >= t_raw : f32_key(u) >= tie_lo;
+        if (ok && is_hit) hit |= 1u << (j * kVec + e);
       }
     }
     int tot;
     int slot = warp_excl_scan(__popc(hit), &tot);
     if (tot == 0) return;
 #pragma unroll
-    for (int m = 0; m < kPer / 4; ++m) {
-      mine[32 * m] = make_uint4(key[4 * m], key[4 * m + 1], key[4 * m + 2], key[4 * m + 3]);
-    }
+    for (int m = 0; m < kUnroll; ++m) mine[32 * m] = r[m];
     int base = 0;
     if (lane == 0) base = atomicAdd(&sh.n_a, tot);
     slot += __shfl_sync(0xFFFFFFFFu, base, 0);
-    // the staged keys are this thread's own: program order is the only ordering needed
+    // the staged words are this thread's own: program order is the only ordering needed
     const uint32_t* mk = reinterpret_cast<const uint32_t*>(mine);
     const int cbase = col0 + (v0 + tid) * kVec;  // column of this thread's first element
     while (hit) {
       const int i = __ffs(hit) - 1;
       hit &= hit - 1;
       if (slot < TopkCfg<kThreads>::kCapA) {
-        keys_a[slot] = mk[(i >> 2) * 128 + (i & 3)];
+        uint32_t u;
+        if constexpr (kBf16) {
+          const uint32_t wd = mk[(i >> 3) * 128 + ((i & 7) >> 1)];
+          u = (i & 1) ? (wd & 0xFFFF0000u) : (wd << 16);
+        } else {
+          u = mk[(i >> 2) * 128 + (i & 3)];
+        }
+        keys_a[slot] = f32_key(u);
         cols_a[slot] = cbase + (i / kVec) * (kThreads * kVec) + i % kVec;
       }
       ++slot;
     }
   };
   const int nfull = nv / kStep * kStep;
-  for (int v0 = 0; v0 < nfull; v0 += kStep) step(v0, std::false_type{});
-  if (nfull < nv) step(nfull, std::true_type{});
+  if (tie_lo >= 0x80000000u) {
+    for (int v0 = 0; v0 < nfull; v0 += kStep) step(v0, std::false_type{}, std::true_type{});
+    if (nfull < nv) step(nfull, std::true_type{}, std::true_type{});
+  } else {
+    for (int v0 = 0; v0 < nfull; v0 += kStep) step(v0, std::false_type{}, std::false_type{});
+    if (nfull < nv) step(nfull, std::true_type{}, std::false_type{});
+  }
 }
 
 // Score of column c as fp32.

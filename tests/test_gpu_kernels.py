@@ -429,6 +429,57 @@ def test_topk_ties_overflow_and_special_values():
     assert 123 in set(out[5].tolist())
 
 
+def _keys(bits_u32):
+    """The selection's order-preserving keys of fp32 bit patterns (NaN above +inf, -NaN below -inf)."""
+    u = np.asarray(bits_u32, dtype=np.uint32)
+    return u ^ (((u.view(np.int32) >> 31).view(np.uint32)) | np.uint32(0x80000000))
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+def test_topk_key_order_special_values_both_compare_paths(bf16):
+    # the level-0 hit test compares raw bit patterns when the threshold is a
+    # non-negative value and keys otherwise: rows with positive and with negative
+    # thresholds, NaNs of both signs, infinities and signed zeros, checked in the
+    # key order itself (the selected keys are the k largest keys)
+    width, k = 20000, 1000
+    rng = np.random.default_rng(77 + bf16)
+    x = rng.standard_normal((6, width)).astype(np.float32)
+    x[1] -= 10.0                                   # every value negative: a negative threshold
+    x[2] = -np.abs(x[2]) - 1.0
+    x[2, 5000:5600] = -0.5                         # the threshold sits in a negative tied bucket
+    for r in (0, 1, 3):
+        x[r, 11] = np.float32(np.nan)              # positive NaN: above +inf
+        x[r, 12] = -np.float32(np.nan)             # negative NaN: below -inf
+        x[r, 13] = np.float32(np.inf)
+        x[r, 14] = -np.float32(np.inf)
+        x[r, 15] = np.float32(0.0)
+        x[r, 16] = -np.float32(0.0)
+    x[3, :] = np.abs(x[3]) * 1e-30                 # tiny positive values, subnormal keys
+    x[4, ::2] = 0.0
+    x[4, 1::2] = -0.0                              # only signed zeros
+    x[5, :] = -np.float32(np.nan)
+    x[5, 100:3000] = rng.standard_normal(2900).astype(np.float32)
+    if bf16:
+        xb = bf16_encode(np.where(np.isnan(x), 0, x))
+        sign = np.signbit(x) & np.isnan(x)
+        xb = np.where(np.isnan(x), np.where(sign, 0xFFC0, 0x7FC0), xb).astype(np.uint16)
+        t = dev_bf16(xb)
+        bits = xb.astype(np.uint32) << 16
+    else:
+        t = dev(x)
+        bits = x.view(np.uint32)
+    out = torch.full((6, k), -7, dtype=torch.int32, device=DEV)
+    idx.idx_topk(t, None, dev(np.full(6, width, dtype=np.int32)), k, out)
+    o = out.cpu().numpy()
+    for r in range(6):
+        keys = _keys(bits[r])
+        assert len(np.unique(o[r])) == k and np.all((o[r] >= 0) & (o[r] < width)), f"row {r}"
+        want = np.sort(keys)[::-1][:k]
+        got = np.sort(keys[o[r]])[::-1]
+        assert np.array_equal(got, want), f"row {r}: selected keys differ from the {k} largest keys"
+    assert 11 in set(o[0].tolist()) and 12 not in set(o[0].tolist())
+
+
 def test_topk_bf16_and_wide_rows():
     x = W.make_logits(10, 4, 131072)
     out, vals = _run_topk(x, None, np.full(4, 131072, dtype=np.int32), 2048, bf16=True)
