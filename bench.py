@@ -616,30 +616,40 @@ class PrefillBench:
 
 
 class HierBench:
-    """V4.1 consumer-layer decode: expand candidates, sparse logits (bf16), top-2048 + remap + slots."""
+    """V4.1 consumer-layer decode: expand candidates, sparse logits (bf16), top-2048 + remap + slots.
+
+    ``hierarchical_mxfp4`` runs the same workload on the MXFP4 indexer cache, the
+    cache format of the V4.1 path."""
 
     launches_per_step = 3
-    dtype = "e4m3xe4m3->f32 (bf16 logits)"
-    metric = "hierarchical sparse decode indexer query-rows/s @128K ctx incl. top-2048"
 
     def __init__(self, name, rank, dev):
         import sparse_attention_indexer_fp8_gb300 as idx
         from sparse_attention_indexer_fp8_gb300.pipeline import HierarchicalStep, fill_paged_cache
 
         self.idx, self.dev, self.name = idx, dev, name
+        self.kv = "mxfp4" if name.endswith("_mxfp4") else "fp8"
         self.wl = wl = W.hierarchical(seed=rank_seed(1004, rank))
         pool = wl.pool
         self.B = B = len(pool.ctx_lens)
-        self.stride = W.block_stride_bytes()
+        self.token_bytes = W.MXFP4_TOKEN_BYTES if self.kv == "mxfp4" else W.TOKEN_BYTES
+        self.stride = W.mxfp4_block_stride_bytes() if self.kv == "mxfp4" else W.block_stride_bytes()
         self.cache = torch.zeros((pool.num_blocks, self.stride), dtype=torch.uint8, device=dev)
-        fill_paged_cache(pool, wl.seed, self.cache, device_k=True)
+        fill_paged_cache(pool, wl.seed, self.cache, device_k=True, kv=self.kv)
+        self.scorer = (idx.idx_paged_mqa_logits_decode_mxfp4 if self.kv == "mxfp4"
+                       else idx.idx_paged_mqa_logits_decode)
         self.q = torch.from_numpy(wl.q8).to(dev)
         self.w = torch.from_numpy(wl.w).to(dev)
         self.bt = torch.from_numpy(pool.block_table).to(dev)
         self.ctx = torch.from_numpy(pool.ctx_lens).to(dev)
         self.cand = torch.from_numpy(wl.cand).to(dev)
-        self.st = HierarchicalStep(B, wl.cand.shape[1], wl.cand_block_size, wl.sbk, wl.topk, pool.block_size, dev)
+        self.st = HierarchicalStep(B, wl.cand.shape[1], wl.cand_block_size, wl.sbk, wl.topk, pool.block_size, dev,
+                                   kv=self.kv)
         self.rows_per_step = B
+
+    metric = property(lambda self: "hierarchical sparse decode indexer query-rows/s @128K ctx incl. top-2048" +
+                      (", MXFP4 indexer cache" if self.kv == "mxfp4" else ""))
+    dtype = property(lambda self: ("e4m3xe2m1(mx)" if self.kv == "mxfp4" else "e4m3xe4m3") + "->f32 (bf16 logits)")
 
     def step(self, stream, ev=None):
         idx, st, wl = self.idx, self.st, self.wl
@@ -647,9 +657,8 @@ class HierBench:
                                   stream=stream)
         if ev is not None:
             ev[0].record(stream)
-        idx.idx_paged_mqa_logits_decode(self.q, self.w, self.cache, wl.pool.block_size, self.bt, self.ctx,
-                                        st.logits, sparse_idx=st.sparse_idx, end=st.end, sbk=wl.sbk, ws=st.ws,
-                                        stream=stream)
+        self.scorer(self.q, self.w, self.cache, wl.pool.block_size, self.bt, self.ctx, st.logits,
+                    sparse_idx=st.sparse_idx, end=st.end, sbk=wl.sbk, ws=st.ws, stream=stream)
         if ev is not None:
             ev[1].record(stream)
         idx.idx_sparse_topk_remap(st.logits, st.end, st.sparse_idx, None, wl.sbk, wl.topk, st.positions,
@@ -672,11 +681,11 @@ class HierBench:
         assert np.array_equal(g_si, o_si) and np.array_equal(g_end, o_end), "bench expansion differs"
         rng = np.random.default_rng(wl.seed)
         sample = sorted(rng.choice(self.B, size=min(n_rows, self.B), replace=False).tolist())
-        kq = {b: oracle_sparse_k(wl, b, o_si[b], int(o_end[b]), self.dev) for b in sample}
+        kq = {b: oracle_sparse_k(wl, b, o_si[b], int(o_end[b]), self.dev, self.kv) for b in sample}
         g_lg = st.logits.float().cpu().numpy()
         g_cols, g_pos, g_slots = st.cols.cpu().numpy(), st.positions.cpu().numpy(), st.slots.cpu().numpy()
         t0 = time.perf_counter()
-        ref = {b: oracle_hier_row(wl, b, kq[b]) for b in sample}
+        ref = {b: oracle_hier_row(wl, b, kq[b], self.kv) for b in sample}
         cpu_s = time.perf_counter() - t0
         for b in sample:
             lg, _, _ = ref[b]
@@ -700,11 +709,15 @@ class HierBench:
         if end_sum is None:
             end_sum = int(self.st.end.sum().item())
         ncols = self.st.logits.shape[1]
-        return hbm_roofline("mqa_logits_kernel<1> (sparse decode, bf16 out)", end_sum * W.TOKEN_BYTES + self.B * (64 * 128 + 64 * 4),
+        return hbm_roofline("mqa_logits_kernel<1%s> (sparse decode, bf16 out)" % (", MXFP4 k" if self.kv == "mxfp4" else ""),
+                            end_sum * self.token_bytes + self.B * (64 * 128 + 64 * 4),
                             self.B * ncols * 2, kernel_ms, peaks, peak_kind)
 
     def config(self, world):
-        return {"workload": self.wl.name, "batch": self.B, "ctx": int(self.wl.pool.ctx_lens[0]),
+        return {"workload": self.wl.name + ("-mxfp4-cache" if self.kv == "mxfp4" else ""), "batch": self.B,
+                "ctx": int(self.wl.pool.ctx_lens[0]),
+                "kv_cache": "MXFP4 (e2m1 + E8M0 per 32, 68 B/token)" if self.kv == "mxfp4"
+                else "e4m3 + fp32 scale (132 B/token)",
                 "candidates": int(self.wl.cand.shape[1]), "cand_block_size": self.wl.cand_block_size,
                 "sbk": self.wl.sbk, "topk": self.wl.topk,
                 "step": "expand + sparse logits (bf16) + top-2048 remap with the slot conversion fused",
@@ -712,8 +725,9 @@ class HierBench:
                 "parallelism": f"rows sharded, {world} independent replica(s)"}
 
 
-def oracle_sparse_k(wl, b, si_row, end, device):
-    """Quantised k of the tokens one hierarchical row scores, from the GPU arm's generator."""
+def oracle_sparse_k(wl, b, si_row, end, device, kv: str = "fp8"):
+    """Quantised k of the tokens one hierarchical row scores, from the GPU arm's generator
+    ((k8, kscale), or MXFP4 k values)."""
     from oracle import indexer as O
     from oracle.codecs import bf16_decode
 
@@ -723,16 +737,20 @@ def oracle_sparse_k(wl, b, si_row, end, device):
     else:
         kall = W.make_k(wl.seed, b, L)
     toks = np.array([O.sparse_column_token(si_row, c, wl.sbk) for c in range(end)], dtype=np.int64)
-    return O.k_quant(bf16_decode(kall[toks]))
+    kf = bf16_decode(kall[toks])
+    return O.mxfp4_values(*O.mxfp4_quant(kf)) if kv == "mxfp4" else O.k_quant(kf)
 
 
-def oracle_hier_row(wl, b, kq):
+def oracle_hier_row(wl, b, kq, kv: str = "fp8"):
     """The oracle's hierarchical step for one row: expand, score the candidates, select, remap, slots."""
     from oracle import indexer as O
 
     si, end = O.expand_candidates_row(wl.cand[b], 0, int(wl.pool.ctx_lens[b]), wl.cand_block_size, wl.sbk)
-    k8, ks = kq
-    lg = O.logits_row(wl.q8[b], wl.w[b], k8[:end], ks[:end])
+    if kv == "mxfp4":
+        lg = O.logits_row_values(wl.q8[b], wl.w[b], kq[:end])
+    else:
+        k8, ks = kq
+        lg = O.logits_row(wl.q8[b], wl.w[b], k8[:end], ks[:end])
     dense = np.full(si.shape[0] * wl.sbk, -np.inf)
     dense[:end] = lg
     cols, pos = O.sparse_topk_remap_row(dense, end, si, 0, wl.sbk, wl.topk)
@@ -1036,7 +1054,7 @@ class QPrepBench:
 
 
 BENCHES = {"long_decode": DecodeBench, "long_decode_mxfp4": DecodeBench, "paged_decode": DecodeBench,
-           "prefill": PrefillBench,
+           "prefill": PrefillBench, "hierarchical_mxfp4": HierBench,
            "hierarchical": HierBench, "hierarchical_mtp": HierMtpBench, "q_prep": QPrepBench,
            "dcp_decode": DcpBench}
 
@@ -1247,17 +1265,21 @@ def run_reference(args, rank):
         from oracle import indexer as O
 
         wl = W.hierarchical()
+        kv = "mxfp4" if name == "hierarchical_mxfp4" else "fp8"
         rows = [0, 1, 2, 3]
         kq = {}
         for b in rows:
             si, end = O.expand_candidates_row(wl.cand[b], 0, int(wl.pool.ctx_lens[b]), 64, 64)
-            kq[b] = oracle_sparse_k(wl, b, si, end, None)
+            kq[b] = oracle_sparse_k(wl, b, si, end, None, kv)
 
         def one(i):
             t0 = time.perf_counter()
-            oracle_hier_row(wl, rows[i % 4], kq[rows[i % 4]])
+            oracle_hier_row(wl, rows[i % 4], kq[rows[i % 4]], kv)
             return time.perf_counter() - t0
-        metric, cfg = HierBench.metric, {"workload": wl.name, "batch": len(wl.pool.ctx_lens), "topk": wl.topk}
+        metric = ("hierarchical sparse decode indexer query-rows/s @128K ctx incl. top-2048" +
+                  (", MXFP4 indexer cache" if kv == "mxfp4" else ""))
+        cfg = {"workload": wl.name + ("-mxfp4-cache" if kv == "mxfp4" else ""), "batch": len(wl.pool.ctx_lens),
+               "topk": wl.topk}
     for i in range(args.warmup):
         one(i)
     t = sum(one(i) for i in range(args.steps))

@@ -1,5 +1,6 @@
 // Integer index kernels of the indexer path:
-//   a7  idx_expand_candidates   (V4.1 candidate-block flattening)
+//   a7  idx_expand_candidates   (V4.1 candidate-block flattening: one warp per row
+//                                up to 256 expanded entries, one block per row beyond)
 //   a6  idx_req_to_global_slots (request-local position -> physical slot)
 #include <climits>
 
@@ -112,6 +113,95 @@ __global__ void expand_candidates_kernel(const int32_t* __restrict__ cand, int64
   }
 }
 
+// One warp per row for rows of at most 256 expanded entries (E = 1, 2, 4 or 8
+// per lane; entry i of the row is element e = i / 32 of lane i % 32). The same
+// steps as expand_candidates_kernel: expand, sort ascending with a bitonic
+// network (partners 32 or more apart within a lane's registers, nearer ones by
+// shuffles, so no barrier), keep first occurrences in order, pad the tail.
+template <int E>
+__global__ void __launch_bounds__(128) expand_candidates_warp_kernel(
+    const int32_t* __restrict__ cand, int64_t ld_c, int rows, int n_cand,
+    const int32_t* __restrict__ row_ks, const int32_t* __restrict__ row_ke, int R, int sbk,
+    int32_t* __restrict__ sparse_idx, int64_t ld_si, int32_t* __restrict__ end) {
+  const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const int width = n_cand * R;
+  const int64_t ks = row_ks ? static_cast<int64_t>(row_ks[row]) : 0;
+  const int64_t ke = row_ke[row];
+  const bool ks_ok = ks >= 0 && (ks % sbk) == 0;
+  const int64_t kv_len = ke > ks ? ke - ks : 0;
+  const int64_t max_block = (kv_len + sbk - 1) / sbk;
+  int key[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int i = e * 32 + lane;
+    key[e] = INT_MAX;
+    if (ks_ok && i < width) {
+      const int c = cand[row * ld_c + i / R];
+      if (c >= 0) {
+        const int64_t x = static_cast<int64_t>(c) * R + (i % R);
+        if (x < max_block) key[e] = static_cast<int>(x);
+      }
+    }
+  }
+#pragma unroll
+  for (int size = 2; size <= 32 * E; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      if (stride >= 32) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const int e2 = e ^ (stride >> 5);
+          if (e < e2) {
+            const bool asc = ((e * 32 + lane) & size) == 0;
+            const int lo = min(key[e], key[e2]);
+            const int hi = max(key[e], key[e2]);
+            key[e] = asc ? lo : hi;
+            key[e2] = asc ? hi : lo;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const bool asc = ((e * 32 + lane) & size) == 0;
+          const int other = __shfl_xor_sync(0xFFFFFFFFu, key[e], stride);
+          const bool lower = (lane & stride) == 0;
+          key[e] = (lower == asc) ? min(key[e], other) : max(key[e], other);
+        }
+      }
+    }
+  }
+  const int32_t base = static_cast<int32_t>(ks / sbk);
+  const unsigned below = (1u << lane) - 1u;
+  int n = 0;
+  int last = 0;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int up = __shfl_up_sync(0xFFFFFFFFu, key[e], 1);
+    const int wrap = e > 0 ? __shfl_sync(0xFFFFFFFFu, key[e > 0 ? e - 1 : 0], 31) : -1;
+    const int prev = lane > 0 ? up : wrap;
+    const bool first = key[e] != INT_MAX && key[e] != prev;
+    const unsigned m = __ballot_sync(0xFFFFFFFFu, first);
+    if (first) sparse_idx[row * ld_si + n + __popc(m & below)] = key[e] + base;
+    if (m) last = __shfl_sync(0xFFFFFFFFu, key[e], 31 - __clz(m));
+    n += __popc(m);
+  }
+  const int32_t pad = n > 0 ? last + base : base;
+  for (int j = n + lane; j < width; j += 32) sparse_idx[row * ld_si + j] = pad;
+  if (lane == 0) {
+    int32_t e = 0;
+    if (n > 0) {
+      const int64_t last_start = static_cast<int64_t>(last) * sbk + ks;
+      int64_t fill = ke - last_start;
+      fill = fill < 1 ? 1 : (fill > sbk ? sbk : fill);
+      e = static_cast<int32_t>(static_cast<int64_t>(n - 1) * sbk + fill);
+    }
+    end[row] = e;
+    if (!ks_ok) atomicOr(&g_index_ops_error, 1u);
+  }
+}
+
 __global__ void req_to_global_kernel(const int32_t* local, int64_t ld_l, int rows, int k,
                                      const int32_t* __restrict__ row_to_req,
                                      const int32_t* __restrict__ block_table, int64_t ld_bt,
@@ -176,6 +266,24 @@ extern "C" idx_status_t idx_expand_candidates(const int32_t* cand, int64_t ld_c,
   if (ld_c < n_cand || ld_si < width) return fail(IDX_ERR_INVALID_ARG, "%s: ld_c or ld_si too small", fn);
   if (rows == 0) return IDX_OK;
   if (!cand || !row_ke || !sparse_idx || !end) return fail(IDX_ERR_INVALID_ARG, "%s: NULL pointer", fn);
+  if (width <= 256) {
+    // one warp per row, four rows per block
+    const unsigned blocks = static_cast<unsigned>((rows + 3) / 4);
+    if (width <= 32) {
+      expand_candidates_warp_kernel<1><<<blocks, 128, 0, stream>>>(cand, ld_c, rows, n_cand, row_ks, row_ke, R,
+                                                                  sbk, sparse_idx, ld_si, end);
+    } else if (width <= 64) {
+      expand_candidates_warp_kernel<2><<<blocks, 128, 0, stream>>>(cand, ld_c, rows, n_cand, row_ks, row_ke, R,
+                                                                  sbk, sparse_idx, ld_si, end);
+    } else if (width <= 128) {
+      expand_candidates_warp_kernel<4><<<blocks, 128, 0, stream>>>(cand, ld_c, rows, n_cand, row_ks, row_ke, R,
+                                                                  sbk, sparse_idx, ld_si, end);
+    } else {
+      expand_candidates_warp_kernel<8><<<blocks, 128, 0, stream>>>(cand, ld_c, rows, n_cand, row_ks, row_ke, R,
+                                                                  sbk, sparse_idx, ld_si, end);
+    }
+    return check_launch(fn);
+  }
   int threads = 32;
   while (threads < width) threads <<= 1;
   expand_candidates_kernel<<<rows, threads, threads * sizeof(int32_t), stream>>>(
