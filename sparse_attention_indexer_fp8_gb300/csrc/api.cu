@@ -57,6 +57,17 @@ int device_sm_count() {
   return n;
 }
 
+int64_t device_l2_bytes() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  static int cache[64] = {0};
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrL2CacheSize, dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
 idx_status_t encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank,
                                const void* base, const uint64_t* dims,
                                const uint64_t* strides_bytes, const uint32_t* box,

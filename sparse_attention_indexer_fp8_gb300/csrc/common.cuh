@@ -23,6 +23,7 @@ constexpr int kMxTokenBytes = 68;  // MXFP4 cache: 64 bytes of e2m1 elements + 4
 idx_status_t fail(idx_status_t st, const char* fmt, ...);
 idx_status_t check_launch(const char* what);
 int device_sm_count();
+int64_t device_l2_bytes();  // 0 when it cannot be queried
 
 // Encodes a tiled TMA descriptor through the driver entry point (no -lcuda link).
 idx_status_t encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank,
@@ -100,6 +101,15 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
   return pol;
+}
+
+// Global stores that carry an L2 eviction policy (an earlier createpolicy).
+__device__ __forceinline__ void st_global_hint(float* ptr, float v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(ptr), "f"(v), "l"(pol) : "memory");
+}
+
+__device__ __forceinline__ void st_global_hint(uint16_t* ptr, uint16_t v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.b16 [%0], %1, %2;" ::"l"(ptr), "h"(v), "l"(pol) : "memory");
 }
 
 // Asks the memory system to bring [ptr, ptr + bytes) into L2 (a bulk

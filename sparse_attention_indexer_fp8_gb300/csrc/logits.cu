@@ -101,6 +101,9 @@ struct LogitsParams {
   void* out;
   int out_bf16;
   int64_t ld_out;
+  // 1: the scores are stored with an L2 evict-last policy, so the selection that
+  // reads them next finds them in L2 rather than behind the evict-first k stream
+  int out_keep_l2;
   // optional: per-row histogram of the top 10 key bits of every visible logit
   // (kHistBins uint32 per row), accumulated for the selection's first digit
   uint32_t* hist;
@@ -718,6 +721,7 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     const int trow = quarter * 32 + lane;
     // this thread's token row inside a stage's scale boxes: word trow % unit of box trow / unit
     const int sc_off = ((trow >> p.unit_shift) << p.slot_shift) + ((trow & (p.unit - 1)) << 2);
+    const uint64_t pol_out = l2_policy_evict_last();
     float* wsm = w_s + ew * NQ * 64;
     // private histogram of this warp's visible logits for the current group;
     // flushed to the row's global histogram when the warp moves to another group
@@ -912,10 +916,18 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
               uint32_t bits;
               if constexpr (kOutBf16) {
                 const __nv_bfloat16 b = __float2bfloat16_rn(v);
-                orow[j][c] = b;
+                if (p.out_keep_l2) {
+                  st_global_hint(reinterpret_cast<uint16_t*>(orow[j] + c), __bfloat16_as_ushort(b), pol_out);
+                } else {
+                  orow[j][c] = b;
+                }
                 bits = static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16;
               } else {
-                orow[j][c] = v;
+                if (p.out_keep_l2) {
+                  st_global_hint(orow[j] + c, v, pol_out);
+                } else {
+                  orow[j][c] = v;
+                }
                 bits = __float_as_uint(v);
               }
               if (do_hist && vis) {
@@ -1074,6 +1086,14 @@ using namespace idx;
 
 namespace {
 
+// Scores that fill at most half of L2 are stored to stay there for the
+// selection that reads them next; larger ones (prefill chunks) are stored plainly.
+int keep_scores_in_l2(int64_t rows, int64_t ld_out, int out_dtype) {
+  const int64_t bytes = rows * ld_out * (out_dtype == IDX_BF16 ? 2 : 4);
+  const int64_t l2 = device_l2_bytes();
+  return l2 > 0 && bytes <= l2 / 2 ? 1 : 0;
+}
+
 // Both paged decode entry points: the e4m3 cache (132 bytes per token, fp32
 // token scale) and the MXFP4 cache (68 bytes per token, E8M0 block scales).
 idx_status_t paged_decode(const char* fn, bool fp4, const uint8_t* q, int64_t ld_q, const void* w,
@@ -1124,6 +1144,7 @@ idx_status_t paged_decode(const char* fn, bool fp4, const uint8_t* q, int64_t ld
   p.out = logits;
   p.out_bf16 = out_dtype == IDX_BF16;
   p.ld_out = ld_out;
+  p.out_keep_l2 = keep_scores_in_l2(rows, ld_out, out_dtype);
   int nq_tmpl = 1;
   long long max_tiles = -1;
   if (sparse_idx) {
@@ -1248,6 +1269,7 @@ extern "C" idx_status_t idx_mqa_logits_prefill(const uint8_t* q, int64_t ld_q, c
   p.out = logits;
   p.out_bf16 = out_dtype == IDX_BF16;
   p.ld_out = ld_out;
+  p.out_keep_l2 = keep_scores_in_l2(T, ld_out, out_dtype);
   int nq_tmpl;
   if (sparse_idx) {
     if (!end) return fail(IDX_ERR_INVALID_ARG, "%s: sparse mode needs end", fn);
