@@ -1081,10 +1081,19 @@ def run_ours(args, rank, world, local, dist):
         for _ in range(5):
             bench.step(stream)
         torch.cuda.synchronize(dev)
-    # the dominant kernel's own duration, from events around it in plain launches
+    # the dominant kernel's own duration, from events around it in plain launches;
+    # a sleep kernel holds the GPU while the host queues every one of these steps,
+    # so no host launch time falls between a pair of events
     n_kev = min(args.steps, 100)
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(n_kev)]
+    torch.cuda.synchronize(dev)
+    h0 = time.perf_counter()
+    for _ in range(3):
+        bench.step(stream)
+    host_s = (time.perf_counter() - h0) / 3
+    torch.cuda.synchronize(dev)
+    torch.cuda._sleep(int(min(0.2, 2.0 * n_kev * host_s) * 2.2e9))
     for i in range(n_kev):
         bench.step(stream, kev[i])
     torch.cuda.synchronize(dev)
