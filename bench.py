@@ -711,7 +711,9 @@ class HierBench:
         ncols = self.st.logits.shape[1]
         return hbm_roofline("mqa_logits_kernel<1%s> (sparse decode, bf16 out)" % (", MXFP4 k" if self.kv == "mxfp4" else ""),
                             end_sum * self.token_bytes + self.B * (64 * 128 + 64 * 4),
-                            self.B * ncols * 2, kernel_ms, peaks, peak_kind)
+                            self.B * ncols * 2, kernel_ms, peaks, peak_kind,
+                            traffic=(profiled_traffic("launches_hierarchical.md", "logits.cu")
+                                     if self.kv == "fp8" else None))
 
     def config(self, world):
         return {"workload": self.wl.name + ("-mxfp4-cache" if self.kv == "mxfp4" else ""), "batch": self.B,
