@@ -153,12 +153,13 @@ def test_prefill_chunk_8192_on_32k():
         assert_topk_row(sl[i], ref, wl.topk, f"prefill top-k row {t}")
 
 
-def _hierarchical(wl, check_rows):
+def _hierarchical(wl, check_rows, kv="fp8"):
     pool = wl.pool
     B = len(pool.ctx_lens)
-    cache = torch.zeros((pool.num_blocks, W.block_stride_bytes()), dtype=torch.uint8, device=DEV)
-    fill_paged_cache(pool, wl.seed, cache, device_k=True)
-    stp = HierarchicalStep(B, wl.cand.shape[1], wl.cand_block_size, wl.sbk, wl.topk)
+    stride = W.mxfp4_block_stride_bytes() if kv == "mxfp4" else W.block_stride_bytes()
+    cache = torch.zeros((pool.num_blocks, stride), dtype=torch.uint8, device=DEV)
+    fill_paged_cache(pool, wl.seed, cache, device_k=True, kv=kv)
+    stp = HierarchicalStep(B, wl.cand.shape[1], wl.cand_block_size, wl.sbk, wl.topk, kv=kv)
     slots = stp.run(torch.from_numpy(wl.q8).to(DEV), torch.from_numpy(wl.w).to(DEV), cache,
                     torch.from_numpy(pool.block_table).to(DEV), torch.from_numpy(pool.ctx_lens).to(DEV),
                     torch.from_numpy(wl.cand).to(DEV))
@@ -174,8 +175,11 @@ def _hierarchical(wl, check_rows):
         e = int(oend[b])
         kall = _k_host(wl.seed, b, int(pool.ctx_lens[b]))
         toks = np.array([O.sparse_column_token(osi[b], c, wl.sbk) for c in range(e)], dtype=np.int64)
-        k8, ks = O.k_quant(kall[toks])
-        ref = O.logits_row(wl.q8[b], wl.w[b], k8, ks)
+        if kv == "mxfp4":
+            ref = O.logits_row_values(wl.q8[b], wl.w[b], O.mxfp4_values(*O.mxfp4_quant(kall[toks])))
+        else:
+            k8, ks = O.k_quant(kall[toks])
+            ref = O.logits_row(wl.q8[b], wl.w[b], k8, ks)
         assert_logits_close(lg[b, :e], ref, f"sparse row {b}", bf16=True)
         assert np.all(np.isneginf(lg[b, e:]))
         assert_topk_row(cols[b], ref, wl.topk, f"sparse top-k row {b}", bf16=True)
@@ -189,6 +193,13 @@ def test_hierarchical_b128_128k():
     wl = W.hierarchical()
     rng = np.random.default_rng(wl.seed)
     _hierarchical(wl, sorted(rng.choice(128, size=6, replace=False).tolist()))
+
+
+def test_hierarchical_mxfp4_b128_128k():
+    # the hierarchical workload on the MXFP4 indexer cache (the V4.1 format)
+    wl = W.hierarchical()
+    rng = np.random.default_rng(wl.seed + 1)
+    _hierarchical(wl, sorted(rng.choice(128, size=6, replace=False).tolist()), kv="mxfp4")
 
 
 def test_hierarchical_many_tiles_per_cta_every_row():
