@@ -320,18 +320,22 @@ class E2EPipeline:
     """End-to-end steps through the public API with host buffers, two steps in flight.
 
     Every step copies all of its inputs from pinned host memory to the device and
-    its result back. The host-to-device copy of step i + 1 (on its own stream, into
-    the second of two device buffer sets) and the device-to-host copy of step i - 1
-    (on a third stream) overlap step i's kernels; events order each copy against
-    the kernels that read or write the same buffer set. The bench's own device
-    tensors are re-pointed (``Tensor.set_``) at the set a step uses, so its ``step``
-    runs unchanged."""
+    its result back. The inputs sit back to back (256-byte aligned) in one pinned
+    staging buffer and move in one host-to-device copy per step into one of two
+    device buffer sets; the results move back in one device-to-host copy. The
+    host-to-device copy of step i + 1 (on its own stream) and the device-to-host
+    copy of step i - 1 (on a third stream) overlap step i's kernels; events order
+    each copy against the kernels that read or write the same buffer set. The
+    bench's own device tensors are re-pointed (``Tensor.set_``) at views of the set
+    a step uses, so its ``step`` runs unchanged."""
+
+    ALIGN = 256
 
     def __init__(self, bench, dev):
         self.bench = bench
         self.inputs, self.outputs = bench.e2e_io()
-        self.sets_in = [[d.clone() for _, d in self.inputs] for _ in range(2)]
-        self.sets_out = [[d.clone() for _, d in self.outputs] for _ in range(2)]
+        self.host_in, self.in_views = self._pack(self.inputs, dev, fill=True)
+        self.host_out, self.out_views = self._pack(self.outputs, dev, fill=False)
         self.h2d = torch.cuda.Stream(dev)
         self.d2h = torch.cuda.Stream(dev)
         self.ev = {k: [torch.cuda.Event() for _ in range(2)]
@@ -339,8 +343,28 @@ class E2EPipeline:
         self.used = [False, False]
         self.i = 0
 
+    def _pack(self, pairs, dev, fill):
+        """One pinned host buffer and two device buffers holding every tensor of
+        ``pairs`` at aligned offsets; per device buffer, a view shaped like each tensor."""
+        offs, total = [], 0
+        for h, _ in pairs:
+            offs.append(total)
+            total += (h.numel() * h.element_size() + self.ALIGN - 1) // self.ALIGN * self.ALIGN
+        host = torch.zeros(total, dtype=torch.uint8).pin_memory()
+        if fill:
+            for (h, _), o in zip(pairs, offs):
+                n = h.numel() * h.element_size()
+                host[o:o + n].copy_(h.contiguous().reshape(-1).view(torch.uint8))
+        sets = []
+        for _ in range(2):
+            buf = torch.zeros(total, dtype=torch.uint8, device=dev)
+            views = [buf[o:o + d.numel() * d.element_size()].view(d.dtype).view(d.shape)
+                     for (_, d), o in zip(pairs, offs)]
+            sets.append((buf, views))
+        return host, sets
+
     def bytes_per_step(self):
-        return _nbytes(*[h for h, _ in self.inputs]), _nbytes(*[h for h, _ in self.outputs])
+        return self.host_in.numel(), self.host_out.numel()
 
     def begin(self, stream):
         """Forks the copy streams from ``stream`` (required inside a graph capture)."""
@@ -353,26 +377,26 @@ class E2EPipeline:
 
     def step(self, stream):
         s, ev = self.i % 2, self.ev
+        buf_in, views_in = self.in_views[s]
+        buf_out, views_out = self.out_views[s]
         with torch.cuda.stream(self.h2d):
             if self.used[s]:
                 self.h2d.wait_event(ev["in_free"][s])      # the kernels of step i - 2 are done with set s
-            for (h, _), buf in zip(self.inputs, self.sets_in[s]):
-                buf.copy_(h, non_blocking=True)
+            buf_in.copy_(self.host_in, non_blocking=True)
             ev["in_ready"][s].record(self.h2d)
         stream.wait_event(ev["in_ready"][s])
         if self.used[s]:
             stream.wait_event(ev["out_free"][s])          # step i - 2's result has left set s
-        for (_, d), buf in zip(self.inputs, self.sets_in[s]):
-            d.set_(buf)
-        for (_, d), buf in zip(self.outputs, self.sets_out[s]):
-            d.set_(buf)
+        for (_, d), v in zip(self.inputs, views_in):
+            d.set_(v)
+        for (_, d), v in zip(self.outputs, views_out):
+            d.set_(v)
         self.bench.step(stream)
         ev["in_free"][s].record(stream)
         ev["out_ready"][s].record(stream)
         with torch.cuda.stream(self.d2h):
             self.d2h.wait_event(ev["out_ready"][s])
-            for (h, _), buf in zip(self.outputs, self.sets_out[s]):
-                h.copy_(buf, non_blocking=True)
+            self.host_out.copy_(buf_out, non_blocking=True)
             ev["out_free"][s].record(self.d2h)
         self.used[s] = True
         self.i += 1
@@ -1192,8 +1216,9 @@ def run_ours(args, rank, world, local, dist):
         "cpu_baseline": cpu,
         "e2e": {"value": round(rows_total / (e2e_ms / 1e3 / args.steps), 1), "unit": "rows/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "copies": "every step: inputs in from pinned host memory, result out; two steps in "
-                          "flight (step i+1's inputs and step i-1's result move during step i)"},
+                "copies": "every step: all inputs in from one pinned host staging buffer (one copy), the "
+                          "result out (one copy); two steps in flight (step i+1's inputs and step "
+                          "i-1's result move during step i)"},
         "gpu_launches": bench.launches_per_step * args.steps,
         "launch": (f"CUDA graph of {GRAPH_STEPS} steps, replayed" if args.graphs else "direct launches"),
         "clocks": sampler.summary(t0, t1) if sampler else None,
