@@ -2,16 +2,19 @@
 """Benchmark of the FP8 lightning indexer on one GB300 (or N, one process per GPU).
 
 Default workload: the 128K long-context decode step - batch 128, contexts
-uniform in [64K, 128K] in a 2.2 GB paged k cache (block 64, 8704-byte blocks,
+uniform in [64K, 128K] in a 1.7 GB paged k cache (block 64, 8704-byte blocks,
 shuffled block tables). One step is the whole decode path: insert the new
 token's k (fused quantisation), paged FP8 MQA logits over every visible
 token, top-2048 per row, request-local -> physical slot conversion.
 ``value`` is query rows per second with every input resident in HBM; the k
-cache (2.2 GB) is larger than L2, so no flush is needed between steps.
+cache (1.7 GB) is larger than L2, so no flush is needed between steps.
 
-Other workloads (``--workload``): ``paged_decode`` (batch 64, 8K-32K),
-``prefill`` (8192 queries on a 32K context), ``hierarchical`` (V4.1 sparse
-decode at 128K).
+Other workloads (``--workload``): ``long_decode_mxfp4`` (the same step on the
+MXFP4 indexer cache), ``paged_decode`` (batch 64, 8K-32K), ``prefill`` (8192
+queries on a 32K context), ``hierarchical`` and ``hierarchical_mxfp4`` (V4.1
+sparse decode at 128K), ``hierarchical_mtp`` (next_n 2, four consumer layers
+per expansion), ``dcp_decode`` (four context-parallel ranks emulated on one
+GPU) and ``q_prep`` (RoPE + q quantisation of an 8192-query chunk).
 
 ``--impl reference`` times the CPU oracle (the only reference implementation
 there is) on the same workload, metric and unit, on a bounded sample of rows.
