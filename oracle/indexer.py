@@ -688,6 +688,40 @@ def mxfp4_gather_values(cache: np.ndarray, block_size: int, block_table_row, pos
     return mxfp4_values(mxfp4_unpack(packed), scales)
 
 
+def mxfp4_gather_k(cache: np.ndarray, block_size: int, block_table_row, n_tok: int):
+    """Copy the first ``n_tok`` tokens of one request out of the MXFP4 cache (prefill).
+
+    The MXFP4 twin of ``gather_k``: [V41] 实现拆解 item 2 (the builder slices the
+    sparse buffers for every prefill chunk as well as for decode, and requires
+    the MXFP4 indexer cache). Token ``p`` is read with ``mxfp4_cache_token`` from
+    block ``block_table_row[p // block_size]`` at offset ``p % block_size``.
+
+    Returns (packed codes uint8 [n_tok, 64], scale codes uint8 [n_tok, 4]).
+    """
+    packed = np.zeros((n_tok, D // 2), dtype=np.uint8)
+    scales = np.zeros((n_tok, D // MX_BLOCK), dtype=np.uint8)
+    for p in range(n_tok):
+        codes, sc = mxfp4_cache_token(cache, block_size, int(block_table_row[p // block_size]), p % block_size)
+        packed[p] = mxfp4_pack(codes[None, :])[0]
+        scales[p] = sc
+    return packed, scales
+
+
+def sparse_logits_prefill_mxfp4(q8, w, packed, scales, si, end, sbk) -> np.ndarray:
+    """``sparse_logits_prefill`` over gathered MXFP4 k (``mxfp4_gather_k``'s layout)."""
+    si = np.asarray(si)
+    rows, n_si = si.shape
+    out = np.full((rows, n_si * sbk), -np.inf)
+    for r in range(rows):
+        e = int(end[r])
+        if e <= 0:
+            continue
+        toks = np.array([sparse_column_token(si[r], c, sbk) for c in range(e)])
+        kv = mxfp4_values(mxfp4_unpack(packed[toks]), scales[toks])
+        out[r, :e] = logits_row_values(q8[r], w[r], kv)
+    return out
+
+
 def paged_decode_logits_mxfp4(q8, w, cache, block_size, block_table, ctx_lens, next_n=1) -> np.ndarray:
     """``paged_decode_logits`` over an MXFP4 cache (same row limits and fill values)."""
     ctx_lens = np.asarray(ctx_lens, dtype=np.int64)

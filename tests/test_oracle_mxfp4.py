@@ -212,3 +212,74 @@ def test_mxfp4_gather_equals_token_by_token_reads():
         for i, p in enumerate(pos):
             c, s = O.mxfp4_cache_token(cache, 64, int(pool.block_table[b][p // 64]), int(p) % 64)
             assert np.array_equal(got[i], O.mxfp4_values(c, s)[0])
+
+
+def test_mxfp4_gather_k_equals_cache_reads_and_quantised_k():
+    # the prefill gather of one request: row p holds token p's packed codes and
+    # scale codes; decoded, the rows equal both the vectorised paged read and the
+    # MXFP4 conversion of the k that filled the cache
+    ctx = np.array([300, 129])
+    pool, cache, ks = _mx_pool(9, ctx, bs=64)
+    for b in range(2):
+        n = int(ctx[b])
+        packed, scales = O.mxfp4_gather_k(cache, 64, pool.block_table[b], n)
+        assert packed.shape == (n, 64) and scales.shape == (n, 4)
+        for p in (0, 1, 63, 64, n - 1):
+            c, s = O.mxfp4_cache_token(cache, 64, int(pool.block_table[b][p // 64]), p % 64)
+            assert np.array_equal(O.mxfp4_unpack(packed[p:p + 1])[0], c) and np.array_equal(scales[p], s)
+        vals = O.mxfp4_values(O.mxfp4_unpack(packed), scales)
+        assert np.array_equal(vals, O.mxfp4_gather_values(cache, 64, pool.block_table[b], range(n)))
+        assert np.array_equal(vals, O.mxfp4_values(*O.mxfp4_quant(ks[b])))
+
+
+def test_mxfp4_sparse_logits_prefill_one_hot_closed_form():
+    rng = np.random.default_rng(10)
+    S, T, sbk = 256, 3, 16
+    for _ in range(10):
+        h, d, t = int(rng.integers(0, 64)), int(rng.integers(0, 128)), int(rng.integers(0, S))
+        a, kc, e = int(rng.integers(1, 126)), int(rng.integers(1, 16)), int(rng.integers(110, 140))
+        q8 = np.zeros((T, 64, 128), dtype=np.uint8)
+        q8[:, h, d] = a
+        w = rng.standard_normal((T, 64))
+        codes = np.zeros((S, 128), dtype=np.uint8)
+        scales = np.full((S, 4), 127, dtype=np.uint8)
+        codes[t, d] = kc
+        scales[t, d // 32] = e
+        packed = O.mxfp4_pack(codes)
+        si = np.tile(np.arange(S // sbk), (T, 1))
+        end = np.array([S, t + 1, t])                      # the last row stops just before token t
+        out = O.sparse_logits_prefill_mxfp4(q8, w, packed, scales, si, end, sbk)
+        for r in range(T):
+            want = np.zeros(S)
+            want[t] = w[r, h] * e4m3_decode(a) * e2m1_decode(kc) * 2.0 ** (e - 127)
+            e_r = int(end[r])
+            assert np.allclose(out[r, :e_r], want[:e_r], rtol=1e-15, atol=0)
+            assert np.all(np.isneginf(out[r, e_r:]))
+
+
+def test_mxfp4_sparse_logits_prefill_equal_dense_at_mapped_positions():
+    # rows of a prefill chunk whose requests start at ks > 0: every valid sparse
+    # column equals the logit of its absolute token over the whole quantised k
+    rng = np.random.default_rng(11)
+    S, T = 700, 6
+    k = rng.standard_normal((S, 128)).astype(np.float32)
+    codes, scales = O.mxfp4_quant(k)
+    packed = O.mxfp4_pack(codes)
+    kv = O.mxfp4_values(codes, scales)
+    q8, w = W.make_q(11, T)
+    for sbk, cbs in ((64, 64), (16, 64), (8, 32)):
+        row_ks = np.array([0, sbk, 3 * sbk, 128, 2 * sbk, 5 * sbk])
+        row_ke = np.array([700, 650, 400, 300, 2 * sbk + 1, 700])
+        cand = rng.integers(-1, 12, (T, 8))
+        si, end = O.expand_candidates(cand, row_ks, row_ke, cbs, sbk)
+        sp = O.sparse_logits_prefill_mxfp4(q8, w, packed, scales, si, end, sbk)
+        assert np.count_nonzero(end) >= T // 2
+        for r in range(T):
+            full = O.logits_row_values(q8[r], w[r], kv)
+            for c in range(sp.shape[1]):
+                if c < end[r]:
+                    tok = O.sparse_column_token(si[r], c, sbk)
+                    assert row_ks[r] <= tok < row_ke[r]
+                    assert sp[r, c] == full[tok]
+                else:
+                    assert sp[r, c] == -np.inf
