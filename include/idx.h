@@ -229,6 +229,26 @@ idx_status_t idx_gather_k(const uint8_t* cache, int32_t block_size, int64_t bloc
                           uint8_t* k8_out, float* kscale_out, cudaStream_t stream);
 
 /*
+ * idx_gather_k_mxfp4 - copy the first n_tok tokens of one request out of an
+ * MXFP4 cache, for the V4.1 sparse prefill (the V4.1 review, "实现拆解" item 2:
+ * the builder slices the sparse buffers for every prefill chunk as well as for
+ * decode, on the MXFP4 indexer cache). Token p comes from block
+ * block_table[p / block_size], offset p % block_size; its 64 bytes of e2m1
+ * codes and its 32-bit word of E8M0 scale codes are copied unchanged.
+ *
+ *   cache         as for idx_k_quant_and_cache_mxfp4 (32-byte aligned, stride a
+ *                 multiple of 32).
+ *   block_table   int32 [ceil(n_tok / block_size)] physical block ids.
+ *   codes_out     uint8 [n_tok, 64] contiguous, 16-byte aligned (32-byte aligned
+ *                 to be scored by idx_mqa_logits_prefill_mxfp4).
+ *   scales_out    uint32 [n_tok], 4-byte aligned (16-byte aligned to be scored).
+ * Errors: IDX_ERR_INVALID_ARG / IDX_ERR_UNSUPPORTED as for the MXFP4 insert.
+ */
+idx_status_t idx_gather_k_mxfp4(const uint8_t* cache, int32_t block_size, int64_t block_stride_bytes,
+                                const int32_t* block_table, int32_t n_tok, uint8_t* codes_out,
+                                uint32_t* scales_out, cudaStream_t stream);
+
+/*
  * idx_mqa_logits_prefill - logits of T query rows against gathered k.
  *
  * Dense mode (sparse_idx == NULL): row t scores tokens s in [row_ks[t], row_ke[t])
@@ -261,6 +281,29 @@ idx_status_t idx_mqa_logits_prefill(const uint8_t* q, int64_t ld_q, const void* 
                                     int32_t n_si, const int32_t* end, int32_t sbk,
                                     void* logits, int out_dtype, int64_t ld_out,
                                     void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * idx_mqa_logits_prefill_mxfp4 - the sparse mode of idx_mqa_logits_prefill over
+ * gathered MXFP4 k (idx_gather_k_mxfp4's layout), the V4.1 sparse prefill
+ * ("实现拆解" items 1-2: the fp8 x fp4 sparse MQA-logits kernel on the MXFP4
+ * indexer cache). Column c < end[t] of row t scores token
+ * sparse_idx[t, c / sbk] * sbk + c % sbk with the block scales applied by the
+ * tensor core (e4m3 q x e2m1 k); the other columns hold -inf.
+ *
+ *   k_codes   uint8 [S, 64] packed e2m1 codes, 32-byte aligned.
+ *   k_scales  uint32 [S] words of four E8M0 codes, 16-byte aligned.
+ *   sparse_idx must be given (the MXFP4 path has no dense prefill mode:
+ *   IDX_ERR_UNSUPPORTED otherwise); row_ks / row_ke are not read. Every other
+ *   argument, the optional workspace and the errors are those of the sparse
+ *   mode of idx_mqa_logits_prefill.
+ */
+idx_status_t idx_mqa_logits_prefill_mxfp4(const uint8_t* q, int64_t ld_q, const void* w, int w_dtype,
+                                          int64_t ld_w, const uint8_t* k_codes, const uint32_t* k_scales,
+                                          int32_t S, const int32_t* row_ks, const int32_t* row_ke,
+                                          int32_t T, const int32_t* sparse_idx, int64_t ld_si,
+                                          int32_t n_si, const int32_t* end, int32_t sbk,
+                                          void* logits, int out_dtype, int64_t ld_out,
+                                          void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
  * idx_paged_mqa_logits_decode - decode logits read straight from the paged cache.

@@ -17,8 +17,8 @@ import torch
 from . import _lib
 
 __all__ = [
-    "IdxError", "idx_k_quant_and_cache", "idx_k_quant_and_cache_mxfp4", "idx_gather_k",
-    "idx_mqa_logits_prefill", "idx_paged_mqa_logits_decode", "idx_paged_mqa_logits_decode_mxfp4", "idx_topk", "idx_expand_candidates", "idx_sparse_topk_remap",
+    "IdxError", "idx_k_quant_and_cache", "idx_k_quant_and_cache_mxfp4", "idx_gather_k", "idx_gather_k_mxfp4",
+    "idx_mqa_logits_prefill", "idx_mqa_logits_prefill_mxfp4", "idx_paged_mqa_logits_decode", "idx_paged_mqa_logits_decode_mxfp4", "idx_topk", "idx_expand_candidates", "idx_sparse_topk_remap",
     "idx_req_to_global_slots", "idx_dcp_topk_merge", "idx_q_rope_quant", "idx_block_span",
     "idx_workspace_bytes", "idx_device_error", "library",
 ]
@@ -94,6 +94,14 @@ def idx_gather_k(cache, block_size, block_table_row, n_tok, k8_out, kscale_out, 
         _ptr(kscale_out), _stream(stream)))
 
 
+def idx_gather_k_mxfp4(cache, block_size, block_table_row, n_tok, codes_out, scales_out, stream=None):
+    """Copy n_tok tokens of one request out of an MXFP4 cache into codes_out uint8 [n, 64] /
+    scales_out int32 [n] (the words of four E8M0 codes)."""
+    _check("idx_gather_k_mxfp4", library().idx_gather_k_mxfp4(
+        _ptr(cache), block_size, cache.stride(0), _ptr(block_table_row), n_tok, _ptr(codes_out),
+        _ptr(scales_out), _stream(stream)))
+
+
 def _q_stride(q: torch.Tensor) -> int:
     if q.dim() != 3 or q.shape[1:] != (64, 128) or q.stride(2) != 1 or q.stride(1) != 128:
         raise ValueError("q must be uint8 [rows, 64, 128] with contiguous heads")
@@ -109,6 +117,17 @@ def idx_mqa_logits_prefill(q, w, k8, kscale, row_ks, row_ke, logits, sparse_idx=
     _check("idx_mqa_logits_prefill", library().idx_mqa_logits_prefill(
         _ptr(q), _q_stride(q), _ptr(w), _dtype_code(w), _rows(w), _ptr(k8), _ptr(kscale),
         k8.shape[0], _ptr(row_ks), _ptr(row_ke), q.shape[0], _ptr(sparse_idx), ld_si, n_si,
+        _ptr(end), sbk, _ptr(logits), _dtype_code(logits), _rows(logits), _ptr(ws),
+        0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def idx_mqa_logits_prefill_mxfp4(q, w, k_codes, k_scales, logits, sparse_idx, end, sbk, n_si=None, ws=None,
+                                 stream=None):
+    """Sparse prefill logits over gathered MXFP4 k (k_codes uint8 [S, 64], k_scales int32 [S])."""
+    n_si = sparse_idx.shape[1] if n_si is None else n_si
+    _check("idx_mqa_logits_prefill_mxfp4", library().idx_mqa_logits_prefill_mxfp4(
+        _ptr(q), _q_stride(q), _ptr(w), _dtype_code(w), _rows(w), _ptr(k_codes), _ptr(k_scales),
+        k_codes.shape[0], None, None, q.shape[0], _ptr(sparse_idx), sparse_idx.stride(0), n_si,
         _ptr(end), sbk, _ptr(logits), _dtype_code(logits), _rows(logits), _ptr(ws),
         0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)))
 

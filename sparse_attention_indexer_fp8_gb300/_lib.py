@@ -34,7 +34,11 @@ SIGNATURES = {
     "idx_k_quant_and_cache_mxfp4": (c_int, [c_ptr, c_int, c_i64, c_i32, c_ptr, c_ptr, c_i32, c_i32, c_i64,
                                             c_ptr]),
     "idx_gather_k": (c_int, [c_ptr, c_i32, c_i64, c_ptr, c_i32, c_ptr, c_ptr, c_ptr]),
+    "idx_gather_k_mxfp4": (c_int, [c_ptr, c_i32, c_i64, c_ptr, c_i32, c_ptr, c_ptr, c_ptr]),
     "idx_mqa_logits_prefill": (c_int, [c_ptr, c_i64, c_ptr, c_int, c_i64, c_ptr, c_ptr, c_i32, c_ptr,
+                                       c_ptr, c_i32, c_ptr, c_i64, c_i32, c_ptr, c_i32, c_ptr, c_int,
+                                       c_i64, c_ptr, c_size, c_ptr]),
+    "idx_mqa_logits_prefill_mxfp4": (c_int, [c_ptr, c_i64, c_ptr, c_int, c_i64, c_ptr, c_ptr, c_i32, c_ptr,
                                        c_ptr, c_i32, c_ptr, c_i64, c_i32, c_ptr, c_i32, c_ptr, c_int,
                                        c_i64, c_ptr, c_size, c_ptr]),
     "idx_paged_mqa_logits_decode": (c_int, [c_ptr, c_i64, c_ptr, c_int, c_i64, c_ptr, c_i32, c_i32,

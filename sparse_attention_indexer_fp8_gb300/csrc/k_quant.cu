@@ -156,6 +156,26 @@ __global__ void gather_k_kernel(const uint8_t* __restrict__ cache, int block_siz
   }
 }
 
+// The MXFP4 twin: one thread per 16-byte chunk, four threads move one token's
+// 64 bytes of e2m1 codes and the first also moves its word of E8M0 scale codes.
+__global__ void gather_k_mxfp4_kernel(const uint8_t* __restrict__ cache, int block_size,
+                                      int64_t block_stride, const int32_t* __restrict__ block_table,
+                                      int n_tok, uint8_t* __restrict__ codes_out,
+                                      uint32_t* __restrict__ scales_out) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t p = i >> 2;
+  const int chunk = static_cast<int>(i & 3);
+  if (p >= n_tok) return;
+  const int64_t blk = __ldg(block_table + p / block_size);
+  const int off = static_cast<int>(p % block_size);
+  const uint8_t* src = cache + blk * block_stride;
+  const uint4 v = __ldg(reinterpret_cast<const uint4*>(src + off * (kDim / 2) + chunk * 16));
+  *reinterpret_cast<uint4*>(codes_out + p * (kDim / 2) + chunk * 16) = v;
+  if (chunk == 0) {
+    scales_out[p] = __ldg(reinterpret_cast<const uint32_t*>(src + block_size * (kDim / 2) + 4 * off));
+  }
+}
+
 bool block_size_ok(int32_t bs) { return bs == 16 || bs == 32 || bs == 64 || bs == 128; }
 
 idx_status_t check_cache(const char* fn, const void* cache, int32_t block_size,
@@ -248,6 +268,27 @@ extern "C" idx_status_t idx_gather_k(const uint8_t* cache, int32_t block_size,
   const dim3 grid(static_cast<unsigned>((threads + block - 1) / block));
   gather_k_kernel<<<grid, block, 0, stream>>>(cache, block_size, block_stride_bytes, block_table,
                                               n_tok, k8_out, kscale_out);
+  return check_launch(fn);
+}
+
+extern "C" idx_status_t idx_gather_k_mxfp4(const uint8_t* cache, int32_t block_size,
+                                           int64_t block_stride_bytes, const int32_t* block_table,
+                                           int32_t n_tok, uint8_t* codes_out, uint32_t* scales_out,
+                                           cudaStream_t stream) {
+  const char* fn = "idx_gather_k_mxfp4";
+  if (n_tok < 0) return fail(IDX_ERR_INVALID_ARG, "%s: negative n_tok", fn);
+  if (n_tok == 0) return IDX_OK;
+  if (!cache || !block_table || !codes_out || !scales_out) return fail(IDX_ERR_INVALID_ARG, "%s: NULL pointer", fn);
+  idx_status_t st = check_cache_mxfp4(fn, cache, block_size, block_stride_bytes);
+  if (st != IDX_OK) return st;
+  if (!aligned(codes_out, 16) || !aligned(scales_out, 4)) {
+    return fail(IDX_ERR_UNSUPPORTED, "%s: codes_out must be 16-byte and scales_out 4-byte aligned", fn);
+  }
+  const int64_t threads = static_cast<int64_t>(n_tok) * 4;
+  const int block = 256;
+  const dim3 grid(static_cast<unsigned>((threads + block - 1) / block));
+  gather_k_mxfp4_kernel<<<grid, block, 0, stream>>>(cache, block_size, block_stride_bytes, block_table,
+                                                    n_tok, codes_out, scales_out);
   return check_launch(fn);
 }
 

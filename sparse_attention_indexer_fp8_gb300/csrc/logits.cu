@@ -1235,23 +1235,28 @@ extern "C" idx_status_t idx_paged_mqa_logits_decode_mxfp4(
                       sparse_idx, ld_si, n_si, end, sbk, logits, out_dtype, ld_out, ws, ws_bytes, stream);
 }
 
-extern "C" idx_status_t idx_mqa_logits_prefill(const uint8_t* q, int64_t ld_q, const void* w,
-                                               int w_dtype, int64_t ld_w, const uint8_t* k8,
-                                               const float* kscale, int32_t S,
-                                               const int32_t* row_ks, const int32_t* row_ke,
-                                               int32_t T, const int32_t* sparse_idx, int64_t ld_si,
-                                               int32_t n_si, const int32_t* end, int32_t sbk,
-                                               void* logits, int out_dtype, int64_t ld_out,
-                                               void* ws, size_t ws_bytes, cudaStream_t stream) {
-  const char* fn = "idx_mqa_logits_prefill";
+namespace {
+
+// Both prefill entry points: e4m3 k (k = k8 [S, 128], kscale = fp32 [S]) and
+// MXFP4 k (k = packed e2m1 codes [S, 64], kscale = 32-bit words of E8M0 codes
+// [S]; sparse mode only, the V4.1 path).
+idx_status_t prefill(const char* fn, bool fp4, const uint8_t* q, int64_t ld_q, const void* w,
+                     int w_dtype, int64_t ld_w, const uint8_t* k8, const void* kscale, int32_t S,
+                     const int32_t* row_ks, const int32_t* row_ke, int32_t T, const int32_t* sparse_idx,
+                     int64_t ld_si, int32_t n_si, const int32_t* end, int32_t sbk, void* logits,
+                     int out_dtype, int64_t ld_out, void* ws, size_t ws_bytes, cudaStream_t stream) {
   if (T < 0 || S < 0) return fail(IDX_ERR_INVALID_ARG, "%s: negative T or S", fn);
+  if (fp4 && !sparse_idx) {
+    return fail(IDX_ERR_UNSUPPORTED, "%s: MXFP4 k is scored in the sparse mode only", fn);
+  }
   if (T == 0) return IDX_OK;
   idx_status_t st = check_common(fn, q, ld_q, w, w_dtype, ld_w, T, logits, out_dtype, ld_out);
   if (st != IDX_OK) return st;
   if (S == 0) return sparse_idx ? fail(IDX_ERR_INVALID_ARG, "%s: sparse mode with S == 0", fn) : IDX_OK;
-  if (!k8 || !kscale) return fail(IDX_ERR_INVALID_ARG, "%s: NULL k8 or kscale", fn);
-  if (!aligned(k8, 16) || !aligned(kscale, 16)) {
-    return fail(IDX_ERR_UNSUPPORTED, "%s: k8 and kscale must be 16-byte aligned", fn);
+  if (!k8 || !kscale) return fail(IDX_ERR_INVALID_ARG, "%s: NULL k or its scales", fn);
+  // the four-bit tensor map reads 32-byte aligned rows
+  if (!aligned(k8, fp4 ? 32 : 16) || !aligned(kscale, 16)) {
+    return fail(IDX_ERR_UNSUPPORTED, "%s: k must be %d-byte and its scales 16-byte aligned", fn, fp4 ? 32 : 16);
   }
   LogitsParams p{};
   p.n_rows = T;
@@ -1307,11 +1312,14 @@ extern "C" idx_status_t idx_mqa_logits_prefill(const uint8_t* q, int64_t ld_q, c
   st = make_q_map(&mq, q, ld_q, T, nq_tmpl);
   if (st != IDX_OK) return st;
   {
+    // MXFP4: 128 four-bit elements per row (64 packed bytes), spread by the copy
+    // into the same 128-byte shared-memory rows and swizzle as e4m3
+    const uint64_t row_bytes = fp4 ? kDim / 2 : kDim;
     const uint64_t dims[3] = {static_cast<uint64_t>(kDim), static_cast<uint64_t>(S), 1ull};
-    const uint64_t strides[2] = {static_cast<uint64_t>(kDim), static_cast<uint64_t>(kDim) * S};
+    const uint64_t strides[2] = {row_bytes, row_bytes * S};
     const uint32_t box[3] = {static_cast<uint32_t>(kDim), static_cast<uint32_t>(p.unit), 1u};
-    st = encode_tensor_map(&mkv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, k8, dims, strides, box,
-                           CU_TENSOR_MAP_SWIZZLE_128B);
+    st = encode_tensor_map(&mkv, fp4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
+                           k8, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != IDX_OK) return st;
   }
   {
@@ -1323,5 +1331,31 @@ extern "C" idx_status_t idx_mqa_logits_prefill(const uint8_t* q, int64_t ld_q, c
     if (st != IDX_OK) return st;
   }
   return dispatch(nq_tmpl, mq, mkv, msc, p, static_cast<long long>(p.n_groups) * p.tiles_per_group,
-                  stream, fn);
+                  stream, fn, fp4);
+}
+
+}  // namespace
+
+extern "C" idx_status_t idx_mqa_logits_prefill(const uint8_t* q, int64_t ld_q, const void* w,
+                                               int w_dtype, int64_t ld_w, const uint8_t* k8,
+                                               const float* kscale, int32_t S,
+                                               const int32_t* row_ks, const int32_t* row_ke,
+                                               int32_t T, const int32_t* sparse_idx, int64_t ld_si,
+                                               int32_t n_si, const int32_t* end, int32_t sbk,
+                                               void* logits, int out_dtype, int64_t ld_out,
+                                               void* ws, size_t ws_bytes, cudaStream_t stream) {
+  return prefill("idx_mqa_logits_prefill", false, q, ld_q, w, w_dtype, ld_w, k8, kscale, S, row_ks, row_ke,
+                 T, sparse_idx, ld_si, n_si, end, sbk, logits, out_dtype, ld_out, ws, ws_bytes, stream);
+}
+
+extern "C" idx_status_t idx_mqa_logits_prefill_mxfp4(const uint8_t* q, int64_t ld_q, const void* w,
+                                                     int w_dtype, int64_t ld_w, const uint8_t* k_codes,
+                                                     const uint32_t* k_scales, int32_t S,
+                                                     const int32_t* row_ks, const int32_t* row_ke,
+                                                     int32_t T, const int32_t* sparse_idx, int64_t ld_si,
+                                                     int32_t n_si, const int32_t* end, int32_t sbk,
+                                                     void* logits, int out_dtype, int64_t ld_out,
+                                                     void* ws, size_t ws_bytes, cudaStream_t stream) {
+  return prefill("idx_mqa_logits_prefill_mxfp4", true, q, ld_q, w, w_dtype, ld_w, k_codes, k_scales, S, row_ks,
+                 row_ke, T, sparse_idx, ld_si, n_si, end, sbk, logits, out_dtype, ld_out, ws, ws_bytes, stream);
 }

@@ -111,6 +111,15 @@ def test_validation_rejects_before_touching_the_device(lib):
                                                  2, 1, None, 0, 0, None, 0, fake, 0, 4096, None, 0, None) == 2
     assert lib.idx_paged_mqa_logits_decode_mxfp4(fake, 8192, fake, 0, 64, fake, 16, 64, 4096, fake, 8, fake,
                                                  2, 1, None, 0, 0, None, 0, fake, 0, 4096, None, 0, None) == 1
+    # MXFP4 prefill gather: block size, stride, NULL output
+    assert lib.idx_gather_k_mxfp4(fake, 48, 4608, fake, 10, fake, fake, None) == 2
+    assert lib.idx_gather_k_mxfp4(fake, 64, 4368, fake, 10, fake, fake, None) == 2
+    assert lib.idx_gather_k_mxfp4(fake, 64, 4608, fake, 10, None, fake, None) == 1
+    # MXFP4 prefill scoring: the dense mode does not exist, codes must be 32-byte aligned
+    assert lib.idx_mqa_logits_prefill_mxfp4(fake, 8192, fake, 0, 64, fake, fake, 64, None, None, 4, None, 0,
+                                            0, None, 0, fake, 0, 64, None, 0, None) == 2
+    assert lib.idx_mqa_logits_prefill_mxfp4(fake, 8192, fake, 0, 64, ctypes.c_void_p(0x1010), fake, 64, None,
+                                            None, 4, fake, 1, 1, fake, 64, fake, 1, 64, None, 0, None) == 2
     # tensor-rate diagnostic: unknown kind, no iterations
     assert lib.idx_diag_mma_peak(7, 100, 0, None, None) == 2
     assert lib.idx_diag_mma_peak(0, 0, 0, None, None) == 1

@@ -198,3 +198,104 @@ def test_mxfp4_decode_many_tiles_per_cta():
     for r in range(len(ctx)):
         L = int(ctx[r])
         assert_logits_close(got[r, :L], ref[r, :L], f"row {r}")
+
+
+@pytest.mark.parametrize("next_n", [2, 3])
+def test_mxfp4_hierarchical_mtp_rows_and_layer_reuse(next_n):
+    # the V4.1 consumer layers on the MXFP4 cache with multi-token prediction:
+    # next_n query rows per request (row r of request r // next_n sees
+    # [0, L - next_n + j + 1)), one expansion reused by two layers, each layer's
+    # scores, selection, positions and slots checked against the oracle
+    from sparse_attention_indexer_fp8_gb300.pipeline import HierarchicalStep
+
+    ctx = np.array([1000, 777, 4096, 2500, 64, 5], dtype=np.int32)
+    B = len(ctx)
+    rows = B * next_n
+    pool = W.make_pool(400 + next_n, ctx)
+    g, o = build_mx_caches(pool, 400 + next_n)
+    cand = W.make_candidates(410 + next_n, rows, 16, 64, n_dup=3, n_pad=2, n_oob=2)
+    r2r = np.repeat(np.arange(B), next_n).astype(np.int32)
+    row_ke = np.array([O.decode_row_limit(int(ctx[r // next_n]), next_n, r % next_n) for r in range(rows)],
+                      dtype=np.int32)
+    k = 200
+    st = HierarchicalStep(rows, cand.shape[1], 64, 64, k, 64, DEV, next_n=next_n, kv="mxfp4")
+    st.expand(dev(cand), dev(ctx), dev(row_ke))
+    osi, oend = O.expand_candidates(cand, None, row_ke, 64, 64)
+    assert np.array_equal(st.sparse_idx.cpu().numpy(), osi) and np.array_equal(st.end.cpu().numpy(), oend)
+    for layer in range(2):
+        q8, w = W.make_q(420 + 10 * layer + next_n, rows)
+        slots = st.score(dev(q8), dev(w), g, dev(pool.block_table), dev(ctx)).cpu().numpy()
+        idx.idx_device_error()
+        ref = O.sparse_logits_decode_mxfp4(q8, w, o, 64, pool.block_table, r2r, osi, oend, 64)
+        got = st.logits.float().cpu().numpy()
+        assert_logits_close(got, ref, f"layer {layer} sparse logits", bf16=True)
+        cols, pos = st.cols.cpu().numpy(), st.positions.cpu().numpy()
+        for r in range(rows):
+            e = int(oend[r])
+            assert_topk_values_exact(cols[r], got[r, :e], k, f"layer {layer} row {r}")
+            assert_topk_row(cols[r], ref[r, :e], k, f"layer {layer} row {r} vs oracle", bf16=True)
+            m = min(k, e)
+            assert pos[r, :m].tolist() == [O.sparse_column_token(osi[r], int(c), 64) for c in cols[r, :m]]
+            assert np.all(pos[r, m:] == -1)
+        assert np.array_equal(slots, O.req_to_global_slots(pos, r2r, pool.block_table, 64, 64))
+
+
+@pytest.mark.parametrize("block_size", [16, 64])
+def test_mxfp4_gather_k_bitexact(block_size):
+    # the prefill gather of every request: the codes and scale words the oracle reads
+    ctx = np.array([300, 1, 65, 2049], dtype=np.int32)
+    pool = W.make_pool(500 + block_size, ctx, block_size=block_size, extra_blocks=3)
+    g, o = build_mx_caches(pool, 500 + block_size, block_size)
+    for b in range(len(ctx)):
+        n = int(ctx[b])
+        codes = torch.full((n, 64), 0xAB, dtype=torch.uint8, device=DEV)
+        scales = torch.full((n,), -1, dtype=torch.int32, device=DEV)
+        idx.idx_gather_k_mxfp4(g, block_size, dev(pool.block_table[b]), n, codes, scales)
+        idx.idx_device_error()
+        opacked, oscales = O.mxfp4_gather_k(o, block_size, pool.block_table[b], n)
+        assert np.array_equal(codes.cpu().numpy(), opacked), f"request {b} codes"
+        assert np.array_equal(scales.cpu().numpy().view(np.uint8).reshape(n, 4), oscales), f"request {b} scales"
+
+
+@pytest.mark.parametrize("sbk,out_bf16", [(16, True), (64, False)])
+def test_mxfp4_sparse_prefill_logits_and_remap(sbk, out_bf16):
+    # the V4.1 sparse prefill on the MXFP4 cache: gather one request's k, score the
+    # candidate sparse blocks of rows that start at ks > 0, select and remap
+    S, T = 3000, 40
+    pool = W.make_pool(520, [S], extra_blocks=2)
+    g, o = build_mx_caches(pool, 520)
+    codes = torch.empty((S, 64), dtype=torch.uint8, device=DEV)
+    scales = torch.empty((S,), dtype=torch.int32, device=DEV)
+    idx.idx_gather_k_mxfp4(g, 64, dev(pool.block_table[0]), S, codes, scales)
+    opacked, oscales = O.mxfp4_gather_k(o, 64, pool.block_table[0], S)
+    q8, w = W.make_q(521, T)
+    rng = np.random.default_rng(522)
+    ks = (rng.integers(0, 60, T) * sbk).astype(np.int32)
+    ke = np.minimum(ks + rng.integers(1, 2000, T), S).astype(np.int32)
+    cand = W.make_candidates(523, T, 16, 40)
+    R = 64 // sbk
+    si = torch.empty((T, 16 * R), dtype=torch.int32, device=DEV)
+    end = torch.empty(T, dtype=torch.int32, device=DEV)
+    idx.idx_expand_candidates(dev(cand), dev(ks), dev(ke), 64, sbk, si, end)
+    osi, oend = O.expand_candidates(cand, ks, ke, 64, sbk)
+    assert np.array_equal(si.cpu().numpy(), osi) and np.array_equal(end.cpu().numpy(), oend)
+    out = torch.empty((T, 16 * R * sbk), device=DEV, dtype=torch.bfloat16 if out_bf16 else torch.float32)
+    ws = torch.zeros((T, 1024), dtype=torch.int32, device=DEV)
+    idx.idx_mqa_logits_prefill_mxfp4(dev(q8), dev(w), codes, scales, out, si, end, sbk, ws=ws)
+    ref = O.sparse_logits_prefill_mxfp4(q8, w, opacked, oscales, osi, oend, sbk)
+    got = out.float().cpu().numpy()
+    assert_logits_close(got, ref, "MXFP4 sparse prefill logits", bf16=out_bf16)
+    k = 512
+    pos = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    cols = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    idx.idx_sparse_topk_remap(out, end, si, dev(ks), sbk, k, pos, col_scratch=cols, ws=ws)
+    idx.idx_device_error()
+    assert not ws.any().item()
+    pos, cols = pos.cpu().numpy(), cols.cpu().numpy()
+    for r in range(T):
+        e = int(oend[r])
+        assert_topk_values_exact(cols[r], got[r, :e], k, f"row {r} on its own scores")
+        assert_topk_row(cols[r], ref[r, :e], k, f"row {r} vs oracle", bf16=out_bf16)
+        m = min(k, e)
+        assert np.array_equal(pos[r, :m], O.sparse_remap_columns(cols[r, :m], osi[r], int(ks[r]), sbk))
+        assert np.all(pos[r, m:] == -1)
