@@ -642,6 +642,166 @@ class PrefillBench:
                 "parallelism": f"chunks sharded, {world} independent replica(s)"}
 
 
+class SparsePrefillBench:
+    """V4.1 sparse prefill chunk: insert the chunk's k, gather the context, expand each row's
+    candidate blocks, score the candidate sparse blocks (bf16), top-2048 + remap per row.
+
+    The 8192-query chunk of a 32K context (the dense prefill workload), each row
+    with 64 candidate 64-token blocks drawn over the context (duplicates, -1 and
+    out-of-range ids included; blocks past the row's causal limit are dropped by
+    the expansion). ``prefill_sparse_mxfp4`` runs it on the MXFP4 indexer cache,
+    the cache of the V4.1 path (gather of the 68-byte records, fp8 x fp4 scores)."""
+
+    launches_per_step = 5
+
+    def __init__(self, name, rank, dev):
+        import sparse_attention_indexer_fp8_gb300 as idx
+
+        self.idx, self.dev, self.name = idx, dev, name
+        self.kv = "mxfp4" if name.endswith("_mxfp4") else "fp8"
+        self.wl = wl = W.prefill_chunk(seed=rank_seed(1006, rank))
+        self.T, self.S = T, S = wl.q8.shape[0], wl.S
+        self.pool = pool = W.make_pool(wl.seed, [S])
+        self.stride = W.mxfp4_block_stride_bytes() if self.kv == "mxfp4" else W.block_stride_bytes()
+        self.cache = torch.zeros((pool.num_blocks, self.stride), dtype=torch.uint8, device=dev)
+        self.insert = idx.idx_k_quant_and_cache_mxfp4 if self.kv == "mxfp4" else idx.idx_k_quant_and_cache
+        k = W.make_k_device(wl.seed, 0, S, dev)
+        sm = torch.from_numpy(pool.slot_mapping(0)).to(dev)
+        # the context before the chunk is state; the chunk's own k is inserted every step
+        self.insert(k[:S - T], sm[:S - T], self.cache, pool.block_size)
+        self.chunk_k, self.chunk_slots = k[S - T:].contiguous(), sm[S - T:].contiguous()
+        self.bt_row = torch.from_numpy(pool.block_table[0]).to(dev)
+        if self.kv == "mxfp4":
+            self.codes = torch.empty((S, 64), dtype=torch.uint8, device=dev)
+            self.scales = torch.empty((S,), dtype=torch.int32, device=dev)
+        else:
+            self.k8 = torch.empty((S, 128), dtype=torch.uint8, device=dev)
+            self.kscale = torch.empty(S, dtype=torch.float32, device=dev)
+        self.q = torch.from_numpy(wl.q8).to(dev)
+        self.w = torch.from_numpy(wl.w.view(np.int16)).to(dev).view(torch.bfloat16)
+        self.ks = torch.from_numpy(wl.row_ks).to(dev)
+        self.ke = torch.from_numpy(wl.row_ke).to(dev)
+        self.h_cand = W.make_candidates(wl.seed, T, 64, S // 64)
+        self.cand = torch.from_numpy(self.h_cand).to(dev)
+        self.sbk = 64
+        self.si = torch.empty((T, 64), dtype=torch.int32, device=dev)
+        self.end = torch.empty(T, dtype=torch.int32, device=dev)
+        self.logits = torch.empty((T, 64 * self.sbk), dtype=torch.bfloat16, device=dev)
+        self.ws = torch.zeros((T, 1024), dtype=torch.int32, device=dev)
+        self.pos = torch.empty((T, wl.topk), dtype=torch.int32, device=dev)
+        self.cols = torch.empty((T, wl.topk), dtype=torch.int32, device=dev)
+        self.rows_per_step = T
+
+    metric = property(lambda self: "V4.1 sparse prefill indexer query-rows/s incl. top-2048 (8192-query chunk "
+                      "of a 32K context, 64 candidate 64-token blocks per row" +
+                      (", MXFP4 indexer cache)" if self.kv == "mxfp4" else ")"))
+    dtype = property(lambda self: ("e4m3xe2m1(mx)" if self.kv == "mxfp4" else "e4m3xe4m3") + "->f32 (bf16 logits)")
+
+    def step(self, stream, ev=None):
+        idx, bs = self.idx, self.pool.block_size
+        self.insert(self.chunk_k, self.chunk_slots, self.cache, bs, stream=stream)
+        if self.kv == "mxfp4":
+            idx.idx_gather_k_mxfp4(self.cache, bs, self.bt_row, self.S, self.codes, self.scales, stream=stream)
+        else:
+            idx.idx_gather_k(self.cache, bs, self.bt_row, self.S, self.k8, self.kscale, stream=stream)
+        idx.idx_expand_candidates(self.cand, self.ks, self.ke, 64, self.sbk, self.si, self.end, stream=stream)
+        if ev is not None:
+            ev[0].record(stream)
+        if self.kv == "mxfp4":
+            idx.idx_mqa_logits_prefill_mxfp4(self.q, self.w, self.codes, self.scales, self.logits, self.si,
+                                             self.end, self.sbk, ws=self.ws, stream=stream)
+        else:
+            idx.idx_mqa_logits_prefill(self.q, self.w, self.k8, self.kscale, self.ks, self.ke, self.logits,
+                                       sparse_idx=self.si, end=self.end, sbk=self.sbk, ws=self.ws, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        idx.idx_sparse_topk_remap(self.logits, self.end, self.si, self.ks, self.sbk, self.wl.topk, self.pos,
+                                  col_scratch=self.cols, ws=self.ws, stream=stream)
+
+    def e2e_io(self):
+        inputs = [(_pin(self.wl.q8), self.q), (self.w.cpu().pin_memory(), self.w),
+                  (self.chunk_k.cpu().pin_memory(), self.chunk_k),
+                  (self.chunk_slots.cpu().pin_memory(), self.chunk_slots), (_pin(self.h_cand), self.cand)]
+        return inputs, [(_pin_like(self.pos), self.pos)]
+
+    def _oracle_k(self):
+        """The context's k as the oracle quantises it: (k8, kscale), or MXFP4 (packed codes, scale codes)."""
+        from oracle import indexer as O
+        from oracle.codecs import bf16_decode
+
+        kb = W.make_k_device(self.wl.seed, 0, self.S, self.dev).view(torch.int16).cpu().numpy().view(np.uint16)
+        kf = bf16_decode(kb)
+        if self.kv == "mxfp4":
+            codes, scales = O.mxfp4_quant(kf)
+            return O.mxfp4_pack(codes), scales
+        return O.k_quant(kf)
+
+    def verify_and_time_oracle(self, n_rows):
+        from oracle import indexer as O
+        from oracle.codecs import bf16_decode
+        from tests.checks import assert_logits_close, assert_topk_row
+
+        wl, sbk = self.wl, self.sbk
+        ka, kb = self._oracle_k()
+        rng = np.random.default_rng(wl.seed)
+        sample = sorted(set([0, self.T - 1] + rng.choice(self.T, size=max(n_rows - 2, 0), replace=False).tolist()))
+        wv = bf16_decode(wl.w)
+        g_si, g_end = self.si.cpu().numpy(), self.end.cpu().numpy()
+        g_lg = self.logits.float().cpu().numpy()
+        g_cols, g_pos = self.cols.cpu().numpy(), self.pos.cpu().numpy()
+        t0 = time.perf_counter()
+        ref = {}
+        for t in sample:
+            osi, oend = O.expand_candidates(self.h_cand[t:t + 1], wl.row_ks[t:t + 1], wl.row_ke[t:t + 1], 64, sbk)
+            if self.kv == "mxfp4":
+                lg = O.sparse_logits_prefill_mxfp4(wl.q8[t:t + 1], wv[t:t + 1], ka, kb, osi, oend, sbk)[0]
+            else:
+                lg = O.sparse_logits_prefill(wl.q8[t:t + 1], wv[t:t + 1], ka, kb, osi, oend, sbk)[0]
+            cols, pos = O.sparse_topk_remap_row(lg, int(oend[0]), osi[0], int(wl.row_ks[t]), sbk, wl.topk)
+            ref[t] = (osi[0], int(oend[0]), lg, pos)
+        cpu_s = time.perf_counter() - t0
+        for t in sample:
+            osi, e, lg, _ = ref[t]
+            assert np.array_equal(g_si[t], osi) and int(g_end[t]) == e, f"bench expansion row {t}"
+            assert_logits_close(g_lg[t, :e], lg[:e], f"bench sparse prefill row {t}", bf16=True)
+            assert np.all(np.isneginf(g_lg[t, e:])), f"bench sparse prefill mask row {t}"
+            assert_topk_row(g_cols[t], lg[:e], wl.topk, f"bench sparse prefill top-k row {t}", bf16=True)
+            m = min(wl.topk, e)
+            want = O.sparse_remap_columns(g_cols[t, :m], osi, int(wl.row_ks[t]), sbk)
+            assert np.array_equal(g_pos[t, :m], want) and np.all(g_pos[t, m:] == -1), f"bench remap row {t}"
+        self.cols_sum = int(g_end.astype(np.int64).sum())
+        cpu = {"value": round(len(sample) / cpu_s, 3), "unit": "rows/s", "cores": os.cpu_count(),
+               "kind": "oracle", "sample": f"{len(sample)} full query rows of the chunk (expansion, candidate "
+                                           f"logits, top-2048 remap), k prepared untimed"}
+        return cpu, f"ok on {len(sample)} sampled rows"
+
+    def roofline(self, kernel_ms, step_ms, peaks, peak_kind):
+        cols = getattr(self, "cols_sum", None)
+        if cols is None:
+            cols = int(self.end.sum().item())
+        flop = cols * 2 * 64 * 128
+        ach = flop / (kernel_ms / 1e3) / 1e12
+        dev_i = torch.cuda.current_device()
+        lib_fp8 = measure_cublas_fp8(dev_i)
+        peak = lib_fp8["tflops"]
+        kern = "mqa_logits_kernel<1%s> (sparse prefill, bf16 out)" % (", MXFP4 k" if self.kv == "mxfp4" else "")
+        return {"kernel": kern, "bound": "tensor", "achieved": round(ach, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(ach / peak, 4),
+                "peak_source": "measured in this run: the e4m3 library GEMM (an fp8 x fp4 product runs at "
+                               "the fp8 rate)",
+                "algorithmic_flop_per_launch": flop, "traffic": None, "kernel_ms": round(kernel_ms, 5)}
+
+    def config(self, world):
+        return {"workload": self.wl.name + "-sparse" + ("-mxfp4-cache" if self.kv == "mxfp4" else ""),
+                "queries": self.T, "ctx": self.S, "topk": self.wl.topk, "candidates": 64,
+                "cand_block_size": 64, "sbk": self.sbk, "weights": "bf16",
+                "kv_cache": "MXFP4 (e2m1 + E8M0 per 32, 68 B/token)" if self.kv == "mxfp4"
+                else "e4m3 + fp32 scale (132 B/token)",
+                "step": "chunk k insert + gather + expand + sparse logits (bf16) + top-2048 remap",
+                "l2": "the gathered k (2-4 MB) stays in L2; q (64 MB) and the scores (64 MB) stream",
+                "parallelism": f"chunks sharded, {world} independent replica(s)"}
+
+
 class HierBench:
     """V4.1 consumer-layer decode: expand candidates, sparse logits (bf16), top-2048 + remap + slots.
 
@@ -1085,7 +1245,8 @@ class QPrepBench:
 BENCHES = {"long_decode": DecodeBench, "long_decode_mxfp4": DecodeBench, "paged_decode": DecodeBench,
            "prefill": PrefillBench, "hierarchical_mxfp4": HierBench,
            "hierarchical": HierBench, "hierarchical_mtp": HierMtpBench, "q_prep": QPrepBench,
-           "dcp_decode": DcpBench}
+           "dcp_decode": DcpBench, "prefill_sparse": SparsePrefillBench,
+           "prefill_sparse_mxfp4": SparsePrefillBench}
 
 
 # ----------------------------------------------------------------------------- harness
@@ -1262,6 +1423,33 @@ def run_reference(args, rank):
             O.topk_row(lg, 0, hi - lo, wl.topk)
             return time.perf_counter() - t0
         metric, cfg = PrefillBench.metric, {"workload": wl.name, "queries": T, "ctx": wl.S, "topk": wl.topk}
+    elif name in ("prefill_sparse", "prefill_sparse_mxfp4"):
+        from oracle import indexer as O
+        from oracle.codecs import bf16_decode
+
+        wl = W.prefill_chunk(seed=rank_seed(1006, 0))
+        kv = "mxfp4" if name.endswith("_mxfp4") else "fp8"
+        kf = bf16_decode(W.make_k(wl.seed, 0, wl.S))
+        if kv == "mxfp4":
+            codes, scales = O.mxfp4_quant(kf)
+            ka, kb = O.mxfp4_pack(codes), scales
+        else:
+            ka, kb = O.k_quant(kf)
+        wv = bf16_decode(wl.w)
+        T = wl.q8.shape[0]
+        cand = W.make_candidates(wl.seed, T, 64, wl.S // 64)
+
+        def one(i):
+            t = (i * 997) % T
+            t0 = time.perf_counter()
+            si, end = O.expand_candidates(cand[t:t + 1], wl.row_ks[t:t + 1], wl.row_ke[t:t + 1], 64, 64)
+            score = O.sparse_logits_prefill_mxfp4 if kv == "mxfp4" else O.sparse_logits_prefill
+            lg = score(wl.q8[t:t + 1], wv[t:t + 1], ka, kb, si, end, 64)[0]
+            O.sparse_topk_remap_row(lg, int(end[0]), si[0], int(wl.row_ks[t]), 64, wl.topk)
+            return time.perf_counter() - t0
+        metric = SparsePrefillBench.metric.fget(type("X", (), {"kv": kv})())
+        cfg = {"workload": wl.name + "-sparse" + ("-mxfp4-cache" if kv == "mxfp4" else ""), "queries": T,
+               "ctx": wl.S, "topk": wl.topk}
     elif name == "q_prep":
         from oracle import indexer as O
 

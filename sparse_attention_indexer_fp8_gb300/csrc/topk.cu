@@ -161,8 +161,8 @@ struct Shared {
 
 // Finds the digit `thr` at which the running count of larger digits reaches
 // `need`; sets sh.thr and reduces sh.need to what must come from bucket `thr`.
-template <int kThreads, int nbins>
-__device__ void find_threshold(Shared& sh, const uint32_t* hist) {
+template <int kThreads, int nbins, typename S>
+__device__ void find_threshold(S& sh, const uint32_t* hist) {
   const int need = sh.need;                // read before any thread can update it
   constexpr int per = nbins / kThreads;    // 1, 2 or 4 (nbins is 1024 or 2048)
   static_assert(per >= 1 && per * kThreads == nbins, "bins per thread");
@@ -443,6 +443,30 @@ __device__ __forceinline__ int32_t slot_of(const TopkParams& p, int row, int32_t
 // indices (and optionally columns and scores), -1 / -inf in the unused slots.
 // In merge mode, candidates without a position are dropped and the remaining
 // entries are compacted to the front in slot order.
+// Output slot i of row `row` takes column c (c < 0: an empty slot): the
+// mode's index (request-local, or the remapped position), optionally the
+// physical slot, the column and the score; -1 / -inf for an empty slot.
+template <bool kBf16, int kMode>
+__device__ __forceinline__ void emit_one(const TopkParams& p, int row, int64_t lo, int64_t base_blk,
+                                         const void* rowp, int i, int64_t c) {
+  int32_t o = -1, cl = -1;
+  float v = -__int_as_float(0x7f800000);
+  if (c >= 0) {
+    cl = static_cast<int32_t>(c);
+    if constexpr (kMode == kRemap) {
+      const int32_t blk = __ldg(p.si + row * p.ld_si + c / p.sbk);
+      o = static_cast<int32_t>((blk - base_blk) * p.sbk + c % p.sbk);
+    } else {
+      o = static_cast<int32_t>(c - lo);
+    }
+    if (p.vals) v = value_at<kBf16>(rowp, c);
+  }
+  p.out[row * p.ld_out + i] = o;
+  if (p.slots) p.slots[row * p.ld_slots + i] = slot_of(p, row, o);
+  if (kMode == kRemap && p.cols) p.cols[row * p.ld_cols + i] = cl;
+  if (p.vals) p.vals[row * p.ld_vals + i] = v;
+}
+
 template <int kThreads, bool kBf16, int kMode>
 __device__ __forceinline__ void write_outputs(const TopkParams& p, Shared& sh, int row, int64_t lo,
                                               const void* rowp, int m) {
@@ -454,23 +478,7 @@ __device__ __forceinline__ void write_outputs(const TopkParams& p, Shared& sh, i
   if constexpr (kMode != kMerge) {
     const int64_t base_blk = (kMode == kRemap && p.row_ks) ? __ldg(p.row_ks + row) / p.sbk : 0;
     for (int i = tid; i < K; i += kThreads) {
-      int32_t o = -1, cl = -1;
-      float v = ninf;
-      if (i < m) {
-        const int64_t c = sh.sel[i];
-        cl = static_cast<int32_t>(c);
-        if constexpr (kMode == kRemap) {
-          const int32_t blk = __ldg(p.si + row * p.ld_si + c / p.sbk);
-          o = static_cast<int32_t>((blk - base_blk) * p.sbk + c % p.sbk);
-        } else {
-          o = static_cast<int32_t>(c - lo);
-        }
-        if (vals) v = value_at<kBf16>(rowp, c);
-      }
-      out[i] = o;
-      if (p.slots) p.slots[row * p.ld_slots + i] = slot_of(p, row, o);
-      if (kMode == kRemap && p.cols) p.cols[row * p.ld_cols + i] = cl;
-      if (vals) vals[i] = v;
+      emit_one<kBf16, kMode>(p, row, lo, base_blk, rowp, i, i < m ? static_cast<int64_t>(sh.sel[i]) : -1);
     }
   } else {
     // each thread owns kMaxK / kThreads consecutive slots; one block scan orders the valid ones
@@ -718,6 +726,178 @@ __global__ void __launch_bounds__(kThreads, 1024 / kThreads) topk_kernel(const T
   write_outputs<kThreads, kBf16, kMode>(p, sh, row, lo, rowp, min(sh.n_out, K));
 }
 
+// Rows of at most kShortMax columns (the sparse rows of the V4.1 path: 64
+// candidate blocks of 64 tokens): the row's keys live in shared memory (16 KB),
+// so a 256-thread block holds about 41 KB and several rows are in flight on
+// every SM, which hides the latency of each row's short chain of passes.
+// Every thread issues all of its loads of the row before it uses one. The
+// three radix digits are found over the shared keys (the first from the
+// workspace histogram when given); a pass over the keys then takes every key
+// above the threshold key and exactly the missing number of keys equal to it
+// into the list of chosen columns, and the outputs are written from that list
+// in batches whose dependent lookups (sparse-block id, block-table entry) are
+// issued together.
+constexpr int kShortThreads = 256;
+constexpr int kShortMax = 4096;
+constexpr int kShortPer = kShortMax / kShortThreads;  // row elements per thread
+constexpr int kEmitBatch = 8;                         // output slots per thread per batch
+
+struct ShortShared {
+  uint32_t keys[kShortMax];
+  int32_t sel[kMaxK];  // chosen columns, in slot order
+  uint32_t hist[kBins];
+  int warp_tot[32];
+  int thr;
+  int need;
+  int n_out;
+  int n_tie;
+};
+
+// Writes output slots s0 + e * kShortThreads + tid (e < kEmitBatch, slot < K)
+// from the chosen columns sh.sel[0, m): the same values as emit_one, with every
+// lookup of the batch issued before any of the batch's stores.
+template <bool kBf16, int kMode>
+__device__ __forceinline__ void emit_batch(const TopkParams& p, const ShortShared& sh, int row, int64_t lo,
+                                           int64_t base_blk, const void* rowp, int s0, int m) {
+  const int K = p.k;
+  const int tid = threadIdx.x;
+  int32_t c[kEmitBatch], o[kEmitBatch], sl[kEmitBatch];
+  float v[kEmitBatch];
+#pragma unroll
+  for (int e = 0; e < kEmitBatch; ++e) {
+    const int s = s0 + e * kShortThreads + tid;
+    c[e] = s < m ? sh.sel[s] : -1;
+  }
+#pragma unroll
+  for (int e = 0; e < kEmitBatch; ++e) {
+    o[e] = -1;
+    v[e] = -__int_as_float(0x7f800000);
+    if (c[e] >= 0) {
+      if constexpr (kMode == kRemap) {
+        const int32_t blk = __ldg(p.si + row * p.ld_si + c[e] / p.sbk);
+        o[e] = static_cast<int32_t>((blk - base_blk) * p.sbk + c[e] % p.sbk);
+      } else {
+        o[e] = static_cast<int32_t>(c[e] - lo);
+      }
+      if (p.vals) v[e] = value_at<kBf16>(rowp, c[e]);
+    }
+  }
+  if (p.slots) {
+#pragma unroll
+    for (int e = 0; e < kEmitBatch; ++e) sl[e] = slot_of(p, row, o[e]);
+  }
+#pragma unroll
+  for (int e = 0; e < kEmitBatch; ++e) {
+    const int s = s0 + e * kShortThreads + tid;
+    if (s < K) {
+      p.out[row * p.ld_out + s] = o[e];
+      if (p.slots) p.slots[row * p.ld_slots + s] = sl[e];
+      if (kMode == kRemap && p.cols) p.cols[row * p.ld_cols + s] = c[e];
+      if (p.vals) p.vals[row * p.ld_vals + s] = v[e];
+    }
+  }
+}
+
+template <bool kBf16, int kMode>
+__global__ void __launch_bounds__(kShortThreads, 4) topk_short_kernel(const TopkParams p) {
+  __shared__ ShortShared sh;
+  const int row = blockIdx.x;
+  const int tid = threadIdx.x;
+  int64_t lo, hi;
+  row_range<kMode>(p, row, lo, hi);
+  const int n = hi > lo ? static_cast<int>(hi - lo) : 0;
+  const int K = p.k;
+  const void* rowp = kBf16
+      ? static_cast<const void*>(static_cast<const uint16_t*>(p.logits) + row * p.ld)
+      : static_cast<const void*>(static_cast<const float*>(p.logits) + row * p.ld);
+  const int64_t base_blk = (kMode == kRemap && p.row_ks) ? __ldg(p.row_ks + row) / p.sbk : 0;
+  uint32_t* gh = p.hist ? p.hist + static_cast<int64_t>(row) * kBins0 : nullptr;
+  if (n <= K) {
+    // every visible column is kept, in column order
+    if (gh) {
+      for (int i = tid; i < kBins0; i += kShortThreads) gh[i] = 0;
+    }
+    for (int i = tid; i < n; i += kShortThreads) sh.sel[i] = static_cast<int32_t>(lo + i);
+    __syncthreads();
+    for (int s0 = 0; s0 < K; s0 += kEmitBatch * kShortThreads) {
+      emit_batch<kBf16, kMode>(p, sh, row, lo, base_blk, rowp, s0, n);
+    }
+    return;
+  }
+  {
+    // all of this thread's elements are loaded before any is stored
+    uint32_t u[kShortPer];
+#pragma unroll
+    for (int j = 0; j < kShortPer; ++j) {
+      const int i = j * kShortThreads + tid;
+      u[j] = i < n ? key_at<kBf16>(rowp, lo + i) : 0u;
+    }
+#pragma unroll
+    for (int j = 0; j < kShortPer; ++j) {
+      const int i = j * kShortThreads + tid;
+      if (i < n) sh.keys[i] = u[j];
+    }
+  }
+  for (int i = tid; i < kBins; i += kShortThreads) sh.hist[i] = 0;
+  if (tid == 0) {
+    sh.need = K;
+    sh.n_out = 0;
+    sh.n_tie = 0;
+  }
+  __syncthreads();
+  // level 0: the top 10 bits (from the scoring kernel's histogram when given,
+  // handed back zeroed)
+  if (gh) {
+    for (int i = tid; i < kBins0; i += kShortThreads) {
+      sh.hist[i] = gh[i];
+      gh[i] = 0;
+    }
+  } else {
+    for (int i = tid; i < n; i += kShortThreads) atomicAdd(&sh.hist[sh.keys[i] >> 22], 1u);
+  }
+  __syncthreads();
+  find_threshold<kShortThreads, kBins0>(sh, sh.hist);
+  const uint32_t d0 = static_cast<uint32_t>(sh.thr);
+  // level 1: the next 11 bits of the keys tied on the first digit
+  for (int i = tid; i < kBins; i += kShortThreads) sh.hist[i] = 0;
+  __syncthreads();
+  for (int i = tid; i < n; i += kShortThreads) {
+    const uint32_t key = sh.keys[i];
+    if ((key >> 22) == d0) atomicAdd(&sh.hist[(key >> 11) & 0x7FFu], 1u);
+  }
+  __syncthreads();
+  find_threshold<kShortThreads, kBins>(sh, sh.hist);
+  const uint32_t p1 = (d0 << 11) | static_cast<uint32_t>(sh.thr);
+  // level 2: the last 11 bits of the keys tied on both
+  for (int i = tid; i < kBins; i += kShortThreads) sh.hist[i] = 0;
+  __syncthreads();
+  for (int i = tid; i < n; i += kShortThreads) {
+    const uint32_t key = sh.keys[i];
+    if ((key >> 11) == p1) atomicAdd(&sh.hist[key & 0x7FFu], 1u);
+  }
+  __syncthreads();
+  find_threshold<kShortThreads, kBins>(sh, sh.hist);
+  const uint32_t tkey = (p1 << 11) | static_cast<uint32_t>(sh.thr);
+  const int need = sh.need;
+  // every key above the threshold key, and `need` of the keys equal to it
+  for (int base = 0; base < n; base += kShortThreads) {
+    const int i = base + tid;
+    const uint32_t key = i < n ? sh.keys[i] : 0u;
+    const bool tie = i < n && key == tkey;
+    const int t = warp_reserve(&sh.n_tie, tie);
+    const bool take = (i < n && key > tkey) || (tie && t < need);
+    const int s = warp_reserve(&sh.n_out, take);
+    if (take && s < K) sh.sel[s] = static_cast<int32_t>(lo + i);
+  }
+  __syncthreads();
+  // with exact counts exactly K columns were chosen; a histogram that does not
+  // match the scores (a misused workspace) can leave slots unfilled: empty
+  const int m = min(sh.n_out, K);
+  for (int s0 = 0; s0 < K; s0 += kEmitBatch * kShortThreads) {
+    emit_batch<kBf16, kMode>(p, sh, row, lo, base_blk, rowp, s0, m);
+  }
+}
+
 }  // namespace
 
 unsigned int topk_read_and_clear_error(cudaStream_t stream, cudaError_t* err) {
@@ -799,6 +979,18 @@ template <bool kBf16, int kMode>
 idx_status_t launch_topk(const TopkParams& p, int rows, int64_t max_cols, cudaStream_t stream,
                          const char* fn) {
   const int sms = device_sm_count();
+  if constexpr (kMode != kMerge) {
+    if (max_cols <= kShortMax && sms > 0 && rows > sms) {
+      // many short rows: one 256-thread block per row with the keys in shared
+      // memory, several rows in flight per SM (with at most one row per SM the
+      // 1024-thread block's lower per-row latency wins)
+      TopkParams q = p;
+      q.rows = rows;
+      q.ahead = 0;
+      topk_short_kernel<kBf16, kMode><<<rows, kShortThreads, 0, stream>>>(q);
+      return check_launch(fn);
+    }
+  }
   if (sms > 0 && rows > 2 * sms && max_cols <= 65536) {
     return launch_topk_cfg<kBf16, kMode, 512>(p, rows, sms, stream, fn);
   }

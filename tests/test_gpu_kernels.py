@@ -413,6 +413,89 @@ def test_topk_random(width, k):
             assert set(out[r, :k].tolist()) == set(ref.tolist())
 
 
+@pytest.mark.parametrize("bf16,width,k,with_ws", [(False, 4096, 2048, False), (True, 4096, 2048, True),
+                                                   (False, 1000, 300, True), (True, 3000, 4096, False)])
+def test_topk_many_short_rows(bf16, width, k, with_ws):
+    # more rows than SMs of at most 4096 columns take the shared-memory selection:
+    # ragged ranges with ks > 0, rows with no more visible columns than k, ties
+    # and special values; the scores, optional values and the workspace path
+    rows = 400
+    rng = np.random.default_rng(width + k + bf16)
+    x = W.make_logits(width + 11, rows, width, ties=True)
+    x[1, :] = 0.5                                        # all equal
+    x[2, ::5] = -np.inf
+    x[3, 7], x[3, 8], x[3, 9] = np.inf, -np.inf, np.float32(-0.0)
+    ks = (rng.integers(0, width // 4, rows)).astype(np.int32)
+    ke = np.minimum(ks + rng.integers(1, width + 1, rows), width).astype(np.int32)
+    ks[:4], ke[:4] = 0, width
+    ke[5] = ks[5] + min(k, width - ks[5])                # exactly k visible (or all of a short row)
+    ke[6] = ks[6] + 1
+    if bf16:
+        xb = bf16_encode(x)
+        t = dev_bf16(xb)
+        vals = bf16_decode(xb)
+    else:
+        t = dev(x)
+        vals = x
+    ws = None
+    if with_ws:
+        # the first-digit histogram the scoring kernel would have accumulated
+        keys = _keys(vals.astype(np.float32).view(np.uint32))
+        h = np.zeros((rows, 1024), dtype=np.int32)
+        for r in range(rows):
+            np.add.at(h[r], (keys[r, ks[r]:ke[r]] >> 22).astype(np.int64), 1)
+        ws = dev(h)
+    out = torch.full((rows, k), -7, dtype=torch.int32, device=DEV)
+    v = torch.empty((rows, k), dtype=torch.float32, device=DEV)
+    idx.idx_topk(t, dev(ks), dev(ke), k, out, vals=v, ws=ws)
+    idx.idx_device_error()
+    if ws is not None:
+        assert not ws.any().item(), "the selection hands the workspace back zeroed"
+    out, v = out.cpu().numpy(), v.cpu().numpy()
+    for r in range(rows):
+        seg = vals[r, ks[r]:ke[r]]
+        assert_topk_values_exact(out[r], seg, k, f"row {r}")
+        n = int(ke[r] - ks[r])
+        got = out[r][out[r] >= 0]
+        assert len(got) == min(k, n) and len(set(got.tolist())) == len(got)
+        assert np.all(out[r, min(k, n):] == -1)
+        if n <= k:
+            assert out[r, :n].tolist() == list(range(n)), f"row {r}: all visible columns in order"
+        sel = out[r, :min(k, n)]
+        assert np.array_equal(v[r, :min(k, n)].view(np.uint32), seg[sel].astype(np.float32).view(np.uint32))
+        assert np.all(np.isneginf(v[r, min(k, n):]))
+
+
+def test_sparse_remap_many_short_rows_with_slots():
+    # 300 sparse rows (more than SMs): the shared-memory selection with the remap
+    # (ks > 0), the fused slot conversion and the column scratch
+    rows, sbk, k = 300, 32, 256
+    rng = np.random.default_rng(91)
+    n_si = 16
+    si = np.stack([np.sort(rng.choice(200, n_si, replace=False)) for _ in range(rows)]).astype(np.int32)
+    row_ks = (rng.integers(0, 4, rows) * sbk).astype(np.int32)
+    si = si + (row_ks // sbk)[:, None]
+    end = rng.integers(1, n_si * sbk + 1, rows).astype(np.int32)
+    end[:3] = [n_si * sbk, k, 5]
+    x = bf16_decode(bf16_encode(rng.standard_normal((rows, n_si * sbk)).astype(np.float32)))
+    x[np.arange(n_si * sbk)[None, :] >= end[:, None]] = -np.inf
+    bt = rng.permutation(rows * 256).astype(np.int32).reshape(rows, 256)
+    pos = torch.empty((rows, k), dtype=torch.int32, device=DEV)
+    cols = torch.empty((rows, k), dtype=torch.int32, device=DEV)
+    slots = torch.empty((rows, k), dtype=torch.int32, device=DEV)
+    idx.idx_sparse_topk_remap(dev_bf16(bf16_encode(x)), dev(end), dev(si), dev(row_ks), sbk, k, pos,
+                              col_scratch=cols, slots=slots, block_table=dev(bt), block_size=64, block_span=64)
+    idx.idx_device_error()
+    pos, cols, slots = pos.cpu().numpy(), cols.cpu().numpy(), slots.cpu().numpy()
+    for r in range(rows):
+        e = int(end[r])
+        assert_topk_values_exact(cols[r], x[r, :e], k, f"row {r}")
+        m = min(k, e)
+        assert np.array_equal(pos[r, :m], O.sparse_remap_columns(cols[r, :m], si[r], int(row_ks[r]), sbk))
+        assert np.all(pos[r, m:] == -1) and np.all(cols[r, m:] == -1)
+        assert slots[r].tolist() == [_slots_closed_form(int(v), bt, r, 64, 64) for v in pos[r]]
+
+
 def test_topk_ties_overflow_and_special_values():
     width, k = 40000, 2048
     x = W.make_logits(9, 6, width, ties=True)
