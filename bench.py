@@ -687,7 +687,9 @@ class SparsePrefillBench:
         self.si = torch.empty((T, 64), dtype=torch.int32, device=dev)
         self.end = torch.empty(T, dtype=torch.int32, device=dev)
         self.logits = torch.empty((T, 64 * self.sbk), dtype=torch.bfloat16, device=dev)
-        self.ws = torch.zeros((T, 1024), dtype=torch.int32, device=dev)
+        # rows this short are selected without the first-digit histogram: no workspace
+        wsb = idx.idx_workspace_bytes("sparse_topk_remap", T, 64 * self.sbk, wl.topk)
+        self.ws = torch.zeros((T, 1024), dtype=torch.int32, device=dev) if wsb else None
         self.pos = torch.empty((T, wl.topk), dtype=torch.int32, device=dev)
         self.cols = torch.empty((T, wl.topk), dtype=torch.int32, device=dev)
         self.rows_per_step = T
@@ -789,7 +791,10 @@ class SparsePrefillBench:
                 "frac": round(ach / peak, 4),
                 "peak_source": "measured in this run: the e4m3 library GEMM (an fp8 x fp4 product runs at "
                                "the fp8 rate)",
-                "algorithmic_flop_per_launch": flop, "traffic": None, "kernel_ms": round(kernel_ms, 5)}
+                "algorithmic_flop_per_launch": flop,
+                "traffic": profiled_traffic("launches_prefill_sparse%s.md" % ("_mxfp4" if self.kv == "mxfp4" else ""),
+                                            "logits.cu"),
+                "kernel_ms": round(kernel_ms, 5)}
 
     def config(self, world):
         return {"workload": self.wl.name + "-sparse" + ("-mxfp4-cache" if self.kv == "mxfp4" else ""),

@@ -46,7 +46,11 @@
  * allocating it); the selection zeroes every row it consumes, so the buffer is
  * ready for the next step. Supported by the kernels with one query per group:
  * dense decode with next_n = 1 and both sparse modes. ws = NULL selects the
- * two-pass selection.
+ * two-pass selection. Rows of at most 4096 columns, when there are more of
+ * them than the device has SMs, are selected from registers in one read and
+ * never use the histogram: the selection only clears a buffer it is given, and
+ * idx_workspace_bytes(op, rows, ld, k) returns 0 for them, meaning pass NULL
+ * to both calls (the logits call then skips the histogram too).
  *
  * Paged cache layout (the "split block" layout)
  * ---------------------------------------------
@@ -606,7 +610,13 @@ idx_status_t idx_block_span(int64_t block_stride, int64_t token_stride, int32_t*
 enum { IDX_DIAG_E4M3 = 0, IDX_DIAG_BF16 = 1 };
 idx_status_t idx_diag_mma_peak(int kind, int32_t iters, int32_t ctas, double* flop_out, cudaStream_t stream);
 
-/* Bytes of the optional selection workspace of an operation for `rows` rows (host only). */
+/*
+ * Bytes of the optional selection workspace of an operation for `rows` rows
+ * (host only). max_cols = 0: the size of the buffer, whatever the row length;
+ * max_cols > 0 (the `ld` the selection will be given): 0 when the selection of
+ * such rows would not read the histogram on the current device (see "Selection
+ * workspace"), so no buffer is needed.
+ */
 size_t idx_workspace_bytes(int op, int32_t rows, int32_t max_cols, int32_t k);
 
 /* Static description of a status code (host only). */

@@ -112,15 +112,16 @@ const char* idx_status_string(idx_status_t status) {
 const char* idx_last_error(void) { return idx::g_last_error; }
 
 size_t idx_workspace_bytes(int op, int32_t rows, int32_t max_cols, int32_t k) {
-  (void)max_cols;
   (void)k;
   switch (op) {
     case IDX_OP_MQA_LOGITS_PREFILL:
     case IDX_OP_PAGED_MQA_LOGITS_DECODE:
     case IDX_OP_TOPK:
     case IDX_OP_SPARSE_TOPK_REMAP:
-      // optional first-digit histogram: 1024 uint32 counters per row
-      return rows > 0 ? static_cast<size_t>(rows) * 1024 * sizeof(uint32_t) : 0;
+      // optional first-digit histogram: 1024 uint32 counters per row; none
+      // when the selection of these rows would not read it
+      if (rows <= 0 || (max_cols > 0 && idx::topk_rows_short(rows, max_cols))) return 0;
+      return static_cast<size_t>(rows) * 1024 * sizeof(uint32_t);
     default:
       return 0;
   }

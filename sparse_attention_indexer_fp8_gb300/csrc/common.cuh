@@ -24,6 +24,9 @@ idx_status_t fail(idx_status_t st, const char* fmt, ...);
 idx_status_t check_launch(const char* what);
 int device_sm_count();
 int64_t device_l2_bytes();  // 0 when it cannot be queried
+// True when a selection over `rows` rows of at most `max_cols` columns runs the
+// short-row kernel, which does not read the first-digit histogram (defined in topk.cu).
+bool topk_rows_short(int64_t rows, int64_t max_cols);
 
 // Encodes a tiled TMA descriptor through the driver entry point (no -lcuda link).
 idx_status_t encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank,

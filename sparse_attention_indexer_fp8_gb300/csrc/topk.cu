@@ -727,38 +727,42 @@ __global__ void __launch_bounds__(kThreads, 1024 / kThreads) topk_kernel(const T
 }
 
 // Rows of at most kShortMax columns (the sparse rows of the V4.1 path: 64
-// candidate blocks of 64 tokens): the row's keys live in shared memory (16 KB),
-// so a 256-thread block holds about 41 KB and several rows are in flight on
-// every SM, which hides the latency of each row's short chain of passes.
-// Every thread issues all of its loads of the row before it uses one. The
-// three radix digits are found over the shared keys (the first from the
-// workspace histogram when given); a pass over the keys then takes every key
-// above the threshold key and exactly the missing number of keys equal to it
-// into the list of chosen columns, and the outputs are written from that list
-// in batches whose dependent lookups (sparse-block id, block-table entry) are
-// issued together.
+// candidate blocks of 64 tokens). One 256-thread block per row, several rows in
+// flight on every SM. Each thread keeps its 16 keys in registers (16-byte loads
+// where the row is aligned), so nothing but the histograms and the chosen
+// columns goes through shared memory. The key has 16 significant bits for bf16
+// scores and 32 for fp32; its 8-bit digits are resolved most significant first
+// (two levels for bf16, four for fp32), each level histogramming only the keys
+// that share the digits above. The last level fixes the threshold key and how
+// many of the keys equal to it are kept. One block-wide scan of per-thread
+// counts (above, tied) in column order then gives every chosen key its output
+// slot directly: the chosen columns come out in column order, and among keys
+// equal to the threshold the lowest columns are kept. The row's sparse-block
+// ids are staged in shared memory with the row loads, so the output pass has
+// no dependent global loads (except for the fused slot conversion).
 constexpr int kShortThreads = 256;
 constexpr int kShortMax = 4096;
 constexpr int kShortPer = kShortMax / kShortThreads;  // row elements per thread
+constexpr int kShortSi = 1024;                        // sparse-block ids staged per row
 constexpr int kEmitBatch = 8;                         // output slots per thread per batch
 
 struct ShortShared {
-  uint32_t keys[kShortMax];
   int32_t sel[kMaxK];  // chosen columns, in slot order
-  uint32_t hist[kBins];
+  int32_t si[kShortSi];
+  uint32_t hist[2][256];
+  uint32_t tot[4][kShortThreads / 32];  // per chunk and warp: packed (above, tied) counts
   int warp_tot[32];
   int thr;
   int need;
-  int n_out;
-  int n_tie;
 };
 
 // Writes output slots s0 + e * kShortThreads + tid (e < kEmitBatch, slot < K)
 // from the chosen columns sh.sel[0, m): the same values as emit_one, with every
-// lookup of the batch issued before any of the batch's stores.
+// lookup of the batch issued before any of the batch's stores. Sparse-block ids
+// below n_si_s come from shared memory.
 template <bool kBf16, int kMode>
 __device__ __forceinline__ void emit_batch(const TopkParams& p, const ShortShared& sh, int row, int64_t lo,
-                                           int64_t base_blk, const void* rowp, int s0, int m) {
+                                           int64_t base_blk, const void* rowp, int s0, int m, int n_si_s) {
   const int K = p.k;
   const int tid = threadIdx.x;
   int32_t c[kEmitBatch], o[kEmitBatch], sl[kEmitBatch];
@@ -774,7 +778,8 @@ __device__ __forceinline__ void emit_batch(const TopkParams& p, const ShortShare
     v[e] = -__int_as_float(0x7f800000);
     if (c[e] >= 0) {
       if constexpr (kMode == kRemap) {
-        const int32_t blk = __ldg(p.si + row * p.ld_si + c[e] / p.sbk);
+        const int b = c[e] / p.sbk;
+        const int32_t blk = b < n_si_s ? sh.si[b] : __ldg(p.si + row * p.ld_si + b);
         o[e] = static_cast<int32_t>((blk - base_blk) * p.sbk + c[e] % p.sbk);
       } else {
         o[e] = static_cast<int32_t>(c[e] - lo);
@@ -798,11 +803,26 @@ __device__ __forceinline__ void emit_batch(const TopkParams& p, const ShortShare
   }
 }
 
+// Order-preserving key of a raw score: the upper 16 bits of the fp32 key for
+// bf16 (its lower 16 bits are a function of the sign), the fp32 key otherwise.
+template <bool kBf16>
+__device__ __forceinline__ uint32_t short_key(uint32_t raw) {
+  return kBf16 ? f32_key(raw << 16) >> 16 : f32_key(raw);
+}
+
 template <bool kBf16, int kMode>
 __global__ void __launch_bounds__(kShortThreads, 4) topk_short_kernel(const TopkParams p) {
   __shared__ ShortShared sh;
+  constexpr int kVec = kBf16 ? 8 : 4;         // elements per 16-byte load
+  constexpr int kEsz = kBf16 ? 2 : 4;
+  constexpr int kChunks = kShortPer / kVec;   // 2 or 4
+  constexpr int kSpan = kVec * kShortThreads; // elements per chunk
+  constexpr int kLevels = kBf16 ? 2 : 4;      // 8-bit digits of the key
+  constexpr int kWarps = kShortThreads / 32;
   const int row = blockIdx.x;
   const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
   int64_t lo, hi;
   row_range<kMode>(p, row, lo, hi);
   const int n = hi > lo ? static_cast<int>(hi - lo) : 0;
@@ -811,90 +831,161 @@ __global__ void __launch_bounds__(kShortThreads, 4) topk_short_kernel(const Topk
       ? static_cast<const void*>(static_cast<const uint16_t*>(p.logits) + row * p.ld)
       : static_cast<const void*>(static_cast<const float*>(p.logits) + row * p.ld);
   const int64_t base_blk = (kMode == kRemap && p.row_ks) ? __ldg(p.row_ks + row) / p.sbk : 0;
-  uint32_t* gh = p.hist ? p.hist + static_cast<int64_t>(row) * kBins0 : nullptr;
+  // Elements [0, lim) of the window may be read. A sparse row's window starts at
+  // column 0, so its loads need not wait for end[row]: every column below
+  // min(ld, kShortMax) lies inside the row.
+  const int lim = kMode == kRemap ? static_cast<int>(p.ld < kShortMax ? p.ld : kShortMax) : n;
+  int n_si_s = 0;
+  if constexpr (kMode == kRemap) {
+    const int nb = (lim + p.sbk - 1) / p.sbk;
+    const int ns = static_cast<int>(nb < p.ld_si ? nb : p.ld_si);
+    if (ns <= kShortSi) {
+      n_si_s = ns;
+      for (int i = tid; i < ns; i += kShortThreads) sh.si[i] = __ldg(p.si + row * p.ld_si + i);
+    }
+  }
+  if (p.hist) {
+    // the workspace histogram is not used for rows this short; it is handed back zeroed
+    uint32_t* g = p.hist + static_cast<int64_t>(row) * kBins0;
+    for (int i = tid; i < kBins0; i += kShortThreads) g[i] = 0;
+  }
   if (n <= K) {
     // every visible column is kept, in column order
-    if (gh) {
-      for (int i = tid; i < kBins0; i += kShortThreads) gh[i] = 0;
-    }
     for (int i = tid; i < n; i += kShortThreads) sh.sel[i] = static_cast<int32_t>(lo + i);
     __syncthreads();
     for (int s0 = 0; s0 < K; s0 += kEmitBatch * kShortThreads) {
-      emit_batch<kBf16, kMode>(p, sh, row, lo, base_blk, rowp, s0, n);
+      emit_batch<kBf16, kMode>(p, sh, row, lo, base_blk, rowp, s0, n, n_si_s);
     }
     return;
   }
+  // key of element h * kSpan + tid * kVec + j at [h * kVec + j]
+  uint32_t key[kShortPer];
   {
-    // all of this thread's elements are loaded before any is stored
-    uint32_t u[kShortPer];
+    const char* wp = static_cast<const char*>(rowp) + lo * kEsz;
+    const bool vec = (reinterpret_cast<uintptr_t>(p.logits) & 15u) == 0 && p.ld % kVec == 0 && lo % kVec == 0;
+    if (vec) {
+      // a vector that starts inside [0, lim) ends inside the row
+      uint4 r[kChunks];
 #pragma unroll
-    for (int j = 0; j < kShortPer; ++j) {
-      const int i = j * kShortThreads + tid;
-      u[j] = i < n ? key_at<kBf16>(rowp, lo + i) : 0u;
-    }
+      for (int h = 0; h < kChunks; ++h) {
+        const int i0 = h * kSpan + tid * kVec;
+        r[h] = i0 < lim ? __ldg(reinterpret_cast<const uint4*>(wp + static_cast<int64_t>(i0) * kEsz))
+                        : make_uint4(0u, 0u, 0u, 0u);
+      }
 #pragma unroll
-    for (int j = 0; j < kShortPer; ++j) {
-      const int i = j * kShortThreads + tid;
-      if (i < n) sh.keys[i] = u[j];
+      for (int h = 0; h < kChunks; ++h) {
+        const uint32_t w[4] = {r[h].x, r[h].y, r[h].z, r[h].w};
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) {
+          const uint32_t raw = kBf16 ? ((w[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu) : w[j];
+          key[h * kVec + j] = short_key<kBf16>(raw);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int h = 0; h < kChunks; ++h) {
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) {
+          const int i = h * kSpan + tid * kVec + j;
+          uint32_t raw = 0;
+          if (i < lim) {
+            raw = kBf16 ? static_cast<uint32_t>(__ldg(reinterpret_cast<const uint16_t*>(wp) + i))
+                        : __float_as_uint(__ldg(reinterpret_cast<const float*>(wp) + i));
+          }
+          key[h * kVec + j] = short_key<kBf16>(raw);
+        }
+      }
     }
   }
-  for (int i = tid; i < kBins; i += kShortThreads) sh.hist[i] = 0;
-  if (tid == 0) {
-    sh.need = K;
-    sh.n_out = 0;
-    sh.n_tie = 0;
-  }
+  sh.hist[0][tid] = 0;
+  sh.hist[1][tid] = 0;
+  if (tid == 0) sh.need = K;
   __syncthreads();
-  // level 0: the top 10 bits (from the scoring kernel's histogram when given,
-  // handed back zeroed)
-  if (gh) {
-    for (int i = tid; i < kBins0; i += kShortThreads) {
-      sh.hist[i] = gh[i];
-      gh[i] = 0;
+  // digits, most significant first; the threshold key collects them
+  uint32_t tkey = 0;
+#pragma unroll
+  for (int L = 0; L < kLevels; ++L) {
+    const int sft = 8 * (kLevels - 1 - L);
+    uint32_t* hist = sh.hist[L & 1];
+#pragma unroll
+    for (int e = 0; e < kShortPer; ++e) {
+      const int i = (e / kVec) * kSpan + tid * kVec + (e % kVec);
+      // the digits above this level equal those chosen so far (none at level 0)
+      const bool in = i < n && (L == 0 || (key[e] >> (sft + 8)) == (tkey >> (sft + 8)));
+      if (in) atomicAdd(&hist[(key[e] >> sft) & 0xFFu], 1u);
     }
-  } else {
-    for (int i = tid; i < n; i += kShortThreads) atomicAdd(&sh.hist[sh.keys[i] >> 22], 1u);
+    __syncthreads();
+    find_threshold<kShortThreads, 256>(sh, hist);
+    tkey |= static_cast<uint32_t>(sh.thr) << sft;
+    // reused two levels down: every read of it ended before find_threshold's last barrier
+    hist[tid] = 0;
+  }
+  const int need = sh.need;  // keys equal to tkey still to take
+  // per-thread counts of keys above and equal to the threshold, per chunk,
+  // packed as above | tied << 16 (each total is at most kShortMax)
+  uint32_t excl[kChunks];
+#pragma unroll
+  for (int h = 0; h < kChunks; ++h) {
+    uint32_t a = 0, t = 0;
+#pragma unroll
+    for (int j = 0; j < kVec; ++j) {
+      const int i = h * kSpan + tid * kVec + j;
+      if (i < n) {
+        a += key[h * kVec + j] > tkey;
+        t += key[h * kVec + j] == tkey;
+      }
+    }
+    const uint32_t cnt = a | (t << 16);
+    uint32_t incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) sh.tot[h][warp] = incl;
+    excl[h] = incl - cnt;
   }
   __syncthreads();
-  find_threshold<kShortThreads, kBins0>(sh, sh.hist);
-  const uint32_t d0 = static_cast<uint32_t>(sh.thr);
-  // level 1: the next 11 bits of the keys tied on the first digit
-  for (int i = tid; i < kBins; i += kShortThreads) sh.hist[i] = 0;
-  __syncthreads();
-  for (int i = tid; i < n; i += kShortThreads) {
-    const uint32_t key = sh.keys[i];
-    if ((key >> 22) == d0) atomicAdd(&sh.hist[(key >> 11) & 0x7FFu], 1u);
+  {
+    // exclusive prefix in column order: earlier chunks, then earlier warps of this chunk
+    uint32_t run = 0;
+#pragma unroll
+    for (int h = 0; h < kChunks; ++h) {
+      uint32_t before = 0, total = 0;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const uint32_t v = sh.tot[h][w];
+        before += w < warp ? v : 0u;
+        total += v;
+      }
+      excl[h] += run + before;
+      run += total;
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < kChunks; ++h) {
+    int a = static_cast<int>(excl[h] & 0xFFFFu);
+    int t = static_cast<int>(excl[h] >> 16);
+#pragma unroll
+    for (int j = 0; j < kVec; ++j) {
+      const int i = h * kSpan + tid * kVec + j;
+      const uint32_t kk = key[h * kVec + j];
+      if (i < n) {
+        if (kk > tkey) {
+          const int s = a + min(t, need);
+          ++a;
+          if (s < K) sh.sel[s] = static_cast<int32_t>(lo + i);
+        } else if (kk == tkey) {
+          if (t < need && a + t < K) sh.sel[a + t] = static_cast<int32_t>(lo + i);
+          ++t;
+        }
+      }
+    }
   }
   __syncthreads();
-  find_threshold<kShortThreads, kBins>(sh, sh.hist);
-  const uint32_t p1 = (d0 << 11) | static_cast<uint32_t>(sh.thr);
-  // level 2: the last 11 bits of the keys tied on both
-  for (int i = tid; i < kBins; i += kShortThreads) sh.hist[i] = 0;
-  __syncthreads();
-  for (int i = tid; i < n; i += kShortThreads) {
-    const uint32_t key = sh.keys[i];
-    if ((key >> 11) == p1) atomicAdd(&sh.hist[key & 0x7FFu], 1u);
-  }
-  __syncthreads();
-  find_threshold<kShortThreads, kBins>(sh, sh.hist);
-  const uint32_t tkey = (p1 << 11) | static_cast<uint32_t>(sh.thr);
-  const int need = sh.need;
-  // every key above the threshold key, and `need` of the keys equal to it
-  for (int base = 0; base < n; base += kShortThreads) {
-    const int i = base + tid;
-    const uint32_t key = i < n ? sh.keys[i] : 0u;
-    const bool tie = i < n && key == tkey;
-    const int t = warp_reserve(&sh.n_tie, tie);
-    const bool take = (i < n && key > tkey) || (tie && t < need);
-    const int s = warp_reserve(&sh.n_out, take);
-    if (take && s < K) sh.sel[s] = static_cast<int32_t>(lo + i);
-  }
-  __syncthreads();
-  // with exact counts exactly K columns were chosen; a histogram that does not
-  // match the scores (a misused workspace) can leave slots unfilled: empty
-  const int m = min(sh.n_out, K);
+  // the keys above the threshold and `need` of those equal to it: exactly K
   for (int s0 = 0; s0 < K; s0 += kEmitBatch * kShortThreads) {
-    emit_batch<kBf16, kMode>(p, sh, row, lo, base_blk, rowp, s0, m);
+    emit_batch<kBf16, kMode>(p, sh, row, lo, base_blk, rowp, s0, K, n_si_s);
   }
 }
 
@@ -973,17 +1064,31 @@ idx_status_t launch_topk_cfg(TopkParams p, int rows, int sms, cudaStream_t strea
   return check_launch(fn);
 }
 
-// Many rows of at most 64K columns (prefill chunks) take the two-blocks-per-SM
-// configuration; anything else one 1024-thread block per SM.
+}  // namespace
+
+namespace idx {
+
+bool topk_rows_short(int64_t rows, int64_t max_cols) {
+  const int sms = device_sm_count();
+  return max_cols <= kShortMax && sms > 0 && rows > sms;
+}
+
+}  // namespace idx
+
+namespace {
+
+// Many rows of at most kShortMax columns take the short-row kernel; many rows
+// of at most 64K columns (prefill chunks) the two-blocks-per-SM configuration;
+// anything else one 1024-thread block per SM.
 template <bool kBf16, int kMode>
 idx_status_t launch_topk(const TopkParams& p, int rows, int64_t max_cols, cudaStream_t stream,
                          const char* fn) {
   const int sms = device_sm_count();
   if constexpr (kMode != kMerge) {
-    if (max_cols <= kShortMax && sms > 0 && rows > sms) {
-      // many short rows: one 256-thread block per row with the keys in shared
-      // memory, several rows in flight per SM (with at most one row per SM the
-      // 1024-thread block's lower per-row latency wins)
+    if (topk_rows_short(rows, max_cols)) {
+      // many short rows: one 256-thread block per row with the keys in
+      // registers, several rows in flight per SM (with at most one row per SM
+      // the 1024-thread block's lower per-row latency wins)
       TopkParams q = p;
       q.rows = rows;
       q.ahead = 0;

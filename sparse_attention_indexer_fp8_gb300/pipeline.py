@@ -19,8 +19,16 @@ import torch
 
 from . import (idx_dcp_topk_merge, idx_expand_candidates, idx_k_quant_and_cache, idx_k_quant_and_cache_mxfp4,
                idx_paged_mqa_logits_decode, idx_paged_mqa_logits_decode_mxfp4, idx_req_to_global_slots,
-               idx_sparse_topk_remap, idx_topk)
+               idx_sparse_topk_remap, idx_topk, idx_workspace_bytes)
 from . import workloads as W
+
+
+def _workspace(op: str, rows: int, ld: int, k: int, device) -> torch.Tensor | None:
+    """The selection workspace (first-digit histograms, zero between steps), or None
+    where the selection of these rows would not read it."""
+    with torch.cuda.device(torch.device(device)):
+        nbytes = idx_workspace_bytes(op, rows, ld, k)
+    return torch.zeros((nbytes // 4,), dtype=torch.int32, device=device).view(rows, 1024) if nbytes else None
 
 
 def _insert(kv: str):
@@ -91,8 +99,7 @@ class DecodeStep:
         self.local = torch.empty((rows, topk), dtype=torch.int32, device=device)
         self.slots = torch.empty((rows, topk), dtype=torch.int32, device=device)
         self.row_ke = torch.empty(rows, dtype=torch.int32, device=device)
-        # selection workspace (first-digit histograms), zero between steps
-        self.ws = torch.zeros((rows, 1024), dtype=torch.int32, device=device) if next_n == 1 else None
+        self.ws = _workspace("topk", rows, ld, topk, device) if next_n == 1 else None
 
     def run(self, q, w, cache, block_table, ctx_lens, new_k=None, new_slots=None, row_ke=None,
             stream=None):
@@ -141,7 +148,7 @@ class HierarchicalStep:
         self.cols = torch.empty((rows, topk), dtype=torch.int32, device=device)
         self.positions = torch.empty((rows, topk), dtype=torch.int32, device=device)
         self.slots = torch.empty((rows, topk), dtype=torch.int32, device=device)
-        self.ws = torch.zeros((rows, 1024), dtype=torch.int32, device=device)
+        self.ws = _workspace("sparse_topk_remap", rows, n_cand * R * sbk, topk, device)
         self.row_to_req = (None if next_n == 1 else
                            torch.arange(rows // next_n, dtype=torch.int32, device=device).repeat_interleave(next_n))
 
@@ -209,7 +216,7 @@ class DcpDecodeStep:
         self.cand_idx = torch.empty((batch, topk), dtype=torch.int32, device=device)
         self.positions = torch.empty((batch, topk), dtype=torch.int32, device=device)
         self.scores = torch.empty((batch, topk), dtype=torch.float32, device=device)
-        self.ws = torch.zeros((batch, 1024), dtype=torch.int32, device=device)
+        self.ws = _workspace("topk", batch, ld, topk, device)
 
     def select_local(self, q, w, cache, block_table, ctx_lens, stream=None):
         idx_paged_mqa_logits_decode(q, w, cache, self.block_size, block_table, ctx_lens, self.logits,

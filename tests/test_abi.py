@@ -54,6 +54,12 @@ def test_host_helpers(lib):
     assert lib.idx_block_span(0, 128, ctypes.byref(span)) == 1
     assert lib.idx_workspace_bytes(5, 128, 131072, 2048) == 128 * 1024 * 4
     assert lib.idx_workspace_bytes(1, 128, 131072, 2048) == 0
+    # max_cols 0: the buffer's size whatever the rows' length
+    assert lib.idx_workspace_bytes(7, 8192, 0, 2048) == 8192 * 1024 * 4
+    # many rows of at most 4096 columns need none on a device with fewer SMs than
+    # rows; without a device the full size is returned
+    assert lib.idx_workspace_bytes(7, 8192, 4096, 2048) in (0, 8192 * 1024 * 4)
+    assert lib.idx_workspace_bytes(7, 0, 4096, 2048) == 0
 
 
 def test_validation_rejects_before_touching_the_device(lib):

@@ -496,6 +496,63 @@ def test_sparse_remap_many_short_rows_with_slots():
         assert slots[r].tolist() == [_slots_closed_form(int(v), bt, r, 64, 64) for v in pos[r]]
 
 
+@pytest.mark.parametrize("bf16,ld_extra,offset", [(False, 0, 0), (False, 3, 0), (False, 0, 2),
+                                                  (True, 0, 0), (True, 5, 0), (True, 0, 1)])
+def test_sparse_remap_short_rows_load_paths_and_digit_ties(bf16, ld_extra, offset):
+    # many sparse rows of at most 4096 columns: 16-byte loads (aligned rows) and
+    # element loads (ld or base not 16-byte aligned), keys equal in every digit but
+    # the last (fp32: 4 levels), many keys equal to the threshold key, and the
+    # workspace, which these rows never need and the selection only clears
+    rows, sbk, k, n_si = 320, 64, 1000, 32
+    width = n_si * sbk
+    ld = width + ld_extra
+    rng = np.random.default_rng(1000 + 10 * ld_extra + offset + bf16)
+    si = np.stack([rng.permutation(4 * n_si)[:n_si] for _ in range(rows)]).astype(np.int32)
+    end = rng.integers(k - 50, width + 1, rows).astype(np.int32)
+    end[:4] = [width, k, k + 1, width - 1]
+    x = rng.standard_normal((rows, width)).astype(np.float32)
+    x[4::3] = (1.0 + rng.integers(0, 64, (len(range(4, rows, 3)), width)) * 2.0 ** -23).astype(np.float32)
+    x[5::3] = rng.integers(-4, 4, (len(range(5, rows, 3)), width)).astype(np.float32) * 0.5
+    x[6, :] = 0.75
+    x[7, ::7] = -np.inf
+    if bf16:
+        xb = bf16_encode(x)
+        vals = bf16_decode(xb)
+        flat = torch.empty(rows * ld + offset, dtype=torch.int16, device=DEV)
+        full = np.zeros((rows, ld), dtype=np.uint16)
+        full[:, :width] = xb
+        flat[offset:] = torch.from_numpy(full.reshape(-1).view(np.int16)).to(DEV)
+        t = flat[offset:].view(rows, ld).view(torch.bfloat16)
+    else:
+        vals = x
+        flat = torch.empty(rows * ld + offset, dtype=torch.float32, device=DEV)
+        full = np.zeros((rows, ld), dtype=np.float32)
+        full[:, :width] = x
+        flat[offset:] = torch.from_numpy(full.reshape(-1)).to(DEV)
+        t = flat[offset:].view(rows, ld)
+    keys = _keys(vals.astype(np.float32).view(np.uint32))
+    h = np.zeros((rows, 1024), dtype=np.int32)
+    for r in range(rows):
+        np.add.at(h[r], (keys[r, :end[r]] >> 22).astype(np.int64), 1)
+    ws = dev(h)
+    if rows > torch.cuda.get_device_properties(0).multi_processor_count:
+        assert idx.idx_workspace_bytes("sparse_topk_remap", rows, ld, k) == 0
+    assert idx.idx_workspace_bytes("sparse_topk_remap", rows, 0, k) == rows * 1024 * 4
+    pos = torch.full((rows, k), -7, dtype=torch.int32, device=DEV)
+    cols = torch.full((rows, k), -7, dtype=torch.int32, device=DEV)
+    idx.idx_sparse_topk_remap(t, dev(end), dev(si), None, sbk, k, pos, col_scratch=cols, ws=ws)
+    idx.idx_device_error()
+    assert not ws.any().item(), "the selection hands the workspace back zeroed"
+    pos, cols = pos.cpu().numpy(), cols.cpu().numpy()
+    for r in range(rows):
+        e = int(end[r])
+        assert_topk_values_exact(cols[r], vals[r, :e], k, f"row {r}")
+        m = min(k, e)
+        assert len(set(cols[r, :m].tolist())) == m
+        assert np.array_equal(pos[r, :m], O.sparse_remap_columns(cols[r, :m], si[r], 0, sbk))
+        assert np.all(pos[r, m:] == -1) and np.all(cols[r, m:] == -1)
+
+
 def test_topk_ties_overflow_and_special_values():
     width, k = 40000, 2048
     x = W.make_logits(9, 6, width, ties=True)
