@@ -13,18 +13,18 @@
 // block's barrier-bound phases overlap the other's passes). Scores are mapped to
 // order-preserving 32-bit keys and selected by three radix digits (10, 11 and 11
 // bits). With more rows than blocks in flight, each block asks for the row one
-// wave ahead to be staged in L2. Level 0
-// histograms the row from global memory (or takes the histogram the scoring
-// kernel accumulated); a second pass over the row keeps only the elements at or
-// above the threshold digit, compacted into shared memory, where they are split
-// into the chosen and the tied. Each later level histograms only the elements
-// that tie with the threshold digit of the level above, so normally the row is
-// read from global memory once or twice. When a bucket overflows its
-// shared-memory buffer the level re-reads global memory with a prefix filter
-// instead (correct for any input, slower). At the last level exactly the
-// number still missing is taken from the fully tied bucket. Writes use
-// warp-aggregated shared-memory counters, so the output is a set in no
-// particular order.
+// wave ahead to be staged in L2. Level 0 histograms the row from global memory
+// (or takes the histogram the scoring kernel accumulated); a second pass over
+// the row keeps only the elements at or above the threshold digit (bucket A, in
+// shared memory) and counts the second digit of those tied with it. The second
+// threshold comes from that histogram, the third from one pass over A, and one
+// block scan of per-thread (above, tied) counts places every key above the
+// threshold key and exactly the number still missing of those equal to it, so
+// normally the row is read from global memory once or twice. When bucket A
+// overflows its shared-memory buffer, the later levels re-read global memory
+// with a prefix filter instead (correct for any input, slower) and reserve
+// output slots with warp-aggregated shared-memory counters. The output is a set
+// in no particular order.
 #include <type_traits>
 
 #include "common.cuh"
@@ -320,8 +320,9 @@ __device__ __forceinline__ int warp_excl_scan(int v, int* total) {
 
 // The level-0 pass over the aligned body of the row. A key is a hit when it is
 // at least the smallest key of the threshold digit (so above it or tied with
-// it); only hits are kept, appended to bucket A with their columns, and sorted
-// into "above" and "tied" afterwards from shared memory. Each thread tests the
+// it); only hits are kept, appended to bucket A with their columns, and the
+// second digit of every tie (a hit of the threshold digit thr0) is counted into
+// sh.hist[1] as it is found. Each thread tests the
 // 16 elements it loaded into a bit mask and parks the loaded words in its own
 // slots of the warp's staging area; one warp scan reserves bucket slots for all
 // hits, and each thread then walks only its own set bits (a few per warp at the
@@ -334,8 +335,8 @@ __device__ __forceinline__ int warp_excl_scan(int v, int* total) {
 // integer compare; otherwise the key itself is compared.
 template <int kThreads, bool kBf16>
 __device__ __forceinline__ void level0_collect(Shared& sh, const void* rowp, int64_t a1, int64_t nvec,
-                                               uint32_t tie_lo, uint32_t* keys_a, int32_t* cols_a,
-                                               uint4* stage) {
+                                               uint32_t tie_lo, uint32_t thr0, uint32_t* keys_a,
+                                               int32_t* cols_a, uint4* stage) {
   constexpr int kVec = kBf16 ? 8 : 4;
   constexpr int kEsz = kBf16 ? 2 : 4;
   constexpr int kUnroll = kBf16 ? 2 : 4;
@@ -390,17 +391,19 @@ __device__ __forceinline__ void level0_collect(Shared& sh, const void* rowp, int
     while (hit) {
       const int i = __ffs(hit) - 1;
       hit &= hit - 1;
+      uint32_t u;
+      if constexpr (kBf16) {
+        const uint32_t wd = mk[(i >> 3) * 128 + ((i & 7) >> 1)];
+        u = (i & 1) ? (wd & 0xFFFF0000u) : (wd << 16);
+      } else {
+        u = mk[(i >> 2) * 128 + (i & 3)];
+      }
+      const uint32_t key = f32_key(u);
       if (slot < TopkCfg<kThreads>::kCapA) {
-        uint32_t u;
-        if constexpr (kBf16) {
-          const uint32_t wd = mk[(i >> 3) * 128 + ((i & 7) >> 1)];
-          u = (i & 1) ? (wd & 0xFFFF0000u) : (wd << 16);
-        } else {
-          u = mk[(i >> 2) * 128 + (i & 3)];
-        }
-        keys_a[slot] = f32_key(u);
+        keys_a[slot] = key;
         cols_a[slot] = cbase + (i / kVec) * (kThreads * kVec) + i % kVec;
       }
+      if ((key >> 22) == thr0) atomicAdd(&sh.hist[1][(key >> 11) & 0x7FFu], 1u);
       ++slot;
     }
   };
@@ -443,28 +446,54 @@ __device__ __forceinline__ int32_t slot_of(const TopkParams& p, int row, int32_t
 // indices (and optionally columns and scores), -1 / -inf in the unused slots.
 // In merge mode, candidates without a position are dropped and the remaining
 // entries are compacted to the front in slot order.
-// Output slot i of row `row` takes column c (c < 0: an empty slot): the
-// mode's index (request-local, or the remapped position), optionally the
-// physical slot, the column and the score; -1 / -inf for an empty slot.
-template <bool kBf16, int kMode>
-__device__ __forceinline__ void emit_one(const TopkParams& p, int row, int64_t lo, int64_t base_blk,
-                                         const void* rowp, int i, int64_t c) {
-  int32_t o = -1, cl = -1;
-  float v = -__int_as_float(0x7f800000);
-  if (c >= 0) {
-    cl = static_cast<int32_t>(c);
-    if constexpr (kMode == kRemap) {
-      const int32_t blk = __ldg(p.si + row * p.ld_si + c / p.sbk);
-      o = static_cast<int32_t>((blk - base_blk) * p.sbk + c % p.sbk);
-    } else {
-      o = static_cast<int32_t>(c - lo);
-    }
-    if (p.vals) v = value_at<kBf16>(rowp, c);
+// Writes output slots s0 + e * kThreads + tid (e < kB, slot < K) of row `row`
+// from the chosen columns sel[0, m); the slots past m are empty. A slot takes
+// the mode's index (request-local, or the remapped position), optionally the
+// physical slot, the column and the score; -1 / -inf for an empty slot. Every
+// lookup of the batch (sparse-block id, score, block-table entry) is issued
+// before any of its stores. Sparse-block ids below n_si_s come from si_s.
+template <int kThreads, int kB, bool kBf16, int kMode>
+__device__ __forceinline__ void emit_batch(const TopkParams& p, const int32_t* sel, const int32_t* si_s,
+                                           int n_si_s, int row, int64_t lo, int64_t base_blk,
+                                           const void* rowp, int s0, int m) {
+  const int K = p.k;
+  const int tid = threadIdx.x;
+  int32_t c[kB], o[kB], sl[kB];
+  float v[kB];
+#pragma unroll
+  for (int e = 0; e < kB; ++e) {
+    const int s = s0 + e * kThreads + tid;
+    c[e] = s < m ? sel[s] : -1;
   }
-  p.out[row * p.ld_out + i] = o;
-  if (p.slots) p.slots[row * p.ld_slots + i] = slot_of(p, row, o);
-  if (kMode == kRemap && p.cols) p.cols[row * p.ld_cols + i] = cl;
-  if (p.vals) p.vals[row * p.ld_vals + i] = v;
+#pragma unroll
+  for (int e = 0; e < kB; ++e) {
+    o[e] = -1;
+    v[e] = -__int_as_float(0x7f800000);
+    if (c[e] >= 0) {
+      if constexpr (kMode == kRemap) {
+        const int b = c[e] / p.sbk;
+        const int32_t blk = b < n_si_s ? si_s[b] : __ldg(p.si + row * p.ld_si + b);
+        o[e] = static_cast<int32_t>((blk - base_blk) * p.sbk + c[e] % p.sbk);
+      } else {
+        o[e] = static_cast<int32_t>(c[e] - lo);
+      }
+      if (p.vals) v[e] = value_at<kBf16>(rowp, c[e]);
+    }
+  }
+  if (p.slots) {
+#pragma unroll
+    for (int e = 0; e < kB; ++e) sl[e] = slot_of(p, row, o[e]);
+  }
+#pragma unroll
+  for (int e = 0; e < kB; ++e) {
+    const int s = s0 + e * kThreads + tid;
+    if (s < K) {
+      p.out[row * p.ld_out + s] = o[e];
+      if (p.slots) p.slots[row * p.ld_slots + s] = sl[e];
+      if (kMode == kRemap && p.cols) p.cols[row * p.ld_cols + s] = c[e];
+      if (p.vals) p.vals[row * p.ld_vals + s] = v[e];
+    }
+  }
 }
 
 template <int kThreads, bool kBf16, int kMode>
@@ -477,8 +506,9 @@ __device__ __forceinline__ void write_outputs(const TopkParams& p, Shared& sh, i
   float* vals = p.vals ? p.vals + row * p.ld_vals : nullptr;
   if constexpr (kMode != kMerge) {
     const int64_t base_blk = (kMode == kRemap && p.row_ks) ? __ldg(p.row_ks + row) / p.sbk : 0;
-    for (int i = tid; i < K; i += kThreads) {
-      emit_one<kBf16, kMode>(p, row, lo, base_blk, rowp, i, i < m ? static_cast<int64_t>(sh.sel[i]) : -1);
+    constexpr int kB = 4;
+    for (int s0 = 0; s0 < K; s0 += kB * kThreads) {
+      emit_batch<kThreads, kB, kBf16, kMode>(p, sh.sel, nullptr, 0, row, lo, base_blk, rowp, s0, m);
     }
   } else {
     // each thread owns kMaxK / kThreads consecutive slots; one block scan orders the valid ones
@@ -549,6 +579,13 @@ __global__ void __launch_bounds__(kThreads, 1024 / kThreads) topk_kernel(const T
   const int row = blockIdx.x;
   const int tid = threadIdx.x;
   const int64_t base_blk = 0;
+  // the workspace histogram is requested before the row's bounds, so the two
+  // lookups overlap (plain loads: this kernel clears the words after reading them)
+  constexpr int kH0 = kBins0 / kThreads;
+  uint32_t* gh = p.hist ? p.hist + static_cast<int64_t>(row) * kBins0 : nullptr;
+  uint32_t h0[kH0];
+#pragma unroll
+  for (int j = 0; j < kH0; ++j) h0[j] = gh ? gh[j * kThreads + tid] : 0u;
   int64_t lo, hi;
   row_range<kMode>(p, row, lo, hi);
   const int64_t n = hi > lo ? hi - lo : 0;
@@ -578,9 +615,8 @@ __global__ void __launch_bounds__(kThreads, 1024 / kThreads) topk_kernel(const T
 
   if (n <= K) {
     // every visible column is kept, in column order
-    if (p.hist) {
-      uint32_t* g = p.hist + static_cast<int64_t>(row) * kBins0;
-      for (int i = tid; i < kBins0; i += kThreads) g[i] = 0;
+    if (gh) {
+      for (int i = tid; i < kBins0; i += kThreads) gh[i] = 0;
     }
     for (int i = tid; i < n; i += kThreads) sh.sel[i] = static_cast<int32_t>(lo + i);
     __syncthreads();
@@ -599,32 +635,32 @@ __global__ void __launch_bounds__(kThreads, 1024 / kThreads) topk_kernel(const T
     sh.n_tie = 0;
     sh.need = K;
   }
-  __syncthreads();
-
-  // level-0 histogram straight from global memory
-  if (p.hist) {
-    // first digit counted by the kernel that wrote the scores; hand the
-    // workspace back zeroed for the next use
-    uint32_t* g = p.hist + static_cast<int64_t>(row) * kBins0;
-    for (int i = tid; i < kBins0; i += kThreads) {
-      sh.hist[0][i] = g[i];
-      g[i] = 0;
+  if (gh) {
+    // first digit counted by the kernel that wrote the scores (the same bins
+    // this thread just cleared); the workspace is handed back zeroed
+#pragma unroll
+    for (int j = 0; j < kH0; ++j) {
+      sh.hist[0][j * kThreads + tid] = h0[j];
+      gh[j * kThreads + tid] = 0;
     }
-  } else {
+  }
+  __syncthreads();
+  if (!gh) {
+    // level-0 histogram straight from global memory
     sweep_row<kThreads, kBf16>(rowp, lo, hi, [&](bool valid, int64_t, uint32_t key) {
       if (valid) atomicAdd(&sh.hist[0][key >> 22], 1u);
     });
+    __syncthreads();
   }
-  __syncthreads();
   find_threshold<kThreads, kBins0>(sh, sh.hist[0]);
+  const uint32_t thr0 = static_cast<uint32_t>(sh.thr);
 
-  // level 0: every key at or above the threshold digit goes to bucket A; A is
-  // then split into the chosen (digit above the threshold) and the tied, whose
-  // next digit is histogrammed
+  // level 0: every key at or above the threshold digit goes to bucket A, and
+  // the second digit of every key tied on the first is counted on the way
   {
     constexpr int kVec = kBf16 ? 8 : 4;
     constexpr int kEsz = kBf16 ? 2 : 4;
-    const uint32_t tie_lo = static_cast<uint32_t>(sh.thr) << 22;
+    const uint32_t tie_lo = thr0 << 22;
     const uintptr_t base = reinterpret_cast<uintptr_t>(rowp);
     int64_t a1 = lo + (kVec - static_cast<int64_t>(((base / kEsz) + lo) % kVec)) % kVec;
     if (a1 > hi) a1 = hi;
@@ -643,34 +679,85 @@ __global__ void __launch_bounds__(kThreads, 1024 / kThreads) topk_kernel(const T
         keys_a[s] = key;
         cols_a[s] = static_cast<int32_t>(c);
       }
+      if (h && (key >> 22) == thr0) atomicAdd(&sh.hist[1][(key >> 11) & 0x7FFu], 1u);
     }
-    level0_collect<kThreads, kBf16>(sh, rowp, a1, nvec, tie_lo, keys_a, cols_a, stage);
+    level0_collect<kThreads, kBf16>(sh, rowp, a1, nvec, tie_lo, thr0, keys_a, cols_a, stage);
     __syncthreads();
-    const int na = sh.n_a;
-    if (na <= kCapA) {
-      const int thr = sh.thr;
-      for (int b = 0; b < na; b += kThreads) {
-        const int i = b + tid;
-        const bool valid = i < na;
-        const uint32_t key = valid ? keys_a[i] : 0u;
-        const bool above = valid && static_cast<int>(key >> 22) > thr;
-        const int s = warp_reserve(&sh.n_out, above);
-        if (above && s < K) store_one(sh, s, cols_a[i]);
-        if (valid && !above) atomicAdd(&sh.hist[1][digit(key, 1)], 1u);
-      }
-    } else {
-      // more hits than bucket A holds: classify the row again from global memory,
-      // storing the chosen directly and keeping as many ties as fit
-      __syncthreads();
-      if (tid == 0) sh.n_a = 0;
-      __syncthreads();
-      sweep_row<kThreads, kBf16>(rowp, lo, hi, [&](bool valid, int64_t c, uint32_t key) {
-        visit(p, sh, row, lo, base_blk, 0, 0u, valid, key, c, keys_a, cols_a, &sh.n_a, kCapA,
-              sh.hist[1]);
-      });
-    }
   }
-  uint32_t prefix = static_cast<uint32_t>(sh.thr) << 22;
+  const int na0 = sh.n_a;
+  if (na0 <= kCapA) {
+    // Bucket A holds every hit. The two remaining digits are found over the
+    // tied keys (the second from the histogram of the pass, the third from one
+    // pass over A), then one block scan of per-thread (above, tied) counts
+    // gives each chosen key its output slot: every key above the threshold key
+    // and `need` of those equal to it.
+    for (int i = tid; i < kBins; i += kThreads) sh.hist[0][i] = 0;  // level 0's search is done
+    find_threshold<kThreads, kBins>(sh, sh.hist[1]);
+    const uint32_t p1 = (thr0 << 11) | static_cast<uint32_t>(sh.thr);
+    for (int i = tid; i < na0; i += kThreads) {
+      const uint32_t key = keys_a[i];
+      if ((key >> 11) == p1) atomicAdd(&sh.hist[0][key & 0x7FFu], 1u);
+    }
+    __syncthreads();
+    find_threshold<kThreads, kBins>(sh, sh.hist[0]);
+    const uint32_t tkey = (p1 << 11) | static_cast<uint32_t>(sh.thr);
+    // a workspace histogram that does not match the scores can leave any count
+    // here; the clamp keeps every slot inside the row's outputs
+    const int need = min(max(sh.need, 0), K);
+    // this thread's keys of A are i = tid, tid + kThreads, ...; the scan runs in thread order
+    uint32_t cnt = 0;  // above | tied << 16 (each total is at most kCapA)
+    for (int i = tid; i < na0; i += kThreads) {
+      const uint32_t key = keys_a[i];
+      cnt += key > tkey ? 1u : (key == tkey ? 0x10000u : 0u);
+    }
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    uint32_t incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) sh.warp_tot[warp] = static_cast<int>(incl);
+    __syncthreads();
+    uint32_t before = incl - cnt;
+    uint32_t total = 0;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) {
+      const uint32_t v = static_cast<uint32_t>(sh.warp_tot[w]);
+      before += w < warp ? v : 0u;
+      total += v;
+    }
+    int a = static_cast<int>(before & 0xFFFFu);
+    int t = static_cast<int>(before >> 16);
+    for (int i = tid; i < na0; i += kThreads) {
+      const uint32_t key = keys_a[i];
+      if (key > tkey) {
+        const int s = a + min(t, need);
+        ++a;
+        if (s < K) sh.sel[s] = cols_a[i];
+      } else if (key == tkey) {
+        if (t < need && a + t < K) sh.sel[a + t] = cols_a[i];
+        ++t;
+      }
+    }
+    __syncthreads();
+    const int a_tot = static_cast<int>(total & 0xFFFFu);
+    const int t_tot = static_cast<int>(total >> 16);
+    write_outputs<kThreads, kBf16, kMode>(p, sh, row, lo, rowp, min(K, a_tot + min(need, t_tot)));
+    return;
+  }
+  // More hits than bucket A holds: classify the row again from global memory,
+  // storing the chosen directly and keeping as many ties as fit (the second
+  // digit's histogram is counted again by this pass).
+  __syncthreads();
+  for (int i = tid; i < kBins; i += kThreads) sh.hist[1][i] = 0;
+  if (tid == 0) sh.n_a = 0;
+  __syncthreads();
+  sweep_row<kThreads, kBf16>(rowp, lo, hi, [&](bool valid, int64_t c, uint32_t key) {
+    visit(p, sh, row, lo, base_blk, 0, 0u, valid, key, c, keys_a, cols_a, &sh.n_a, kCapA, sh.hist[1]);
+  });
+  uint32_t prefix = thr0 << 22;
   __syncthreads();
   for (int i = tid; i < kBins; i += kThreads) sh.hist[0][i] = 0;  // free since level 0 is done
   find_threshold<kThreads, kBins>(sh, sh.hist[1]);
@@ -756,53 +843,6 @@ struct ShortShared {
   int need;
 };
 
-// Writes output slots s0 + e * kShortThreads + tid (e < kEmitBatch, slot < K)
-// from the chosen columns sh.sel[0, m): the same values as emit_one, with every
-// lookup of the batch issued before any of the batch's stores. Sparse-block ids
-// below n_si_s come from shared memory.
-template <bool kBf16, int kMode>
-__device__ __forceinline__ void emit_batch(const TopkParams& p, const ShortShared& sh, int row, int64_t lo,
-                                           int64_t base_blk, const void* rowp, int s0, int m, int n_si_s) {
-  const int K = p.k;
-  const int tid = threadIdx.x;
-  int32_t c[kEmitBatch], o[kEmitBatch], sl[kEmitBatch];
-  float v[kEmitBatch];
-#pragma unroll
-  for (int e = 0; e < kEmitBatch; ++e) {
-    const int s = s0 + e * kShortThreads + tid;
-    c[e] = s < m ? sh.sel[s] : -1;
-  }
-#pragma unroll
-  for (int e = 0; e < kEmitBatch; ++e) {
-    o[e] = -1;
-    v[e] = -__int_as_float(0x7f800000);
-    if (c[e] >= 0) {
-      if constexpr (kMode == kRemap) {
-        const int b = c[e] / p.sbk;
-        const int32_t blk = b < n_si_s ? sh.si[b] : __ldg(p.si + row * p.ld_si + b);
-        o[e] = static_cast<int32_t>((blk - base_blk) * p.sbk + c[e] % p.sbk);
-      } else {
-        o[e] = static_cast<int32_t>(c[e] - lo);
-      }
-      if (p.vals) v[e] = value_at<kBf16>(rowp, c[e]);
-    }
-  }
-  if (p.slots) {
-#pragma unroll
-    for (int e = 0; e < kEmitBatch; ++e) sl[e] = slot_of(p, row, o[e]);
-  }
-#pragma unroll
-  for (int e = 0; e < kEmitBatch; ++e) {
-    const int s = s0 + e * kShortThreads + tid;
-    if (s < K) {
-      p.out[row * p.ld_out + s] = o[e];
-      if (p.slots) p.slots[row * p.ld_slots + s] = sl[e];
-      if (kMode == kRemap && p.cols) p.cols[row * p.ld_cols + s] = c[e];
-      if (p.vals) p.vals[row * p.ld_vals + s] = v[e];
-    }
-  }
-}
-
 // Order-preserving key of a raw score: the upper 16 bits of the fp32 key for
 // bf16 (its lower 16 bits are a function of the sign), the fp32 key otherwise.
 template <bool kBf16>
@@ -854,7 +894,7 @@ __global__ void __launch_bounds__(kShortThreads, 4) topk_short_kernel(const Topk
     for (int i = tid; i < n; i += kShortThreads) sh.sel[i] = static_cast<int32_t>(lo + i);
     __syncthreads();
     for (int s0 = 0; s0 < K; s0 += kEmitBatch * kShortThreads) {
-      emit_batch<kBf16, kMode>(p, sh, row, lo, base_blk, rowp, s0, n, n_si_s);
+      emit_batch<kShortThreads, kEmitBatch, kBf16, kMode>(p, sh.sel, sh.si, n_si_s, row, lo, base_blk, rowp, s0, n);
     }
     return;
   }
@@ -985,7 +1025,7 @@ __global__ void __launch_bounds__(kShortThreads, 4) topk_short_kernel(const Topk
   __syncthreads();
   // the keys above the threshold and `need` of those equal to it: exactly K
   for (int s0 = 0; s0 < K; s0 += kEmitBatch * kShortThreads) {
-    emit_batch<kBf16, kMode>(p, sh, row, lo, base_blk, rowp, s0, K, n_si_s);
+    emit_batch<kShortThreads, kEmitBatch, kBf16, kMode>(p, sh.sel, sh.si, n_si_s, row, lo, base_blk, rowp, s0, K);
   }
 }
 
