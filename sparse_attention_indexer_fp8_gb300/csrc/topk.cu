@@ -720,14 +720,16 @@ __global__ void __launch_bounds__(kThreads, 1024 / kThreads) topk_kernel(const T
     }
     if (lane == 31) sh.warp_tot[warp] = static_cast<int>(incl);
     __syncthreads();
-    uint32_t before = incl - cnt;
-    uint32_t total = 0;
+    // every warp scans the warp totals itself
+    const uint32_t wt = lane < kThreads / 32 ? static_cast<uint32_t>(sh.warp_tot[lane]) : 0u;
+    uint32_t wi = wt;
 #pragma unroll
-    for (int w = 0; w < kThreads / 32; ++w) {
-      const uint32_t v = static_cast<uint32_t>(sh.warp_tot[w]);
-      before += w < warp ? v : 0u;
-      total += v;
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, wi, o);
+      if (lane >= o) wi += y;
     }
+    const uint32_t before = __shfl_sync(0xFFFFFFFFu, wi - wt, warp) + (incl - cnt);
+    const uint32_t total = __shfl_sync(0xFFFFFFFFu, wi, 31);
     int a = static_cast<int>(before & 0xFFFFu);
     int t = static_cast<int>(before >> 16);
     for (int i = tid; i < na0; i += kThreads) {
