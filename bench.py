@@ -194,6 +194,51 @@ def measure_mma_rate(kind: int, seconds: float, device_index: int, stream):
                     f"sustained = the second half of {seconds:.1f} s of back-to-back launches")}
 
 
+def l2_stream(nbytes: int, kernel_ms: float, what: str):
+    """A kernel's L2-resident read bytes per launch against the L2 read rate measured now."""
+    peak = measure_l2_read()
+    ach = nbytes / (kernel_ms / 1e3) / 1e9
+    return {"achieved_gbs": round(ach, 1), "peak_gbs": peak["gbs"], "frac": round(ach / peak["gbs"], 4),
+            "bytes_per_launch": int(nbytes), "bytes": what, "peak_source": peak["how"]}
+
+
+def measure_l2_read(mb: int = 64, passes: int = 40):
+    """The rate at which every SM together reads a buffer that L2 holds.
+
+    ``idx_diag_l2_read`` (the library's own diagnostic) has one 1024-thread CTA
+    per SM read one chunk of a 64 MB buffer (half of L2 at most) per pass, a
+    different chunk each pass, with 16-byte loads that bypass L1; one warm-up
+    launch brings the buffer into L2, then one launch of ``passes`` passes is
+    timed with CUDA events.
+    """
+    import ctypes
+
+    import sparse_attention_indexer_fp8_gb300 as idx
+
+    lib = idx.library()
+    stream = torch.cuda.current_stream()
+    sptr = ctypes.c_void_p(stream.cuda_stream)
+    buf = torch.ones(mb << 20, dtype=torch.uint8, device="cuda")
+
+    def launch(n):
+        st = lib.idx_diag_l2_read(ctypes.c_void_p(buf.data_ptr()), buf.numel(), n, 0, sptr)
+        if st != 0:
+            raise RuntimeError(lib.idx_last_error().decode())
+
+    launch(2)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    launch(passes)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    gbs = buf.numel() * passes / (ms / 1e3) / 1e9
+    del buf
+    return {"gbs": round(gbs, 1), "how": f"own diagnostic: every SM reads a different chunk of a {mb} MB buffer "
+                                         f"that L2 holds in each of {passes} passes of one launch, 16-byte loads "
+                                         f"past L1, CUDA events"}
+
+
 def measure_cublas_fp8(device_index: int, n: int = 8192, reps: int = 10):
     """Dense e4m3 GEMM rate of the vendor library on this GPU (torch._scaled_mm, n^3, best of reps).
 
@@ -794,7 +839,11 @@ class SparsePrefillBench:
                 "algorithmic_flop_per_launch": flop,
                 "traffic": profiled_traffic("launches_prefill_sparse%s.md" % ("_mxfp4" if self.kv == "mxfp4" else ""),
                                             "logits.cu"),
-                "kernel_ms": round(kernel_ms, 5)}
+                "kernel_ms": round(kernel_ms, 5),
+                # what actually bounds it: every visible candidate column's k record comes out of L2
+                "l2": l2_stream(cols * (68 if self.kv == "mxfp4" else 132), kernel_ms,
+                                "one k record (%d B) out of L2 per visible candidate column per query row"
+                                % (68 if self.kv == "mxfp4" else 132))}
 
     def config(self, world):
         return {"workload": self.wl.name + "-sparse" + ("-mxfp4-cache" if self.kv == "mxfp4" else ""),

@@ -611,6 +611,26 @@ enum { IDX_DIAG_E4M3 = 0, IDX_DIAG_BF16 = 1 };
 idx_status_t idx_diag_mma_peak(int kind, int32_t iters, int32_t ctas, double* flop_out, cudaStream_t stream);
 
 /*
+ * idx_diag_l2_read - diagnostic: read a device buffer with every SM.
+ *
+ * Not part of the indexer's path: the denominator for kernels that stream data
+ * L2 already holds (the sparse prefill reads its gathered k from L2 once per
+ * query row; the selection reads scores the scoring kernel just wrote).
+ * Launches `ctas` CTAs of 1024 threads (<= 0: one per SM). The buffer is cut
+ * into `ctas` contiguous chunks; in each of `passes` passes every CTA reads one
+ * chunk, a different one in consecutive passes (CTA b in pass k reads chunk
+ * (b + 77 k) mod ctas), with 16-byte loads that bypass L1, four in flight per
+ * thread. The caller times the launch on
+ * `stream`: for a buffer that fits in L2 and was read once before, that is the
+ * L2 read rate, bytes * passes / time. Allocates nothing and writes nothing the
+ * caller can see. `buf` 16-byte aligned device memory of at least `bytes`.
+ * Errors: IDX_ERR_INVALID_ARG for a NULL or unaligned buffer, bytes not a
+ * positive multiple of 16, passes < 1, or more CTAs than SMs.
+ */
+idx_status_t idx_diag_l2_read(const void* buf, int64_t bytes, int32_t passes, int32_t ctas,
+                              cudaStream_t stream);
+
+/*
  * Bytes of the optional selection workspace of an operation for `rows` rows
  * (host only). max_cols = 0: the size of the buffer, whatever the row length;
  * max_cols > 0 (the `ld` the selection will be given): 0 when the selection of

@@ -71,6 +71,7 @@ SIGNATURES = {
                                                   c_i32, c_i64, c_ptr, c_i64, c_ptr, c_i32, c_ptr,
                                                   c_i64, c_i32, c_ptr, c_i64, c_ptr]),
     "idx_diag_mma_peak": (c_int, [c_int, c_i32, c_i32, ctypes.POINTER(ctypes.c_double), c_ptr]),
+    "idx_diag_l2_read": (c_int, [c_ptr, c_i64, c_i32, c_i32, c_ptr]),
     "idx_block_span": (c_int, [c_i64, c_i64, ctypes.POINTER(c_i32)]),
     "idx_workspace_bytes": (c_size, [c_int, c_i32, c_i32, c_i32]),
     "idx_status_string": (ctypes.c_char_p, [c_int]),

@@ -1,5 +1,7 @@
-// Diagnostic: the dense tensor-core issue rate of this GPU, for the roofline of
-// the tensor-bound prefill scoring.
+// Diagnostics: the dense tensor-core issue rate of this GPU, for the roofline of
+// the tensor-bound prefill scoring; and the rate at which every SM together
+// reads a buffer that L2 holds, for kernels that stream L2-resident data (the
+// sparse prefill's gathered k, the selection's just-written scores).
 //
 // One persistent CTA per SM (or `ctas`) keeps its SM's tensor core busy with
 // back-to-back tcgen05.mma of the largest single-CTA shape, M = 128, N = 256,
@@ -126,9 +128,58 @@ unsigned int diag_read_and_clear_error(cudaStream_t stream, cudaError_t* err) {
   return v;
 }
 
+// The buffer is cut into one chunk per CTA. In pass k, CTA b reads chunk
+// (b + 77 k) mod gridDim.x (77 shares no factor with the SM counts this runs
+// on, so consecutive passes of one SM read chunks far apart, never its own chunk
+// twice in a row), with 16-byte loads through L2 only (ld.global.cg), four per
+// thread in flight. The words are folded into one value that is stored only if
+// it matches a constant no input of the diagnostic produces, so the loads
+// cannot be dropped.
+__device__ unsigned int g_diag_sink = 0;
+
+__global__ void __launch_bounds__(1024, 1) l2_read_kernel(const uint4* __restrict__ buf, int64_t n_vec,
+                                                         int64_t per_cta, int passes) {
+  constexpr int kU = 4;
+  uint32_t acc = 0;
+  for (int pass = 0; pass < passes; ++pass) {
+    const int64_t chunk = (static_cast<int64_t>(blockIdx.x) + 77ll * pass) % gridDim.x;
+    const int64_t lo = chunk * per_cta;
+    const int64_t hi = lo + per_cta < n_vec ? lo + per_cta : n_vec;
+    for (int64_t v0 = lo; v0 < hi; v0 += static_cast<int64_t>(blockDim.x) * kU) {
+      uint4 r[kU];
+#pragma unroll
+      for (int j = 0; j < kU; ++j) {
+        const int64_t v = v0 + static_cast<int64_t>(j) * blockDim.x + threadIdx.x;
+        r[j] = v < hi ? __ldcg(buf + v) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int j = 0; j < kU; ++j) acc ^= r[j].x ^ r[j].y ^ r[j].z ^ r[j].w;
+    }
+    acc = acc * 2654435761u + static_cast<uint32_t>(pass);
+  }
+  if (acc == 0x9E3779B9u) g_diag_sink = acc;
+}
+
 }  // namespace idx
 
 using namespace idx;
+
+extern "C" idx_status_t idx_diag_l2_read(const void* buf, int64_t bytes, int32_t passes, int32_t ctas,
+                                         cudaStream_t stream) {
+  const char* fn = "idx_diag_l2_read";
+  if (!buf) return fail(IDX_ERR_INVALID_ARG, "%s: NULL buffer", fn);
+  if (bytes < 16 || bytes % 16 != 0) return fail(IDX_ERR_INVALID_ARG, "%s: bytes must be a positive multiple of 16", fn);
+  if (!aligned(buf, 16)) return fail(IDX_ERR_INVALID_ARG, "%s: buffer must be 16-byte aligned", fn);
+  if (passes < 1) return fail(IDX_ERR_INVALID_ARG, "%s: passes < 1", fn);
+  const int sms = device_sm_count();
+  if (sms <= 0) return fail(IDX_ERR_CUDA, "%s: cannot query the SM count", fn);
+  if (ctas <= 0) ctas = sms;
+  if (ctas > sms) return fail(IDX_ERR_INVALID_ARG, "%s: %d CTAs for %d SMs", fn, ctas, sms);
+  const int64_t n_vec = bytes / 16;
+  const int64_t per = (n_vec + ctas - 1) / ctas;
+  l2_read_kernel<<<ctas, 1024, 0, stream>>>(static_cast<const uint4*>(buf), n_vec, per, passes);
+  return check_launch(fn);
+}
 
 extern "C" idx_status_t idx_diag_mma_peak(int kind, int32_t iters, int32_t ctas, double* flop_out,
                                           cudaStream_t stream) {

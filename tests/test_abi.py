@@ -129,6 +129,10 @@ def test_validation_rejects_before_touching_the_device(lib):
     # tensor-rate diagnostic: unknown kind, no iterations
     assert lib.idx_diag_mma_peak(7, 100, 0, None, None) == 2
     assert lib.idx_diag_mma_peak(0, 0, 0, None, None) == 1
+    assert lib.idx_diag_l2_read(None, 1 << 20, 1, 0, None) == 1              # NULL buffer
+    assert lib.idx_diag_l2_read(fake, 15, 1, 0, None) == 1                   # not a multiple of 16
+    assert lib.idx_diag_l2_read(ctypes.c_void_p(0x1008), 1 << 20, 1, 0, None) == 1   # unaligned
+    assert lib.idx_diag_l2_read(fake, 1 << 20, 0, 0, None) == 1              # passes < 1
     # misaligned q stride
     assert lib.idx_mqa_logits_prefill(fake, 8200, fake, 0, 64, fake, fake, 64, None, fake, 4, None, 0,
                                       0, None, 0, fake, 0, 64, None, 0, None) == 2

@@ -1116,3 +1116,14 @@ def test_selection_workspace_sparse_paths():
         idx.idx_mqa_logits_prefill(dev(q2), dev(w2), dev(k8), dev(ks), None,
                                    dev(np.full(8, 256, np.int32)), lo,
                                    ws=torch.zeros((8, 1024), dtype=torch.int32, device=DEV))
+
+
+def test_diag_l2_read_rate_is_plausible():
+    # the L2 read-rate diagnostic: a 64 MB buffer (inside L2) read by every SM;
+    # the rate must lie between the HBM copy rate's order and far below any
+    # physical limit (a dropped load would show as an absurd rate)
+    import bench
+
+    r = bench.measure_l2_read(mb=64, passes=10)
+    idx.idx_device_error()
+    assert 1000.0 < r["gbs"] < 100000.0, r
