@@ -115,7 +115,7 @@ constexpr int kHistBins = 1024;  // first selection digit: the top 10 bits of th
 // copies each tile's block scales into tensor memory ahead of its MMAs; they
 // take columns from the accumulators: three accumulator stages, a commit per
 // tile, then one 4-column scale slot per k stage and one for q.
-template <int NQ, bool kFp4 = false>
+template <int NQ, bool kFp4 = false, bool kHist = true>
 struct Cfg {
   static_assert(!kFp4 || NQ == 1, "the MXFP4 path serves one query per group");
   static constexpr int N = 64 * NQ;
@@ -124,7 +124,9 @@ struct Cfg {
   static constexpr int kEpiWG = NQ == 4 ? 2 : 1;
   static constexpr int kEpiWarps = 4 * kEpiWG;
   static constexpr int kThreads = 64 + kEpiWarps * 32;
-  static constexpr int kStages = NQ == 4 ? 8 : 4;
+  // k stages; one query per group without the workspace histogram: the
+  // histogram area's shared memory holds a fifth stage instead
+  static constexpr int kStages = NQ == 4 ? 8 : (NQ == 1 && !kHist ? 5 : 4);
   static constexpr int kAccStages = NQ == 1 ? (kFp4 ? 3 : 4) : 2;
   // tiles per tcgen05.commit: one commit covers the MMAs of kCommit consecutive
   // tiles (commits are costly next to a 4-MMA tile); one accumulator-ready
@@ -143,7 +145,7 @@ struct Cfg {
   static constexpr int kOffScale = kOffQ + 2 * kQStageBytes;
   static constexpr int kOffW = kOffScale + kStages * kScaleStageBytes;
   // per epilogue warp, one query per group: 1024 bins of 16-bit counts
-  static constexpr int kHistWords = NQ == 1 ? kHistBins / 2 : 0;
+  static constexpr int kHistWords = NQ == 1 && kHist ? kHistBins / 2 : 0;
   static constexpr int kOffHist = kOffW + kEpiWarps * NQ * 64 * 4;
   static constexpr int kOffSf = kOffHist + kEpiWarps * kHistWords * 4;
   // MXFP4: per k stage the tile's 128 scale words as 32 lines of 16 bytes (line m
@@ -343,11 +345,11 @@ __device__ __forceinline__ float weighted_head_sum(const uint32_t (&a0)[32], con
   return (hsum2(acc[0]) + hsum2(acc[1])) + (hsum2(acc[2]) + hsum2(acc[3]));
 }
 
-template <int NQ, bool kOutBf16, bool kFp4>
-__global__ void __launch_bounds__(Cfg<NQ, kFp4>::kThreads, Cfg<NQ, kFp4>::kCtasPerSm)
+template <int NQ, bool kOutBf16, bool kFp4, bool kHist>
+__global__ void __launch_bounds__(Cfg<NQ, kFp4, kHist>::kThreads, Cfg<NQ, kFp4, kHist>::kCtasPerSm)
 mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_kv,
                   const __grid_constant__ CUtensorMap map_scale, const LogitsParams p) {
-  using C = Cfg<NQ, kFp4>;
+  using C = Cfg<NQ, kFp4, kHist>;
   constexpr int kThreads = C::kThreads;
   constexpr int kEpiWG = C::kEpiWG;
   extern __shared__ uint8_t smem_raw[];
@@ -959,11 +961,11 @@ mqa_logits_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   if (warp == 1) tmem_dealloc(tmem_base, C::kTmemCols);
 }
 
-template <int NQ, bool kOutBf16, bool kFp4 = false>
+template <int NQ, bool kOutBf16, bool kFp4 = false, bool kHist = true>
 idx_status_t launch_logits(const CUtensorMap& mq, const CUtensorMap& mkv, const CUtensorMap& msc,
                            const LogitsParams& p, int grid, cudaStream_t stream, const char* fn) {
-  using C = Cfg<NQ, kFp4>;
-  auto kern = mqa_logits_kernel<NQ, kOutBf16, kFp4>;
+  using C = Cfg<NQ, kFp4, kHist>;
+  auto kern = mqa_logits_kernel<NQ, kOutBf16, kFp4, kHist>;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -994,15 +996,27 @@ idx_status_t dispatch(int nq_tmpl, const CUtensorMap& mq, const CUtensorMap& mkv
   long long grid = static_cast<long long>(sms) * per_sm;
   if (max_tiles >= 0 && max_tiles < grid) grid = max_tiles;
   if (grid <= 0) return IDX_OK;
+  // one query per group: the workspace histogram's variant (four k stages) only
+  // when a workspace is given
+  const int g = static_cast<int>(grid);
+  const bool h = p.hist != nullptr;
   if (fp4) {
     if (nq_tmpl != 1) return fail(IDX_ERR_UNSUPPORTED, "%s: the MXFP4 path serves one query per group", fn);
-    return p.out_bf16 ? launch_logits<1, true, true>(mq, mkv, msc, p, static_cast<int>(grid), stream, fn)
-                      : launch_logits<1, false, true>(mq, mkv, msc, p, static_cast<int>(grid), stream, fn);
+    if (h) {
+      return p.out_bf16 ? launch_logits<1, true, true, true>(mq, mkv, msc, p, g, stream, fn)
+                        : launch_logits<1, false, true, true>(mq, mkv, msc, p, g, stream, fn);
+    }
+    return p.out_bf16 ? launch_logits<1, true, true, false>(mq, mkv, msc, p, g, stream, fn)
+                      : launch_logits<1, false, true, false>(mq, mkv, msc, p, g, stream, fn);
   }
   switch (nq_tmpl) {
     case 1:
-      return p.out_bf16 ? launch_logits<1, true>(mq, mkv, msc, p, static_cast<int>(grid), stream, fn)
-                        : launch_logits<1, false>(mq, mkv, msc, p, static_cast<int>(grid), stream, fn);
+      if (h) {
+        return p.out_bf16 ? launch_logits<1, true, false, true>(mq, mkv, msc, p, g, stream, fn)
+                          : launch_logits<1, false, false, true>(mq, mkv, msc, p, g, stream, fn);
+      }
+      return p.out_bf16 ? launch_logits<1, true, false, false>(mq, mkv, msc, p, g, stream, fn)
+                        : launch_logits<1, false, false, false>(mq, mkv, msc, p, g, stream, fn);
     case 2:
       return p.out_bf16 ? launch_logits<2, true>(mq, mkv, msc, p, static_cast<int>(grid), stream, fn)
                         : launch_logits<2, false>(mq, mkv, msc, p, static_cast<int>(grid), stream, fn);
