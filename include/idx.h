@@ -46,11 +46,11 @@
  * allocating it); the selection zeroes every row it consumes, so the buffer is
  * ready for the next step. Supported by the kernels with one query per group:
  * dense decode with next_n = 1 and both sparse modes. ws = NULL selects the
- * two-pass selection. Rows of at most 4096 columns, when there are more of
- * them than the device has SMs, are selected from registers in one read and
- * never use the histogram: the selection only clears a buffer it is given, and
- * idx_workspace_bytes(op, rows, ld, k) returns 0 for them, meaning pass NULL
- * to both calls (the logits call then skips the histogram too).
+ * two-pass selection. Rows of at most 4096 columns are selected from
+ * registers in one read and never use the histogram: the selection only clears
+ * a buffer it is given, and idx_workspace_bytes(op, rows, ld, k) returns 0 for
+ * them, meaning pass NULL to both calls (the logits call then skips the
+ * histogram and keeps more k in flight).
  *
  * Paged cache layout (the "split block" layout)
  * ---------------------------------------------

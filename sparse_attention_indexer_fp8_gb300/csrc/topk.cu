@@ -1112,15 +1112,15 @@ namespace idx {
 
 bool topk_rows_short(int64_t rows, int64_t max_cols) {
   const int sms = device_sm_count();
-  return max_cols <= kShortMax && sms > 0 && rows > sms;
+  return rows > 0 && max_cols <= kShortMax && sms > 0;
 }
 
 }  // namespace idx
 
 namespace {
 
-// Many rows of at most kShortMax columns take the short-row kernel; many rows
-// of at most 64K columns (prefill chunks) the two-blocks-per-SM configuration;
+// Rows of at most kShortMax columns take the short-row kernel; many rows of at
+// most 64K columns (prefill chunks) the two-blocks-per-SM configuration;
 // anything else one 1024-thread block per SM.
 template <bool kBf16, int kMode>
 idx_status_t launch_topk(const TopkParams& p, int rows, int64_t max_cols, cudaStream_t stream,
@@ -1128,9 +1128,9 @@ idx_status_t launch_topk(const TopkParams& p, int rows, int64_t max_cols, cudaSt
   const int sms = device_sm_count();
   if constexpr (kMode != kMerge) {
     if (topk_rows_short(rows, max_cols)) {
-      // many short rows: one 256-thread block per row with the keys in
-      // registers, several rows in flight per SM (with at most one row per SM
-      // the 1024-thread block's lower per-row latency wins)
+      // short rows: one 256-thread block per row with the keys in registers,
+      // several rows in flight per SM; with one row per SM as well (128-row
+      // sparse decode) its short chain beats the 1024-thread block's passes
       TopkParams q = p;
       q.rows = rows;
       q.ahead = 0;

@@ -535,8 +535,8 @@ def test_sparse_remap_short_rows_load_paths_and_digit_ties(bf16, ld_extra, offse
     for r in range(rows):
         np.add.at(h[r], (keys[r, :end[r]] >> 22).astype(np.int64), 1)
     ws = dev(h)
-    if rows > torch.cuda.get_device_properties(0).multi_processor_count:
-        assert idx.idx_workspace_bytes("sparse_topk_remap", rows, ld, k) == 0
+    assert idx.idx_workspace_bytes("sparse_topk_remap", rows, ld, k) == 0
+    assert idx.idx_workspace_bytes("sparse_topk_remap", 8, ld, k) == 0     # fewer rows than SMs too
     assert idx.idx_workspace_bytes("sparse_topk_remap", rows, 0, k) == rows * 1024 * 4
     pos = torch.full((rows, k), -7, dtype=torch.int32, device=DEV)
     cols = torch.full((rows, k), -7, dtype=torch.int32, device=DEV)
