@@ -551,9 +551,10 @@ class DecodeBench:
         return hbm_roofline("mqa_logits_kernel<1, MXFP4 k> (paged decode)" if self.kv == "mxfp4"
                             else "mqa_logits_kernel<1> (paged decode)", tok * tb + self.B * (64 * 128 + 64 * 4),
                             tok * 4, kernel_ms, peaks, peak_kind,
-                            # the committed counters were taken on the launch with the workspace
-                            # histogram (four k stages), not on this one
-                            traffic=None,
+                            # the committed e4m3 counters are of this launch (no workspace, five k
+                            # stages); the MXFP4 ones were taken with the workspace histogram
+                            traffic=(None if self.kv == "mxfp4" else
+                                     profiled_traffic(f"mqa_logits_decode_{self.name}.md", "logits.cu")),
                             step_kcache_frac=round(tok * tb / (step_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4))
 
     def config(self, world):
