@@ -21,6 +21,16 @@ def test_hbm_roofline_arithmetic():
     assert r["algorithmic_bytes_per_launch"] == 3_000_000_000 and r["kernel_ms"] == 0.5
 
 
+def test_l2_stream_arithmetic(monkeypatch):
+    # the L2 side of the sparse prefill line: bytes out of L2 per launch over the
+    # kernel time, against the rate the diagnostic measured in the same run
+    monkeypatch.setattr(bench, "measure_l2_read", lambda: {"gbs": 20000.0, "how": "stub"})
+    r = bench.l2_stream(4_000_000_000, 0.5, "k records")
+    assert r["achieved_gbs"] == pytest.approx(8000.0)
+    assert r["peak_gbs"] == 20000.0 and r["frac"] == pytest.approx(0.4)
+    assert r["bytes_per_launch"] == 4_000_000_000 and r["bytes"] == "k records" and r["peak_source"] == "stub"
+
+
 def test_profiled_traffic_only_for_the_profiled_source(tmp_path, monkeypatch):
     src = tmp_path / "sparse_attention_indexer_fp8_gb300" / "csrc"
     src.mkdir(parents=True)
